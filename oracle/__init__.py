@@ -1,0 +1,206 @@
+"""CPU oracle for the fused all-reduce epilogue -- TEST INFRASTRUCTURE.
+
+A plain C implementation (``oracle.c``, fp64 for the rank sum / residual /
+RMSNorm, IEEE binary32 for the NVFP4 quantiser) wrapped with ctypes and numpy.
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline
+leg may import this package. The product library never imports it; the two
+share no code.
+
+bf16 tensors cross this interface as ``numpy.uint16`` bit patterns.
+
+Sources (pages as titled): "Deep Dive: AllReduce and AllReduce Fusion in
+TensorRT-LLM", 2.1.1 AllReduce, 6.3 Inside the Fused Kernel, 6.5 NVFP4
+Quantization Fusion; "Collectives, topology, custom all-reduce", the vLLM
+custom all-reduce (fixed rank order).
+
+Parity pins: every function here is pinned by ``tests/test_oracle_pins.py``
+(closed forms, invariants, format tables, library cross-checks, brute force).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_LIB_PATH = os.path.join(_HERE, "_build", "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+# -std=c11 and -ffp-contract=off: no fused multiply-add on any host
+# (aarch64 gcc contracts by default in GNU mode); no fast-math.
+CFLAGS = ["-std=c11", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC", "-shared"]
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into oracle/_build/liboracle.so with the host gcc."""
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    os.makedirs(os.path.dirname(_LIB_PATH), exist_ok=True)
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    subprocess.run(["gcc", *CFLAGS, "-o", tmp, _SRC, "-lm"], check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        # ORACLE_LIB lets the mutation tests load a deliberately broken copy.
+        override = os.environ.get("ORACLE_LIB")
+        lib = ctypes.CDLL(override if override else build())
+        P = ctypes.c_void_p
+        i64 = ctypes.c_int64
+        lib.orc_bf16_to_double.restype = ctypes.c_double
+        lib.orc_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.orc_bf16_from_double.restype = ctypes.c_uint16
+        lib.orc_bf16_from_double.argtypes = [ctypes.c_double]
+        lib.orc_e4m3_to_float.restype = ctypes.c_float
+        lib.orc_e4m3_to_float.argtypes = [ctypes.c_uint8]
+        lib.orc_e4m3_from_float.restype = ctypes.c_uint8
+        lib.orc_e4m3_from_float.argtypes = [ctypes.c_float]
+        lib.orc_e2m1_to_float.restype = ctypes.c_float
+        lib.orc_e2m1_to_float.argtypes = [ctypes.c_uint8]
+        lib.orc_e2m1_from_float.restype = ctypes.c_uint8
+        lib.orc_e2m1_from_float.argtypes = [ctypes.c_float]
+        for name in ("orc_bf16_from_double_n", "orc_e4m3_from_float_n", "orc_e2m1_from_float_n"):
+            getattr(lib, name).restype = None
+            getattr(lib, name).argtypes = [P, P, i64]
+        lib.orc_fused_rmsnorm.restype = ctypes.c_int
+        lib.orc_fused_rmsnorm.argtypes = [P, ctypes.c_int, P, P, ctypes.c_float, i64, i64,
+                                          P, P, P, P]
+        lib.orc_nvfp4_quantize.restype = ctypes.c_int
+        lib.orc_nvfp4_quantize.argtypes = [P, i64, i64, ctypes.c_int, ctypes.c_float, P, P, P]
+        lib.orc_bf16_amax.restype = ctypes.c_float
+        lib.orc_bf16_amax.argtypes = [P, i64]
+        _lib = lib
+        return lib
+
+
+def _ptr(a: np.ndarray | None):
+    return None if a is None else a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _u16(a) -> np.ndarray:
+    a = np.ascontiguousarray(a)
+    if a.dtype != np.uint16:
+        raise TypeError(f"bf16 data must be passed as uint16 bit patterns, got {a.dtype}")
+    return a
+
+
+# ---------------------------------------------------------------- formats
+
+def bf16_to_float64(bits) -> np.ndarray:
+    """Decode bf16 bit patterns (exact)."""
+    b = _u16(bits)
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def bf16_from_float64(x) -> np.ndarray:
+    """Round fp64 values to bf16 (nearest, ties to even), as uint16 bits."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().orc_bf16_from_double_n(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def e4m3_from_float32(x) -> np.ndarray:
+    """binary32 -> E4M3 bytes, nearest-even, saturating at +-448."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().orc_e4m3_from_float_n(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def e2m1_from_float32(x) -> np.ndarray:
+    """binary32 -> E2M1 nibbles (0..15), nearest-even, saturating at +-6."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().orc_e2m1_from_float_n(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def e4m3_to_float32(codes) -> np.ndarray:
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([lib.orc_e4m3_to_float(int(v)) for v in c.ravel()],
+                    dtype=np.float32).reshape(c.shape)
+
+
+def e2m1_to_float32(codes) -> np.ndarray:
+    lib = _load()
+    c = np.asarray(codes, dtype=np.uint8)
+    return np.array([lib.orc_e2m1_to_float(int(v)) for v in c.ravel()],
+                    dtype=np.float32).reshape(c.shape)
+
+
+# ---------------------------------------------------------------- the method
+
+def fused_rmsnorm(partials, residual, gamma, eps: float, want_ref: bool = True):
+    """Rank sum -> residual add -> RMSNorm on bf16 bit-pattern arrays.
+
+    partials : list of n uint16 arrays [T, d]; residual: uint16 [T, d] or None;
+    gamma: uint16 [d]; eps: the fp32 epsilon.
+    Returns dict with ``out_residual`` and ``out_norm`` (uint16 [T, d]) and,
+    when ``want_ref``, the unrounded fp64 ``h`` and ``y``.
+    """
+    parts = [_u16(p) for p in partials]
+    if not parts:
+        raise ValueError("need at least one partial")
+    T, d = parts[0].shape
+    for p in parts:
+        if p.shape != (T, d):
+            raise ValueError("all partials must have the same [T, d] shape")
+    res = None if residual is None else _u16(residual)
+    if res is not None and res.shape != (T, d):
+        raise ValueError("residual shape mismatch")
+    g = _u16(gamma)
+    if g.shape != (d,):
+        raise ValueError("gamma must be [d]")
+    arr = (ctypes.c_void_p * len(parts))(*[p.ctypes.data for p in parts])
+    out_r = np.empty((T, d), np.uint16)
+    out_n = np.empty((T, d), np.uint16)
+    h = np.empty((T, d), np.float64) if want_ref else None
+    y = np.empty((T, d), np.float64) if want_ref else None
+    rc = _load().orc_fused_rmsnorm(ctypes.cast(arr, ctypes.c_void_p), len(parts), _ptr(res),
+                                   _ptr(g), ctypes.c_float(eps), T, d, _ptr(h), _ptr(y),
+                                   _ptr(out_r), _ptr(out_n))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    out = {"out_residual": out_r, "out_norm": out_n}
+    if want_ref:
+        out["h"] = h
+        out["y"] = y
+    return out
+
+
+def nvfp4_quantize(x, global_scale: float | None = None):
+    """NVFP4 quantisation of a bf16 [T, d] tensor (d % 16 == 0).
+
+    global_scale None -> dynamic g = amax / (6 * 448); else the given g.
+    Returns (codes uint8 [T, d/2], scales uint8 [T, d/16], g as np.float32).
+    """
+    xb = _u16(x)
+    T, d = xb.shape
+    codes = np.empty((T, d // 2), np.uint8)
+    scales = np.empty((T, d // 16), np.uint8)
+    g = ctypes.c_float(0.0)
+    given = global_scale is not None
+    rc = _load().orc_nvfp4_quantize(_ptr(xb), T, d, int(given),
+                                    ctypes.c_float(global_scale if given else 0.0),
+                                    _ptr(codes), _ptr(scales), ctypes.byref(g))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return codes, scales, np.float32(g.value)
+
+
+def bf16_amax(x) -> np.float32:
+    xb = _u16(x)
+    return np.float32(_load().orc_bf16_amax(_ptr(xb), xb.size))

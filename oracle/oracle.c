@@ -1,0 +1,345 @@
+/*
+ * oracle.c -- plain, slow CPU reference for the fused tensor-parallel
+ * all-reduce epilogue (rank sum -> residual add -> RMSNorm -> optional NVFP4).
+ *
+ * TEST INFRASTRUCTURE. This file exists only so the CUDA library can be
+ * checked against something obviously correct. Only the test suite, the smoke
+ * check and the benchmark's CPU-baseline leg load it. The product library
+ * neither links nor calls it, and the two share no code, header or table.
+ *
+ * Sources (pages as titled):
+ *   [AR] "Deep Dive: AllReduce and AllReduce Fusion in TensorRT-LLM"
+ *        - 2.1.1 AllReduce: element-wise sum of the ranks' partial outputs.
+ *        - 6.3 Inside the Fused Kernel: FusedOp order -- residual add, store
+ *          residual_out, RMSNorm with gamma, store norm_out, then quantise.
+ *        - 6.5 NVFP4 Quantization Fusion: the bf16 norm output is quantised
+ *          to NVFP4 before the final write.
+ *   [CT] "Collectives, topology, custom all-reduce"
+ *        - vLLM's custom all-reduce: the ranks are summed in one fixed order.
+ *
+ * Readings where the pages are silent (each is a plain textbook reading):
+ *   - RMSNorm: y_i = h_i / sqrt(mean_i(h_i^2) + eps) * gamma_i over the last
+ *     (hidden) dimension, eps inside the square root.
+ *   - The norm sees the unrounded sum h, not bf16(h): in 6.3 the norm is
+ *     applied to the same register value whose copy is stored.
+ *   - NVFP4: 16-element blocks along a row, one E4M3 scale per block, E2M1
+ *     codes, fp32 global scale g = amax / (6 * 448). The element scaling uses
+ *     one IEEE reciprocal per block and one multiply per element (see
+ *     orc_nvfp4_quantize). Codes are packed low nibble first.
+ *
+ * Arithmetic: steps 1-5 in fp64; the NVFP4 quantiser in IEEE binary32 with
+ * one round-to-nearest-even per operation. Build with -ffp-contract=off and
+ * without fast-math so no multiply-add is fused.
+ */
+#include <float.h>
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+
+/* ------------------------------------------------------------------------ */
+/* Number formats (definitions, no lookup tables shared with anything).     */
+/* ------------------------------------------------------------------------ */
+
+/* bf16 is the upper half of an IEEE binary32: decoding is exact. */
+double orc_bf16_to_double(uint16_t b)
+{
+    uint32_t u = (uint32_t)b << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/*
+ * Round a double straight to bf16 (8 significant bits, exponent range of
+ * binary32), nearest, ties to even. The value is scaled by the bf16 spacing
+ * at its magnitude (a power of two, so exactly), rounded to an integer with
+ * rint() in the default nearest-even mode, and scaled back.
+ */
+uint16_t orc_bf16_from_double(double x)
+{
+    uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    if (isnan(x))
+        return 0x7FC0u;
+    double a = fabs(x);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a) || a >= 0x1p128)
+        return (uint16_t)(sign | 0x7F80u);
+    int e;
+    frexp(a, &e); /* a in [2^(e-1), 2^e) */
+    int qexp = (e - 1) - 7; /* 7 fraction bits below the leading one */
+    if (qexp < -133)
+        qexp = -133; /* subnormal spacing 2^-126 * 2^-7 */
+    double q = ldexp(1.0, qexp);
+    double r = rint(a / q) * q;
+    if (r >= 0x1p128)
+        return (uint16_t)(sign | 0x7F80u);
+    float f = (float)r; /* exact: r has at most 8 significant bits */
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    return (uint16_t)(sign | (uint16_t)(u >> 16));
+}
+
+/* E4M3 (OCP FP8): 1 sign, 4 exponent bits (bias 7), 3 mantissa bits,
+ * subnormals at exponent field 0, S.1111.111 is NaN, no infinities,
+ * largest finite 448. */
+float orc_e4m3_to_float(uint8_t c)
+{
+    int s = (c >> 7) & 1, e = (c >> 3) & 0xF, m = c & 7;
+    double v;
+    if (e == 15 && m == 7)
+        return NAN;
+    if (e == 0)
+        v = ldexp((double)m, -9); /* m/8 * 2^(1-7) */
+    else
+        v = ldexp(1.0 + m / 8.0, e - 7);
+    return (float)(s ? -v : v);
+}
+
+/* Code of a non-negative value that is exactly an E4M3 number (<= 448). */
+static uint8_t e4m3_code_of_exact(double r)
+{
+    if (r < 0x1p-6)
+        return (uint8_t)(r / 0x1p-9); /* subnormal: m * 2^-9, m in 0..7 */
+    int e;
+    double f = frexp(r, &e); /* r = f * 2^e, f in [0.5, 1) */
+    int ub = e - 1;         /* r = (1 + m/8) * 2^ub */
+    int m = (int)((2.0 * f - 1.0) * 8.0);
+    return (uint8_t)(((ub + 7) << 3) | m);
+}
+
+/* binary32 -> E4M3, round to nearest even, saturating to +-448 (satfinite).
+ * NaN maps to the NaN pattern. */
+uint8_t orc_e4m3_from_float(float v)
+{
+    uint8_t sign = signbit(v) ? 0x80u : 0u;
+    if (isnan(v))
+        return 0x7Fu;
+    double a = fabs((double)v);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a))
+        return (uint8_t)(sign | e4m3_code_of_exact(448.0));
+    int e;
+    frexp(a, &e);
+    int qexp = (e - 1) - 3; /* 3 mantissa bits */
+    if (qexp < -9)
+        qexp = -9; /* subnormal spacing 2^-6 * 2^-3 */
+    double q = ldexp(1.0, qexp);
+    double r = rint(a / q) * q;
+    if (r > 448.0)
+        r = 448.0;
+    return (uint8_t)(sign | e4m3_code_of_exact(r));
+}
+
+/* E2M1 (OCP FP4): 1 sign, 2 exponent bits (bias 1), 1 mantissa bit.
+ * Magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6 for codes 0..7; bit 3 is the sign. */
+float orc_e2m1_to_float(uint8_t c)
+{
+    int s = (c >> 3) & 1, e = (c >> 1) & 3, m = c & 1;
+    double v = (e == 0) ? 0.5 * m : ldexp(1.0 + 0.5 * m, e - 1);
+    return (float)(s ? -v : v);
+}
+
+/* binary32 -> E2M1, round to nearest even, saturating to +-6 (satfinite).
+ * The sign bit follows the input's sign, so a negative value that rounds to
+ * zero gives 0x8. */
+uint8_t orc_e2m1_from_float(float v)
+{
+    uint8_t sign = signbit(v) ? 0x8u : 0u;
+    double a = fabs((double)v);
+    if (isnan(v))
+        return 0x7u; /* outside the contract; never produced from finite data */
+    if (a == 0.0)
+        return sign;
+    double r;
+    if (isinf(a)) {
+        r = 6.0;
+    } else {
+        int e;
+        frexp(a, &e);
+        int qexp = (e - 1) - 1; /* 1 mantissa bit */
+        if (qexp < -1)
+            qexp = -1; /* subnormal spacing 2^0 * 2^-1 */
+        double q = ldexp(1.0, qexp);
+        r = rint(a / q) * q;
+        if (r > 6.0)
+            r = 6.0;
+    }
+    uint8_t code;
+    if (r < 1.0) {
+        code = (uint8_t)(r / 0.5); /* 0 or 1 */
+    } else {
+        int e;
+        double f = frexp(r, &e); /* r = (1 + m/2) * 2^(e-1) */
+        int m = (int)((2.0 * f - 1.0) * 2.0);
+        code = (uint8_t)(((e - 1 + 1) << 1) | m);
+    }
+    return (uint8_t)(sign | code);
+}
+
+/* Vector forms, for the Python wrapper. */
+void orc_bf16_from_double_n(const double* x, uint16_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_bf16_from_double(x[i]);
+}
+void orc_e4m3_from_float_n(const float* x, uint8_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_e4m3_from_float(x[i]);
+}
+void orc_e2m1_from_float_n(const float* x, uint8_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_e2m1_from_float(x[i]);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Steps 1-5: rank sum, residual add, RMSNorm ([AR] 2.1.1, 6.3; [CT]).     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * partials  : n host pointers, each bf16 bits [T, d] row-major
+ * residual  : bf16 bits [T, d] or NULL (no residual: h = s)
+ * gamma     : bf16 bits [d]
+ * eps       : the caller's fp32 epsilon, used at its exact value
+ * h_ref     : fp64 [T, d] or NULL -- the unrounded new residual
+ * y_ref     : fp64 [T, d] or NULL -- the unrounded normed output
+ * out_res   : bf16 bits [T, d] or NULL -- bf16_rne(h)
+ * out_norm  : bf16 bits [T, d] or NULL -- bf16_rne(y)
+ * Returns 0, or -1 on a bad argument.
+ */
+int orc_fused_rmsnorm(const uint16_t* const* partials, int n, const uint16_t* residual,
+                      const uint16_t* gamma, float eps, int64_t T, int64_t d, double* h_ref,
+                      double* y_ref, uint16_t* out_res, uint16_t* out_norm)
+{
+    if (n < 1 || T < 0 || d < 1 || !partials || !gamma)
+        return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        const int64_t row = t * d;
+        double sumsq = 0.0;
+        /* 1-3: fixed-order rank sum, residual add, store new residual */
+        for (int64_t i = 0; i < d; ++i) {
+            double s = 0.0;
+            for (int r = 0; r < n; ++r)
+                s += orc_bf16_to_double(partials[r][row + i]);
+            double h = residual ? s + orc_bf16_to_double(residual[row + i]) : s;
+            if (h_ref)
+                h_ref[row + i] = h;
+            if (out_res)
+                out_res[row + i] = orc_bf16_from_double(h);
+            sumsq += h * h;
+        }
+        /* 4: mean square over the hidden dimension */
+        double ms = sumsq / (double)d;
+        double denom = sqrt(ms + (double)eps);
+        /* 5: normalise, scale by gamma, store */
+        for (int64_t i = 0; i < d; ++i) {
+            double s = 0.0;
+            for (int r = 0; r < n; ++r)
+                s += orc_bf16_to_double(partials[r][row + i]);
+            double h = residual ? s + orc_bf16_to_double(residual[row + i]) : s;
+            double y = h / denom * orc_bf16_to_double(gamma[i]);
+            if (y_ref)
+                y_ref[row + i] = y;
+            if (out_norm)
+                out_norm[row + i] = orc_bf16_from_double(y);
+        }
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Step 6: NVFP4 quantiser ([AR] 6.5), binary32 arithmetic.                 */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * x        : bf16 bits [T, d] (d % 16 == 0), the normed output
+ * given    : nonzero -> g = g_in (a calibrated scale supplied by the caller);
+ *            zero    -> g = amax(|x|) / 2688 over the whole tensor
+ * codes    : [T, d/2] bytes; byte k of a row = code(2k) | code(2k+1) << 4
+ * scales   : [T, d/16] E4M3 bytes, row-major, one per 16-element block
+ * g_out    : receives g (may be NULL)
+ *
+ * Per block b of 16 consecutive elements x_i of one row:
+ *   amax_b = max |x_i|
+ *   s_b    = E4M3(amax_b / (6 g))           scale byte, RNE, saturating
+ *   inv    = 1 / (float(s_b) * g)           one reciprocal per block,
+ *            capped at FLT_MAX; inv = 0 when s_b is zero
+ *   q_i    = x_i * inv                      one multiply per element
+ *   code_i = E2M1(q_i)                      RNE, saturating, sign of q_i
+ * A g that is not a positive finite number makes every scale 0 and every
+ * code a signed zero.
+ */
+int orc_nvfp4_quantize(const uint16_t* x, int64_t T, int64_t d, int given, float g_in,
+                       uint8_t* codes, uint8_t* scales, float* g_out)
+{
+    if (T < 0 || d < 16 || d % 16 != 0 || !x)
+        return -1;
+    float g;
+    if (given) {
+        g = g_in;
+    } else {
+        float amax = 0.0f;
+        for (int64_t k = 0; k < T * d; ++k) {
+            float a = fabsf((float)orc_bf16_to_double(x[k]));
+            if (a > amax)
+                amax = a;
+        }
+        g = amax / 2688.0f; /* 6 * 448, exact in binary32 */
+    }
+    if (g_out)
+        *g_out = g;
+    int degenerate = !(g > 0.0f) || isinf(g);
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t b = 0; b < d / 16; ++b) {
+            const uint16_t* xb = x + t * d + b * 16;
+            float xv[16];
+            float amax_b = 0.0f;
+            for (int i = 0; i < 16; ++i) {
+                xv[i] = (float)orc_bf16_to_double(xb[i]);
+                float a = fabsf(xv[i]);
+                if (a > amax_b)
+                    amax_b = a;
+            }
+            uint8_t sbyte = 0;
+            float inv = 0.0f;
+            if (!degenerate) {
+                float den6 = 6.0f * g;
+                float sraw = amax_b / den6;
+                sbyte = orc_e4m3_from_float(sraw);
+                if (sbyte != 0) {
+                    float den = orc_e4m3_to_float(sbyte) * g;
+                    inv = 1.0f / den;
+                    if (inv > FLT_MAX)
+                        inv = FLT_MAX;
+                }
+            }
+            if (scales)
+                scales[t * (d / 16) + b] = sbyte;
+            if (codes) {
+                for (int k = 0; k < 8; ++k) {
+                    float q0 = xv[2 * k] * inv;
+                    float q1 = xv[2 * k + 1] * inv;
+                    uint8_t lo = orc_e2m1_from_float(q0);
+                    uint8_t hi = orc_e2m1_from_float(q1);
+                    codes[t * (d / 2) + b * 8 + k] = (uint8_t)(lo | (hi << 4));
+                }
+            }
+        }
+    }
+    return 0;
+}
+
+/* Absolute maximum of a bf16 tensor, as the binary32 bit pattern. */
+float orc_bf16_amax(const uint16_t* x, int64_t n)
+{
+    float amax = 0.0f;
+    for (int64_t k = 0; k < n; ++k) {
+        float a = fabsf((float)orc_bf16_to_double(x[k]));
+        if (a > amax)
+            amax = a;
+    }
+    return amax;
+}

@@ -1,0 +1,62 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each case plants one mistake in a copy of oracle/oracle.c (on the CPU), builds
+it, and runs the pin tests against that copy; the pins must fail. A mutant
+that survives would mean a part of the oracle is not really pinned.
+"""
+import os
+import subprocess
+import sys
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+SRC = os.path.join(ROOT, "oracle", "oracle.c")
+
+# (name, original text, planted mistake)
+MUTANTS = [
+    ("mean_as_sum", "double ms = sumsq / (double)d;", "double ms = sumsq;"),
+    ("eps_outside_sqrt", "double denom = sqrt(ms + (double)eps);", "double denom = sqrt(ms) + (double)eps;"),
+    ("eps_dropped", "double denom = sqrt(ms + (double)eps);", "double denom = sqrt(ms);"),
+    ("last_rank_dropped", "for (int r = 0; r < n; ++r)\n                s += orc_bf16_to_double(partials[r][row + i]);\n            double h = residual ? s + orc_bf16_to_double(residual[row + i]) : s;\n            if (h_ref)",
+     "for (int r = 0; r < n - 1; ++r)\n                s += orc_bf16_to_double(partials[r][row + i]);\n            double h = residual ? s + orc_bf16_to_double(residual[row + i]) : s;\n            if (h_ref)"),
+    ("residual_dropped", "double h = residual ? s + orc_bf16_to_double(residual[row + i]) : s;\n            if (h_ref)",
+     "double h = s;\n            if (h_ref)"),
+    ("gamma_reversed", "orc_bf16_to_double(gamma[i])", "orc_bf16_to_double(gamma[d - 1 - i])"),
+    ("gamma_dropped", "double y = h / denom * orc_bf16_to_double(gamma[i]);", "double y = h / denom;"),
+    ("bf16_truncates", "double r = rint(a / q) * q;\n    if (r >= 0x1p128)", "double r = floor(a / q) * q;\n    if (r >= 0x1p128)"),
+    ("bf16_ties_away", "double r = rint(a / q) * q;\n    if (r >= 0x1p128)", "double r = round(a / q) * q;\n    if (r >= 0x1p128)"),
+    ("e4m3_wrong_bias", "return (uint8_t)(((ub + 7) << 3) | m);", "return (uint8_t)(((ub + 8) << 3) | m);"),
+    ("e4m3_no_saturation", "    if (r > 448.0)\n        r = 448.0;\n", ""),
+    ("e4m3_ties_away", "qexp = -9; /* subnormal spacing 2^-6 * 2^-3 */\n    double q = ldexp(1.0, qexp);\n    double r = rint(a / q) * q;",
+     "qexp = -9; /* subnormal spacing 2^-6 * 2^-3 */\n    double q = ldexp(1.0, qexp);\n    double r = round(a / q) * q;"),
+    ("e2m1_ties_away", "        r = rint(a / q) * q;\n        if (r > 6.0)", "        r = round(a / q) * q;\n        if (r > 6.0)"),
+    ("e2m1_sign_dropped", "return (uint8_t)(sign | code);", "return (uint8_t)(code);"),
+    ("nibbles_swapped", "(uint8_t)(lo | (hi << 4))", "(uint8_t)(hi | (lo << 4))"),
+    ("gscale_not_448", "g = amax / 2688.0f;", "g = amax / 6.0f;"),
+    ("scale_without_6", "float den6 = 6.0f * g;", "float den6 = g;"),
+    ("block_amax_not_abs", "float a = fabsf(xv[i]);", "float a = xv[i];"),
+]
+
+
+def _build(tmp_path, name, old, new):
+    src = open(SRC).read()
+    assert src.count(old) >= 1, f"mutation anchor for {name} not found"
+    mutated = src.replace(old, new, 1)
+    assert mutated != src
+    c = tmp_path / f"{name}.c"
+    c.write_text(mutated)
+    so = tmp_path / f"lib{name}.so"
+    subprocess.run(["gcc", "-std=c11", "-O2", "-ffp-contract=off", "-fPIC", "-shared", "-o", str(so), str(c), "-lm"],
+                   check=True)
+    return so
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_pins_catch_mutant(tmp_path, name, old, new):
+    so = _build(tmp_path, name, old, new)
+    env = dict(os.environ, ORACLE_LIB=str(so))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-p", "no:cacheprovider",
+                        os.path.join(ROOT, "tests", "test_oracle_pins.py")],
+                       env=env, cwd=ROOT, capture_output=True, text=True, timeout=600)
+    assert r.returncode != 0, f"mutant {name} survived the pins:\n{r.stdout[-2000:]}"

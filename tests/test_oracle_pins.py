@@ -1,0 +1,486 @@
+"""Pins for the CPU oracle: each check ties it to something other than itself.
+
+Kinds of pin used here (no page prints a worked numeric example):
+  * closed forms of RMSNorm (constant rows, +-c rows, a hand-worked d=2 row),
+  * a library routine for the special case it reduces to
+    (torch.nn.functional.rms_norm for N=1 with no residual; torch's float32 ->
+    bf16 and float32 -> float8_e4m3fn conversions),
+  * the number formats' definitions (E4M3 / E2M1 bit fields, value tables),
+  * brute force (nearest representable value by exhaustive search),
+  * invariants (rank order, row independence, scale invariance, RMS of the
+    output, NVFP4 dequantisation error),
+  * a hand-derived NVFP4 example in tests/golden/.
+
+The method: "Deep Dive: AllReduce and AllReduce Fusion in TensorRT-LLM",
+6.3 Inside the Fused Kernel (residual add -> RMSNorm -> quantise) and 6.5
+NVFP4 Quantization Fusion.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def f32_to_bf16_torch(x: np.ndarray) -> np.ndarray:
+    t = torch.from_numpy(np.ascontiguousarray(x, dtype=np.float32)).to(torch.bfloat16)
+    return t.view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_bits_of(values) -> np.ndarray:
+    """bf16 bit patterns of values that are exactly representable in bf16."""
+    v = np.asarray(values, dtype=np.float32)
+    b = f32_to_bf16_torch(v)
+    assert np.array_equal((b.astype(np.uint32) << 16).view(np.float32), v), "not bf16-exact"
+    return b
+
+
+# --------------------------------------------------------------------- bf16
+
+def all_positive_finite_bf16():
+    codes = np.arange(0, 0x7F80, dtype=np.uint16)  # +0 .. largest finite
+    vals = (codes.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return codes, vals
+
+
+def test_bf16_rounding_matches_torch_on_float32(orc):
+    rng = np.random.default_rng(1)
+    x = np.concatenate([
+        rng.standard_normal(20000).astype(np.float32),
+        (rng.standard_normal(20000) * np.exp2(rng.integers(-140, 127, 20000))).astype(np.float32),
+        # exact ties: bf16 value + half an ulp (low 16 bits = 0x8000)
+        ((rng.integers(0, 0x7F00, 5000).astype(np.uint32) << 16) | 0x8000).view(np.float32),
+        np.array([0.0, -0.0, 1.0, -1.0, 3.3895314e38, 1e-45, -1e-45, 1.17549435e-38], np.float32),
+    ])
+    want = f32_to_bf16_torch(x)
+    got = orc.bf16_from_float64(x.astype(np.float64))
+    assert np.array_equal(got, want)
+
+
+def test_bf16_rounding_brute_force_on_float64(orc):
+    codes, vals = all_positive_finite_bf16()
+    rng = np.random.default_rng(2)
+    x = np.abs(rng.standard_normal(4000)) * np.exp2(rng.integers(-130, 120, 4000).astype(np.float64))
+    # exact midpoints between neighbours (ties) in fp64
+    k = rng.integers(1, 0x7F7F, 1000)
+    x = np.concatenate([x, (vals[k] + vals[k + 1]) / 2])
+    got = orc.bf16_from_float64(x)
+    for xi, gi in zip(x, got):
+        j = np.searchsorted(vals, xi)  # vals[j-1] < xi <= vals[j]
+        lo, hi = j - 1, j
+        if vals[hi] == xi:
+            want = codes[hi]
+        else:
+            dlo, dhi = xi - vals[lo], vals[hi] - xi
+            if dlo < dhi:
+                want = codes[lo]
+            elif dhi < dlo:
+                want = codes[hi]
+            else:
+                want = codes[lo] if codes[lo] % 2 == 0 else codes[hi]
+        assert gi == want, (xi, hex(gi), hex(want))
+    # negative values mirror the positive ones
+    assert np.array_equal(orc.bf16_from_float64(-x), got | 0x8000)
+
+
+def test_bf16_overflow_and_specials(orc):
+    big = float(np.float32(3.3895314e38))  # largest finite bf16
+    assert orc.bf16_from_float64(np.array([big]))[0] == 0x7F7F
+    assert orc.bf16_from_float64(np.array([2.0 ** 128]))[0] == 0x7F80
+    assert orc.bf16_from_float64(np.array([-math.inf]))[0] == 0xFF80
+    assert orc.bf16_from_float64(np.array([-0.0]))[0] == 0x8000
+    # halfway between the largest finite and 2^128 rounds to infinity (even)
+    assert orc.bf16_from_float64(np.array([(2 - 2 ** -8) * 2.0 ** 127]))[0] == 0x7F80
+
+
+# --------------------------------------------------------------------- E4M3
+
+def e4m3_definition(c: int) -> float:
+    """OCP FP8 E4M3: bias 7, 3 mantissa bits, subnormals, S.1111.111 = NaN."""
+    s, e, m = c >> 7, (c >> 3) & 15, c & 7
+    if e == 15 and m == 7:
+        return math.nan
+    v = (m / 8) * 2.0 ** -6 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7)
+    return -v if s else v
+
+
+def test_e4m3_decode_all_256_codes(orc):
+    got = orc.e4m3_to_float32(np.arange(256))
+    for c in range(256):
+        want = e4m3_definition(c)
+        if math.isnan(want):
+            assert math.isnan(got[c])
+        else:
+            assert got[c] == want and math.copysign(1, got[c]) == math.copysign(1, want), c
+    assert got[0x7E] == 448.0 and got[0x38] == 1.0 and got[0x08] == 2.0 ** -6
+    assert got[0x01] == 2.0 ** -9 and got[0x20] == 0.125
+
+
+def test_e4m3_round_trip(orc):
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    vals = np.array([e4m3_definition(int(c)) for c in codes], np.float32)
+    assert np.array_equal(orc.e4m3_from_float32(vals), codes)
+
+
+def test_e4m3_matches_torch_float8_in_range(orc):
+    rng = np.random.default_rng(3)
+    pos = np.array(sorted({e4m3_definition(c) for c in range(0, 0x7F)}), np.float64)
+    mids = ((pos[1:] + pos[:-1]) / 2).astype(np.float32)  # every tie, exact in fp32
+    x = np.concatenate([
+        mids, -mids,
+        rng.uniform(0, 463.9, 50000).astype(np.float32),
+        (np.abs(rng.standard_normal(20000)) * np.exp2(rng.integers(-14, 8, 20000))).astype(np.float32),
+    ])
+    x = x[np.abs(x) < 464.0]  # torch gives NaN beyond the top rounding boundary
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(orc.e4m3_from_float32(x), want)
+
+
+def test_e4m3_saturates(orc):
+    x = np.array([448.0, 449.0, 464.0, 480.0, 1e6, np.inf, -500.0, -np.inf], np.float32)
+    assert list(orc.e4m3_from_float32(x)) == [0x7E] * 6 + [0xFE] * 2
+
+
+def test_e4m3_brute_force_nearest(orc):
+    codes = np.arange(0, 0x7F)
+    vals = np.array([e4m3_definition(int(c)) for c in codes])
+    rng = np.random.default_rng(4)
+    x = np.concatenate([rng.uniform(0, 448, 3000), np.exp2(rng.uniform(-12, 8.8, 3000))]).astype(np.float32)
+    got = orc.e4m3_from_float32(x)
+    for xi, gi in zip(x.astype(np.float64), got):
+        if xi >= 448:
+            assert gi == 0x7E
+            continue
+        dist = np.abs(vals - xi)
+        best = np.flatnonzero(dist == dist.min())
+        want = best[0] if len(best) == 1 else [b for b in best if b % 2 == 0][0]
+        assert gi == want, (xi, gi, want)
+
+
+# --------------------------------------------------------------------- E2M1
+
+E2M1_TABLE = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]  # the format's magnitudes, codes 0..7
+
+
+def test_e2m1_decode_table(orc):
+    got = orc.e2m1_to_float32(np.arange(16))
+    assert list(got[:8]) == E2M1_TABLE
+    assert list(got[8:]) == [-v for v in E2M1_TABLE]
+    assert math.copysign(1, got[8]) == -1.0
+
+
+def test_e2m1_round_trip_and_ties(orc):
+    vals = np.array(E2M1_TABLE + [-v for v in E2M1_TABLE[1:]], np.float32)
+    assert list(orc.e2m1_from_float32(vals)) == list(range(8)) + list(range(9, 16))
+    # every midpoint between neighbours goes to the even code
+    ties = {0.25: 0, 0.75: 2, 1.25: 2, 1.75: 4, 2.5: 4, 3.5: 6, 5.0: 6}
+    for x, c in ties.items():
+        assert orc.e2m1_from_float32(np.array([x], np.float32))[0] == c, x
+        assert orc.e2m1_from_float32(np.array([-x], np.float32))[0] == c | 8, -x
+
+
+def test_e2m1_saturation_and_signed_zero(orc):
+    x = np.array([6.0, 6.5, 7.0, 100.0, np.inf, -9.0, -0.0, -0.1, 0.1], np.float32)
+    assert list(orc.e2m1_from_float32(x)) == [7, 7, 7, 7, 7, 15, 8, 8, 0]
+
+
+def test_e2m1_brute_force_nearest(orc):
+    rng = np.random.default_rng(5)
+    x = np.concatenate([np.linspace(0, 8, 4097), rng.uniform(0, 7, 20000)]).astype(np.float32)
+    got = orc.e2m1_from_float32(x)
+    tab = np.array(E2M1_TABLE)
+    for xi, gi in zip(x.astype(np.float64), got):
+        if xi > 6:
+            assert gi == 7
+            continue
+        dist = np.abs(tab - xi)
+        best = np.flatnonzero(dist == dist.min())
+        want = best[0] if len(best) == 1 else [b for b in best if b % 2 == 0][0]
+        assert gi == want, (xi, gi, want)
+
+
+# ------------------------------------------------------- rank sum + RMSNorm
+
+def run(orc, parts, res, gamma, eps):
+    return orc.fused_rmsnorm(parts, res, gamma, eps)
+
+
+@pytest.mark.parametrize("c", [1.0, 0.5, 3.0, -2.0, 0.015625, 96.0])
+@pytest.mark.parametrize("eps", [1e-6, 1e-5, 0.75, 3.0])
+def test_closed_form_constant_row(orc, c, eps):
+    """A constant row c with gamma = 1 normalises to c / sqrt(c^2 + eps)."""
+    d, T = 48, 2
+    eps32 = float(np.float32(eps))
+    half = bf16_bits_of(np.full((T, d), c / 2))
+    zero = bf16_bits_of(np.zeros((T, d)))
+    ones = bf16_bits_of(np.ones(d))
+    want = c / math.sqrt(c * c + eps32)
+    for parts, res in (([half, half], zero), ([zero, zero, zero], bf16_bits_of(np.full((T, d), c)))):
+        out = run(orc, parts, res, ones, eps)
+        assert np.allclose(out["y"], want, rtol=1e-15, atol=0)
+        assert np.all(out["h"] == c)
+
+
+def test_worked_example_d2():
+    """Hand-worked: h = (3, 4), eps = 0: ms = 25/2, y = (3, 4) * sqrt(2)/5 * gamma."""
+    import oracle as orc
+    p0 = bf16_bits_of([[1.0, 1.0]])
+    p1 = bf16_bits_of([[1.0, 2.0]])
+    r = bf16_bits_of([[1.0, 1.0]])
+    gamma = bf16_bits_of([2.0, 0.5])
+    out = orc.fused_rmsnorm([p0, p1], r, gamma, 0.0)
+    assert list(out["h"][0]) == [3.0, 4.0]
+    want = [3 * math.sqrt(2) / 5 * 2.0, 4 * math.sqrt(2) / 5 * 0.5]
+    assert np.allclose(out["y"][0], want, rtol=1e-15, atol=0)
+    assert list(out["out_residual"][0]) == list(bf16_bits_of([3.0, 4.0]))
+
+
+def test_closed_form_pm_c_rows_with_gamma(orc):
+    """h_i = +-c: mean square is c^2, so y_i = gamma_i * h_i / sqrt(c^2 + eps)."""
+    rng = np.random.default_rng(6)
+    T, d, c, eps = 3, 64, 2.0, 0.25
+    signs = rng.choice([-1.0, 1.0], size=(T, d))
+    gam = f32_to_bf16_torch((1 + 0.1 * rng.standard_normal(d)).astype(np.float32))
+    gvals = orc.bf16_to_float64(gam)
+    parts = [bf16_bits_of(signs * c / 2), bf16_bits_of(signs * c / 4), bf16_bits_of(signs * c / 4)]
+    out = orc.fused_rmsnorm(parts, None, gam, eps)
+    want = gvals[None, :] * signs * c / math.sqrt(c * c + eps)
+    assert np.allclose(out["y"], want, rtol=1e-15, atol=0)
+
+
+def test_rank_sum_is_exact_and_uses_every_rank(orc):
+    """P_r = 2^r * k(t, i): the sum over N ranks is (2^N - 1) * k, exactly."""
+    T, d, N = 3, 40, 5
+    t, i = np.meshgrid(np.arange(T), np.arange(d), indexing="ij")
+    k = 1.0 + ((t + i) % 3)
+    parts = [bf16_bits_of(2.0 ** r * k) for r in range(N)]
+    res = bf16_bits_of(-(i % 2) * 1.0)
+    ones = bf16_bits_of(np.ones(d))
+    out = orc.fused_rmsnorm(parts, res, ones, 1e-6)
+    want = (2 ** N - 1) * k - (i % 2)
+    assert np.array_equal(out["h"], want)
+    assert np.array_equal(out["out_residual"], bf16_bits_of(want))
+
+
+def test_rows_are_normalised_along_d(orc):
+    """Row t scaled by 10^t: every row of y has unit RMS when gamma = 1, eps = 0."""
+    rng = np.random.default_rng(7)
+    T, d = 4, 96
+    base = rng.standard_normal((T, d)) * (10.0 ** np.arange(T))[:, None]
+    p = f32_to_bf16_torch(base.astype(np.float32))
+    out = orc.fused_rmsnorm([p], None, bf16_bits_of(np.ones(d)), 0.0)
+    rms = np.sqrt(np.mean(out["y"] ** 2, axis=1))
+    assert np.allclose(rms, 1.0, rtol=1e-13)
+
+
+def test_n1_no_residual_is_textbook_rmsnorm(orc):
+    """N = 1 without residual reduces to torch.nn.functional.rms_norm."""
+    rng = np.random.default_rng(8)
+    T, d, eps = 5, 256, 1e-5
+    x = f32_to_bf16_torch(rng.standard_normal((T, d)).astype(np.float32))
+    g = f32_to_bf16_torch((1 + 0.1 * rng.standard_normal(d)).astype(np.float32))
+    out = orc.fused_rmsnorm([x], None, g, eps)
+    xt = torch.from_numpy(orc.bf16_to_float64(x))
+    gt = torch.from_numpy(orc.bf16_to_float64(g))
+    want = torch.nn.functional.rms_norm(xt, (d,), weight=gt, eps=float(np.float32(eps))).numpy()
+    assert np.allclose(out["y"], want, rtol=1e-12, atol=1e-15)
+
+
+def test_output_rms_invariant(orc):
+    """gamma = 1: RMS(y) = sqrt(ms / (ms + eps)), ms the row's mean square."""
+    rng = np.random.default_rng(9)
+    T, d, eps = 6, 512, 0.05
+    parts = [f32_to_bf16_torch((0.3 * rng.standard_normal((T, d))).astype(np.float32)) for _ in range(4)]
+    res = f32_to_bf16_torch(rng.standard_normal((T, d)).astype(np.float32))
+    out = orc.fused_rmsnorm(parts, res, bf16_bits_of(np.ones(d)), eps)
+    ms = np.mean(out["h"] ** 2, axis=1)
+    rms = np.sqrt(np.mean(out["y"] ** 2, axis=1))
+    assert np.allclose(rms, np.sqrt(ms / (ms + float(np.float32(eps)))), rtol=1e-13)
+
+
+def test_rank_permutation_and_row_independence(orc):
+    rng = np.random.default_rng(10)
+    T, d = 4, 128
+    parts = [f32_to_bf16_torch((0.5 * rng.standard_normal((T, d))).astype(np.float32)) for _ in range(6)]
+    res = f32_to_bf16_torch(rng.standard_normal((T, d)).astype(np.float32))
+    g = f32_to_bf16_torch((1 + 0.1 * rng.standard_normal(d)).astype(np.float32))
+    a = orc.fused_rmsnorm(parts, res, g, 1e-5)
+    b = orc.fused_rmsnorm(parts[::-1], res, g, 1e-5)
+    assert np.array_equal(a["h"], b["h"]) and np.array_equal(a["y"], b["y"])
+    # changing row 2 leaves the other rows bit-identical
+    parts2 = [p.copy() for p in parts]
+    parts2[3][2] = f32_to_bf16_torch(rng.standard_normal(d).astype(np.float32))
+    c = orc.fused_rmsnorm(parts2, res, g, 1e-5)
+    keep = [0, 1, 3]
+    assert np.array_equal(a["y"][keep], c["y"][keep])
+    assert not np.array_equal(a["y"][2], c["y"][2])
+    # permuting rows permutes the outputs
+    perm = [2, 0, 3, 1]
+    e = orc.fused_rmsnorm([p[perm] for p in parts], res[perm], g, 1e-5)
+    assert np.array_equal(e["y"], a["y"][perm])
+
+
+def test_residual_out_ignores_norm_params_and_null_residual_is_zero(orc):
+    rng = np.random.default_rng(11)
+    T, d = 3, 64
+    parts = [f32_to_bf16_torch(rng.standard_normal((T, d)).astype(np.float32)) for _ in range(3)]
+    res = f32_to_bf16_torch(rng.standard_normal((T, d)).astype(np.float32))
+    g1 = bf16_bits_of(np.ones(d))
+    g2 = f32_to_bf16_torch((2 + rng.standard_normal(d)).astype(np.float32))
+    a = orc.fused_rmsnorm(parts, res, g1, 1e-6)
+    b = orc.fused_rmsnorm(parts, res, g2, 0.5)
+    assert np.array_equal(a["out_residual"], b["out_residual"])
+    z = orc.fused_rmsnorm(parts, bf16_bits_of(np.zeros((T, d))), g2, 0.5)
+    n = orc.fused_rmsnorm(parts, None, g2, 0.5)
+    assert np.array_equal(z["out_norm"], n["out_norm"]) and np.array_equal(z["y"], n["y"])
+
+
+def test_scale_invariance_without_eps(orc):
+    """eps = 0: multiplying every input by 2^k leaves y unchanged."""
+    rng = np.random.default_rng(12)
+    T, d = 3, 80
+    raw = [rng.standard_normal((T, d)).astype(np.float32) for _ in range(3)]
+    g = f32_to_bf16_torch((1 + 0.1 * rng.standard_normal(d)).astype(np.float32))
+    a = orc.fused_rmsnorm([f32_to_bf16_torch(x) for x in raw[:2]], f32_to_bf16_torch(raw[2]), g, 0.0)
+    b = orc.fused_rmsnorm([f32_to_bf16_torch(x * 8) for x in raw[:2]], f32_to_bf16_torch(raw[2] * 8), g, 0.0)
+    assert np.array_equal(a["y"], b["y"])
+    assert np.array_equal(b["h"], a["h"] * 8)
+
+
+def test_out_norm_is_rounded_y(orc):
+    rng = np.random.default_rng(13)
+    T, d = 2, 64
+    parts = [f32_to_bf16_torch(rng.standard_normal((T, d)).astype(np.float32)) for _ in range(2)]
+    g = f32_to_bf16_torch((1 + 0.1 * rng.standard_normal(d)).astype(np.float32))
+    out = orc.fused_rmsnorm(parts, None, g, 1e-6)
+    assert np.array_equal(out["out_norm"], orc.bf16_from_float64(out["y"]))
+    assert np.array_equal(out["out_residual"], orc.bf16_from_float64(out["h"]))
+
+
+def test_empty_rows(orc):
+    z = np.zeros((0, 32), np.uint16)
+    out = orc.fused_rmsnorm([z, z], z, bf16_bits_of(np.ones(32)), 1e-6)
+    assert out["out_norm"].shape == (0, 32)
+
+
+# -------------------------------------------------------------------- NVFP4
+
+def load_worked_example():
+    with open(os.path.join(GOLDEN, "nvfp4_worked_example.json")) as f:
+        return json.load(f)
+
+
+def test_nvfp4_hand_worked_example(orc):
+    ex = load_worked_example()
+    x = bf16_bits_of(np.array(ex["x"], np.float64).reshape(1, -1))
+    codes, scales, g = orc.nvfp4_quantize(x, global_scale=ex["global_scale"])
+    assert [int(v) for v in scales[0]] == [int(s, 16) for s in ex["scales_hex"]]
+    assert [int(v) for v in codes[0]] == [int(c, 16) for c in ex["codes_hex"]]
+    assert g == np.float32(ex["global_scale"])
+
+
+def test_nvfp4_zero_tensor(orc):
+    x = np.zeros((3, 64), np.uint16)
+    codes, scales, g = orc.nvfp4_quantize(x)
+    assert g == 0.0 and not codes.any() and not scales.any()
+    # negative zeros keep their sign in the codes
+    codes, scales, g = orc.nvfp4_quantize(np.full((1, 32), 0x8000, np.uint16))
+    assert not scales.any() and np.all(codes == 0x88)
+
+
+def decode_nvfp4(orc, codes, scales, g):
+    T = codes.shape[0]
+    lo = codes & 0xF
+    hi = codes >> 4
+    nib = np.stack([lo, hi], axis=-1).reshape(T, -1)
+    vals = orc.e2m1_to_float32(nib).astype(np.float64)
+    s = orc.e4m3_to_float32(scales).astype(np.float64)
+    return vals * np.repeat(s, 16, axis=1) * float(g)
+
+
+@pytest.mark.parametrize("given", [False, True])
+def test_nvfp4_invariants_random(orc, given):
+    rng = np.random.default_rng(14)
+    T, d = 8, 256
+    x = rng.standard_normal((T, d)) * 1.5
+    x[rng.random((T, d)) < 0.01] *= 50
+    xb = f32_to_bf16_torch(x.astype(np.float32))
+    xv = orc.bf16_to_float64(xb)
+    amax = np.abs(xv).max()
+    g_dyn = np.float32(np.float32(amax) / np.float32(2688.0))
+    codes, scales, g = orc.nvfp4_quantize(xb, global_scale=float(g_dyn) if given else None)
+    assert g == g_dyn
+    assert scales.max() <= 0x7E
+    # the block holding the tensor's amax gets the largest scale, its element code +-6
+    t, i = np.unravel_index(np.argmax(np.abs(xv)), xv.shape)
+    assert scales[t, i // 16] == 0x7E
+    nib = (codes[t, i // 2] >> (4 * (i % 2))) & 7
+    assert nib == 7
+    # every block's own maximum element quantises to magnitude 6 (code 7)
+    xb3 = np.abs(xv).reshape(T, d // 16, 16)
+    arg = xb3.argmax(axis=2)
+    s = orc.e4m3_to_float32(scales)
+    for tt in range(T):
+        for b in range(d // 16):
+            if s[tt, b] >= 2.0 ** -6:  # normal scale
+                j = b * 16 + arg[tt, b]
+                assert (codes[tt, j // 2] >> (4 * (j % 2))) & 7 == 7
+    # dequantisation error: at most half an E2M1 step (step <= 2 at |q| in [4, 6])
+    # plus saturation, times the block's scale
+    xhat = decode_nvfp4(orc, codes, scales, g)
+    den = np.repeat(s.astype(np.float64), 16, axis=1) * float(g)
+    err = np.abs(xhat - xv)
+    q = np.abs(xv) / den
+    half_step = np.where(q < 2, 0.25, np.where(q < 4, 0.5, 1.0))
+    bound = den * (half_step + np.maximum(q - 6, 0)) * (1 + 1e-5) + 1e-30
+    assert np.all(err <= bound)
+    # sign is kept
+    nz = xhat != 0
+    assert np.all(np.sign(xhat[nz]) == np.sign(xv[nz]))
+
+
+def test_nvfp4_given_equals_dynamic_with_same_scale(orc):
+    rng = np.random.default_rng(15)
+    xb = f32_to_bf16_torch(rng.standard_normal((4, 128)).astype(np.float32))
+    c1, s1, g1 = orc.nvfp4_quantize(xb)
+    c2, s2, g2 = orc.nvfp4_quantize(xb, global_scale=float(g1))
+    assert np.array_equal(c1, c2) and np.array_equal(s1, s2) and g1 == g2
+
+
+def test_nvfp4_rows_and_blocks_are_independent_given_g(orc):
+    rng = np.random.default_rng(16)
+    xb = f32_to_bf16_torch(rng.standard_normal((4, 64)).astype(np.float32))
+    c1, s1, _ = orc.nvfp4_quantize(xb, global_scale=0.01)
+    c2, s2, _ = orc.nvfp4_quantize(xb[:, 16:32].copy(), global_scale=0.01)
+    assert np.array_equal(c1[:, 8:16], c2) and np.array_equal(s1[:, 1:2], s2)
+
+
+def test_nvfp4_degenerate_given_scale(orc):
+    xb = f32_to_bf16_torch(np.linspace(-3, 3, 32, dtype=np.float32).reshape(1, 32))
+    for g in (0.0, -1.0, float("inf"), float("nan")):
+        codes, scales, _ = orc.nvfp4_quantize(xb, global_scale=g)
+        assert not scales.any()
+        assert np.all((codes & 0x77) == 0)
+
+
+def test_golden_small_case_regression(orc):
+    """Oracle output for the small N=2, T=4, d=256 case, written by
+    tests/golden/make_golden.py (which calls only the oracle)."""
+    with open(os.path.join(GOLDEN, "small_case_oracle.json")) as f:
+        gold = json.load(f)
+    dec = lambda s: np.frombuffer(bytes.fromhex(s), dtype="<u2").reshape(gold["T"], gold["d"])
+    parts = [dec(p) for p in gold["partials"]]
+    res = dec(gold["residual"])
+    gamma = np.frombuffer(bytes.fromhex(gold["gamma"]), dtype="<u2")
+    out = orc.fused_rmsnorm(parts, res, gamma, gold["eps"])
+    assert out["out_norm"].astype("<u2").tobytes().hex() == gold["out_norm"]
+    assert out["out_residual"].astype("<u2").tobytes().hex() == gold["out_residual"]
+    xb = out["out_norm"]
+    codes, scales, g = orc.nvfp4_quantize(xb)
+    assert codes.tobytes().hex() == gold["nvfp4_codes"]
+    assert scales.tobytes().hex() == gold["nvfp4_scales"]
+    assert float(g) == gold["nvfp4_global_scale"]
