@@ -1,0 +1,202 @@
+/*
+ * tpar.h -- C ABI of the fused tensor-parallel all-reduce epilogue for one
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The operation ("Deep Dive: AllReduce and AllReduce Fusion in TensorRT-LLM",
+ * 2.1.1 AllReduce, 3.1.2 Optimization 2 and 6.3 Inside the Fused Kernel):
+ * for every row t of T tokens and every hidden index i < d,
+ *
+ *   s[t,i]   = P_0[t,i] + P_1[t,i] + ... + P_{N-1}[t,i]   (fp32, fixed rank order)
+ *   h[t,i]   = s[t,i] + R[t,i]                             (residual add)
+ *   out_residual[t,i] = bf16(h[t,i])
+ *   y[t,i]   = h[t,i] / sqrt(mean_i h[t,i]^2 + eps) * gamma[i]   (RMSNorm)
+ *   out_norm[t,i]     = bf16(y[t,i])
+ *
+ * optionally followed by NVFP4 quantisation of bf16(y) (6.5 NVFP4
+ * Quantization Fusion): 16-element blocks along a row, one E4M3 scale byte
+ * per block, E2M1 codes packed two per byte (low nibble = even element), and
+ * an fp32 global scale g. The N "ranks" are N bf16 buffers already resident
+ * in this GPU's memory; the fixed summation order follows the vLLM custom
+ * all-reduce ("Collectives, topology, custom all-reduce").
+ *
+ * Conventions for every entry point:
+ *   - Tensors are row-major and contiguous: [T, d] bf16 (2 bytes per element),
+ *     gamma [d] bf16, codes [T, d/2] bytes, scales [T, d/16] bytes.
+ *   - Pointers to tensors are DEVICE pointers; `partials` itself is a HOST
+ *     array holding n_ranks device pointers. The caller owns every buffer; no
+ *     entry point allocates or frees per call.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
+ *     default stream): no host synchronisation, no memcpy, no allocation.
+ *     They may be captured in a CUDA graph once tpar_init() has run for the
+ *     device.
+ *   - Arguments are checked on the host before anything is launched; a
+ *     rejected call writes nothing. No exception crosses this interface.
+ *   - Kernels launch with programmatic dependent launch (PDL) unless
+ *     TPAR_NO_PDL is given: they wait for the preceding kernel on the stream
+ *     to finish before reading any input.
+ */
+#ifndef TPAR_H
+#define TPAR_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum tpar_status {
+    TPAR_OK = 0,
+    TPAR_ERR_INVALID_ARG = 1,  /* a size, count, NULL or overlap rule broken  */
+    TPAR_ERR_MISALIGNED = 2,   /* a tensor pointer not 16-byte aligned        */
+    TPAR_ERR_UNSUPPORTED = 3,  /* valid but outside what this build handles   */
+    TPAR_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed        */
+    TPAR_ERR_NOT_INITIALIZED = 5 /* needs tpar_init() first (during capture)  */
+} tpar_status;
+
+/* A cudaStream_t, passed as an opaque pointer so this header needs no CUDA
+ * headers. NULL means the legacy default stream. */
+typedef void* tpar_stream_t;
+
+#define TPAR_MAX_RANKS 16
+#define TPAR_MAX_HIDDEN 32768
+
+/* Flags for the _ex / unfused / quantize entry points. */
+#define TPAR_GSCALE_GIVEN 0x1u  /* *global_scale is an INPUT (calibrated g)   */
+#define TPAR_FORCE_ROW 0x2u     /* one CTA per row (bandwidth path)           */
+#define TPAR_FORCE_CLUSTER 0x4u /* rows split over a thread-block cluster     */
+#define TPAR_NO_PDL 0x8u        /* plain stream ordering, no PDL attribute    */
+#define TPAR_DRY_RUN 0x10u      /* check the arguments (and a given plan) on
+                                   the host, launch nothing, touch no GPU     */
+
+/* Launch plan of the fused kernel. kernel: 0 = row kernel, 1 = cluster-split
+ * rows. split: CTAs per row (the cluster size, 1 for the row kernel).
+ * threads: threads per CTA. vec_per_thread: 16-byte vectors of a row each
+ * thread owns (1, 2, 4 or 8). grid_rows: CTAs (clusters) along the rows; each
+ * strides over rows t = blockIdx.y, blockIdx.y + grid_rows, ... */
+typedef struct tpar_plan {
+    int32_t kernel;
+    int32_t split;
+    int32_t threads;
+    int32_t vec_per_thread;
+    int64_t grid_rows;
+} tpar_plan;
+
+/*
+ * tpar_init -- once per device, before any graph capture that uses the
+ * dynamic-scale NVFP4 path. Selects nothing permanently (the caller's current
+ * device is restored), queries the SM count and allocates the device's
+ * 256-byte workspace (the running amax of the dynamic global scale and a
+ * completion counter), zeroed. Idempotent. Returns TPAR_ERR_CUDA if the
+ * device cannot be used.
+ */
+tpar_status tpar_init(int device);
+
+/*
+ * tpar_fused_rmsnorm -- the fused epilogue in one pass over HBM (two kernels
+ * when a dynamic NVFP4 global scale is requested).
+ *
+ *   partials     host array of n_ranks device pointers, each bf16 [T, d]
+ *   n_ranks      1 .. TPAR_MAX_RANKS
+ *   residual     bf16 [T, d], or NULL for no residual (h = s)
+ *   gamma        bf16 [d]
+ *   eps          >= 0 and finite; used as this fp32 value
+ *   T            rows (tokens), >= 0; T == 0 is a no-op that writes nothing
+ *   d            hidden size: 8 <= d <= TPAR_MAX_HIDDEN, d % 8 == 0,
+ *                and d % 16 == 0 when NVFP4 output is requested
+ *   out_norm     bf16 [T, d]; may be NULL only for NVFP4 with
+ *                TPAR_GSCALE_GIVEN (via the _ex entry point)
+ *   out_residual bf16 [T, d], or NULL to skip it; may be exactly `residual`
+ *                (updated in place) but must not otherwise overlap an input
+ *   nvfp4_codes, nvfp4_scales, global_scale
+ *                all NULL (no quantisation) or all non-NULL. codes [T, d/2],
+ *                scales [T, d/16] E4M3 bytes, global_scale -> one device fp32.
+ *                Here global_scale is an OUTPUT: g = amax(|out_norm|) / 2688
+ *                over the whole [T, d] tensor, computed on the device.
+ *   stream       cudaStream_t
+ *
+ * The dynamic-scale path uses the device workspace from tpar_init (made on
+ * first use when not capturing): two such calls that run at the same time
+ * on one device (unordered streams) race on it.
+ * Alignment: every tensor pointer 16-byte aligned, global_scale 4-byte.
+ * Overlap: out_norm, out_residual (unless in place), codes and scales must
+ * not overlap any input or each other.
+ */
+tpar_status tpar_fused_rmsnorm(const void* const* partials, int n_ranks, const void* residual,
+                               const void* gamma, float eps, int64_t T, int64_t d, void* out_norm,
+                               void* out_residual, uint8_t* nvfp4_codes, uint8_t* nvfp4_scales,
+                               float* global_scale, tpar_stream_t stream);
+
+/*
+ * tpar_fused_rmsnorm_ex -- as tpar_fused_rmsnorm, plus:
+ *   flags  TPAR_GSCALE_GIVEN: *global_scale is an INPUT (a calibrated g read
+ *          on the device); quantisation happens in the same single pass, and
+ *          out_norm may be NULL. A g that is not positive and finite gives
+ *          all-zero scales and signed-zero codes.
+ *          TPAR_FORCE_ROW / TPAR_FORCE_CLUSTER: pick the kernel; TPAR_NO_PDL.
+ *   plan   NULL for the automatic plan, else a complete plan to launch
+ *          (validated: TPAR_ERR_INVALID_ARG if it does not cover a row).
+ *   workspace  NULL for the device workspace, else a caller-owned device
+ *          buffer of tpar_workspace_bytes() bytes, zeroed once by the caller;
+ *          every call leaves it zeroed again.
+ */
+tpar_status tpar_fused_rmsnorm_ex(const void* const* partials, int n_ranks, const void* residual,
+                                  const void* gamma, float eps, int64_t T, int64_t d,
+                                  void* out_norm, void* out_residual, uint8_t* nvfp4_codes,
+                                  uint8_t* nvfp4_scales, float* global_scale, uint32_t flags,
+                                  const tpar_plan* plan, void* workspace, tpar_stream_t stream);
+
+/*
+ * tpar_unfused_rmsnorm -- the same result from separate kernels through HBM,
+ * the unfused path of "Deep Dive ..." 6.1 (all-reduce -> HBM -> residual add
+ * -> HBM -> RMSNorm, then a separate quantiser): K1 reduced = bf16(sum of
+ * partials); K2 out_residual = bf16(reduced + residual); K3 out_norm =
+ * RMSNorm(out_residual); K4 NVFP4 quantisation when requested. Because the
+ * sum is rounded to bf16 before the residual add and the norm reads the
+ * rounded residual, results differ from the fused path by rounding only.
+ *   reduced      caller scratch, bf16 [T, d], must not overlap anything else
+ *   out_residual required here (the norm reads it back)
+ *   out_norm     required
+ *   flags        TPAR_GSCALE_GIVEN, TPAR_NO_PDL
+ * Other arguments as tpar_fused_rmsnorm.
+ */
+tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const void* residual,
+                                 const void* gamma, float eps, int64_t T, int64_t d,
+                                 void* reduced, void* out_norm, void* out_residual,
+                                 uint8_t* nvfp4_codes, uint8_t* nvfp4_scales, float* global_scale,
+                                 uint32_t flags, tpar_stream_t stream);
+
+/*
+ * tpar_nvfp4_quantize -- NVFP4 quantisation of a bf16 [T, d] tensor x
+ * (d % 16 == 0) ("Deep Dive ..." 6.5), the separate quantiser of the unfused
+ * path. With TPAR_GSCALE_GIVEN, *global_scale is the input g; otherwise g =
+ * amax(|x|) / 2688 is computed on the device (two kernels, using the device
+ * workspace) and written to *global_scale. Per block: s = E4M3(amax_b/(6g)),
+ * inv = min(1/(s g), FLT_MAX) (0 when s is 0), code = E2M1(x * inv); all
+ * binary32, round to nearest even, saturating.
+ */
+tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* codes,
+                                uint8_t* scales, float* global_scale, uint32_t flags,
+                                tpar_stream_t stream);
+
+/*
+ * tpar_plan_launch -- the launch plan the fused entry points would use for
+ * (T, d, n_ranks) on a GPU with sm_count SMs, honouring TPAR_FORCE_ROW /
+ * TPAR_FORCE_CLUSTER. Host-only: touches no GPU.
+ */
+tpar_status tpar_plan_launch(int64_t T, int64_t d, int n_ranks, int sm_count, uint32_t flags,
+                             tpar_plan* out);
+
+/* Bytes of a caller-owned workspace for tpar_fused_rmsnorm_ex. */
+int64_t tpar_workspace_bytes(void);
+
+/* Static message for a status code. */
+const char* tpar_status_string(tpar_status status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+int tpar_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPAR_H */

@@ -1,0 +1,42 @@
+"""Fused tensor-parallel all-reduce epilogue for one GB300 (sm_103a).
+
+The work happens in ``libtpar.so`` (hand-written CUDA, C ABI in
+``include/tpar.h``). This package is a thin ctypes binding: the C entry points
+under the same names (``tpar_fused_rmsnorm`` ...) taking raw integers /
+pointers, plus :func:`fused_rmsnorm`, :func:`unfused_rmsnorm` and
+:func:`nvfp4_quantize`, which marshal PyTorch CUDA tensors (device memory and
+streams only) into those calls. There is no CPU or PyTorch fallback: when the
+library is missing or no GPU is present, calls raise.
+"""
+from __future__ import annotations
+
+from ._abi import (  # noqa: F401
+    TPAR_FORCE_CLUSTER,
+    TPAR_FORCE_ROW,
+    TPAR_GSCALE_GIVEN,
+    TPAR_MAX_HIDDEN,
+    TPAR_MAX_RANKS,
+    TPAR_NO_PDL,
+    TPAR_DRY_RUN,
+    TparError,
+    TparPlan,
+    library,
+    library_path,
+    tpar_fused_rmsnorm,
+    tpar_fused_rmsnorm_ex,
+    tpar_init,
+    tpar_nvfp4_quantize,
+    tpar_plan_launch,
+    tpar_status_string,
+    tpar_unfused_rmsnorm,
+    tpar_version,
+    tpar_workspace_bytes,
+)
+from .ops import fused_rmsnorm, nvfp4_quantize, unfused_rmsnorm  # noqa: F401
+
+__all__ = [
+    "fused_rmsnorm", "unfused_rmsnorm", "nvfp4_quantize", "TparError", "TparPlan",
+    "tpar_init", "tpar_fused_rmsnorm", "tpar_fused_rmsnorm_ex", "tpar_unfused_rmsnorm",
+    "tpar_nvfp4_quantize", "tpar_plan_launch", "tpar_status_string", "tpar_version",
+    "tpar_workspace_bytes", "library", "library_path",
+]

@@ -1,0 +1,174 @@
+"""ctypes declarations of include/tpar.h: argument marshalling only.
+
+The functions named ``tpar_*`` take plain integers for device pointers and
+the stream (``cudaStream_t`` as an int) and return the status code; they
+raise :class:`TparError` on a non-zero status. ``partials`` is a sequence of
+device pointers (ints), copied into a host array for the call.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch  # noqa: F401  -- loads PyTorch's CUDA runtime first, so the
+# library below binds to the same libcudart.so.13 instance.
+
+TPAR_MAX_RANKS = 16
+TPAR_MAX_HIDDEN = 32768
+TPAR_GSCALE_GIVEN = 0x1
+TPAR_FORCE_ROW = 0x2
+TPAR_FORCE_CLUSTER = 0x4
+TPAR_NO_PDL = 0x8
+TPAR_DRY_RUN = 0x10
+
+_STATUS = {
+    0: "TPAR_OK", 1: "TPAR_ERR_INVALID_ARG", 2: "TPAR_ERR_MISALIGNED",
+    3: "TPAR_ERR_UNSUPPORTED", 4: "TPAR_ERR_CUDA", 5: "TPAR_ERR_NOT_INITIALIZED",
+}
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+
+
+def library_path() -> str:
+    return os.path.join(_HERE, "_build", "libtpar.so")
+
+
+class TparError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        msg = _lib_status_string(status)
+        super().__init__(f"{where}: {_STATUS.get(status, status)} ({msg})")
+
+
+class TparPlan(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int32), ("split", ctypes.c_int32), ("threads", ctypes.c_int32),
+                ("vec_per_thread", ctypes.c_int32), ("grid_rows", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library() -> ctypes.CDLL:
+    """Load libtpar.so (built by residual_rmsnorm_gb300.build); raise if absent."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        path = library_path()
+        if not os.path.exists(path):
+            raise ImportError(
+                f"{path} is missing: build the CUDA library first "
+                "(python -c 'import __graft_entry__ as g; g.build()')")
+        lib = ctypes.CDLL(path)
+        P, i32, i64, u32, f32 = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint32,
+                                 ctypes.c_float)
+        lib.tpar_init.argtypes = [i32]
+        lib.tpar_init.restype = i32
+        lib.tpar_fused_rmsnorm.argtypes = [P, i32, P, P, f32, i64, i64, P, P, P, P, P, P]
+        lib.tpar_fused_rmsnorm.restype = i32
+        lib.tpar_fused_rmsnorm_ex.argtypes = [P, i32, P, P, f32, i64, i64, P, P, P, P, P, u32,
+                                              ctypes.POINTER(TparPlan), P, P]
+        lib.tpar_fused_rmsnorm_ex.restype = i32
+        lib.tpar_unfused_rmsnorm.argtypes = [P, i32, P, P, f32, i64, i64, P, P, P, P, P, P, u32, P]
+        lib.tpar_unfused_rmsnorm.restype = i32
+        lib.tpar_nvfp4_quantize.argtypes = [P, i64, i64, P, P, P, u32, P]
+        lib.tpar_nvfp4_quantize.restype = i32
+        lib.tpar_plan_launch.argtypes = [i64, i64, i32, i32, u32, ctypes.POINTER(TparPlan)]
+        lib.tpar_plan_launch.restype = i32
+        lib.tpar_workspace_bytes.argtypes = []
+        lib.tpar_workspace_bytes.restype = i64
+        lib.tpar_status_string.argtypes = [i32]
+        lib.tpar_status_string.restype = ctypes.c_char_p
+        lib.tpar_version.argtypes = []
+        lib.tpar_version.restype = i32
+        _lib = lib
+        return lib
+
+
+def _lib_status_string(status: int) -> str:
+    try:
+        return library().tpar_status_string(status).decode()
+    except Exception:  # pragma: no cover - only when the library is unloadable
+        return "?"
+
+
+def _check(status: int, where: str) -> int:
+    if status != 0:
+        raise TparError(status, where)
+    return status
+
+
+def _ptr_array(ptrs):
+    arr = (ctypes.c_void_p * max(1, len(ptrs)))(*[int(p) if p else None for p in ptrs])
+    return arr
+
+
+def _p(x):
+    return None if not x else ctypes.c_void_p(int(x))
+
+
+def tpar_init(device: int) -> int:
+    return _check(library().tpar_init(device), "tpar_init")
+
+
+def tpar_fused_rmsnorm(partials, n_ranks, residual, gamma, eps, T, d, out_norm, out_residual,
+                       nvfp4_codes, nvfp4_scales, global_scale, stream, check=True) -> int:
+    arr = _ptr_array(partials)
+    st = library().tpar_fused_rmsnorm(ctypes.cast(arr, ctypes.c_void_p), n_ranks, _p(residual),
+                                      _p(gamma), eps, T, d, _p(out_norm), _p(out_residual),
+                                      _p(nvfp4_codes), _p(nvfp4_scales), _p(global_scale),
+                                      _p(stream))
+    return _check(st, "tpar_fused_rmsnorm") if check else st
+
+
+def tpar_fused_rmsnorm_ex(partials, n_ranks, residual, gamma, eps, T, d, out_norm, out_residual,
+                          nvfp4_codes, nvfp4_scales, global_scale, flags, plan, workspace, stream,
+                          check=True) -> int:
+    arr = _ptr_array(partials)
+    plan_p = ctypes.byref(plan) if plan is not None else None
+    st = library().tpar_fused_rmsnorm_ex(ctypes.cast(arr, ctypes.c_void_p), n_ranks, _p(residual),
+                                         _p(gamma), eps, T, d, _p(out_norm), _p(out_residual),
+                                         _p(nvfp4_codes), _p(nvfp4_scales), _p(global_scale),
+                                         flags, plan_p, _p(workspace), _p(stream))
+    return _check(st, "tpar_fused_rmsnorm_ex") if check else st
+
+
+def tpar_unfused_rmsnorm(partials, n_ranks, residual, gamma, eps, T, d, reduced, out_norm,
+                         out_residual, nvfp4_codes, nvfp4_scales, global_scale, flags, stream,
+                         check=True) -> int:
+    arr = _ptr_array(partials)
+    st = library().tpar_unfused_rmsnorm(ctypes.cast(arr, ctypes.c_void_p), n_ranks, _p(residual),
+                                        _p(gamma), eps, T, d, _p(reduced), _p(out_norm),
+                                        _p(out_residual), _p(nvfp4_codes), _p(nvfp4_scales),
+                                        _p(global_scale), flags, _p(stream))
+    return _check(st, "tpar_unfused_rmsnorm") if check else st
+
+
+def tpar_nvfp4_quantize(x, T, d, codes, scales, global_scale, flags, stream, check=True) -> int:
+    st = library().tpar_nvfp4_quantize(_p(x), T, d, _p(codes), _p(scales), _p(global_scale),
+                                       flags, _p(stream))
+    return _check(st, "tpar_nvfp4_quantize") if check else st
+
+
+def tpar_plan_launch(T, d, n_ranks, sm_count, flags=0) -> TparPlan:
+    plan = TparPlan()
+    _check(library().tpar_plan_launch(T, d, n_ranks, sm_count, flags, ctypes.byref(plan)),
+           "tpar_plan_launch")
+    return plan
+
+
+def tpar_workspace_bytes() -> int:
+    return int(library().tpar_workspace_bytes())
+
+
+def tpar_status_string(status: int) -> str:
+    return library().tpar_status_string(status).decode()
+
+
+def tpar_version() -> int:
+    return int(library().tpar_version())

@@ -1,0 +1,83 @@
+"""Build the CUDA library libtpar.so in-tree (residual_rmsnorm_gb300/_build).
+
+Each translation unit is compiled by nvcc for sm_103a only, in parallel, then
+linked into one shared library against the shared CUDA runtime (so a process
+that already loaded PyTorch's libcudart.so.13 keeps a single runtime).
+No fast-math: the NVFP4 scale arithmetic must round exactly as IEEE binary32.
+"""
+from __future__ import annotations
+
+import concurrent.futures as cf
+import os
+import shutil
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(HERE, "csrc")
+BUILD = os.path.join(HERE, "_build")
+LIB = os.path.join(BUILD, "libtpar.so")
+SOURCES = ["api.cu", "kernels_q0.cu", "kernels_q1.cu", "kernels_q2.cu", "unfused.cu"]
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+
+
+def nvcc() -> str:
+    for cand in (os.environ.get("NVCC"), shutil.which("nvcc"), "/usr/local/cuda/bin/nvcc"):
+        if cand and os.path.exists(cand):
+            return cand
+    raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libtpar.so")
+
+
+def cuda_lib_dir() -> str:
+    root = os.path.dirname(os.path.dirname(os.path.realpath(nvcc())))
+    return os.path.join(root, "lib64")
+
+
+def flags() -> list[str]:
+    return ["-std=c++17", "-O3", *ARCH, "-lineinfo", "-Xcompiler", "-fPIC,-O2",
+            "-I", os.path.join(ROOT, "include"), "-I", CSRC, "-Xptxas", "-v"]
+
+
+def _needs_rebuild() -> bool:
+    if not os.path.exists(LIB):
+        return True
+    t = os.path.getmtime(LIB)
+    deps = [os.path.join(CSRC, f) for f in os.listdir(CSRC)] + [os.path.join(ROOT, "include", "tpar.h"), __file__]
+    return any(os.path.getmtime(p) > t for p in deps)
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile and link libtpar.so; returns its path. Raises on failure."""
+    if not force and not _needs_rebuild():
+        return LIB
+    os.makedirs(BUILD, exist_ok=True)
+    cc = nvcc()
+
+    def compile_one(src: str) -> tuple[str, str]:
+        obj = os.path.join(BUILD, src.replace(".cu", ".o"))
+        cmd = [cc, *flags(), "-c", os.path.join(CSRC, src), "-o", obj]
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError(f"nvcc failed on {src}:\n{r.stdout}\n{r.stderr}")
+        return obj, r.stderr
+
+    with cf.ThreadPoolExecutor(max_workers=len(SOURCES)) as ex:
+        results = list(ex.map(compile_one, SOURCES))
+    with open(os.path.join(BUILD, "ptxas.log"), "w") as f:
+        for _, log in results:
+            f.write(log)
+    tmp = LIB + f".tmp{os.getpid()}"
+    link = [cc, "-shared", *ARCH, "-cudart", "shared", "-o", tmp, *[o for o, _ in results],
+            "-Xlinker", f"-rpath,{cuda_lib_dir()}"]
+    r = subprocess.run(link, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, LIB)
+    if verbose:
+        print("built", LIB)
+    return LIB
+
+
+if __name__ == "__main__":
+    build(force="--force" in sys.argv, verbose=True)

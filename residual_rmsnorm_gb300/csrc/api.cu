@@ -1,0 +1,652 @@
+// api.cu -- the C ABI declared in include/tpar.h: argument checks, launch
+// planning and kernel launches. No entry point allocates per call; the only
+// allocation is the 256-byte per-device workspace made by tpar_init.
+#include "tpar.h"
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cuda_runtime.h>
+
+#include "dispatch.h"
+#include "kernels.cuh"
+
+namespace {
+
+using tpar::FusedArgs;
+using tpar::QuantArgs;
+using tpar::ReduceArgs;
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kWorkspaceBytes = 256;
+constexpr int64_t kMaxGridY = 65535;
+
+struct DeviceState {
+    int sm_count = 0;          // 0 until queried
+    uint32_t* ws = nullptr;    // dynamic-scale workspace (tpar_init)
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Byte range [lo, hi) of a buffer; empty when n == 0 or p is null.
+struct Range {
+    uintptr_t lo = 0, hi = 0;
+    Range() = default;
+    Range(const void* p, int64_t n)
+    {
+        if (p && n > 0) {
+            lo = reinterpret_cast<uintptr_t>(p);
+            hi = lo + static_cast<uintptr_t>(n);
+        }
+    }
+    bool empty() const { return hi == lo; }
+    bool overlaps(const Range& o) const { return !empty() && !o.empty() && lo < o.hi && o.lo < hi; }
+};
+
+tpar_status sm_count_of(int dev, int* out)
+{
+    if (dev < 0 || dev >= kMaxDevices)
+        return TPAR_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_dev[dev].sm_count == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            return TPAR_ERR_CUDA;
+        g_dev[dev].sm_count = n;
+    }
+    *out = g_dev[dev].sm_count;
+    return TPAR_OK;
+}
+
+tpar_status init_device(int dev)
+{
+    if (dev < 0 || dev >= kMaxDevices)
+        return TPAR_ERR_UNSUPPORTED;
+    int sm = 0;
+    tpar_status st = sm_count_of(dev, &sm);
+    if (st != TPAR_OK)
+        return st;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (g_dev[dev].ws)
+        return TPAR_OK;
+    int prev = -1;
+    if (cudaGetDevice(&prev) != cudaSuccess)
+        return TPAR_ERR_CUDA;
+    if (cudaSetDevice(dev) != cudaSuccess)
+        return TPAR_ERR_CUDA;
+    void* p = nullptr;
+    cudaError_t e = cudaMalloc(&p, kWorkspaceBytes);
+    if (e == cudaSuccess)
+        e = cudaMemset(p, 0, kWorkspaceBytes);
+    if (e == cudaSuccess)
+        e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) {
+        if (p)
+            cudaFree(p);
+        cudaSetDevice(prev);
+        return TPAR_ERR_CUDA;
+    }
+    g_dev[dev].ws = static_cast<uint32_t*>(p);
+    cudaSetDevice(prev);
+    return TPAR_OK;
+}
+
+// The workspace for a dynamic-scale call on the current device: the
+// caller's, else the device's own (made here unless the stream is capturing).
+tpar_status workspace_for(void* user_ws, cudaStream_t stream, uint32_t** out)
+{
+    if (user_ws) {
+        if (!aligned(user_ws, 16))
+            return TPAR_ERR_MISALIGNED;
+        *out = static_cast<uint32_t*>(user_ws);
+        return TPAR_OK;
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return TPAR_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices)
+        return TPAR_ERR_UNSUPPORTED;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        if (g_dev[dev].ws) {
+            *out = g_dev[dev].ws;
+            return TPAR_OK;
+        }
+    }
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cs) != cudaSuccess)
+        return TPAR_ERR_CUDA;
+    if (cs != cudaStreamCaptureStatusNone)
+        return TPAR_ERR_NOT_INITIALIZED;
+    tpar_status st = init_device(dev);
+    if (st != TPAR_OK)
+        return st;
+    std::lock_guard<std::mutex> lk(g_mu);
+    *out = g_dev[dev].ws;
+    return TPAR_OK;
+}
+
+tpar_status current_sm_count(int* sm)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return TPAR_ERR_CUDA;
+    return sm_count_of(dev, sm);
+}
+
+cudaError_t launch(const void* fn, dim3 grid, dim3 block, void* arg, cudaStream_t stream, int cluster_x,
+                   bool pdl)
+{
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attrs[2];
+    unsigned na = 0;
+    if (cluster_x > 1) {
+        attrs[na].id = cudaLaunchAttributeClusterDimension;
+        attrs[na].val.clusterDim.x = static_cast<unsigned>(cluster_x);
+        attrs[na].val.clusterDim.y = 1;
+        attrs[na].val.clusterDim.z = 1;
+        ++na;
+    }
+    if (pdl) {
+        attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attrs[na].val.programmaticStreamSerializationAllowed = 1;
+        ++na;
+    }
+    cfg.attrs = attrs;
+    cfg.numAttrs = na;
+    void* args[1] = {arg};
+    return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int pow2_at_least(int64_t n)
+{
+    int p = 1;
+    while (p < n)
+        p *= 2;
+    return p;
+}
+
+// Vectors of a row owned by one CTA of a `split`-wide cluster (even, so the
+// two halves of every 16-element NVFP4 block stay in one CTA).
+int slice_for(int nvec, int split)
+{
+    int64_t s = ceil_div(nvec, split);
+    return static_cast<int>(s + (s & 1));
+}
+
+tpar_status check_plan(const tpar_plan& p, int64_t d)
+{
+    const int nvec = static_cast<int>(d / 8);
+    if (p.kernel != 0 && p.kernel != 1)
+        return TPAR_ERR_INVALID_ARG;
+    if (p.kernel == 0 && p.split != 1)
+        return TPAR_ERR_INVALID_ARG;
+    if (p.kernel == 1 && (p.split < 2 || p.split > 16))
+        return TPAR_ERR_INVALID_ARG;
+    if (p.threads < 32 || p.threads > 1024 || p.threads % 32 != 0)
+        return TPAR_ERR_INVALID_ARG;
+    const int v = p.vec_per_thread;
+    if (v != 1 && v != 2 && v != 4 && v != 8)
+        return TPAR_ERR_INVALID_ARG;
+    if (v >= 4 && p.threads > 512)
+        return TPAR_ERR_INVALID_ARG;
+    if (p.kernel == 1 && v > 2)
+        return TPAR_ERR_INVALID_ARG;
+    const int slice = p.kernel == 1 ? slice_for(nvec, p.split) : nvec;
+    if (static_cast<int64_t>(p.threads) * v < slice)
+        return TPAR_ERR_INVALID_ARG;
+    if (p.grid_rows < 1 || p.grid_rows > kMaxGridY)
+        return TPAR_ERR_INVALID_ARG;
+    return TPAR_OK;
+}
+
+struct Call {
+    const void* const* partials;
+    int n_ranks;
+    const void* residual;
+    const void* gamma;
+    float eps;
+    int64_t T, d;
+    void* out_norm;
+    void* out_residual;
+    uint8_t* codes;
+    uint8_t* scales;
+    float* gscale;
+    uint32_t flags;
+    void* reduced;  // unfused only
+};
+
+// Host-side checks shared by the fused and unfused entry points.
+tpar_status validate(const Call& c, bool unfused)
+{
+    if (!c.partials || c.n_ranks < 1 || c.n_ranks > TPAR_MAX_RANKS || !c.gamma)
+        return TPAR_ERR_INVALID_ARG;
+    for (int r = 0; r < c.n_ranks; ++r)
+        if (!c.partials[r])
+            return TPAR_ERR_INVALID_ARG;
+    if (c.T < 0 || c.d < 8 || c.d % 8 != 0)
+        return TPAR_ERR_INVALID_ARG;
+    if (c.d > TPAR_MAX_HIDDEN)
+        return TPAR_ERR_UNSUPPORTED;
+    if (c.T > (INT64_MAX / 4) / c.d)
+        return TPAR_ERR_INVALID_ARG;
+    if (!std::isfinite(c.eps) || c.eps < 0.0f)
+        return TPAR_ERR_INVALID_ARG;
+    const int nq = (c.codes != nullptr) + (c.scales != nullptr) + (c.gscale != nullptr);
+    if (nq != 0 && nq != 3)
+        return TPAR_ERR_INVALID_ARG;
+    const bool nvfp4 = nq == 3;
+    const bool given = (c.flags & TPAR_GSCALE_GIVEN) != 0;
+    if (nvfp4 && c.d % 16 != 0)
+        return TPAR_ERR_INVALID_ARG;
+    if (!nvfp4 && given)
+        return TPAR_ERR_INVALID_ARG;
+    if (!c.out_norm && !(nvfp4 && given && !unfused))
+        return TPAR_ERR_INVALID_ARG;
+    if (unfused && (!c.out_residual || !c.reduced))
+        return TPAR_ERR_INVALID_ARG;
+    if ((c.flags & TPAR_FORCE_ROW) && (c.flags & TPAR_FORCE_CLUSTER))
+        return TPAR_ERR_INVALID_ARG;
+
+    for (int r = 0; r < c.n_ranks; ++r)
+        if (!aligned(c.partials[r], 16))
+            return TPAR_ERR_MISALIGNED;
+    if (!aligned(c.residual, 16) || !aligned(c.gamma, 16) || !aligned(c.out_norm, 16) ||
+        !aligned(c.out_residual, 16) || !aligned(c.codes, 16) || !aligned(c.scales, 16) ||
+        !aligned(c.gscale, 4) || !aligned(c.reduced, 16))
+        return TPAR_ERR_MISALIGNED;
+
+    // Overlap rules: no output may overlap an input or another output, except
+    // that out_residual may be exactly the residual (in place).
+    const int64_t td2 = c.T * c.d * 2;
+    Range ins[TPAR_MAX_RANKS + 3];
+    int ni = 0;
+    for (int r = 0; r < c.n_ranks; ++r)
+        ins[ni++] = Range(c.partials[r], td2);
+    const bool in_place = c.out_residual && c.out_residual == c.residual;
+    if (!in_place)
+        ins[ni++] = Range(c.residual, td2);
+    ins[ni++] = Range(c.gamma, c.d * 2);
+    if (given)
+        ins[ni++] = Range(c.gscale, 4);
+    Range outs[6];
+    int no = 0;
+    outs[no++] = Range(c.out_norm, td2);
+    outs[no++] = Range(c.out_residual, td2);
+    outs[no++] = Range(c.codes, c.T * c.d / 2);
+    outs[no++] = Range(c.scales, c.T * c.d / 16);
+    if (nvfp4 && !given)
+        outs[no++] = Range(c.gscale, 4);
+    outs[no++] = Range(c.reduced, td2);
+    for (int o = 0; o < no; ++o) {
+        for (int i = 0; i < ni; ++i)
+            if (outs[o].overlaps(ins[i]))
+                return TPAR_ERR_INVALID_ARG;
+        for (int p = o + 1; p < no; ++p)
+            if (outs[o].overlaps(outs[p]))
+                return TPAR_ERR_INVALID_ARG;
+    }
+    return TPAR_OK;
+}
+
+tpar_status plan_impl(int64_t T, int64_t d, int n_ranks, int sm_count, uint32_t flags, tpar_plan* out)
+{
+    if (!out || T < 0 || d < 8 || d % 8 != 0 || n_ranks < 1 || n_ranks > TPAR_MAX_RANKS || sm_count < 1)
+        return TPAR_ERR_INVALID_ARG;
+    if (d > TPAR_MAX_HIDDEN)
+        return TPAR_ERR_UNSUPPORTED;
+    if ((flags & TPAR_FORCE_ROW) && (flags & TPAR_FORCE_CLUSTER))
+        return TPAR_ERR_INVALID_ARG;
+    const int nvec = static_cast<int>(d / 8);
+    int split = 1;
+    if (!(flags & TPAR_FORCE_ROW)) {
+        // Latency path: split each row over a cluster while the rows alone
+        // would leave SMs idle and every CTA keeps at least a warp of vectors.
+        while (split < 16 && T * (2 * split) <= sm_count && nvec / (2 * split) >= 32)
+            split *= 2;
+        if ((flags & TPAR_FORCE_CLUSTER) && split == 1) {
+            if (nvec < 4)
+                return TPAR_ERR_UNSUPPORTED;
+            split = 2;
+        }
+    }
+    tpar_plan p;
+    p.grid_rows = T < 1 ? 1 : (T < kMaxGridY ? T : kMaxGridY);
+    if (split > 1) {
+        const int slice = slice_for(nvec, split);
+        p.kernel = 1;
+        p.split = split;
+        p.threads = static_cast<int>(std::min<int64_t>(1024, ceil_div(slice, 32) * 32));
+        p.vec_per_thread = pow2_at_least(ceil_div(slice, p.threads));
+    } else {
+        p.kernel = 0;
+        p.split = 1;
+        if (nvec <= 256) {
+            p.threads = static_cast<int>(ceil_div(nvec, 32) * 32);
+            p.vec_per_thread = 1;
+        } else if (nvec <= 1024) {
+            p.threads = 256;
+            p.vec_per_thread = pow2_at_least(ceil_div(nvec, 256));
+        } else if (nvec <= 2048) {
+            p.threads = 512;
+            p.vec_per_thread = 4;
+        } else {
+            p.threads = 512;
+            p.vec_per_thread = 8;
+        }
+    }
+    *out = p;
+    return check_plan(p, d);
+}
+
+const void* fused_kernel(int qmode, int nr, int vpt, bool cluster)
+{
+    switch (qmode) {
+    case 0: return tpar::fused_kernel_q0(nr, vpt, cluster);
+    case 1: return tpar::fused_kernel_q1(nr, vpt, cluster);
+    case 2: return tpar::fused_kernel_q2(nr, vpt, cluster);
+    default: return nullptr;
+    }
+}
+
+tpar_status launch_fused(const FusedArgs& a, int qmode, const tpar_plan& p, cudaStream_t stream, bool pdl)
+{
+    const int nr = tpar::rank_bound(a.n_ranks);
+    const void* fn = fused_kernel(qmode, nr, p.vec_per_thread, p.kernel == 1);
+    if (!fn)
+        return TPAR_ERR_UNSUPPORTED;
+    if (p.kernel == 1 && p.split > 8) {
+        if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+            return TPAR_ERR_CUDA;
+    }
+    FusedArgs args = a;
+    dim3 grid(static_cast<unsigned>(p.split), static_cast<unsigned>(p.grid_rows), 1);
+    dim3 block(static_cast<unsigned>(p.threads), 1, 1);
+    if (launch(fn, grid, block, &args, stream, p.kernel == 1 ? p.split : 1, pdl) != cudaSuccess)
+        return TPAR_ERR_CUDA;
+    return TPAR_OK;
+}
+
+unsigned flat_grid(int64_t nvec, int sm_count)
+{
+    int64_t blocks = ceil_div(nvec, 256);
+    int64_t cap = static_cast<int64_t>(sm_count) * 8;
+    if (blocks > cap)
+        blocks = cap;
+    return static_cast<unsigned>(blocks < 1 ? 1 : blocks);
+}
+
+tpar_status launch_quantize(const void* x, int64_t T, int64_t d, uint8_t* codes, uint8_t* scales,
+                            float* gscale, uint32_t* ws, bool dynamic, int sm_count, cudaStream_t stream,
+                            bool pdl)
+{
+    QuantArgs q;
+    q.x = static_cast<const uint4*>(x);
+    q.codes = reinterpret_cast<uint32_t*>(codes);
+    q.scales = scales;
+    q.gscale = gscale;
+    q.ws = ws;
+    q.nvec = T * d / 8;
+    const unsigned grid = flat_grid(q.nvec, sm_count);
+    if (launch(tpar::quantize_kernel_for(dynamic), dim3(grid), dim3(256), &q, stream, 1, pdl) != cudaSuccess)
+        return TPAR_ERR_CUDA;
+    return TPAR_OK;
+}
+
+FusedArgs fused_args(const Call& c)
+{
+    FusedArgs a;
+    std::memset(&a, 0, sizeof a);
+    for (int r = 0; r < c.n_ranks; ++r)
+        a.partials[r] = static_cast<const uint4*>(c.partials[r]);
+    a.residual = static_cast<const uint4*>(c.residual);
+    a.gamma = static_cast<const uint4*>(c.gamma);
+    a.out_norm = static_cast<uint4*>(c.out_norm);
+    a.out_residual = static_cast<uint4*>(c.out_residual);
+    a.codes = reinterpret_cast<uint32_t*>(c.codes);
+    a.scales = c.scales;
+    a.gscale = c.gscale;
+    a.amax_bits = nullptr;
+    a.T = c.T;
+    a.n_ranks = c.n_ranks;
+    a.nvec = static_cast<int>(c.d / 8);
+    a.slice = a.nvec;
+    a.eps = c.eps;
+    a.inv_d = 1.0f / static_cast<float>(c.d);
+    return a;
+}
+
+tpar_status fused_impl(const Call& c, const tpar_plan* user_plan, void* user_ws, cudaStream_t stream)
+{
+    tpar_status st = validate(c, false);
+    if (st != TPAR_OK)
+        return st;
+    if (c.flags & TPAR_DRY_RUN)
+        return user_plan ? check_plan(*user_plan, c.d) : TPAR_OK;
+    if (c.T == 0)
+        return TPAR_OK;
+    int sm = 0;
+    if ((st = current_sm_count(&sm)) != TPAR_OK)
+        return st;
+    tpar_plan p;
+    if (user_plan) {
+        p = *user_plan;
+        if ((st = check_plan(p, c.d)) != TPAR_OK)
+            return st;
+    } else if ((st = plan_impl(c.T, c.d, c.n_ranks, sm, c.flags, &p)) != TPAR_OK) {
+        return st;
+    }
+    const bool nvfp4 = c.codes != nullptr;
+    const bool given = (c.flags & TPAR_GSCALE_GIVEN) != 0;
+    const bool pdl = (c.flags & TPAR_NO_PDL) == 0;
+    FusedArgs a = fused_args(c);
+    a.slice = p.kernel == 1 ? slice_for(a.nvec, p.split) : a.nvec;
+    if (!nvfp4)
+        return launch_fused(a, tpar::kQuantNone, p, stream, pdl);
+    if (given)
+        return launch_fused(a, tpar::kQuantGiven, p, stream, pdl);
+    // Dynamic global scale: phase A (the fused pass, folding |out_norm| into
+    // the device amax), then phase B (quantise out_norm, publish g, reset).
+    uint32_t* ws = nullptr;
+    if ((st = workspace_for(user_ws, stream, &ws)) != TPAR_OK)
+        return st;
+    a.amax_bits = ws;
+    a.codes = nullptr;
+    a.scales = nullptr;
+    if ((st = launch_fused(a, tpar::kQuantAmax, p, stream, pdl)) != TPAR_OK)
+        return st;
+    st = launch_quantize(c.out_norm, c.T, c.d, c.codes, c.scales, c.gscale, ws, true, sm, stream, pdl);
+    if (st != TPAR_OK)
+        cudaMemsetAsync(ws, 0, 8, stream);  // leave the workspace zeroed
+    return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+tpar_status tpar_init(int device) { return init_device(device); }
+
+tpar_status tpar_fused_rmsnorm(const void* const* partials, int n_ranks, const void* residual,
+                               const void* gamma, float eps, int64_t T, int64_t d, void* out_norm,
+                               void* out_residual, uint8_t* nvfp4_codes, uint8_t* nvfp4_scales,
+                               float* global_scale, tpar_stream_t stream)
+{
+    Call c{partials, n_ranks, residual, gamma, eps, T, d, out_norm, out_residual,
+           nvfp4_codes, nvfp4_scales, global_scale, 0u, nullptr};
+    return fused_impl(c, nullptr, nullptr, static_cast<cudaStream_t>(stream));
+}
+
+tpar_status tpar_fused_rmsnorm_ex(const void* const* partials, int n_ranks, const void* residual,
+                                  const void* gamma, float eps, int64_t T, int64_t d,
+                                  void* out_norm, void* out_residual, uint8_t* nvfp4_codes,
+                                  uint8_t* nvfp4_scales, float* global_scale, uint32_t flags,
+                                  const tpar_plan* plan, void* workspace, tpar_stream_t stream)
+{
+    Call c{partials, n_ranks, residual, gamma, eps, T, d, out_norm, out_residual,
+           nvfp4_codes, nvfp4_scales, global_scale, flags, nullptr};
+    return fused_impl(c, plan, workspace, static_cast<cudaStream_t>(stream));
+}
+
+tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const void* residual,
+                                 const void* gamma, float eps, int64_t T, int64_t d,
+                                 void* reduced, void* out_norm, void* out_residual,
+                                 uint8_t* nvfp4_codes, uint8_t* nvfp4_scales, float* global_scale,
+                                 uint32_t flags, tpar_stream_t stream_)
+{
+    Call c{partials, n_ranks, residual, gamma, eps, T, d, out_norm, out_residual,
+           nvfp4_codes, nvfp4_scales, global_scale, flags & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL), reduced};
+    tpar_status st = validate(c, true);
+    if (st != TPAR_OK || (flags & TPAR_DRY_RUN))
+        return st;
+    if (T == 0)
+        return TPAR_OK;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    int sm = 0;
+    if ((st = current_sm_count(&sm)) != TPAR_OK)
+        return st;
+    const bool pdl = (flags & TPAR_NO_PDL) == 0;
+    const bool nvfp4 = nvfp4_codes != nullptr;
+    const bool given = (flags & TPAR_GSCALE_GIVEN) != 0;
+    const int64_t nvec = T * d / 8;
+    uint32_t* ws = nullptr;
+    if (nvfp4 && !given && (st = workspace_for(nullptr, stream, &ws)) != TPAR_OK)
+        return st;
+
+    // K1: reduced = bf16(sum of partials)
+    ReduceArgs ra;
+    std::memset(&ra, 0, sizeof ra);
+    for (int r = 0; r < n_ranks; ++r)
+        ra.partials[r] = static_cast<const uint4*>(partials[r]);
+    ra.reduced = static_cast<uint4*>(reduced);
+    ra.nvec = nvec;
+    ra.n_ranks = n_ranks;
+    if (launch(tpar::reduce_kernel_for(tpar::rank_bound(n_ranks)), dim3(flat_grid(nvec, sm)), dim3(256), &ra,
+               stream, 1, pdl) != cudaSuccess)
+        return TPAR_ERR_CUDA;
+    // K2: out_residual = bf16(reduced + residual)
+    {
+        const uint4* red = static_cast<const uint4*>(reduced);
+        const uint4* res = static_cast<const uint4*>(residual);
+        uint4* outr = static_cast<uint4*>(out_residual);
+        int64_t n = nvec;
+        void* args[4] = {&red, &res, &outr, &n};
+        cudaLaunchConfig_t cfg;
+        std::memset(&cfg, 0, sizeof cfg);
+        cfg.gridDim = dim3(flat_grid(nvec, sm));
+        cfg.blockDim = dim3(256);
+        cfg.stream = stream;
+        cudaLaunchAttribute at;
+        at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at.val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = &at;
+        cfg.numAttrs = pdl ? 1 : 0;
+        if (cudaLaunchKernelExC(&cfg, tpar::residual_add_kernel_ptr(), args) != cudaSuccess)
+            return TPAR_ERR_CUDA;
+    }
+    // K3: out_norm = RMSNorm(out_residual) (+ amax for a dynamic NVFP4 scale)
+    const void* k3_in[1] = {out_residual};
+    Call k3{k3_in, 1, nullptr, gamma, eps, T, d, out_norm, nullptr, nullptr, nullptr, nullptr,
+            TPAR_FORCE_ROW, nullptr};
+    FusedArgs a = fused_args(k3);
+    a.amax_bits = ws;
+    tpar_plan p;
+    if ((st = plan_impl(T, d, 1, sm, TPAR_FORCE_ROW, &p)) != TPAR_OK)
+        return st;
+    if ((st = launch_fused(a, (nvfp4 && !given) ? tpar::kQuantAmax : tpar::kQuantNone, p, stream, pdl)) !=
+        TPAR_OK)
+        return st;
+    // K4: the separate NVFP4 quantiser
+    if (nvfp4) {
+        st = launch_quantize(out_norm, T, d, nvfp4_codes, nvfp4_scales, global_scale, ws, !given, sm, stream,
+                             pdl);
+        if (st != TPAR_OK && ws)
+            cudaMemsetAsync(ws, 0, 8, stream);
+    }
+    return st;
+}
+
+tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* codes, uint8_t* scales,
+                                float* global_scale, uint32_t flags, tpar_stream_t stream_)
+{
+    if (!x || !codes || !scales || !global_scale || T < 0 || d < 16 || d % 16 != 0)
+        return TPAR_ERR_INVALID_ARG;
+    if (d > TPAR_MAX_HIDDEN)
+        return TPAR_ERR_UNSUPPORTED;
+    if (T > (INT64_MAX / 4) / d)
+        return TPAR_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(scales, 16) || !aligned(global_scale, 4))
+        return TPAR_ERR_MISALIGNED;
+    const bool given = (flags & TPAR_GSCALE_GIVEN) != 0;
+    Range rx(x, T * d * 2), rc(codes, T * d / 2), rs(scales, T * d / 16), rg(global_scale, 4);
+    if (rc.overlaps(rx) || rs.overlaps(rx) || rc.overlaps(rs) || rg.overlaps(rx) || rg.overlaps(rc) ||
+        rg.overlaps(rs))
+        return TPAR_ERR_INVALID_ARG;
+    if (T == 0 || (flags & TPAR_DRY_RUN))
+        return TPAR_OK;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    const bool pdl = (flags & TPAR_NO_PDL) == 0;
+    int sm = 0;
+    tpar_status st = current_sm_count(&sm);
+    if (st != TPAR_OK)
+        return st;
+    uint32_t* ws = nullptr;
+    if (!given) {
+        if ((st = workspace_for(nullptr, stream, &ws)) != TPAR_OK)
+            return st;
+        const uint4* xv = static_cast<const uint4*>(x);
+        int64_t nvec = T * d / 8;
+        void* args[3] = {&xv, &nvec, &ws};
+        cudaLaunchConfig_t cfg;
+        std::memset(&cfg, 0, sizeof cfg);
+        cfg.gridDim = dim3(flat_grid(nvec, sm));
+        cfg.blockDim = dim3(256);
+        cfg.stream = stream;
+        cudaLaunchAttribute at;
+        at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at.val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = &at;
+        cfg.numAttrs = pdl ? 1 : 0;
+        if (cudaLaunchKernelExC(&cfg, tpar::amax_kernel_ptr(), args) != cudaSuccess)
+            return TPAR_ERR_CUDA;
+    }
+    st = launch_quantize(x, T, d, codes, scales, global_scale, ws, !given, sm, stream, pdl);
+    if (st != TPAR_OK && ws)
+        cudaMemsetAsync(ws, 0, 8, stream);
+    return st;
+}
+
+tpar_status tpar_plan_launch(int64_t T, int64_t d, int n_ranks, int sm_count, uint32_t flags, tpar_plan* out)
+{
+    return plan_impl(T, d, n_ranks, sm_count, flags, out);
+}
+
+int64_t tpar_workspace_bytes(void) { return kWorkspaceBytes; }
+
+const char* tpar_status_string(tpar_status s)
+{
+    switch (s) {
+    case TPAR_OK: return "ok";
+    case TPAR_ERR_INVALID_ARG: return "invalid argument (size, count, null pointer or overlap)";
+    case TPAR_ERR_MISALIGNED: return "tensor pointer not 16-byte aligned";
+    case TPAR_ERR_UNSUPPORTED: return "unsupported by this build (e.g. hidden size above the maximum)";
+    case TPAR_ERR_CUDA: return "CUDA runtime error or launch failure";
+    case TPAR_ERR_NOT_INITIALIZED: return "device workspace missing: call tpar_init before stream capture";
+    default: return "unknown status";
+    }
+}
+
+int tpar_version(void) { return 100; }
+
+}  // extern "C"

@@ -1,0 +1,215 @@
+// device.cuh -- small sm_103a device helpers shared by the epilogue kernels:
+// vector memory access with explicit cache qualifiers, bf16 packing, PDL,
+// thread-block-cluster barriers / distributed shared memory, and the
+// hardware E4M3 / E2M1 conversions.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+namespace tpar {
+
+// ---------------------------------------------------------------- memory
+
+// Read-once input (a partial): non-coherent path, no L1 allocation.
+__device__ __forceinline__ uint4 ld_stream(const uint4* p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Input that the same kernel may overwrite in place (the residual):
+// coherent load, no L1 allocation.
+__device__ __forceinline__ uint4 ld_coherent(const uint4* p)
+{
+    uint4 v;
+    asm volatile("ld.global.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+// Input re-read by every row (gamma): non-coherent path, cached in L1.
+__device__ __forceinline__ uint4 ld_reuse(const uint4* p)
+{
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void st_v4(uint4* p, uint4 v)
+{
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                 "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+__device__ __forceinline__ void st_u32(uint32_t* p, uint32_t v)
+{
+    asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void st_u8(uint8_t* p, uint32_t v)
+{
+    asm volatile("st.global.u8 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// ---------------------------------------------------------------- bf16
+
+__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Unpack 8 bf16 (one 16-byte vector) to fp32, element k of the vector -> f[k].
+__device__ __forceinline__ void unpack8(const uint4& v, float f[8])
+{
+    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+__device__ __forceinline__ void add8(const uint4& v, float f[8])
+{
+    f[0] += bf16_lo(v.x); f[1] += bf16_hi(v.x);
+    f[2] += bf16_lo(v.y); f[3] += bf16_hi(v.y);
+    f[4] += bf16_lo(v.z); f[5] += bf16_hi(v.z);
+    f[6] += bf16_lo(v.w); f[7] += bf16_hi(v.w);
+}
+
+// Round 2 floats to bf16 (nearest even); lo lands in the low half.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&b);
+}
+
+__device__ __forceinline__ uint4 pack8(const float f[8])
+{
+    return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                      pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+}
+
+// ---------------------------------------------------------------- reductions
+
+// Butterfly all-reduce over the warp. Every lane ends with the same bits
+// (fp32 addition is commutative, and each level pairs the same two values).
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+
+__device__ __forceinline__ float warp_max(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+// ---------------------------------------------------------------- PDL
+
+// Wait until the preceding grid on the stream has completed and its memory
+// is visible. A no-op when the launch did not use PDL.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next grid on the stream to start launching (its own
+// pdl_wait still waits for this grid to complete).
+__device__ __forceinline__ void pdl_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- clusters
+
+__device__ __forceinline__ uint32_t cluster_ctarank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Full cluster barrier; release/acquire orders shared-memory writes before it
+// with distributed-shared-memory reads after it.
+__device__ __forceinline__ void cluster_sync_all()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
+                 "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Read a float from the same shared-memory variable in CTA `rank` of the
+// cluster.
+__device__ __forceinline__ float ld_dsmem(const float* local, uint32_t rank)
+{
+    uint32_t a = static_cast<uint32_t>(__cvta_generic_to_shared(local));
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(a), "r"(rank));
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(remote) : "memory");
+    return v;
+}
+
+// ---------------------------------------------------------------- NVFP4 formats
+
+// binary32 -> E4M3 byte, round to nearest even, saturating to +-448.
+__device__ __forceinline__ uint32_t e4m3_from_f32(float x)
+{
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(x));
+    return r & 0xFFu;  // the second source lands in the low byte
+}
+
+// E4M3 byte -> binary32 (exact, via f16 which holds every E4M3 value).
+__device__ __forceinline__ float e4m3_to_f32(uint32_t c)
+{
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(static_cast<uint16_t>(c)));
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(h2 & 0xFFFFu)));
+}
+
+// Eight binary32 -> eight E2M1 codes (round to nearest even, saturating to
+// +-6), packed two per byte with element 2k in the low nibble of byte k.
+__device__ __forceinline__ uint32_t e2m1x8_from_f32(const float q[8])
+{
+    uint32_t out;
+    asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+        "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+        "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+        : "=r"(out)
+        : "f"(q[0]), "f"(q[1]), "f"(q[2]), "f"(q[3]), "f"(q[4]), "f"(q[5]), "f"(q[6]), "f"(q[7]));
+    return out;
+}
+
+// The per-block scale of NVFP4 for a given global scale g and block maximum
+// |x|: writes the E4M3 scale byte and returns the element multiplier
+// inv = min(1 / (s * g), FLT_MAX), or 0 when the scale byte is 0 or g is not
+// a positive finite number. Every step is one IEEE binary32 operation,
+// rounded to nearest even, with no fused multiply-add.
+__device__ __forceinline__ float nvfp4_block_scale(float g, float block_amax, uint32_t& sbyte)
+{
+    sbyte = 0;
+    const bool usable = (g > 0.0f) && (g <= 3.402823466e38f);
+    if (!usable)
+        return 0.0f;
+    const float den6 = __fmul_rn(6.0f, g);
+    const float sraw = __fdiv_rn(block_amax, den6);
+    sbyte = e4m3_from_f32(sraw);
+    if (sbyte == 0)
+        return 0.0f;
+    const float den = __fmul_rn(e4m3_to_f32(sbyte), g);
+    return fminf(__fdiv_rn(1.0f, den), 3.402823466e38f);
+}
+
+}  // namespace tpar

@@ -1,0 +1,30 @@
+// dispatch.h -- host-side lookup of kernel instantiations (compiled in
+// kernels_q0.cu, kernels_q1.cu, kernels_q2.cu and unfused.cu).
+#pragma once
+
+#include <cstdint>
+
+namespace tpar {
+
+// Fused kernel for quantisation mode q (0 none, 1 given scale, 2 dynamic
+// amax), rank bound nr (1, 2, 4, 8, 16), vectors per thread vpt (1, 2, 4, 8;
+// the cluster form only 1, 2). Returns null for a combination not built.
+const void* fused_kernel_q0(int nr, int vpt, bool cluster);
+const void* fused_kernel_q1(int nr, int vpt, bool cluster);
+const void* fused_kernel_q2(int nr, int vpt, bool cluster);
+
+const void* reduce_kernel_for(int nr);
+const void* residual_add_kernel_ptr();
+const void* quantize_kernel_for(bool dynamic);
+const void* amax_kernel_ptr();
+
+// Smallest power of two >= n among {1, 2, 4, 8, 16}; 0 if n > 16.
+inline int rank_bound(int n)
+{
+    int b = 1;
+    while (b < n && b < 16)
+        b *= 2;
+    return b >= n ? b : 0;
+}
+
+}  // namespace tpar

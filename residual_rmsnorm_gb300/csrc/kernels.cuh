@@ -1,0 +1,298 @@
+// kernels.cuh -- the epilogue kernels (templates; instantiated in
+// kernels_q*.cu and unfused.cu).
+//
+// Fused kernel ("Deep Dive: AllReduce and AllReduce Fusion in TensorRT-LLM",
+// 3.1.2 Optimization 2 and 6.3 Inside the Fused Kernel): the rank sum is
+// accumulated in fp32 registers straight from 16-byte vector loads, then
+// residual add -> store residual_out -> RMSNorm(gamma) -> store norm_out ->
+// optional NVFP4 (6.5), in that order, without an intermediate trip to HBM.
+//
+// One kernel covers both regimes:
+//   * row kernel (CLUSTER = false): one CTA owns a whole row; the row's sum
+//     of squares is reduced with warp shuffles and one shared-memory step.
+//   * cluster kernel (CLUSTER = true): a row is split across the `split` CTAs
+//     of a thread-block cluster so that a handful of decode tokens still
+//     spreads over ~all SMs; the CTAs exchange their partial sums of squares
+//     through distributed shared memory behind one cluster barrier.
+// Thread k of a CTA owns the 16-byte vectors vbeg + k + j*blockDim.x,
+// j < VPT, of its slice of the row, so every load and store instruction of a
+// warp touches 512 contiguous bytes.
+#pragma once
+
+#include "device.cuh"
+
+namespace tpar {
+
+constexpr int kMaxRanks = 16;
+
+enum QuantMode : int {
+    kQuantNone = 0,     // bf16 outputs only
+    kQuantGiven = 1,    // NVFP4 with a caller-given global scale, same pass
+    kQuantAmax = 2,     // dynamic scale, phase A: fold |bf16(y)| into a device max
+};
+
+struct FusedArgs {
+    const uint4* partials[kMaxRanks];  // bf16 [T, d] each, as 16-byte vectors
+    const uint4* residual;             // bf16 [T, d] or null
+    const uint4* gamma;                // bf16 [d]
+    uint4* out_norm;                   // bf16 [T, d] or null
+    uint4* out_residual;               // bf16 [T, d] or null
+    uint32_t* codes;                   // [T, d/2] bytes = one word per input vector
+    uint8_t* scales;                   // [T, d/16]
+    const float* gscale;               // given g (kQuantGiven)
+    uint32_t* amax_bits;               // running max of |out_norm| bits (kQuantAmax)
+    int64_t T;
+    int n_ranks;
+    int nvec;   // d / 8
+    int slice;  // vectors per CTA along a row (even); nvec for the row kernel
+    float eps;
+    float inv_d;
+};
+
+template <int NR, int VPT, bool CLUSTER, int QMODE>
+__global__ void __launch_bounds__(VPT >= 4 ? 512 : 1024)
+    fused_rmsnorm_kernel(const __grid_constant__ FusedArgs a)
+{
+    // PDL: nothing below may read an input before the previous grid is done.
+    pdl_wait();
+    pdl_launch_dependents();
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int crank = CLUSTER ? static_cast<int>(cluster_ctarank()) : 0;
+    const int split = CLUSTER ? static_cast<int>(gridDim.x) : 1;
+    const int vbeg = crank * a.slice;
+    const int vend = min(vbeg + a.slice, a.nvec);
+
+    __shared__ float warp_ss[2][32];  // per-warp sums of squares, by iteration parity
+    __shared__ float cta_ss[2];       // this CTA's sum of squares, read by its cluster
+
+    float g_given = 0.0f;
+    if constexpr (QMODE == kQuantGiven)
+        g_given = *a.gscale;
+    float amax_local = 0.0f;
+
+    int it = 0;
+    for (int64_t t = blockIdx.y; t < a.T; t += gridDim.y, ++it) {
+        const int64_t rowv = t * static_cast<int64_t>(a.nvec);
+        float h[VPT][8];
+        // gamma is fetched with the partials so its latency is not exposed
+        // after the reduction (wide rows fetch it late to save registers).
+        constexpr bool kEarlyGamma = VPT <= 4;
+        uint4 gv[kEarlyGamma ? VPT : 1];
+        float ss = 0.0f;
+
+        // ---- rank sum (fixed order 0..N-1), residual add, store new residual
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int v = vbeg + tid + j * static_cast<int>(blockDim.x);
+            if (v < vend) {
+                uint4 x[NR];
+#pragma unroll
+                for (int r = 0; r < NR; ++r)
+                    if (r < a.n_ranks)
+                        x[r] = ld_stream(a.partials[r] + rowv + v);
+                uint4 rv = make_uint4(0u, 0u, 0u, 0u);
+                if (a.residual)
+                    rv = ld_coherent(a.residual + rowv + v);
+                if constexpr (kEarlyGamma)
+                    gv[j] = ld_reuse(a.gamma + v);
+                unpack8(x[0], h[j]);
+#pragma unroll
+                for (int r = 1; r < NR; ++r)
+                    if (r < a.n_ranks)
+                        add8(x[r], h[j]);
+                if (a.residual)
+                    add8(rv, h[j]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    ss = fmaf(h[j][e], h[j][e], ss);
+                if (a.out_residual)
+                    st_v4(a.out_residual + rowv + v, pack8(h[j]));
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    h[j][e] = 0.0f;
+            }
+        }
+
+        // ---- row sum of squares: warp -> CTA -> (cluster)
+        const int buf = it & 1;
+        ss = warp_sum(ss);
+        if (lane == 0)
+            warp_ss[buf][warp] = ss;
+        __syncthreads();
+        float tot = warp_sum(lane < nwarps ? warp_ss[buf][lane] : 0.0f);
+        if constexpr (CLUSTER) {
+            if (tid == 0)
+                cta_ss[buf] = tot;
+            cluster_sync_all();
+            tot = warp_sum(lane < split ? ld_dsmem(&cta_ss[buf], static_cast<uint32_t>(lane)) : 0.0f);
+        }
+        const float rinv = rsqrtf(fmaf(tot, a.inv_d, a.eps));
+
+        // ---- normalise, scale by gamma, store; optional NVFP4
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int v = vbeg + tid + j * static_cast<int>(blockDim.x);
+            const bool valid = v < vend;
+            float yq[8];
+            if (valid) {
+                float gm[8];
+                if constexpr (kEarlyGamma)
+                    unpack8(gv[kEarlyGamma ? j : 0], gm);
+                else
+                    unpack8(ld_reuse(a.gamma + v), gm);
+                float y[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    y[e] = h[j][e] * rinv * gm[e];
+                const uint4 yb = pack8(y);
+                if (a.out_norm)
+                    st_v4(a.out_norm + rowv + v, yb);
+                unpack8(yb, yq);  // the emitted bf16 values, as fp32
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    yq[e] = 0.0f;
+            }
+            if constexpr (QMODE == kQuantAmax) {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    amax_local = fmaxf(amax_local, fabsf(yq[e]));
+            }
+            if constexpr (QMODE == kQuantGiven) {
+                // 16-element block = this lane's vector + its neighbour's.
+                float bmax = 0.0f;
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    bmax = fmaxf(bmax, fabsf(yq[e]));
+                bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));
+                if (valid) {
+                    uint32_t sbyte;
+                    const float inv = nvfp4_block_scale(g_given, bmax, sbyte);
+                    float q[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        q[e] = __fmul_rn(yq[e], inv);
+                    st_u32(a.codes + rowv + v, e2m1x8_from_f32(q));
+                    if ((v & 1) == 0)
+                        st_u8(a.scales + (rowv + v) / 2, sbyte);
+                }
+            }
+        }
+    }
+
+    if constexpr (QMODE == kQuantAmax) {
+        const float m = warp_max(amax_local);
+        if (lane == 0 && m > 0.0f)
+            atomicMax(a.amax_bits, __float_as_uint(m));  // |y| >= 0 orders like its bits
+    }
+    if constexpr (CLUSTER) {
+        // No CTA may leave while a peer could still read its shared memory.
+        cluster_sync_all();
+    }
+}
+
+// ---------------------------------------------------------------- NVFP4 quantiser
+
+struct QuantArgs {
+    const uint4* x;      // bf16 [T, d] viewed as n16 = T*d/8 vectors
+    uint32_t* codes;     // one word (8 codes) per vector
+    uint8_t* scales;     // one byte per pair of vectors
+    float* gscale;       // given: input; dynamic: output
+    uint32_t* ws;        // dynamic: ws[0] = amax bits, ws[1] = completion counter
+    int64_t nvec;        // T * d / 8 (even)
+};
+
+// Lane pairs (2k, 2k+1) own one 16-element block per iteration. In dynamic
+// mode g = amax / 2688 is read from the workspace; the last CTA to have read
+// it zeroes the workspace for the next call (no CTA waits on another).
+template <bool DYNAMIC>
+__global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __grid_constant__ QuantArgs a)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+
+    __shared__ float g_sh;
+    if constexpr (DYNAMIC) {
+        if (threadIdx.x == 0) {
+            const uint32_t bits = *reinterpret_cast<volatile uint32_t*>(a.ws);
+            const float g = __fdiv_rn(__uint_as_float(bits), 2688.0f);
+            g_sh = g;
+            if (blockIdx.x == 0)
+                *a.gscale = g;
+            __threadfence();
+            const uint32_t done = atomicAdd(a.ws + 1, 1u);
+            if (done == gridDim.x - 1) {
+                a.ws[0] = 0u;
+                a.ws[1] = 0u;
+            }
+        }
+    } else {
+        if (threadIdx.x == 0)
+            g_sh = *a.gscale;
+    }
+    __syncthreads();
+    const float g = g_sh;
+
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    // nvec is even and stride is a multiple of 32, so lane pairs stay aligned
+    // to block boundaries and a whole warp is either in or out of the loop
+    // together only at the tail -- the shuffle below uses the active mask.
+    for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < a.nvec; v += stride) {
+        float x[8];
+        unpack8(ld_stream(a.x + v), x);
+        float bmax = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            bmax = fmaxf(bmax, fabsf(x[e]));
+        const unsigned mask = __activemask();
+        bmax = fmaxf(bmax, __shfl_xor_sync(mask, bmax, 1));
+        uint32_t sbyte;
+        const float inv = nvfp4_block_scale(g, bmax, sbyte);
+        float q[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            q[e] = __fmul_rn(x[e], inv);
+        st_u32(a.codes + v, e2m1x8_from_f32(q));
+        if ((v & 1) == 0)
+            st_u8(a.scales + v / 2, sbyte);
+    }
+}
+
+// ---------------------------------------------------------------- unfused baseline
+
+struct ReduceArgs {
+    const uint4* partials[kMaxRanks];
+    uint4* reduced;
+    int64_t nvec;  // T * d / 8
+    int n_ranks;
+};
+
+// K1: reduced = bf16(sum of partials), fixed rank order.
+template <int NR>
+__global__ void __launch_bounds__(256) reduce_kernel(const __grid_constant__ ReduceArgs a)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < a.nvec; v += stride) {
+        uint4 x[NR];
+#pragma unroll
+        for (int r = 0; r < NR; ++r)
+            if (r < a.n_ranks)
+                x[r] = ld_stream(a.partials[r] + v);
+        float s[8];
+        unpack8(x[0], s);
+#pragma unroll
+        for (int r = 1; r < NR; ++r)
+            if (r < a.n_ranks)
+                add8(x[r], s);
+        st_v4(a.reduced + v, pack8(s));
+    }
+}
+
+}  // namespace tpar

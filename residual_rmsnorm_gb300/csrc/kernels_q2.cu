@@ -1,0 +1,43 @@
+// kernels_q2.cu -- instantiations of the fused kernel for quantisation
+// mode 2 (0: bf16 outputs only, 1: NVFP4 with a given global scale,
+// 2: dynamic-scale phase A). One translation unit per mode so the build
+// compiles them in parallel.
+#include "dispatch.h"
+#include "kernels.cuh"
+
+namespace tpar {
+
+namespace {
+template <int NR>
+const void* pick(int vpt, bool cluster)
+{
+    if (cluster) {
+        switch (vpt) {
+        case 1: return reinterpret_cast<const void*>(&fused_rmsnorm_kernel<NR, 1, true, 2>);
+        case 2: return reinterpret_cast<const void*>(&fused_rmsnorm_kernel<NR, 2, true, 2>);
+        default: return nullptr;
+        }
+    }
+    switch (vpt) {
+    case 1: return reinterpret_cast<const void*>(&fused_rmsnorm_kernel<NR, 1, false, 2>);
+    case 2: return reinterpret_cast<const void*>(&fused_rmsnorm_kernel<NR, 2, false, 2>);
+    case 4: return reinterpret_cast<const void*>(&fused_rmsnorm_kernel<NR, 4, false, 2>);
+    case 8: return reinterpret_cast<const void*>(&fused_rmsnorm_kernel<NR, 8, false, 2>);
+    default: return nullptr;
+    }
+}
+}  // namespace
+
+const void* fused_kernel_q2(int nr, int vpt, bool cluster)
+{
+    switch (nr) {
+    case 1: return pick<1>(vpt, cluster);
+    case 2: return pick<2>(vpt, cluster);
+    case 4: return pick<4>(vpt, cluster);
+    case 8: return pick<8>(vpt, cluster);
+    case 16: return pick<16>(vpt, cluster);
+    default: return nullptr;
+    }
+}
+
+}  // namespace tpar

@@ -1,0 +1,66 @@
+// unfused.cu -- instantiations of the separate kernels: the unfused
+// baseline's rank reduction and residual add, the NVFP4 quantiser and the
+// amax pass of the standalone quantiser.
+#include "dispatch.h"
+#include "kernels.cuh"
+
+namespace tpar {
+
+// amax of |x| over a bf16 tensor into ws[0] (for the standalone quantiser).
+__global__ void __launch_bounds__(256) amax_kernel(const uint4* x, int64_t nvec, uint32_t* ws)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    float m = 0.0f;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec; v += stride) {
+        float f[8];
+        unpack8(ld_stream(x + v), f);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            m = fmaxf(m, fabsf(f[e]));
+    }
+    m = warp_max(m);
+    if ((threadIdx.x & 31) == 0 && m > 0.0f)
+        atomicMax(ws, __float_as_uint(m));
+}
+
+// K2: out_residual = bf16(reduced + residual) (a copy when residual is null).
+__global__ void __launch_bounds__(256) residual_add_kernel(const uint4* reduced, const uint4* residual,
+                                                           uint4* out_residual, int64_t nvec)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec; v += stride) {
+        float s[8];
+        unpack8(ld_stream(reduced + v), s);
+        if (residual)
+            add8(ld_coherent(residual + v), s);
+        st_v4(out_residual + v, pack8(s));
+    }
+}
+
+const void* reduce_kernel_for(int nr)
+{
+    switch (nr) {
+    case 1: return reinterpret_cast<const void*>(&reduce_kernel<1>);
+    case 2: return reinterpret_cast<const void*>(&reduce_kernel<2>);
+    case 4: return reinterpret_cast<const void*>(&reduce_kernel<4>);
+    case 8: return reinterpret_cast<const void*>(&reduce_kernel<8>);
+    case 16: return reinterpret_cast<const void*>(&reduce_kernel<16>);
+    default: return nullptr;
+    }
+}
+
+const void* residual_add_kernel_ptr() { return reinterpret_cast<const void*>(&residual_add_kernel); }
+
+const void* quantize_kernel_for(bool dynamic)
+{
+    return dynamic ? reinterpret_cast<const void*>(&nvfp4_quantize_kernel<true>)
+                   : reinterpret_cast<const void*>(&nvfp4_quantize_kernel<false>);
+}
+
+const void* amax_kernel_ptr() { return reinterpret_cast<const void*>(&amax_kernel); }
+
+}  // namespace tpar

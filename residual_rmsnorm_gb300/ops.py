@@ -1,0 +1,135 @@
+"""PyTorch-tensor front end of the C ABI (marshalling only).
+
+PyTorch supplies device memory and the current CUDA stream; every step of the
+epilogue runs in libtpar.so. Tensors must be CUDA, contiguous, bf16 (gamma
+too) and 16-byte aligned, as include/tpar.h requires.
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _abi
+
+
+def _check_bf16(name, t, shape=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must live on a CUDA device (no CPU path exists)")
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bf16, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+
+
+def _stream_handle(device, stream):
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def _nvfp4_outputs(T, d, device, global_scale):
+    codes = torch.empty((T, d // 2), dtype=torch.uint8, device=device)
+    scales = torch.empty((T, d // 16), dtype=torch.uint8, device=device)
+    if global_scale is None:
+        g = torch.empty((1,), dtype=torch.float32, device=device)
+        given = False
+    else:
+        g = global_scale
+        if g.dtype != torch.float32 or g.numel() != 1 or g.device.type != "cuda":
+            raise ValueError("global_scale must be a 1-element fp32 CUDA tensor")
+        given = True
+    return codes, scales, g, given
+
+
+def fused_rmsnorm(partials, residual, gamma, eps: float, *, out_norm=None, out_residual=None,
+                  nvfp4: bool = False, global_scale: torch.Tensor | None = None,
+                  emit_norm: bool = True, flags: int = 0, plan: _abi.TparPlan | None = None,
+                  workspace: torch.Tensor | None = None, stream=None):
+    """sum(partials) + residual -> RMSNorm(gamma, eps) [-> NVFP4], one fused pass.
+
+    partials: list of N bf16 [T, d] CUDA tensors; residual: bf16 [T, d] or None;
+    gamma: bf16 [d]. With ``nvfp4=True`` also returns E2M1 codes [T, d/2],
+    E4M3 scales [T, d/16] and the global scale; ``global_scale`` given (a
+    1-element fp32 tensor) selects the calibrated single-pass mode, in which
+    ``emit_norm=False`` skips the bf16 normed output.
+    Returns dict(out_norm, out_residual, codes, scales, global_scale).
+    """
+    partials = list(partials)
+    if not partials:
+        raise ValueError("need at least one partial")
+    T, d = partials[0].shape
+    dev = partials[0].device
+    for i, p in enumerate(partials):
+        _check_bf16(f"partials[{i}]", p, (T, d))
+    if residual is not None:
+        _check_bf16("residual", residual, (T, d))
+    _check_bf16("gamma", gamma, (d,))
+    if out_norm is None and (emit_norm or not nvfp4 or global_scale is None):
+        out_norm = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    if out_norm is not None:
+        _check_bf16("out_norm", out_norm, (T, d))
+    if out_residual is None:
+        out_residual = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    _check_bf16("out_residual", out_residual, (T, d))
+    codes = scales = g = None
+    if nvfp4:
+        codes, scales, g, given = _nvfp4_outputs(T, d, dev, global_scale)
+        if given:
+            flags |= _abi.TPAR_GSCALE_GIVEN
+    with torch.cuda.device(dev):
+        _abi.tpar_fused_rmsnorm_ex(
+            [p.data_ptr() for p in partials], len(partials),
+            residual.data_ptr() if residual is not None else 0, gamma.data_ptr(), float(eps), T, d,
+            out_norm.data_ptr() if out_norm is not None else 0, out_residual.data_ptr(),
+            codes.data_ptr() if nvfp4 else 0, scales.data_ptr() if nvfp4 else 0,
+            g.data_ptr() if nvfp4 else 0, flags, plan,
+            workspace.data_ptr() if workspace is not None else 0, _stream_handle(dev, stream))
+    return {"out_norm": out_norm, "out_residual": out_residual, "codes": codes, "scales": scales,
+            "global_scale": g}
+
+
+def unfused_rmsnorm(partials, residual, gamma, eps: float, *, reduced=None, out_norm=None,
+                    out_residual=None, nvfp4: bool = False, global_scale=None, flags: int = 0,
+                    stream=None):
+    """The same epilogue as separate kernels through HBM (the comparison baseline)."""
+    partials = list(partials)
+    T, d = partials[0].shape
+    dev = partials[0].device
+    for i, p in enumerate(partials):
+        _check_bf16(f"partials[{i}]", p, (T, d))
+    if residual is not None:
+        _check_bf16("residual", residual, (T, d))
+    _check_bf16("gamma", gamma, (d,))
+    reduced = torch.empty((T, d), dtype=torch.bfloat16, device=dev) if reduced is None else reduced
+    out_norm = torch.empty((T, d), dtype=torch.bfloat16, device=dev) if out_norm is None else out_norm
+    out_residual = (torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+                    if out_residual is None else out_residual)
+    codes = scales = g = None
+    if nvfp4:
+        codes, scales, g, given = _nvfp4_outputs(T, d, dev, global_scale)
+        if given:
+            flags |= _abi.TPAR_GSCALE_GIVEN
+    with torch.cuda.device(dev):
+        _abi.tpar_unfused_rmsnorm(
+            [p.data_ptr() for p in partials], len(partials),
+            residual.data_ptr() if residual is not None else 0, gamma.data_ptr(), float(eps), T, d,
+            reduced.data_ptr(), out_norm.data_ptr(), out_residual.data_ptr(),
+            codes.data_ptr() if nvfp4 else 0, scales.data_ptr() if nvfp4 else 0,
+            g.data_ptr() if nvfp4 else 0, flags, _stream_handle(dev, stream))
+    return {"out_norm": out_norm, "out_residual": out_residual, "codes": codes, "scales": scales,
+            "global_scale": g, "reduced": reduced}
+
+
+def nvfp4_quantize(x, global_scale: torch.Tensor | None = None, flags: int = 0, stream=None):
+    """NVFP4 quantisation of a bf16 [T, d] CUDA tensor -> (codes, scales, global_scale)."""
+    _check_bf16("x", x)
+    T, d = x.shape
+    codes, scales, g, given = _nvfp4_outputs(T, d, x.device, global_scale)
+    if given:
+        flags |= _abi.TPAR_GSCALE_GIVEN
+    with torch.cuda.device(x.device):
+        _abi.tpar_nvfp4_quantize(x.data_ptr(), T, d, codes.data_ptr(), scales.data_ptr(),
+                                 g.data_ptr(), flags, _stream_handle(x.device, stream))
+    return codes, scales, g

@@ -17,3 +17,7 @@ def orc():
     import oracle
     oracle.build()
     return oracle
+
+TESTS = os.path.dirname(os.path.abspath(__file__))
+if TESTS not in sys.path:
+    sys.path.insert(0, TESTS)

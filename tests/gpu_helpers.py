@@ -1,0 +1,66 @@
+"""Shared helpers of the GPU parity tests (imported only by tests/)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+# bf16 outputs vs the oracle's unrounded fp64 value, elementwise
+RTOL, ATOL = 1e-2, 1e-3
+
+
+def need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+
+
+def lib():
+    need_gpu()
+    import residual_rmsnorm_gb300 as tp
+    from residual_rmsnorm_gb300 import build
+    build.build()
+    tp.library()
+    tp.tpar_init(torch.cuda.current_device())
+    return tp
+
+
+def assert_close_to_ref(got_bf16: torch.Tensor, ref64: np.ndarray, what: str):
+    got = oracle.bf16_to_float64(synth.bits(got_bf16))
+    assert got.shape == ref64.shape, (got.shape, ref64.shape)
+    err = np.abs(got - ref64)
+    bad = err > RTOL * np.abs(ref64) + ATOL
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance; "
+                             f"first {idx.tolist()}: got {got[bad][:5]}, want {ref64[bad][:5]}")
+
+
+def oracle_rows(inputs, rows, eps, residual=True):
+    """Oracle outputs for the selected rows (rows are independent)."""
+    sel = lambda t: synth.bits(t[rows])
+    parts = [sel(p) for p in inputs["partials"]]
+    res = sel(inputs["residual"]) if residual and inputs.get("residual") is not None else None
+    return oracle.fused_rmsnorm(parts, res, synth.bits(inputs["gamma"]), eps)
+
+
+def to_device(inputs, dev="cuda"):
+    return {"partials": [p.to(dev) for p in inputs["partials"]],
+            "residual": None if inputs["residual"] is None else inputs["residual"].to(dev),
+            "gamma": inputs["gamma"].to(dev)}
+
+
+def assert_nvfp4_bit_exact(out_norm: torch.Tensor, codes, scales, g, given=None, what="nvfp4"):
+    """The oracle quantiser run on the kernel's own bf16 normed tensor."""
+    oc, os_, og = oracle.nvfp4_quantize(synth.bits(out_norm), global_scale=given)
+    gc = codes.cpu().numpy()
+    gs = scales.cpu().numpy()
+    gg = np.float32(g.item()) if isinstance(g, torch.Tensor) else np.float32(g)
+    if not np.array_equal(os_, gs):
+        bad = np.argwhere(os_ != gs)[:5].tolist()
+        raise AssertionError(f"{what}: {int((os_ != gs).sum())} scale bytes differ, first {bad}")
+    if not np.array_equal(oc, gc):
+        bad = np.argwhere(oc != gc)[:5].tolist()
+        raise AssertionError(f"{what}: {int((oc != gc).sum())} code bytes differ, first {bad}: "
+                             f"got {[hex(gc[tuple(b)]) for b in bad]}, want {[hex(oc[tuple(b)]) for b in bad]}")
+    assert og == gg, (what, og, gg)

@@ -1,0 +1,206 @@
+"""Host-side checks of the C ABI: no GPU needed, no kernel launched.
+
+* libtpar.so loads and exports every function include/tpar.h declares;
+* the argument checks reject what the header says they reject (dry runs and
+  invalid calls return before any CUDA call);
+* the launch planner covers every row with a legal plan.
+"""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tpar.h")
+
+
+@pytest.fixture(scope="module")
+def tp():
+    from residual_rmsnorm_gb300 import build
+    build.build()
+    import residual_rmsnorm_gb300 as tp
+    tp.library()
+    return tp
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:[\w\s\*]+?)\b(tpar_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("tpar_init", "tpar_fused_rmsnorm", "tpar_fused_rmsnorm_ex", "tpar_unfused_rmsnorm",
+              "tpar_nvfp4_quantize", "tpar_plan_launch", "tpar_status_string", "tpar_version",
+              "tpar_workspace_bytes"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(tp):
+    lib = ctypes.CDLL(tp.library_path())
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", tp.library_path()], capture_output=True, text=True).stdout
+    exported = set(re.findall(r" T (tpar_\w+)", out))
+    assert set(declared_functions()) <= exported
+    # nothing else of the C ABI leaks out under the tpar_ prefix
+    assert exported <= set(declared_functions())
+
+
+def test_header_compiles_as_c():
+    src = f'#include "{HEADER}"\nint main(void) {{ tpar_plan p; (void)p; return TPAR_OK; }}\n'
+    r = subprocess.run(["gcc", "-std=c99", "-Wall", "-Werror", "-x", "c", "-", "-fsyntax-only"],
+                       input=src, capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+
+
+def test_status_strings_and_version(tp):
+    for s in range(6):
+        assert tp.tpar_status_string(s)
+    assert tp.tpar_version() >= 100
+    assert tp.tpar_workspace_bytes() >= 8
+
+
+# Fake device addresses: never dereferenced (dry runs and rejected calls only).
+BASE = 0x7F0000000000
+MB = 1 << 20
+
+
+def call(tp, *, parts=None, n=None, residual=BASE + 64 * MB, gamma=BASE + 96 * MB, eps=1e-5, T=8,
+         d=4096, out_norm=BASE + 128 * MB, out_residual=BASE + 160 * MB, codes=0, scales=0, g=0,
+         flags=None, plan=None, workspace=0):
+    if parts is None:
+        parts = [BASE + r * 4 * MB for r in range(8)]
+    n = len(parts) if n is None else n
+    fl = tp.TPAR_DRY_RUN if flags is None else flags
+    return tp.tpar_fused_rmsnorm_ex(parts, n, residual, gamma, eps, T, d, out_norm, out_residual,
+                                    codes, scales, g, fl, plan, workspace, 0, check=False)
+
+
+OK, INVALID, MISALIGNED, UNSUPPORTED = 0, 1, 2, 3
+
+
+def test_dry_run_accepts_a_valid_call(tp):
+    assert call(tp) == OK
+    assert call(tp, residual=0) == OK  # no residual
+    assert call(tp, out_residual=0) == OK  # residual output skipped
+    assert call(tp, out_residual=BASE + 64 * MB) == OK  # in place
+    nv = dict(codes=BASE + 200 * MB, scales=BASE + 210 * MB, g=BASE + 220 * MB)
+    assert call(tp, **nv) == OK
+    assert call(tp, out_norm=0, flags=tp.TPAR_DRY_RUN | tp.TPAR_GSCALE_GIVEN, **nv) == OK
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(n=0), INVALID),
+    (dict(parts=[BASE + r * 4 * MB for r in range(17)]), INVALID),
+    (dict(parts=[BASE, 0]), INVALID),
+    (dict(T=-1), INVALID),
+    (dict(d=0), INVALID),
+    (dict(d=12), INVALID),
+    (dict(d=4), INVALID),
+    (dict(d=32768 + 8), UNSUPPORTED),
+    (dict(eps=-1.0), INVALID),
+    (dict(eps=float("inf")), INVALID),
+    (dict(eps=float("nan")), INVALID),
+    (dict(gamma=0), INVALID),
+    (dict(out_norm=0), INVALID),
+    (dict(codes=BASE + 200 * MB), INVALID),  # incomplete NVFP4 triple
+    (dict(codes=BASE + 200 * MB, scales=BASE + 210 * MB), INVALID),
+    (dict(d=4104, codes=BASE + 200 * MB, scales=BASE + 210 * MB, g=BASE + 220 * MB), INVALID),  # d % 16
+    (dict(flags=0x10 | 0x1), INVALID),  # given scale without NVFP4 outputs
+    (dict(flags=0x10 | 0x2 | 0x4), INVALID),  # both kernels forced
+    (dict(parts=[BASE + 8] + [BASE + r * 4 * MB for r in range(1, 8)]), MISALIGNED),
+    (dict(residual=BASE + 64 * MB + 2), MISALIGNED),
+    (dict(gamma=BASE + 96 * MB + 4), MISALIGNED),
+    (dict(out_norm=BASE + 128 * MB + 8), MISALIGNED),
+    (dict(codes=BASE + 200 * MB + 4, scales=BASE + 210 * MB, g=BASE + 220 * MB), MISALIGNED),
+    (dict(codes=BASE + 200 * MB, scales=BASE + 210 * MB, g=BASE + 220 * MB + 2), MISALIGNED),
+    # overlaps
+    (dict(out_norm=BASE + 4 * MB), INVALID),  # out_norm on partial 1
+    (dict(out_norm=BASE + 64 * MB), INVALID),  # out_norm on the residual
+    (dict(out_norm=BASE + 96 * MB - 16), INVALID),  # out_norm running into gamma
+    (dict(out_residual=BASE + 64 * MB + 16), INVALID),  # partial overlap with the residual
+    (dict(out_residual=BASE), INVALID),  # out_residual on partial 0
+    (dict(out_residual=BASE + 128 * MB), INVALID),  # the two outputs coincide
+    (dict(codes=BASE + 128 * MB, scales=BASE + 210 * MB, g=BASE + 220 * MB), INVALID),
+    (dict(codes=BASE + 200 * MB, scales=BASE + 200 * MB + 1024, g=BASE + 220 * MB), INVALID),
+])
+def test_dry_run_rejects(tp, kw, status):
+    assert call(tp, **kw) == status
+
+
+def test_invalid_calls_return_before_touching_cuda(tp):
+    # Without TPAR_DRY_RUN a rejected call must still return its status; no GPU
+    # is needed for that (this also holds on a GPU machine: nothing is launched).
+    assert call(tp, n=0, flags=0) == INVALID
+    assert call(tp, d=12, flags=0) == INVALID
+    assert call(tp, residual=BASE + 64 * MB + 2, flags=0) == MISALIGNED
+    # T == 0 is a valid no-op that needs no device
+    assert call(tp, T=0, flags=0) == OK
+
+
+def test_user_plan_is_checked(tp):
+    P = tp.TparPlan
+    good = P(kernel=0, split=1, threads=256, vec_per_thread=2, grid_rows=8)
+    assert call(tp, plan=good) == OK
+    for bad in (P(0, 2, 256, 2, 8), P(1, 1, 256, 2, 8), P(0, 1, 100, 2, 8), P(0, 1, 256, 3, 8),
+                P(0, 1, 128, 2, 8), P(0, 1, 1024, 4, 8), P(1, 4, 256, 4, 8), P(0, 1, 256, 2, 0),
+                P(1, 32, 32, 1, 8)):
+        assert call(tp, plan=bad) == INVALID, bad.as_dict()
+
+
+def test_unfused_and_quantize_checks(tp):
+    parts = [BASE + r * 4 * MB for r in range(4)]
+    u = lambda **kw: tp.tpar_unfused_rmsnorm(
+        parts, 4, kw.get("res", BASE + 64 * MB), BASE + 96 * MB, 1e-5, 8, 4096,
+        kw.get("reduced", BASE + 300 * MB), kw.get("out_norm", BASE + 128 * MB),
+        kw.get("out_residual", BASE + 160 * MB), 0, 0, 0, tp.TPAR_DRY_RUN, 0, check=False)
+    assert u() == OK
+    assert u(reduced=0) == INVALID
+    assert u(out_residual=0) == INVALID
+    assert u(reduced=BASE + 128 * MB) == INVALID
+    q = lambda x=BASE, T=8, d=4096, c=BASE + 64 * MB, s=BASE + 80 * MB, g=BASE + 90 * MB: \
+        tp.tpar_nvfp4_quantize(x, T, d, c, s, g, tp.TPAR_DRY_RUN, 0, check=False)
+    assert q() == OK
+    assert q(d=4104) == INVALID
+    assert q(c=0) == INVALID
+    assert q(c=BASE + 1024) == INVALID
+    assert q(x=BASE + 8) == MISALIGNED
+
+
+@pytest.mark.parametrize("sm", [152, 148, 132])
+def test_planner_covers_every_row(tp, sm):
+    for d in list(range(8, 1025, 8)) + [2048, 4096, 5120, 7168, 8192, 12288, 16384, 24576, 32768]:
+        nvec = d // 8
+        for T in (1, 2, 3, 4, 8, 16, 32, 64, 76, 77, 152, 4096, 70000):
+            p = tp.tpar_plan_launch(T, d, 8, sm)
+            assert p.threads % 32 == 0 and 32 <= p.threads <= 1024
+            assert p.vec_per_thread in (1, 2, 4, 8)
+            if p.kernel == 1:
+                assert 2 <= p.split <= 16
+                s = -(-nvec // p.split)
+                s += s & 1
+                assert p.threads * p.vec_per_thread >= s
+                assert s >= 32 or p.split == 2
+                assert T * p.split <= sm
+            else:
+                assert p.split == 1 and p.threads * p.vec_per_thread >= nvec
+            assert 1 <= p.grid_rows <= min(T, 65535)
+
+
+def test_planner_choices_for_the_pages_shapes(tp):
+    # decode: rows split over clusters so ~all SMs take part
+    p = tp.tpar_plan_launch(8, 4096, 8, 152)
+    assert (p.kernel, p.split, p.threads, p.vec_per_thread) == (1, 16, 32, 1)
+    p = tp.tpar_plan_launch(1, 8192, 8, 152)
+    assert (p.kernel, p.split) == (1, 16)
+    p = tp.tpar_plan_launch(32, 8192, 8, 152)
+    assert (p.kernel, p.split) == (1, 4)
+    # prefill: one CTA per row
+    p = tp.tpar_plan_launch(4096, 8192, 8, 152)
+    assert (p.kernel, p.split, p.threads, p.vec_per_thread) == (0, 1, 256, 4)
+    assert tp.tpar_plan_launch(8, 4096, 8, 152, tp.TPAR_FORCE_ROW).kernel == 0
+    assert tp.tpar_plan_launch(4096, 4096, 8, 152, tp.TPAR_FORCE_CLUSTER).kernel == 1

@@ -1,0 +1,162 @@
+"""GPU NVFP4 quantiser against the CPU oracle, bit for bit.
+
+The standalone quantiser is fed seeded bf16 tensors straight from the
+generator (no CUDA-path output enters the oracle), including every E2M1 tie,
+E4M3 rounding boundaries, signed zeros, tiny and saturating values and the
+hand-derived example of tests/golden/. The fused single-pass mode (given
+global scale) and the unfused quantiser are checked the same way.
+"""
+import json
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_helpers import assert_close_to_ref, assert_nvfp4_bit_exact, lib, oracle_rows, to_device
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def gpu_quantize(tp, x_bits: np.ndarray, g=None):
+    x = synth.from_bits(x_bits, "cuda")
+    gs = None if g is None else torch.tensor([g], dtype=torch.float32, device="cuda")
+    codes, scales, gout = tp.nvfp4_quantize(x, global_scale=gs)
+    torch.cuda.synchronize()
+    return codes.cpu().numpy(), scales.cpu().numpy(), np.float32(gout.item())
+
+
+def assert_same(tp, x_bits, g=None, what=""):
+    c, s, gg = gpu_quantize(tp, x_bits, g)
+    oc, os_, og = oracle.nvfp4_quantize(x_bits, global_scale=g)
+    assert og == gg, (what, og, gg)
+    assert np.array_equal(os_, s), f"{what}: {int((os_ != s).sum())} scale bytes differ"
+    if not np.array_equal(oc, c):
+        bad = np.argwhere(oc != c)[:8]
+        raise AssertionError(f"{what}: {int((oc != c).sum())} code bytes differ at {bad.tolist()}: "
+                             f"gpu {[hex(c[tuple(b)]) for b in bad]} oracle {[hex(oc[tuple(b)]) for b in bad]}")
+
+
+def test_hand_worked_example():
+    tp = lib()
+    with open(os.path.join(GOLDEN, "nvfp4_worked_example.json")) as f:
+        ex = json.load(f)
+    x = oracle.bf16_from_float64(np.array(ex["x"], np.float64).reshape(1, -1))
+    c, s, _ = gpu_quantize(tp, x, ex["global_scale"])
+    assert [int(v) for v in s[0]] == [int(h, 16) for h in ex["scales_hex"]]
+    assert [int(v) for v in c[0]] == [int(h, 16) for h in ex["codes_hex"]]
+
+
+@pytest.mark.parametrize("dynamic", [True, False])
+@pytest.mark.parametrize("T,d", [(1, 16), (3, 48), (64, 4096), (257, 8192)])
+def test_random_tensors(dynamic, T, d):
+    tp = lib()
+    x = synth.random_bf16((T, d), 1.0, seed=T * 31 + d)
+    xb = synth.bits(x)
+    g = None if dynamic else float(np.float32(0.0371))
+    assert_same(tp, xb, g, f"random T{T} d{d}")
+
+
+def test_every_e2m1_tie_and_e4m3_boundary():
+    """Blocks whose scale is an exact power of two put x * inv exactly on every
+    E2M1 midpoint; a sweep of block maxima walks the E4M3 rounding boundaries
+    and the subnormal scales."""
+    tp = lib()
+    mids = [0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0]
+    rows = []
+    for k in range(-8, 8):
+        blk = [6.0] + mids + [-m for m in mids] + [0.0]
+        rows.append(np.array(blk) * 2.0 ** k)
+    # block maxima sweeping E4M3 scale values (including ties between scales)
+    rng = np.random.default_rng(1)
+    for amax in np.concatenate([np.exp2(np.linspace(-12, 9, 200)), 6.0 * (1 + np.arange(1, 64) / 128)]):
+        blk = rng.uniform(-1, 1, 16) * amax
+        blk[rng.integers(16)] = amax
+        rows.append(blk)
+    blocks = np.array(rows)
+    blocks = np.concatenate([blocks, np.zeros(((-len(blocks)) % 4, 16))])
+    x = oracle.bf16_from_float64(blocks.reshape(-1, 64))
+    assert_same(tp, x, 1.0, "ties, g=1")
+    assert_same(tp, x, 0.125, "ties, g=1/8")
+    assert_same(tp, x, None, "ties, dynamic")
+
+
+def test_signed_zeros_tiny_and_huge():
+    tp = lib()
+    vals = np.array([0.0, -0.0, 1e-30, -1e-30, 3e-39, -3e-39, 1e30, -1e30, 3.3e38, -3.3e38,
+                     1.0, -1.0, 0.5, -6.0, 448.0, -448.0], np.float64)
+    x = oracle.bf16_from_float64(np.tile(vals, (4, 4)))
+    for g in (None, 1.0, 1e-20, 1e20, 3e-39):
+        assert_same(tp, x, g, f"specials g={g}")
+    z = np.zeros((2, 32), np.uint16)
+    z[1] = 0x8000  # negative zeros
+    assert_same(tp, z, None, "zero tensor")
+
+
+def test_degenerate_given_scales():
+    tp = lib()
+    x = synth.bits(synth.random_bf16((4, 64), 1.0, seed=7))
+    for g in (0.0, -1.0, float("inf"), float("nan")):
+        assert_same(tp, x, g, f"given g={g}")
+
+
+@pytest.mark.parametrize("emit_norm", [True, False])
+@pytest.mark.parametrize("T", [1, 8, 333])
+def test_fused_given_scale_single_pass(T, emit_norm):
+    tp = lib()
+    w = synth.NVFP4.with_(T=T, d=4096)
+    inputs = synth.make_inputs(w)
+    dev = to_device(inputs)
+    g = torch.tensor([0.0625], dtype=torch.float32, device="cuda")
+    out = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True,
+                           global_scale=g, emit_norm=emit_norm)
+    torch.cuda.synchronize()
+    ref = oracle_rows(inputs, slice(None), w.eps)
+    assert_close_to_ref(out["out_residual"], ref["h"], "given-scale out_residual")
+    if emit_norm:
+        assert_close_to_ref(out["out_norm"], ref["y"], "given-scale out_norm")
+        norm = out["out_norm"]
+    else:
+        assert out["out_norm"] is None
+        norm = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps)["out_norm"]
+        torch.cuda.synchronize()
+    assert_nvfp4_bit_exact(norm, out["codes"], out["scales"], 0.0625, given=0.0625, what="given")
+
+
+@pytest.mark.parametrize("given", [False, True])
+def test_unfused_nvfp4(given):
+    tp = lib()
+    w = synth.NVFP4.with_(T=40, d=2048)
+    inputs = synth.make_inputs(w)
+    dev = to_device(inputs)
+    g = torch.tensor([0.02], dtype=torch.float32, device="cuda") if given else None
+    out = tp.unfused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True,
+                             global_scale=g)
+    torch.cuda.synchronize()
+    ref = oracle_rows(inputs, slice(None), w.eps)
+    assert_close_to_ref(out["out_residual"], ref["h"], "unfused out_residual")
+    assert_close_to_ref(out["out_norm"], ref["y"], "unfused out_norm")
+    gv = 0.02 if given else out["global_scale"]
+    assert_nvfp4_bit_exact(out["out_norm"], out["codes"], out["scales"], gv,
+                           given=0.02 if given else None, what="unfused")
+
+
+def test_workspace_is_left_zeroed_and_reused():
+    """Back-to-back dynamic calls (device workspace and a caller workspace)
+    each see only their own amax."""
+    tp = lib()
+    ws = torch.zeros(tp.tpar_workspace_bytes() // 4, dtype=torch.int32, device="cuda")
+    for i, scale in enumerate((50.0, 0.5, 3.0)):
+        x = (synth.random_bf16((16, 256), 1.0, seed=i).float() * scale).to(torch.bfloat16)
+        parts = [x, torch.zeros_like(x)]
+        gam = torch.ones(256, dtype=torch.bfloat16, device="cuda")
+        for w_ in (None, ws):
+            out = tp.fused_rmsnorm([p.cuda() for p in parts], None, gam, 1e-6, nvfp4=True, workspace=w_)
+            torch.cuda.synchronize()
+            assert_nvfp4_bit_exact(out["out_norm"], out["codes"], out["scales"], out["global_scale"],
+                                   what=f"call {i}")
+        assert int(ws.abs().sum().item()) == 0

@@ -1,0 +1,175 @@
+"""GPU parity: the CUDA path through the C ABI against the CPU oracle.
+
+bf16 outputs: |gpu - ref| <= 1e-2 |ref| + 1e-3 elementwise, ref = the
+oracle's unrounded fp64 value. NVFP4: codes, scales and global scale
+bit-exact against the oracle quantiser run on the kernel's own bf16 normed
+output. Inputs: the seeded recipe of synth.py at the pages' shapes, plus
+ragged and degenerate cases.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_helpers import (assert_close_to_ref, assert_nvfp4_bit_exact, lib, oracle_rows,
+                         to_device)
+
+pytestmark = pytest.mark.gpu
+
+
+def run_full(tp, w, inputs=None, residual=True, **kw):
+    inputs = inputs or synth.make_inputs(w)
+    if not residual:
+        inputs = dict(inputs, residual=None)
+    dev = to_device(inputs)
+    out = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, **kw)
+    torch.cuda.synchronize()
+    ref = oracle_rows(inputs, slice(None), w.eps, residual=residual)
+    return inputs, out, ref
+
+
+def check(out, ref, name):
+    assert_close_to_ref(out["out_residual"], ref["h"], f"{name} out_residual")
+    if out["out_norm"] is not None:
+        assert_close_to_ref(out["out_norm"], ref["y"], f"{name} out_norm")
+
+
+def test_small_case():
+    tp = lib()
+    w = synth.SMALL
+    _, out, ref = run_full(tp, w)
+    check(out, ref, w.name)
+
+
+def test_decode_8b_shape():
+    tp = lib()
+    w = synth.DECODE_8B
+    _, out, ref = run_full(tp, w)
+    check(out, ref, w.name)
+
+
+@pytest.mark.parametrize("n", synth.DECODE_70B_NS)
+@pytest.mark.parametrize("T", synth.DECODE_70B_TS)
+def test_decode_70b_sweep(n, T):
+    tp = lib()
+    w = synth.DECODE_70B.with_(n_ranks=n, T=T)
+    _, out, ref = run_full(tp, w)
+    check(out, ref, w.name)
+
+
+def test_prefill_full_size_sampled_rows():
+    """N=8, [4096, 8192] in the launch configuration the benchmark uses;
+    the oracle checks 48 rows (first, last, seeded random)."""
+    tp = lib()
+    w = synth.PREFILL
+    inputs = synth.make_inputs(w, device="cuda")
+    out = tp.fused_rmsnorm(inputs["partials"], inputs["residual"], inputs["gamma"], w.eps)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(0)
+    rows = np.unique(np.concatenate([[0, 1, w.T - 1], rng.choice(w.T, 45, replace=False)]))
+    ref = oracle_rows(inputs, rows, w.eps)
+    assert_close_to_ref(out["out_residual"][rows], ref["h"], "prefill out_residual")
+    assert_close_to_ref(out["out_norm"][rows], ref["y"], "prefill out_norm")
+
+
+@pytest.mark.parametrize("T", synth.NVFP4_TS)
+def test_nvfp4_sweep(T):
+    """N=4, d=8192, 1% x50 outliers, dynamic global scale, T = 1 .. 16384."""
+    tp = lib()
+    w = synth.NVFP4.with_(T=T)
+    inputs = synth.make_inputs(w, device="cuda")
+    out = tp.fused_rmsnorm(inputs["partials"], inputs["residual"], inputs["gamma"], w.eps, nvfp4=True)
+    torch.cuda.synchronize()
+    rows = np.arange(T) if T <= 64 else np.unique(
+        np.concatenate([[0, T - 1], np.random.default_rng(T).choice(T, 30, replace=False)]))
+    ref = oracle_rows(inputs, rows, w.eps)
+    assert_close_to_ref(out["out_residual"][rows], ref["h"], f"T={T} out_residual")
+    assert_close_to_ref(out["out_norm"][rows], ref["y"], f"T={T} out_norm")
+    assert_nvfp4_bit_exact(out["out_norm"], out["codes"], out["scales"], out["global_scale"],
+                           what=f"T={T}")
+    amax = out["out_norm"].float().abs().max().item()
+    assert out["global_scale"].item() == np.float32(np.float32(amax) / np.float32(2688.0))
+
+
+@pytest.mark.parametrize("n", [1, 2, 3, 5, 8, 16])
+@pytest.mark.parametrize("T,d", [(1, 8), (3, 16), (3, 24), (4, 256), (5, 8200), (2, 32768), (3, 2056)])
+def test_ragged_shapes(n, T, d):
+    tp = lib()
+    w = synth.Workload(f"ragged N{n} T{T} d{d}", n, T, d, 1e-5, 0.5, seed=n * 1000 + T * 7 + d)
+    _, out, ref = run_full(tp, w)
+    check(out, ref, w.name)
+
+
+@pytest.mark.parametrize("flags", ["row", "cluster"])
+@pytest.mark.parametrize("T,d", [(1, 256), (8, 4096), (32, 8192), (100, 1024), (7, 8200)])
+def test_both_kernels(flags, T, d):
+    tp = lib()
+    f = tp.TPAR_FORCE_ROW if flags == "row" else tp.TPAR_FORCE_CLUSTER
+    w = synth.Workload("paths", 8, T, d, 1e-5, 0.5, seed=T + d)
+    _, out, ref = run_full(tp, w, flags=f)
+    check(out, ref, f"{flags} T{T} d{d}")
+
+
+@pytest.mark.parametrize("plan", [
+    dict(kernel=0, split=1, threads=1024, vec_per_thread=1, grid_rows=3),
+    dict(kernel=0, split=1, threads=512, vec_per_thread=2, grid_rows=5),
+    dict(kernel=0, split=1, threads=256, vec_per_thread=4, grid_rows=64),
+    dict(kernel=0, split=1, threads=128, vec_per_thread=8, grid_rows=2),
+    dict(kernel=1, split=2, threads=512, vec_per_thread=1, grid_rows=7),
+    dict(kernel=1, split=4, threads=128, vec_per_thread=2, grid_rows=64),
+    dict(kernel=1, split=8, threads=128, vec_per_thread=1, grid_rows=1),
+    dict(kernel=1, split=16, threads=64, vec_per_thread=1, grid_rows=33),
+])
+def test_explicit_plans_with_row_striding(plan):
+    """Every legal plan, including grids smaller than T (rows strided)."""
+    tp = lib()
+    w = synth.Workload("plans", 4, 67, 8192, 1e-5, 0.5, seed=5)
+    _, out, ref = run_full(tp, w, plan=tp.TparPlan(**plan))
+    check(out, ref, str(plan))
+
+
+def test_no_residual_and_in_place_and_skipped_residual_output():
+    tp = lib()
+    w = synth.Workload("no residual", 3, 5, 1024, 1e-6, 1.0, seed=9)
+    _, out, ref = run_full(tp, w, residual=False)
+    check(out, ref, "no residual")
+    # in place: out_residual is the residual buffer
+    inputs = synth.make_inputs(w)
+    dev = to_device(inputs)
+    res = dev["residual"].clone()
+    out = tp.fused_rmsnorm(dev["partials"], res, dev["gamma"], w.eps, out_residual=res)
+    torch.cuda.synchronize()
+    ref = oracle_rows(inputs, slice(None), w.eps)
+    assert_close_to_ref(res, ref["h"], "in-place residual")
+    assert_close_to_ref(out["out_norm"], ref["y"], "in-place out_norm")
+
+
+def test_empty_batch_is_a_noop():
+    tp = lib()
+    z = [torch.empty((0, 256), dtype=torch.bfloat16, device="cuda") for _ in range(2)]
+    g = torch.ones(256, dtype=torch.bfloat16, device="cuda")
+    out = tp.fused_rmsnorm(z, z[0], g, 1e-6, nvfp4=True)
+    assert out["out_norm"].shape == (0, 256) and out["codes"].shape == (0, 128)
+
+
+def test_degenerate_rows():
+    """Zero rows (h = 0 -> y = 0), a constant row (closed form), huge and tiny
+    magnitudes."""
+    tp = lib()
+    T, d = 4, 512
+    z = torch.zeros((T, d), dtype=torch.float32)
+    p0 = z.clone()
+    p0[1] = 3.0            # constant row: y = 3 / sqrt(9 + eps) * gamma
+    p0[2] = 1.0e15         # large: the fp32 sum of squares (~5e32) stays finite
+    p0[3, ::2] = 1e-20     # tiny: squares are fp32 subnormals
+    parts = [p0.to(torch.bfloat16), z.to(torch.bfloat16)]
+    g = synth.random_bf16((d,), 0.1, seed=3).float().add(1.0).to(torch.bfloat16)
+    inputs = {"partials": parts, "residual": None, "gamma": g}
+    dev = to_device(inputs)
+    out = tp.fused_rmsnorm(dev["partials"], None, dev["gamma"], 1e-6)
+    torch.cuda.synchronize()
+    ref = oracle.fused_rmsnorm([synth.bits(p) for p in parts], None, synth.bits(g), 1e-6)
+    assert_close_to_ref(out["out_residual"], ref["h"], "degenerate h")
+    assert_close_to_ref(out["out_norm"], ref["y"], "degenerate y")
+    assert torch.all(out["out_norm"][0] == 0)

@@ -1,0 +1,169 @@
+"""GPU self-consistency: determinism, CUDA-graph replay, guard bands, rank
+order, fused vs unfused, and the two kernels against each other."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from gpu_helpers import ATOL, RTOL, assert_close_to_ref, lib, oracle_rows, to_device
+
+pytestmark = pytest.mark.gpu
+
+
+def same_bits(a: torch.Tensor, b: torch.Tensor) -> bool:
+    return torch.equal(a.view(torch.int16) if a.dtype == torch.bfloat16 else a,
+                       b.view(torch.int16) if b.dtype == torch.bfloat16 else b)
+
+
+@pytest.mark.parametrize("w", [synth.DECODE_8B, synth.DECODE_70B.with_(T=32),
+                               synth.PREFILL.with_(T=300), synth.NVFP4.with_(T=64)])
+def test_bitwise_deterministic(w):
+    tp = lib()
+    dev = to_device(synth.make_inputs(w))
+    a = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=w.nvfp4)
+    b = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=w.nvfp4)
+    torch.cuda.synchronize()
+    for k in ("out_norm", "out_residual", "codes", "scales", "global_scale"):
+        if a[k] is not None:
+            assert same_bits(a[k], b[k]), k
+
+
+def test_graph_replay_matches_eager():
+    """1000 back-to-back calls captured in one CUDA graph (the decode bench
+    shape) give exactly the eager result."""
+    tp = lib()
+    w = synth.DECODE_8B
+    dev = to_device(synth.make_inputs(w))
+    eager = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps)
+    out_n = torch.empty_like(eager["out_norm"])
+    out_r = torch.empty_like(eager["out_residual"])
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, out_norm=out_n,
+                         out_residual=out_r)  # warm-up outside the capture
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(1000):
+                tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps,
+                                 out_norm=out_n, out_residual=out_r)
+    out_n.zero_()
+    out_r.zero_()
+    g.replay()
+    torch.cuda.synchronize()
+    assert same_bits(out_n, eager["out_norm"]) and same_bits(out_r, eager["out_residual"])
+
+
+def test_graph_capture_of_dynamic_nvfp4():
+    tp = lib()
+    w = synth.NVFP4.with_(T=8, d=4096)
+    dev = to_device(synth.make_inputs(w))
+    eager = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True)
+    outs = {k: torch.empty_like(v) for k, v in eager.items() if v is not None}
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+
+    def call():
+        from residual_rmsnorm_gb300 import _abi
+        _abi.tpar_fused_rmsnorm(
+            [p.data_ptr() for p in dev["partials"]], w.n_ranks, dev["residual"].data_ptr(),
+            dev["gamma"].data_ptr(), w.eps, w.T, w.d, outs["out_norm"].data_ptr(),
+            outs["out_residual"].data_ptr(), outs["codes"].data_ptr(), outs["scales"].data_ptr(),
+            outs["global_scale"].data_ptr(), torch.cuda.current_stream().cuda_stream)
+
+    with torch.cuda.stream(s):
+        call()
+        with torch.cuda.graph(g, stream=s):
+            for _ in range(3):
+                call()
+    for v in outs.values():
+        v.zero_()
+    g.replay()
+    g.replay()
+    torch.cuda.synchronize()
+    for k, v in outs.items():
+        assert same_bits(v, eager[k]), k
+
+
+def test_guard_bands_untouched():
+    """Outputs sit inside sentinel-filled pads; no kernel writes outside."""
+    tp = lib()
+    pad = 4096
+    for w in (synth.DECODE_8B, synth.NVFP4.with_(T=37, d=1024), synth.SMALL.with_(T=3, d=24)):
+        dev = to_device(synth.make_inputs(w))
+        T, d = w.T, w.d
+
+        def padded(n, dtype):
+            buf = torch.full((n + 2 * pad,), 0x5A, dtype=torch.uint8, device="cuda")
+            return buf, buf[pad:pad + n * torch.empty((), dtype=dtype).element_size()].view(dtype)
+
+        bn, on = padded(T * d, torch.bfloat16)
+        br, orr = padded(T * d, torch.bfloat16)
+        nv = w.d % 16 == 0
+        out = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps,
+                               out_norm=on.view(T, d), out_residual=orr.view(T, d), nvfp4=nv)
+        torch.cuda.synchronize()
+        for b in (bn, br):
+            assert torch.all(b[:pad] == 0x5A) and torch.all(b[-pad:] == 0x5A)
+        ref = oracle_rows(synth.make_inputs(w), slice(None), w.eps)
+        assert_close_to_ref(out["out_norm"], ref["y"], "padded out_norm")
+
+
+def test_rank_permutation_within_tolerance():
+    tp = lib()
+    w = synth.DECODE_70B.with_(T=16)
+    inputs = synth.make_inputs(w)
+    dev = to_device(inputs)
+    a = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps)
+    b = tp.fused_rmsnorm(dev["partials"][::-1], dev["residual"], dev["gamma"], w.eps)
+    torch.cuda.synchronize()
+    ref = oracle_rows(inputs, slice(None), w.eps)
+    assert_close_to_ref(b["out_norm"], ref["y"], "permuted ranks")
+    diff = (a["out_norm"].float() - b["out_norm"].float()).abs()
+    assert torch.all(diff <= RTOL * a["out_norm"].float().abs() + ATOL)
+
+
+@pytest.mark.parametrize("w", [synth.DECODE_8B, synth.PREFILL.with_(T=257), synth.SMALL])
+def test_fused_matches_unfused_and_oracle(w):
+    tp = lib()
+    inputs = synth.make_inputs(w)
+    dev = to_device(inputs)
+    f = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps)
+    u = tp.unfused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps)
+    torch.cuda.synchronize()
+    ref = oracle_rows(inputs, slice(None), w.eps)
+    assert_close_to_ref(u["out_residual"], ref["h"], "unfused out_residual")
+    assert_close_to_ref(u["out_norm"], ref["y"], "unfused out_norm")
+    assert_close_to_ref(f["out_norm"], ref["y"], "fused out_norm")
+    # the unfused K1 output is the bf16-rounded rank sum
+    s = sum(p.double() for p in dev["partials"])
+    assert torch.allclose(u["reduced"].double(), s, rtol=2 ** -8, atol=1e-30)
+
+
+def test_row_and_cluster_kernels_agree():
+    tp = lib()
+    w = synth.DECODE_70B.with_(T=8)
+    dev = to_device(synth.make_inputs(w))
+    a = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, flags=tp.TPAR_FORCE_ROW)
+    b = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, flags=tp.TPAR_FORCE_CLUSTER)
+    torch.cuda.synchronize()
+    assert same_bits(a["out_residual"], b["out_residual"])  # no reduction involved
+    diff = (a["out_norm"].float() - b["out_norm"].float()).abs()
+    assert torch.all(diff <= RTOL * a["out_norm"].float().abs() + ATOL)
+
+
+def test_no_pdl_flag_gives_same_result():
+    tp = lib()
+    w = synth.DECODE_8B
+    dev = to_device(synth.make_inputs(w))
+    a = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps)
+    b = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, flags=tp.TPAR_NO_PDL)
+    torch.cuda.synchronize()
+    assert same_bits(a["out_norm"], b["out_norm"])
+
+
+def test_init_is_idempotent():
+    tp = lib()
+    tp.tpar_init(torch.cuda.current_device())
+    tp.tpar_init(torch.cuda.current_device())
