@@ -101,6 +101,8 @@ tpar_status tpar_init(int device);
  *   gamma        bf16 [d]
  *   eps          >= 0 and finite; used as this fp32 value
  *   T            rows (tokens), >= 0; T == 0 is a no-op that writes nothing
+ *                (then only n_ranks, d, eps and flags are checked, and the
+ *                tensor pointers may be NULL)
  *   d            hidden size: 8 <= d <= TPAR_MAX_HIDDEN, d % 8 == 0,
  *                and d % 16 == 0 when NVFP4 output is requested
  *   out_norm     bf16 [T, d]; may be NULL only for NVFP4 with

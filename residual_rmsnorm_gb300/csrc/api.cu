@@ -230,11 +230,8 @@ struct Call {
 // Host-side checks shared by the fused and unfused entry points.
 tpar_status validate(const Call& c, bool unfused)
 {
-    if (!c.partials || c.n_ranks < 1 || c.n_ranks > TPAR_MAX_RANKS || !c.gamma)
+    if (!c.partials || c.n_ranks < 1 || c.n_ranks > TPAR_MAX_RANKS)
         return TPAR_ERR_INVALID_ARG;
-    for (int r = 0; r < c.n_ranks; ++r)
-        if (!c.partials[r])
-            return TPAR_ERR_INVALID_ARG;
     if (c.T < 0 || c.d < 8 || c.d % 8 != 0)
         return TPAR_ERR_INVALID_ARG;
     if (c.d > TPAR_MAX_HIDDEN)
@@ -243,6 +240,16 @@ tpar_status validate(const Call& c, bool unfused)
         return TPAR_ERR_INVALID_ARG;
     if (!std::isfinite(c.eps) || c.eps < 0.0f)
         return TPAR_ERR_INVALID_ARG;
+    if ((c.flags & TPAR_FORCE_ROW) && (c.flags & TPAR_FORCE_CLUSTER))
+        return TPAR_ERR_INVALID_ARG;
+    // An empty batch is a no-op: its tensors may be NULL (empty allocations).
+    if (c.T == 0)
+        return TPAR_OK;
+    if (!c.gamma)
+        return TPAR_ERR_INVALID_ARG;
+    for (int r = 0; r < c.n_ranks; ++r)
+        if (!c.partials[r])
+            return TPAR_ERR_INVALID_ARG;
     const int nq = (c.codes != nullptr) + (c.scales != nullptr) + (c.gscale != nullptr);
     if (nq != 0 && nq != 3)
         return TPAR_ERR_INVALID_ARG;
@@ -255,8 +262,6 @@ tpar_status validate(const Call& c, bool unfused)
     if (!c.out_norm && !(nvfp4 && given && !unfused))
         return TPAR_ERR_INVALID_ARG;
     if (unfused && (!c.out_residual || !c.reduced))
-        return TPAR_ERR_INVALID_ARG;
-    if ((c.flags & TPAR_FORCE_ROW) && (c.flags & TPAR_FORCE_CLUSTER))
         return TPAR_ERR_INVALID_ARG;
 
     for (int r = 0; r < c.n_ranks; ++r)
@@ -580,11 +585,15 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
 tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* codes, uint8_t* scales,
                                 float* global_scale, uint32_t flags, tpar_stream_t stream_)
 {
-    if (!x || !codes || !scales || !global_scale || T < 0 || d < 16 || d % 16 != 0)
+    if (T < 0 || d < 16 || d % 16 != 0)
         return TPAR_ERR_INVALID_ARG;
     if (d > TPAR_MAX_HIDDEN)
         return TPAR_ERR_UNSUPPORTED;
     if (T > (INT64_MAX / 4) / d)
+        return TPAR_ERR_INVALID_ARG;
+    if (T == 0)
+        return TPAR_OK;  // empty batch: a no-op, tensors may be NULL
+    if (!x || !codes || !scales || !global_scale)
         return TPAR_ERR_INVALID_ARG;
     if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(scales, 16) || !aligned(global_scale, 4))
         return TPAR_ERR_MISALIGNED;

@@ -25,11 +25,14 @@ def lib():
     return tp
 
 
-def assert_close_to_ref(got_bf16: torch.Tensor, ref64: np.ndarray, what: str):
+def assert_close_to_ref(got_bf16: torch.Tensor, ref64: np.ndarray, what: str, extra=None):
     got = oracle.bf16_to_float64(synth.bits(got_bf16))
     assert got.shape == ref64.shape, (got.shape, ref64.shape)
     err = np.abs(got - ref64)
-    bad = err > RTOL * np.abs(ref64) + ATOL
+    bound = RTOL * np.abs(ref64) + ATOL
+    if extra is not None:
+        bound = bound + extra
+    bad = err > bound
     if bad.any():
         idx = np.argwhere(bad)[:5]
         raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance; "
@@ -64,3 +67,18 @@ def assert_nvfp4_bit_exact(out_norm: torch.Tensor, codes, scales, g, given=None,
         raise AssertionError(f"{what}: {int((oc != gc).sum())} code bytes differ, first {bad}: "
                              f"got {[hex(gc[tuple(b)]) for b in bad]}, want {[hex(oc[tuple(b)]) for b in bad]}")
     assert og == gg, (what, og, gg)
+
+
+# The unfused path rounds the rank sum s to bf16 before adding the residual
+# (the all-reduce result is a bf16 tensor in HBM). That one extra rounding
+# moves h by at most half a bf16 ulp of s, <= 2^-8 |s|, which near
+# cancellation (|h| << |s|) exceeds the fused tolerance. The derived extra
+# bound per element: 2^-8 * sum_r |P_r| for h, and the same times
+# |gamma| / sqrt(ms + eps) for y.
+def unfused_extra_tolerance(inputs, ref, eps):
+    s_abs = sum(np.abs(oracle.bf16_to_float64(synth.bits(p))) for p in inputs["partials"])
+    eh = 2.0 ** -8 * s_abs
+    gam = np.abs(oracle.bf16_to_float64(synth.bits(inputs["gamma"])))
+    ms = np.mean(ref["h"] ** 2, axis=1, keepdims=True)
+    ey = eh * gam[None, :] / np.sqrt(ms + float(np.float32(eps))) * 1.01
+    return eh, ey

@@ -138,8 +138,10 @@ def test_invalid_calls_return_before_touching_cuda(tp):
     assert call(tp, n=0, flags=0) == INVALID
     assert call(tp, d=12, flags=0) == INVALID
     assert call(tp, residual=BASE + 64 * MB + 2, flags=0) == MISALIGNED
-    # T == 0 is a valid no-op that needs no device
+    # T == 0 is a valid no-op that needs no device; empty tensors may be NULL
     assert call(tp, T=0, flags=0) == OK
+    assert call(tp, T=0, flags=0, parts=[0] * 8, residual=0, gamma=0, out_norm=0, out_residual=0) == OK
+    assert call(tp, T=0, flags=0, d=12) == INVALID
 
 
 def test_user_plan_is_checked(tp):

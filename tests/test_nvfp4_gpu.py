@@ -15,7 +15,8 @@ import torch
 
 import oracle
 import synth
-from gpu_helpers import assert_close_to_ref, assert_nvfp4_bit_exact, lib, oracle_rows, to_device
+from gpu_helpers import (assert_close_to_ref, assert_nvfp4_bit_exact, lib, oracle_rows, to_device,
+                         unfused_extra_tolerance)
 
 pytestmark = pytest.mark.gpu
 
@@ -33,7 +34,7 @@ def gpu_quantize(tp, x_bits: np.ndarray, g=None):
 def assert_same(tp, x_bits, g=None, what=""):
     c, s, gg = gpu_quantize(tp, x_bits, g)
     oc, os_, og = oracle.nvfp4_quantize(x_bits, global_scale=g)
-    assert og == gg, (what, og, gg)
+    assert og == gg or (np.isnan(og) and np.isnan(gg)), (what, og, gg)
     assert np.array_equal(os_, s), f"{what}: {int((os_ != s).sum())} scale bytes differ"
     if not np.array_equal(oc, c):
         bad = np.argwhere(oc != c)[:8]
@@ -138,8 +139,9 @@ def test_unfused_nvfp4(given):
                              global_scale=g)
     torch.cuda.synchronize()
     ref = oracle_rows(inputs, slice(None), w.eps)
-    assert_close_to_ref(out["out_residual"], ref["h"], "unfused out_residual")
-    assert_close_to_ref(out["out_norm"], ref["y"], "unfused out_norm")
+    eh, ey = unfused_extra_tolerance(inputs, ref, w.eps)
+    assert_close_to_ref(out["out_residual"], ref["h"], "unfused out_residual", extra=eh)
+    assert_close_to_ref(out["out_norm"], ref["y"], "unfused out_norm", extra=ey)
     gv = 0.02 if given else out["global_scale"]
     assert_nvfp4_bit_exact(out["out_norm"], out["codes"], out["scales"], gv,
                            given=0.02 if given else None, what="unfused")
