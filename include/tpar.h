@@ -50,7 +50,8 @@ typedef enum tpar_status {
     TPAR_ERR_MISALIGNED = 2,   /* a tensor pointer not 16-byte aligned        */
     TPAR_ERR_UNSUPPORTED = 3,  /* valid but outside what this build handles   */
     TPAR_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed        */
-    TPAR_ERR_NOT_INITIALIZED = 5 /* needs tpar_init() first (during capture)  */
+    TPAR_ERR_NOT_INITIALIZED = 5, /* needs tpar_init() first (during capture) */
+    TPAR_ERR_SCRATCH_TOO_SMALL = 6 /* T*d above TPAR_NOALLOC_MAX_ELEMENTS     */
 } tpar_status;
 
 /* A cudaStream_t, passed as an opaque pointer so this header needs no CUDA
@@ -190,6 +191,42 @@ tpar_status tpar_plan_launch(int64_t T, int64_t d, int n_ranks, int sm_count, ui
 
 /* Bytes of a caller-owned workspace for tpar_fused_rmsnorm_ex. */
 int64_t tpar_workspace_bytes(void);
+
+/*
+ * tpar_unfused_rmsnorm_noalloc -- tpar_unfused_rmsnorm for callers that
+ * cannot allocate device memory. (The pages have no counterpart: this is a
+ * deployment variant of the unfused baseline.) Such callers include code that
+ * runs while a framework owns the device allocator (a caching pool or an
+ * arena that must see every allocation), plugins and hooks that must not
+ * allocate by contract, code that may first run inside a CUDA-graph capture
+ * (where cudaMalloc is not allowed) and latency-critical paths that cannot
+ * afford an allocation's implicit synchronisation. They cannot provide the
+ * `reduced` scratch tensor nor call tpar_init.
+ *
+ * Here the bf16 `reduced` tensor and the dynamic-scale accumulator live in
+ * one static device array inside the library, of fixed size: 256 bytes plus
+ * 2 * TPAR_NOALLOC_MAX_ELEMENTS bytes (16 MiB + 256 B). Every GPU that loads
+ * the library holds that array until the process exits. The entry point
+ * calls no cudaMalloc, cudaFree or allocating routine.
+ *
+ * Arguments, results and rounding are those of tpar_unfused_rmsnorm without
+ * `reduced`. T * d above TPAR_NOALLOC_MAX_ELEMENTS is rejected with
+ * TPAR_ERR_SCRATCH_TOO_SMALL before anything is launched.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ * first call before any stream capture. All calls share the one array, which
+ * keeps the last call's contents: each call clears the part that must start
+ * at zero (the accumulator), and two calls that overlap on the GPU (on
+ * unordered streams) race on it and give wrong results.
+ */
+#define TPAR_NOALLOC_MAX_ELEMENTS (8LL * 1024 * 1024)
+tpar_status tpar_unfused_rmsnorm_noalloc(const void* const* partials, int n_ranks,
+                                         const void* residual, const void* gamma, float eps,
+                                         int64_t T, int64_t d, void* out_norm, void* out_residual,
+                                         uint8_t* nvfp4_codes, uint8_t* nvfp4_scales,
+                                         float* global_scale, uint32_t flags,
+                                         tpar_stream_t stream);
 
 /* Static message for a status code. */
 const char* tpar_status_string(tpar_status status);

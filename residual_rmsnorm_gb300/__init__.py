@@ -29,6 +29,8 @@ from ._abi import (  # noqa: F401
     tpar_plan_launch,
     tpar_status_string,
     tpar_unfused_rmsnorm,
+    tpar_unfused_rmsnorm_noalloc,
+    TPAR_NOALLOC_MAX_ELEMENTS,
     tpar_version,
     tpar_workspace_bytes,
 )
@@ -37,6 +39,6 @@ from .ops import fused_rmsnorm, nvfp4_quantize, unfused_rmsnorm  # noqa: F401
 __all__ = [
     "fused_rmsnorm", "unfused_rmsnorm", "nvfp4_quantize", "TparError", "TparPlan",
     "tpar_init", "tpar_fused_rmsnorm", "tpar_fused_rmsnorm_ex", "tpar_unfused_rmsnorm",
-    "tpar_nvfp4_quantize", "tpar_plan_launch", "tpar_status_string", "tpar_version",
+    "tpar_nvfp4_quantize", "tpar_unfused_rmsnorm_noalloc", "tpar_plan_launch", "tpar_status_string", "tpar_version",
     "tpar_workspace_bytes", "library", "library_path",
 ]

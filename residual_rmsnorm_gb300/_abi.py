@@ -25,7 +25,9 @@ TPAR_DRY_RUN = 0x10
 _STATUS = {
     0: "TPAR_OK", 1: "TPAR_ERR_INVALID_ARG", 2: "TPAR_ERR_MISALIGNED",
     3: "TPAR_ERR_UNSUPPORTED", 4: "TPAR_ERR_CUDA", 5: "TPAR_ERR_NOT_INITIALIZED",
+    6: "TPAR_ERR_SCRATCH_TOO_SMALL",
 }
+TPAR_NOALLOC_MAX_ELEMENTS = 8 * 1024 * 1024
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 
@@ -76,6 +78,8 @@ def library() -> ctypes.CDLL:
         lib.tpar_fused_rmsnorm_ex.restype = i32
         lib.tpar_unfused_rmsnorm.argtypes = [P, i32, P, P, f32, i64, i64, P, P, P, P, P, P, u32, P]
         lib.tpar_unfused_rmsnorm.restype = i32
+        lib.tpar_unfused_rmsnorm_noalloc.argtypes = [P, i32, P, P, f32, i64, i64, P, P, P, P, P, u32, P]
+        lib.tpar_unfused_rmsnorm_noalloc.restype = i32
         lib.tpar_nvfp4_quantize.argtypes = [P, i64, i64, P, P, P, u32, P]
         lib.tpar_nvfp4_quantize.restype = i32
         lib.tpar_plan_launch.argtypes = [i64, i64, i32, i32, u32, ctypes.POINTER(TparPlan)]
@@ -147,6 +151,19 @@ def tpar_unfused_rmsnorm(partials, n_ranks, residual, gamma, eps, T, d, reduced,
                                         _p(out_residual), _p(nvfp4_codes), _p(nvfp4_scales),
                                         _p(global_scale), flags, _p(stream))
     return _check(st, "tpar_unfused_rmsnorm") if check else st
+
+
+def tpar_unfused_rmsnorm_noalloc(partials, n_ranks, residual, gamma, eps, T, d, out_norm,
+                                 out_residual, nvfp4_codes, nvfp4_scales, global_scale, flags, stream,
+                                 check=True) -> int:
+    """The unfused baseline with its scratch in the library's static device
+    array, for callers that cannot allocate (see include/tpar.h)."""
+    arr = _ptr_array(partials)
+    st = library().tpar_unfused_rmsnorm_noalloc(ctypes.cast(arr, ctypes.c_void_p), n_ranks,
+                                                _p(residual), _p(gamma), eps, T, d, _p(out_norm),
+                                                _p(out_residual), _p(nvfp4_codes), _p(nvfp4_scales),
+                                                _p(global_scale), flags, _p(stream))
+    return _check(st, "tpar_unfused_rmsnorm_noalloc") if check else st
 
 
 def tpar_nvfp4_quantize(x, T, d, codes, scales, global_scale, flags, stream, check=True) -> int:

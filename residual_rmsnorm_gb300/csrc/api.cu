@@ -652,6 +652,8 @@ const char* tpar_status_string(tpar_status s)
     case TPAR_ERR_UNSUPPORTED: return "unsupported by this build (e.g. hidden size above the maximum)";
     case TPAR_ERR_CUDA: return "CUDA runtime error or launch failure";
     case TPAR_ERR_NOT_INITIALIZED: return "device workspace missing: call tpar_init before stream capture";
+    case TPAR_ERR_SCRATCH_TOO_SMALL:
+        return "T*d exceeds the static scratch of the no-allocation entry point (TPAR_NOALLOC_MAX_ELEMENTS)";
     default: return "unknown status";
     }
 }
@@ -659,3 +661,133 @@ const char* tpar_status_string(tpar_status s)
 int tpar_version(void) { return 100; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- no-allocation unfused entry point
+//
+// The unfused baseline for callers that cannot allocate: its bf16 `reduced`
+// tensor and the dynamic-scale accumulator live in this file-scope device
+// array instead of caller or tpar_init memory. Host code must not use the
+// array's name as an address: the device address is looked up once per
+// device with cudaGetSymbolAddress and passed to the kernels.
+namespace {
+
+constexpr int64_t kNoAllocHeaderBytes = 256;  // [0] amax bits, [1] completion counter
+constexpr int64_t kNoAllocMaxElems = TPAR_NOALLOC_MAX_ELEMENTS;
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocHeaderBytes + 2 * kNoAllocMaxElems];
+
+std::mutex g_noalloc_mu;
+void* g_noalloc_addr[kMaxDevices];
+
+// Device address of the scratch array on the current device (set-up on the
+// first call per device, with that device current).
+tpar_status noalloc_scratch(unsigned char** out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return TPAR_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices)
+        return TPAR_ERR_UNSUPPORTED;
+    std::lock_guard<std::mutex> lk(g_noalloc_mu);
+    if (!g_noalloc_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p)
+            return TPAR_ERR_CUDA;
+        g_noalloc_addr[dev] = p;
+    }
+    *out = static_cast<unsigned char*>(g_noalloc_addr[dev]);
+    return TPAR_OK;
+}
+
+}  // namespace
+
+extern "C" tpar_status tpar_unfused_rmsnorm_noalloc(const void* const* partials, int n_ranks,
+                                                    const void* residual, const void* gamma, float eps,
+                                                    int64_t T, int64_t d, void* out_norm, void* out_residual,
+                                                    uint8_t* nvfp4_codes, uint8_t* nvfp4_scales,
+                                                    float* global_scale, uint32_t flags,
+                                                    tpar_stream_t stream_)
+{
+    if (T > 0 && d > 0 && T > kNoAllocMaxElems / d)
+        return TPAR_ERR_SCRATCH_TOO_SMALL;
+    const uint32_t fl = flags & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_DRY_RUN);
+    const bool dry = (fl & TPAR_DRY_RUN) != 0;
+    unsigned char* scratch = nullptr;
+    if (!dry && T > 0) {
+        tpar_status st = noalloc_scratch(&scratch);
+        if (st != TPAR_OK)
+            return st;
+    }
+    // A dry run checks the arguments with a stand-in for the scratch address.
+    void* reduced = scratch ? static_cast<void*>(scratch + kNoAllocHeaderBytes)
+                            : reinterpret_cast<void*>(static_cast<uintptr_t>(kNoAllocHeaderBytes));
+    Call c{partials, n_ranks, residual, gamma, eps, T, d, out_norm, out_residual,
+           nvfp4_codes, nvfp4_scales, global_scale, fl & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL), reduced};
+    tpar_status st = validate(c, true);
+    if (st != TPAR_OK || dry || T == 0)
+        return st;
+
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    int sm = 0;
+    if ((st = current_sm_count(&sm)) != TPAR_OK)
+        return st;
+    const bool pdl = (fl & TPAR_NO_PDL) == 0;
+    const bool nvfp4 = nvfp4_codes != nullptr;
+    const bool given = (fl & TPAR_GSCALE_GIVEN) != 0;
+    const int64_t nvec = T * d / 8;
+    uint32_t* ws = reinterpret_cast<uint32_t*>(scratch);
+    if (nvfp4 && !given) {
+        // The accumulator must start at zero; the array keeps the last call's contents.
+        if (cudaMemsetAsync(ws, 0, 2 * sizeof(uint32_t), stream) != cudaSuccess)
+            return TPAR_ERR_CUDA;
+    }
+
+    // K1: reduced = bf16(sum of partials)
+    ReduceArgs ra;
+    std::memset(&ra, 0, sizeof ra);
+    for (int r = 0; r < n_ranks; ++r)
+        ra.partials[r] = static_cast<const uint4*>(partials[r]);
+    ra.reduced = static_cast<uint4*>(reduced);
+    ra.nvec = nvec;
+    ra.n_ranks = n_ranks;
+    if (launch(tpar::reduce_kernel_for(tpar::rank_bound(n_ranks)), dim3(flat_grid(nvec, sm)), dim3(256), &ra,
+               stream, 1, pdl) != cudaSuccess)
+        return TPAR_ERR_CUDA;
+    // K2: out_residual = bf16(reduced + residual)
+    {
+        const uint4* red = static_cast<const uint4*>(reduced);
+        const uint4* res = static_cast<const uint4*>(residual);
+        uint4* outr = static_cast<uint4*>(out_residual);
+        int64_t n = nvec;
+        void* args[4] = {&red, &res, &outr, &n};
+        cudaLaunchConfig_t cfg;
+        std::memset(&cfg, 0, sizeof cfg);
+        cfg.gridDim = dim3(flat_grid(nvec, sm));
+        cfg.blockDim = dim3(256);
+        cfg.stream = stream;
+        cudaLaunchAttribute at;
+        at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at.val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = &at;
+        cfg.numAttrs = pdl ? 1 : 0;
+        if (cudaLaunchKernelExC(&cfg, tpar::residual_add_kernel_ptr(), args) != cudaSuccess)
+            return TPAR_ERR_CUDA;
+    }
+    // K3: out_norm = RMSNorm(out_residual) (+ amax for a dynamic NVFP4 scale)
+    const void* k3_in[1] = {out_residual};
+    Call k3{k3_in, 1, nullptr, gamma, eps, T, d, out_norm, nullptr, nullptr, nullptr, nullptr,
+            TPAR_FORCE_ROW, nullptr};
+    FusedArgs a = fused_args(k3);
+    a.amax_bits = (nvfp4 && !given) ? ws : nullptr;
+    tpar_plan p;
+    if ((st = plan_impl(T, d, 1, sm, TPAR_FORCE_ROW, &p)) != TPAR_OK)
+        return st;
+    if ((st = launch_fused(a, (nvfp4 && !given) ? tpar::kQuantAmax : tpar::kQuantNone, p, stream, pdl)) !=
+        TPAR_OK)
+        return st;
+    // K4: the separate NVFP4 quantiser
+    if (nvfp4)
+        st = launch_quantize(out_norm, T, d, nvfp4_codes, nvfp4_scales, global_scale, given ? nullptr : ws,
+                             !given, sm, stream, pdl);
+    return st;
+}
