@@ -185,7 +185,7 @@ int slice_for(int nvec, int split)
     return static_cast<int>(s + (s & 1));
 }
 
-tpar_status check_plan(const tpar_plan& p, int64_t d)
+tpar_status check_plan(const tpar_plan& p, int64_t d, int n_ranks)
 {
     const int nvec = static_cast<int>(d / 8);
     if (p.kernel != 0 && p.kernel != 1)
@@ -199,7 +199,7 @@ tpar_status check_plan(const tpar_plan& p, int64_t d)
     const int v = p.vec_per_thread;
     if (v != 1 && v != 2 && v != 4 && v != 8)
         return TPAR_ERR_INVALID_ARG;
-    if (v >= 4 && p.threads > 512)
+    if (p.threads > tpar::fused_thread_cap(tpar::rank_bound(n_ranks), v))
         return TPAR_ERR_INVALID_ARG;
     if (p.kernel == 1 && v > 2)
         return TPAR_ERR_INVALID_ARG;
@@ -316,43 +316,51 @@ tpar_status plan_impl(int64_t T, int64_t d, int n_ranks, int sm_count, uint32_t 
     const int nvec = static_cast<int>(d / 8);
     int split = 1;
     if (!(flags & TPAR_FORCE_ROW)) {
-        // Latency path: split each row over a cluster while the rows alone
-        // would leave SMs idle and every CTA keeps at least a warp of vectors.
-        while (split < 16 && T * (2 * split) <= sm_count && nvec / (2 * split) >= 32)
-            split *= 2;
+        // Latency path. A CTA that owns a whole row pulls (N+1)*2d bytes
+        // through one SM; when that is large and the rows are few, split each
+        // row over a thread-block cluster so that every CTA pulls about
+        // kClusterSliceBytes (measured on GB300: one 147 KB row per CTA costs
+        // ~0.6 us more than 8 CTAs of 18 KB plus the cluster exchange, while
+        // for rows <= ~80 KB or T > 16 the exchange costs more than it saves).
+        constexpr int64_t kClusterRowBytes = 96 * 1024;
+        constexpr int64_t kClusterSliceBytes = 16 * 1024;
+        constexpr int64_t kClusterMaxRows = 16;
+        const int64_t row_bytes = static_cast<int64_t>(n_ranks + 1) * d * 2;
+        if (T <= kClusterMaxRows && row_bytes >= kClusterRowBytes) {
+            while (split < 16 && row_bytes / (2 * split) >= kClusterSliceBytes && T * (2 * split) <= sm_count &&
+                   nvec / (2 * split) >= 32)
+                split *= 2;
+        }
         if ((flags & TPAR_FORCE_CLUSTER) && split == 1) {
             if (nvec < 4)
                 return TPAR_ERR_UNSUPPORTED;
             split = 2;
+            while (split < 16 && T * (2 * split) <= sm_count && nvec / (2 * split) >= 32)
+                split *= 2;
         }
+    }
+    const int nr = tpar::rank_bound(n_ranks);
+    // CTA shape for `vectors` vectors: one vector per thread while the CTA
+    // stays within 1024 (or the instantiation's cap) threads, else 2, 4, 8.
+    auto shape = [&](int vectors, int* threads, int* vpt) {
+        int v = 1;
+        while (v < 8 && ceil_div(vectors, v) > tpar::fused_thread_cap(nr, v))
+            v *= 2;
+        *vpt = v;
+        *threads = static_cast<int>(ceil_div(ceil_div(vectors, v), 32) * 32);
+    };
+    if (split > 1) {
+        // cluster CTAs are built for at most 2 vectors per thread
+        while (split < 16 && slice_for(nvec, split) > 2 * tpar::fused_thread_cap(nr, 2))
+            split *= 2;
     }
     tpar_plan p;
     p.grid_rows = T < 1 ? 1 : (T < kMaxGridY ? T : kMaxGridY);
-    if (split > 1) {
-        const int slice = slice_for(nvec, split);
-        p.kernel = 1;
-        p.split = split;
-        p.threads = static_cast<int>(std::min<int64_t>(1024, ceil_div(slice, 32) * 32));
-        p.vec_per_thread = pow2_at_least(ceil_div(slice, p.threads));
-    } else {
-        p.kernel = 0;
-        p.split = 1;
-        if (nvec <= 256) {
-            p.threads = static_cast<int>(ceil_div(nvec, 32) * 32);
-            p.vec_per_thread = 1;
-        } else if (nvec <= 1024) {
-            p.threads = 256;
-            p.vec_per_thread = pow2_at_least(ceil_div(nvec, 256));
-        } else if (nvec <= 2048) {
-            p.threads = 512;
-            p.vec_per_thread = 4;
-        } else {
-            p.threads = 512;
-            p.vec_per_thread = 8;
-        }
-    }
+    p.kernel = split > 1 ? 1 : 0;
+    p.split = split;
+    shape(split > 1 ? slice_for(nvec, split) : nvec, &p.threads, &p.vec_per_thread);
     *out = p;
-    return check_plan(p, d);
+    return check_plan(p, d, n_ranks);
 }
 
 const void* fused_kernel(int qmode, int nr, int vpt, bool cluster)
@@ -438,7 +446,7 @@ tpar_status fused_impl(const Call& c, const tpar_plan* user_plan, void* user_ws,
     if (st != TPAR_OK)
         return st;
     if (c.flags & TPAR_DRY_RUN)
-        return user_plan ? check_plan(*user_plan, c.d) : TPAR_OK;
+        return user_plan ? check_plan(*user_plan, c.d, c.n_ranks) : TPAR_OK;
     if (c.T == 0)
         return TPAR_OK;
     int sm = 0;
@@ -447,7 +455,7 @@ tpar_status fused_impl(const Call& c, const tpar_plan* user_plan, void* user_ws,
     tpar_plan p;
     if (user_plan) {
         p = *user_plan;
-        if ((st = check_plan(p, c.d)) != TPAR_OK)
+        if ((st = check_plan(p, c.d, c.n_ranks)) != TPAR_OK)
             return st;
     } else if ((st = plan_impl(c.T, c.d, c.n_ranks, sm, c.flags, &p)) != TPAR_OK) {
         return st;

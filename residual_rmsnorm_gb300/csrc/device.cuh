@@ -146,6 +146,20 @@ __device__ __forceinline__ void cluster_sync_all()
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Split-phase halves of the cluster barrier: every thread alternates
+// arrive and wait. A release arrive orders this thread's earlier
+// shared-memory accesses (including distributed reads) before any peer's
+// accesses that follow its matching acquire wait.
+__device__ __forceinline__ void cluster_arrive_release()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void cluster_wait_acquire()
+{
+    asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Read a float from the same shared-memory variable in CTA `rank` of the
 // cluster.
 __device__ __forceinline__ float ld_dsmem(const float* local, uint32_t rank)

@@ -49,8 +49,12 @@ struct FusedArgs {
     float inv_d;
 };
 
+// Largest CTA a fused-kernel instantiation is built for: wide rows (VPT >= 2)
+// and many ranks need more than the 64 registers a 1024-thread CTA allows.
+constexpr int fused_max_threads(int nr, int vpt) { return (vpt >= 2 || nr >= 16) ? 512 : 1024; }
+
 template <int NR, int VPT, bool CLUSTER, int QMODE>
-__global__ void __launch_bounds__(VPT >= 4 ? 512 : 1024)
+__global__ void __launch_bounds__(fused_max_threads(NR, VPT))
     fused_rmsnorm_kernel(const __grid_constant__ FusedArgs a)
 {
     // PDL: nothing below may read an input before the previous grid is done.
@@ -67,7 +71,7 @@ __global__ void __launch_bounds__(VPT >= 4 ? 512 : 1024)
     const int vend = min(vbeg + a.slice, a.nvec);
 
     __shared__ float warp_ss[2][32];  // per-warp sums of squares, by iteration parity
-    __shared__ float cta_ss[2];       // this CTA's sum of squares, read by its cluster
+    __shared__ float cta_ss;          // this CTA's sum of squares, read by its cluster
 
     float g_given = 0.0f;
     if constexpr (QMODE == kQuantGiven)
@@ -84,37 +88,49 @@ __global__ void __launch_bounds__(VPT >= 4 ? 512 : 1024)
         uint4 gv[kEarlyGamma ? VPT : 1];
         float ss = 0.0f;
 
-        // ---- rank sum (fixed order 0..N-1), residual add, store new residual
+        // ---- rank sum (fixed order 0..N-1), residual add, store new residual.
+        // All loads of a group of G vectors are issued before any of them is
+        // used or any store is made, so their memory latencies overlap.
+        constexpr int G = (NR >= 16 || VPT == 1 || VPT >= 8) ? 1 : 2;
 #pragma unroll
-        for (int j = 0; j < VPT; ++j) {
-            const int v = vbeg + tid + j * static_cast<int>(blockDim.x);
-            if (v < vend) {
-                uint4 x[NR];
+        for (int j0 = 0; j0 < VPT; j0 += G) {
+            uint4 x[G][NR];
+            uint4 rv[G];
 #pragma unroll
-                for (int r = 0; r < NR; ++r)
-                    if (r < a.n_ranks)
-                        x[r] = ld_stream(a.partials[r] + rowv + v);
-                uint4 rv = make_uint4(0u, 0u, 0u, 0u);
-                if (a.residual)
-                    rv = ld_coherent(a.residual + rowv + v);
-                if constexpr (kEarlyGamma)
-                    gv[j] = ld_reuse(a.gamma + v);
-                unpack8(x[0], h[j]);
+            for (int jj = 0; jj < G; ++jj) {
+                const int v = vbeg + tid + (j0 + jj) * static_cast<int>(blockDim.x);
+                if (v < vend) {
 #pragma unroll
-                for (int r = 1; r < NR; ++r)
-                    if (r < a.n_ranks)
-                        add8(x[r], h[j]);
-                if (a.residual)
-                    add8(rv, h[j]);
+                    for (int r = 0; r < NR; ++r)
+                        if (r < a.n_ranks)
+                            x[jj][r] = ld_stream(a.partials[r] + rowv + v);
+                    rv[jj] = a.residual ? ld_coherent(a.residual + rowv + v) : make_uint4(0u, 0u, 0u, 0u);
+                    if constexpr (kEarlyGamma)
+                        gv[kEarlyGamma ? j0 + jj : 0] = ld_reuse(a.gamma + v);
+                }
+            }
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    ss = fmaf(h[j][e], h[j][e], ss);
-                if (a.out_residual)
-                    st_v4(a.out_residual + rowv + v, pack8(h[j]));
-            } else {
+            for (int jj = 0; jj < G; ++jj) {
+                const int j = j0 + jj;
+                const int v = vbeg + tid + j * static_cast<int>(blockDim.x);
+                if (v < vend) {
+                    unpack8(x[jj][0], h[j]);
 #pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    h[j][e] = 0.0f;
+                    for (int r = 1; r < NR; ++r)
+                        if (r < a.n_ranks)
+                            add8(x[jj][r], h[j]);
+                    if (a.residual)
+                        add8(rv[jj], h[j]);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        ss = fmaf(h[j][e], h[j][e], ss);
+                    if (a.out_residual)
+                        st_v4(a.out_residual + rowv + v, pack8(h[j]));
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        h[j][e] = 0.0f;
+                }
             }
         }
 
@@ -126,10 +142,18 @@ __global__ void __launch_bounds__(VPT >= 4 ? 512 : 1024)
         __syncthreads();
         float tot = warp_sum(lane < nwarps ? warp_ss[buf][lane] : 0.0f);
         if constexpr (CLUSTER) {
+            // The peers' "done reading" arrive of the previous row must be
+            // matched before this CTA's slot is overwritten.
+            if (it > 0)
+                cluster_wait_acquire();
             if (tid == 0)
-                cta_ss[buf] = tot;
-            cluster_sync_all();
-            tot = warp_sum(lane < split ? ld_dsmem(&cta_ss[buf], static_cast<uint32_t>(lane)) : 0.0f);
+                cta_ss = tot;
+            cluster_arrive_release();
+            cluster_wait_acquire();
+            tot = warp_sum(lane < split ? ld_dsmem(&cta_ss, static_cast<uint32_t>(lane)) : 0.0f);
+            // Done reading the peers' slots; the matching wait comes only
+            // before the next overwrite (or exit), off the critical path.
+            cluster_arrive_release();
         }
         const float rinv = rsqrtf(fmaf(tot, a.inv_d, a.eps));
 
@@ -192,7 +216,8 @@ __global__ void __launch_bounds__(VPT >= 4 ? 512 : 1024)
     }
     if constexpr (CLUSTER) {
         // No CTA may leave while a peer could still read its shared memory.
-        cluster_sync_all();
+        if (it > 0)
+            cluster_wait_acquire();
     }
 }
 

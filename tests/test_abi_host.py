@@ -187,22 +187,29 @@ def test_planner_covers_every_row(tp, sm):
                 s += s & 1
                 assert p.threads * p.vec_per_thread >= s
                 assert s >= 32 or p.split == 2
-                assert T * p.split <= sm
+                assert T * 2 <= sm and T <= 16  # rows are split only while SMs would idle
             else:
                 assert p.split == 1 and p.threads * p.vec_per_thread >= nvec
             assert 1 <= p.grid_rows <= min(T, 65535)
 
 
 def test_planner_choices_for_the_pages_shapes(tp):
-    # decode: rows split over clusters so ~all SMs take part
+    # decode, 73 KB rows (N=8, d=4096): one CTA of 512 threads per row
     p = tp.tpar_plan_launch(8, 4096, 8, 152)
-    assert (p.kernel, p.split, p.threads, p.vec_per_thread) == (1, 16, 32, 1)
+    assert (p.kernel, p.split, p.threads, p.vec_per_thread) == (0, 1, 512, 1)
+    # decode, 147 KB rows (N=8, d=8192), few tokens: rows split over clusters
     p = tp.tpar_plan_launch(1, 8192, 8, 152)
-    assert (p.kernel, p.split) == (1, 16)
-    p = tp.tpar_plan_launch(32, 8192, 8, 152)
-    assert (p.kernel, p.split) == (1, 4)
-    # prefill: one CTA per row
+    assert (p.kernel, p.split, p.threads) == (1, 8, 128)
+    p = tp.tpar_plan_launch(8, 8192, 8, 152)
+    assert (p.kernel, p.split) == (1, 8)
+    p = tp.tpar_plan_launch(16, 8192, 8, 152)
+    assert (p.kernel, p.split) == (1, 8)
+    assert tp.tpar_plan_launch(32, 8192, 8, 152).kernel == 0
+    # prefill: one CTA of 1024 threads per row
     p = tp.tpar_plan_launch(4096, 8192, 8, 152)
-    assert (p.kernel, p.split, p.threads, p.vec_per_thread) == (0, 1, 256, 4)
-    assert tp.tpar_plan_launch(8, 4096, 8, 152, tp.TPAR_FORCE_ROW).kernel == 0
+    assert (p.kernel, p.split, p.threads, p.vec_per_thread) == (0, 1, 1024, 1)
+    # more than 8 ranks: CTAs capped at 512 threads
+    p = tp.tpar_plan_launch(4096, 8192, 16, 152)
+    assert (p.threads, p.vec_per_thread) == (512, 2)
+    assert tp.tpar_plan_launch(1, 8192, 8, 152, tp.TPAR_FORCE_ROW).kernel == 0
     assert tp.tpar_plan_launch(4096, 4096, 8, 152, tp.TPAR_FORCE_CLUSTER).kernel == 1
