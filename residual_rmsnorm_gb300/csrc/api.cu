@@ -3,6 +3,7 @@
 // allocation is the 256-byte per-device workspace made by tpar_init.
 #include "tpar.h"
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -355,7 +356,11 @@ tpar_status plan_impl(int64_t T, int64_t d, int n_ranks, int sm_count, uint32_t 
             split *= 2;
     }
     tpar_plan p;
-    p.grid_rows = T < 1 ? 1 : (T < kMaxGridY ? T : kMaxGridY);
+    // Row kernels stride over rows with at most 8 CTAs per SM in the grid:
+    // as fast as one CTA per row (measured), and it bounds the per-CTA
+    // epilogue work (such as the dynamic-scale amax atomic).
+    const int64_t row_cap = std::min<int64_t>(kMaxGridY, static_cast<int64_t>(sm_count) * 8);
+    p.grid_rows = T < 1 ? 1 : (split > 1 ? std::min<int64_t>(T, kMaxGridY) : std::min<int64_t>(T, row_cap));
     p.kernel = split > 1 ? 1 : 0;
     p.split = split;
     shape(split > 1 ? slice_for(nvec, split) : nvec, &p.threads, &p.vec_per_thread);

@@ -210,9 +210,18 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT))
     }
 
     if constexpr (QMODE == kQuantAmax) {
+        // One atomic per CTA: same-address atomics serialise in L2, so a
+        // per-warp atomic over thousands of CTAs would dominate the kernel.
+        __shared__ float warp_max_sh[32];
         const float m = warp_max(amax_local);
-        if (lane == 0 && m > 0.0f)
-            atomicMax(a.amax_bits, __float_as_uint(m));  // |y| >= 0 orders like its bits
+        if (lane == 0)
+            warp_max_sh[warp] = m;
+        __syncthreads();
+        if (warp == 0) {
+            const float c = warp_max(lane < nwarps ? warp_max_sh[lane] : 0.0f);
+            if (lane == 0 && c > 0.0f)
+                atomicMax(a.amax_bits, __float_as_uint(c));  // |y| >= 0 orders like its bits
+        }
     }
     if constexpr (CLUSTER) {
         // No CTA may leave while a peer could still read its shared memory.
