@@ -165,6 +165,12 @@ def max_over_ranks(dist, value: float, device) -> float:
     return float(t.item())
 
 
+def job_us_per_call(ms_total_max: float, steps: int, calls_per_step: int, world: int) -> float:
+    """Whole-job time per call: the slowest rank's elapsed time over every
+    call that all ranks made (each rank runs the same per-GPU workload)."""
+    return ms_total_max * 1e3 / (steps * calls_per_step * world)
+
+
 def barrier(dist, device):
     import torch
     if dist is not None:
@@ -421,7 +427,7 @@ def ours_arm(args, w):
     ms_total = max_over_ranks(dist, ms_total, device)
     ms_step = ms_total / args.steps
     us_per_call_rank = ms_step * 1e3 / CALLS_PER_STEP
-    us_per_call_job = ms_total * 1e3 / (args.steps * CALLS_PER_STEP * world)
+    us_per_call_job = job_us_per_call(ms_total, args.steps, CALLS_PER_STEP, world)
 
     # L2-hot variant (all calls on one input set), for reference
     g_hot = capture(torch, lambda i: sets[0].call(tp, w, torch.cuda.current_stream().cuda_stream),
@@ -458,7 +464,7 @@ def ours_arm(args, w):
     e2e_steps = max(3, min(args.steps, 50))
     ms_e2e = time_graph(torch, g_e2e, e2e_steps, 3)
     ms_e2e = max_over_ranks(dist, ms_e2e, device)
-    us_e2e_job = ms_e2e * 1e3 / (CALLS_PER_STEP * world)
+    us_e2e_job = job_us_per_call(ms_e2e, 1, CALLS_PER_STEP, world)
     del g_e2e
 
     # ---- roofline of the fused kernel (the only kernel in the step)

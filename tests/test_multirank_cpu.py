@@ -1,0 +1,69 @@
+"""The benchmark's multi-rank host logic on CPU: world_size 2 over gloo.
+
+Each rank runs the same per-GPU workload (weak scaling, no data-path
+collective); the only collectives are the timing barrier and the max over
+ranks of the elapsed time. The reference arm runs on rank 0 only.
+"""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _rank_main(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    sys.path.insert(0, ROOT)
+    import torch
+    import bench
+    dist = bench.init_dist(world)
+    dev = torch.device("cpu")
+    bench.barrier(dist, dev)
+    mx = bench.max_over_ranks(dist, 10.0 + 5.0 * rank, dev)
+    q.put((rank, mx, bench.job_us_per_call(mx, 4, 1000, world)))
+    dist.destroy_process_group()
+
+
+def test_max_over_ranks_and_job_value_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank_main, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, mx, us in got:
+        assert mx == 15.0  # the slowest rank's time
+        assert abs(us - 15.0 * 1e3 / (4 * 1000 * 2)) < 1e-12  # all calls of both ranks
+
+
+def test_reference_arm_only_on_rank_zero():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--gpus", "2", "--steps", "3", "--warmup", "3"],
+                       env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0 and r.stdout.strip() == ""
+    env["RANK"] = "0"
+    env["LOCAL_RANK"] = "0"
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--gpus", "2", "--steps", "3", "--warmup", "3"],
+                       env=env, capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["higher_is_better"] is False
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["e2e"]["h2d_bytes_per_step"] == 0
+    assert line["value"] > 0 and line["unit"] == "us/call"
