@@ -416,7 +416,7 @@ tpar_status launch_quantize(const void* x, int64_t T, int64_t d, uint8_t* codes,
     q.gscale = gscale;
     q.ws = ws;
     q.nvec = T * d / 8;
-    const unsigned grid = flat_grid(q.nvec, sm_count);
+    const unsigned grid = flat_grid(q.nvec / 2, sm_count);  // one thread per 16-element block
     if (launch(tpar::quantize_kernel_for(dynamic), dim3(grid), dim3(256), &q, stream, 1, pdl) != cudaSuccess)
         return TPAR_ERR_CUDA;
     return TPAR_OK;

@@ -51,6 +51,11 @@ __device__ __forceinline__ void st_v4(uint4* p, uint4 v)
                  : "memory");
 }
 
+__device__ __forceinline__ void st_v2(uint32_t* p, uint32_t lo, uint32_t hi)
+{
+    asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(lo), "r"(hi) : "memory");
+}
+
 __device__ __forceinline__ void st_u32(uint32_t* p, uint32_t v)
 {
     asm volatile("st.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");

@@ -241,9 +241,11 @@ struct QuantArgs {
     int64_t nvec;        // T * d / 8 (even)
 };
 
-// Lane pairs (2k, 2k+1) own one 16-element block per iteration. In dynamic
-// mode g = amax / 2688 is read from the workspace; the last CTA to have read
-// it zeroes the workspace for the next call (no CTA waits on another).
+// One thread owns one 16-element block (two consecutive 16-byte vectors) per
+// iteration, so the block-scale arithmetic (two IEEE divisions and the E4M3
+// round trip) runs once per block. In dynamic mode g = amax / 2688 is read
+// from the workspace; the last CTA to have read it zeroes the workspace for
+// the next call (no CTA waits on another).
 template <bool DYNAMIC>
 __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __grid_constant__ QuantArgs a)
 {
@@ -272,28 +274,26 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __grid_consta
     __syncthreads();
     const float g = g_sh;
 
+    const int64_t nblocks = a.nvec / 2;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    // nvec is even and stride is a multiple of 32, so lane pairs stay aligned
-    // to block boundaries and a whole warp is either in or out of the loop
-    // together only at the tail -- the shuffle below uses the active mask.
-    for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < a.nvec; v += stride) {
-        float x[8];
-        unpack8(ld_stream(a.x + v), x);
+    for (int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; b < nblocks; b += stride) {
+        // the two halves of the block; the second load hits the lines the
+        // first brought into L1
+        float x[16];
+        unpack8(ld_reuse(a.x + 2 * b), x);
+        unpack8(ld_reuse(a.x + 2 * b + 1), x + 8);
         float bmax = 0.0f;
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
+        for (int e = 0; e < 16; ++e)
             bmax = fmaxf(bmax, fabsf(x[e]));
-        const unsigned mask = __activemask();
-        bmax = fmaxf(bmax, __shfl_xor_sync(mask, bmax, 1));
         uint32_t sbyte;
         const float inv = nvfp4_block_scale(g, bmax, sbyte);
-        float q[8];
+        float q[16];
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
+        for (int e = 0; e < 16; ++e)
             q[e] = __fmul_rn(x[e], inv);
-        st_u32(a.codes + v, e2m1x8_from_f32(q));
-        if ((v & 1) == 0)
-            st_u8(a.scales + v / 2, sbyte);
+        st_v2(a.codes + 2 * b, e2m1x8_from_f32(q), e2m1x8_from_f32(q + 8));
+        st_u8(a.scales + b, sbyte);
     }
 }
 
