@@ -189,6 +189,15 @@ tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* co
 tpar_status tpar_plan_launch(int64_t T, int64_t d, int n_ranks, int sm_count, uint32_t flags,
                              tpar_plan* out);
 
+/*
+ * tpar_device_error -- read and clear the device's error word (kept in the
+ * tpar_init workspace; 0 when tpar_init never ran for `device`). Bit 0: a
+ * bounded wait inside the cluster-split kernel expired, so that call's
+ * outputs are wrong. Synchronises the device; a diagnostic, not for the hot
+ * path.
+ */
+tpar_status tpar_device_error(int device, uint32_t* code);
+
 /* Bytes of a caller-owned workspace for tpar_fused_rmsnorm_ex. */
 int64_t tpar_workspace_bytes(void);
 

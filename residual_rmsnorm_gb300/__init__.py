@@ -24,6 +24,7 @@ from ._abi import (  # noqa: F401
     library_path,
     tpar_fused_rmsnorm,
     tpar_fused_rmsnorm_ex,
+    tpar_device_error,
     tpar_init,
     tpar_nvfp4_quantize,
     tpar_plan_launch,
@@ -40,5 +41,5 @@ __all__ = [
     "fused_rmsnorm", "unfused_rmsnorm", "nvfp4_quantize", "TparError", "TparPlan",
     "tpar_init", "tpar_fused_rmsnorm", "tpar_fused_rmsnorm_ex", "tpar_unfused_rmsnorm",
     "tpar_nvfp4_quantize", "tpar_unfused_rmsnorm_noalloc", "tpar_plan_launch", "tpar_status_string", "tpar_version",
-    "tpar_workspace_bytes", "library", "library_path",
+    "tpar_workspace_bytes", "tpar_device_error", "library", "library_path",
 ]

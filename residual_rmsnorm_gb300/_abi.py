@@ -84,6 +84,8 @@ def library() -> ctypes.CDLL:
         lib.tpar_nvfp4_quantize.restype = i32
         lib.tpar_plan_launch.argtypes = [i64, i64, i32, i32, u32, ctypes.POINTER(TparPlan)]
         lib.tpar_plan_launch.restype = i32
+        lib.tpar_device_error.argtypes = [i32, ctypes.POINTER(ctypes.c_uint32)]
+        lib.tpar_device_error.restype = i32
         lib.tpar_workspace_bytes.argtypes = []
         lib.tpar_workspace_bytes.restype = i64
         lib.tpar_status_string.argtypes = [i32]
@@ -177,6 +179,13 @@ def tpar_plan_launch(T, d, n_ranks, sm_count, flags=0) -> TparPlan:
     _check(library().tpar_plan_launch(T, d, n_ranks, sm_count, flags, ctypes.byref(plan)),
            "tpar_plan_launch")
     return plan
+
+
+def tpar_device_error(device: int) -> int:
+    """Read and clear the device error word (0: no bounded wait expired)."""
+    code = ctypes.c_uint32(0)
+    _check(library().tpar_device_error(device, ctypes.byref(code)), "tpar_device_error")
+    return int(code.value)
 
 
 def tpar_workspace_bytes() -> int:

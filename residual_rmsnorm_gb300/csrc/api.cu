@@ -96,6 +96,18 @@ tpar_status init_device(int dev)
     return TPAR_OK;
 }
 
+// The device error word (word 2 of the device workspace) of the current
+// device, or null when tpar_init has not run for it. Bounded device-side
+// waits that expire set bits here.
+uint32_t* device_error_word()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return nullptr;
+    std::lock_guard<std::mutex> lk(g_mu);
+    return g_dev[dev].ws ? g_dev[dev].ws + 2 : nullptr;
+}
+
 // The workspace for a dynamic-scale call on the current device: the
 // caller's, else the device's own (made here unless the stream is capturing).
 tpar_status workspace_for(void* user_ws, cudaStream_t stream, uint32_t** out)
@@ -200,7 +212,7 @@ tpar_status check_plan(const tpar_plan& p, int64_t d, int n_ranks)
     const int v = p.vec_per_thread;
     if (v != 1 && v != 2 && v != 4 && v != 8)
         return TPAR_ERR_INVALID_ARG;
-    if (p.threads > tpar::fused_thread_cap(tpar::rank_bound(n_ranks), v))
+    if (p.threads > tpar::fused_thread_cap(tpar::rank_bound(n_ranks), v, p.kernel == 1))
         return TPAR_ERR_INVALID_ARG;
     if (p.kernel == 1 && v > 2)
         return TPAR_ERR_INVALID_ARG;
@@ -343,16 +355,16 @@ tpar_status plan_impl(int64_t T, int64_t d, int n_ranks, int sm_count, uint32_t 
     const int nr = tpar::rank_bound(n_ranks);
     // CTA shape for `vectors` vectors: one vector per thread while the CTA
     // stays within 1024 (or the instantiation's cap) threads, else 2, 4, 8.
-    auto shape = [&](int vectors, int* threads, int* vpt) {
+    auto shape = [&](int vectors, bool cluster, int* threads, int* vpt) {
         int v = 1;
-        while (v < 8 && ceil_div(vectors, v) > tpar::fused_thread_cap(nr, v))
+        while (v < 8 && ceil_div(vectors, v) > tpar::fused_thread_cap(nr, v, cluster))
             v *= 2;
         *vpt = v;
         *threads = static_cast<int>(ceil_div(ceil_div(vectors, v), 32) * 32);
     };
     if (split > 1) {
         // cluster CTAs are built for at most 2 vectors per thread
-        while (split < 16 && slice_for(nvec, split) > 2 * tpar::fused_thread_cap(nr, 2))
+        while (split < 16 && slice_for(nvec, split) > 2 * tpar::fused_thread_cap(nr, 2, true))
             split *= 2;
     }
     tpar_plan p;
@@ -363,7 +375,7 @@ tpar_status plan_impl(int64_t T, int64_t d, int n_ranks, int sm_count, uint32_t 
     p.grid_rows = T < 1 ? 1 : (split > 1 ? std::min<int64_t>(T, kMaxGridY) : std::min<int64_t>(T, row_cap));
     p.kernel = split > 1 ? 1 : 0;
     p.split = split;
-    shape(split > 1 ? slice_for(nvec, split) : nvec, &p.threads, &p.vec_per_thread);
+    shape(split > 1 ? slice_for(nvec, split) : nvec, split > 1, &p.threads, &p.vec_per_thread);
     *out = p;
     return check_plan(p, d, n_ranks);
 }
@@ -389,6 +401,7 @@ tpar_status launch_fused(const FusedArgs& a, int qmode, const tpar_plan& p, cuda
             return TPAR_ERR_CUDA;
     }
     FusedArgs args = a;
+    args.err = device_error_word();
     dim3 grid(static_cast<unsigned>(p.split), static_cast<unsigned>(p.grid_rows), 1);
     dim3 block(static_cast<unsigned>(p.threads), 1, 1);
     if (launch(fn, grid, block, &args, stream, p.kernel == 1 ? p.split : 1, pdl) != cudaSuccess)
@@ -655,6 +668,32 @@ tpar_status tpar_plan_launch(int64_t T, int64_t d, int n_ranks, int sm_count, ui
 }
 
 int64_t tpar_workspace_bytes(void) { return kWorkspaceBytes; }
+
+tpar_status tpar_device_error(int device, uint32_t* code)
+{
+    if (!code || device < 0 || device >= kMaxDevices)
+        return TPAR_ERR_INVALID_ARG;
+    uint32_t* ws = nullptr;
+    {
+        std::lock_guard<std::mutex> lk(g_mu);
+        ws = g_dev[device].ws;
+    }
+    *code = 0;
+    if (!ws)
+        return TPAR_OK;  // no workspace: no kernel could have recorded an error
+    int prev = -1;
+    if (cudaGetDevice(&prev) != cudaSuccess || cudaSetDevice(device) != cudaSuccess)
+        return TPAR_ERR_CUDA;
+    uint32_t v = 0;
+    cudaError_t e = cudaMemcpy(&v, ws + 2, sizeof v, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && v != 0)
+        e = cudaMemset(ws + 2, 0, sizeof v);
+    cudaSetDevice(prev);
+    if (e != cudaSuccess)
+        return TPAR_ERR_CUDA;
+    *code = v;
+    return TPAR_OK;
+}
 
 const char* tpar_status_string(tpar_status s)
 {

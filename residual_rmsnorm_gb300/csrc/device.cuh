@@ -165,6 +165,78 @@ __device__ __forceinline__ void cluster_wait_acquire()
     asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+
+// Shared-memory address (32-bit, shared::cta window) of a local object.
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// The shared::cluster address of the same object in CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank)
+{
+    uint32_t remote;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(local), "r"(rank));
+    return remote;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+// Make this thread's mbarrier initialisations visible to the cluster.
+__device__ __forceinline__ void fence_mbar_init_cluster()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+// Asynchronous 4-byte store into a peer CTA's shared memory; its arrival
+// counts `4` transaction bytes on the peer's mbarrier.
+__device__ __forceinline__ void st_async_f32(uint32_t remote_dst, float v, uint32_t remote_bar)
+{
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(remote_dst),
+                 "r"(__float_as_uint(v)), "r"(remote_bar)
+                 : "memory");
+}
+
+__device__ __forceinline__ uint64_t global_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for the given phase parity of a local mbarrier, for at most
+// `limit_ns` nanoseconds. Returns false on timeout (the caller records an
+// error and carries on: no wait in this library can hang the GPU).
+__device__ __forceinline__ bool mbar_wait_parity_bounded(uint32_t bar, uint32_t parity, uint64_t limit_ns)
+{
+    const uint64_t t0 = global_ns();
+    while (true) {
+        uint32_t done;
+        asm volatile("{\n\t.reg .pred p;\n\t"
+                     "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+                     "selp.u32 %0, 1, 0, p;\n\t}"
+                     : "=r"(done)
+                     : "r"(bar), "r"(parity)
+                     : "memory");
+        if (done)
+            return true;
+        if (global_ns() - t0 > limit_ns)
+            return false;
+    }
+}
+
 // Read a float from the same shared-memory variable in CTA `rank` of the
 // cluster.
 __device__ __forceinline__ float ld_dsmem(const float* local, uint32_t rank)

@@ -18,9 +18,13 @@ const void* residual_add_kernel_ptr();
 const void* quantize_kernel_for(bool dynamic);
 const void* amax_kernel_ptr();
 
-// Largest CTA the fused kernel for rank bound nr and vpt vectors per thread
-// is compiled for (mirrors fused_max_threads in kernels.cuh).
-inline int fused_thread_cap(int nr, int vpt) { return (vpt >= 2 || nr >= 16) ? 512 : 1024; }
+// Largest CTA the fused kernel for rank bound nr, vpt vectors per thread and
+// the row (cluster = false) or cluster form is compiled for (mirrors
+// fused_max_threads in kernels.cuh).
+inline int fused_thread_cap(int nr, int vpt, bool cluster)
+{
+    return (vpt >= 2 || nr >= 16 || cluster) ? 512 : 1024;
+}
 
 // Smallest power of two >= n among {1, 2, 4, 8, 16}; 0 if n > 16.
 inline int rank_bound(int n)

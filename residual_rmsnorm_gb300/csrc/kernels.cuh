@@ -41,6 +41,7 @@ struct FusedArgs {
     uint8_t* scales;                   // [T, d/16]
     const float* gscale;               // given g (kQuantGiven)
     uint32_t* amax_bits;               // running max of |out_norm| bits (kQuantAmax)
+    uint32_t* err;                     // device error word (bounded wait expired) or null
     int64_t T;
     int n_ranks;
     int nvec;   // d / 8
@@ -49,12 +50,16 @@ struct FusedArgs {
     float inv_d;
 };
 
-// Largest CTA a fused-kernel instantiation is built for: wide rows (VPT >= 2)
-// and many ranks need more than the 64 registers a 1024-thread CTA allows.
-constexpr int fused_max_threads(int nr, int vpt) { return (vpt >= 2 || nr >= 16) ? 512 : 1024; }
+// Largest CTA a fused-kernel instantiation is built for: wide rows (VPT >= 2),
+// many ranks and the cluster exchange need more than the 64 registers a
+// 1024-thread CTA allows.
+constexpr int fused_max_threads(int nr, int vpt, bool cluster)
+{
+    return (vpt >= 2 || nr >= 16 || cluster) ? 512 : 1024;
+}
 
 template <int NR, int VPT, bool CLUSTER, int QMODE>
-__global__ void __launch_bounds__(fused_max_threads(NR, VPT))
+__global__ void __launch_bounds__(fused_max_threads(NR, VPT, CLUSTER))
     fused_rmsnorm_kernel(const __grid_constant__ FusedArgs a)
 {
     // PDL: nothing below may read an input before the previous grid is done.
@@ -71,7 +76,20 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT))
     const int vend = min(vbeg + a.slice, a.nvec);
 
     __shared__ float warp_ss[2][32];  // per-warp sums of squares, by iteration parity
-    __shared__ float cta_ss;          // this CTA's sum of squares, read by its cluster
+    // Cluster exchange: every CTA pushes its row sum of squares into slot
+    // [crank] of every peer (st.async), counted on the peer's mbarrier.
+    __shared__ __align__(8) uint64_t xbar[2];
+    __shared__ float xslot[2][16];
+    if constexpr (CLUSTER) {
+        if (tid == 0) {
+            mbar_init(smem_addr(&xbar[0]), 1);
+            mbar_init(smem_addr(&xbar[1]), 1);
+            fence_mbar_init_cluster();
+        }
+        // Matched by the wait before the first push: the peers' mbarriers
+        // are initialised by then (the row's loads hide this barrier).
+        cluster_arrive_relaxed();
+    }
 
     float g_given = 0.0f;
     if constexpr (QMODE == kQuantGiven)
@@ -88,7 +106,7 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT))
         uint4 gv[kEarlyGamma ? VPT : 1];
         float ss = 0.0f;
 
-        // ---- rank sum (fixed order 0..N-1), residual add, store new residual.
+        // ---- rank sum (fixed order 0..N-1) and residual add.
         // All loads of a group of G vectors are issued before any of them is
         // used or any store is made, so their memory latencies overlap.
         constexpr int G = (NR >= 16 || VPT == 1 || VPT >= 8) ? 1 : 2;
@@ -124,7 +142,7 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT))
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         ss = fmaf(h[j][e], h[j][e], ss);
-                    if (a.out_residual)
+                    if (!CLUSTER && a.out_residual)
                         st_v4(a.out_residual + rowv + v, pack8(h[j]));
                 } else {
 #pragma unroll
@@ -142,18 +160,22 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT))
         __syncthreads();
         float tot = warp_sum(lane < nwarps ? warp_ss[buf][lane] : 0.0f);
         if constexpr (CLUSTER) {
-            // The peers' "done reading" arrive of the previous row must be
-            // matched before this CTA's slot is overwritten.
-            if (it > 0)
-                cluster_wait_acquire();
-            if (tid == 0)
-                cta_ss = tot;
-            cluster_arrive_release();
+            // The previous arrive (set-up, or "done with the last row") must
+            // be matched before pushing into the peers' slots.
             cluster_wait_acquire();
-            tot = warp_sum(lane < split ? ld_dsmem(&cta_ss, static_cast<uint32_t>(lane)) : 0.0f);
-            // Done reading the peers' slots; the matching wait comes only
-            // before the next overwrite (or exit), off the critical path.
-            cluster_arrive_release();
+            const int b = it & 1;
+            const uint32_t parity = static_cast<uint32_t>(it >> 1) & 1u;
+            const uint32_t bar = smem_addr(&xbar[b]);
+            if (tid == 0)
+                mbar_arrive_expect_tx(bar, 4u * static_cast<uint32_t>(split));
+            if (tid < split)
+                st_async_f32(cluster_addr(smem_addr(&xslot[b][crank]), static_cast<uint32_t>(tid)), tot,
+                             cluster_addr(bar, static_cast<uint32_t>(tid)));
+            if (!mbar_wait_parity_bounded(bar, parity, 200ull * 1000 * 1000) && a.err && tid == 0)
+                atomicOr(a.err, 1u);
+            // fixed order over the cluster ranks, identical in every CTA
+            tot = warp_sum(lane < split ? xslot[b][lane] : 0.0f);
+            cluster_arrive_relaxed();
         }
         const float rinv = rsqrtf(fmaf(tot, a.inv_d, a.eps));
 
@@ -174,6 +196,11 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT))
                 for (int e = 0; e < 8; ++e)
                     y[e] = h[j][e] * rinv * gm[e];
                 const uint4 yb = pack8(y);
+                // The cluster form stores the residual only now: a store
+                // issued before the exchange would delay it (measured); the
+                // bandwidth form gains from issuing it early.
+                if (CLUSTER && a.out_residual)
+                    st_v4(a.out_residual + rowv + v, pack8(h[j]));
                 if (a.out_norm)
                     st_v4(a.out_norm + rowv + v, yb);
                 unpack8(yb, yq);  // the emitted bf16 values, as fp32
@@ -224,9 +251,8 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT))
         }
     }
     if constexpr (CLUSTER) {
-        // No CTA may leave while a peer could still read its shared memory.
-        if (it > 0)
-            cluster_wait_acquire();
+        // No CTA leaves before every peer is done with this cluster's rows.
+        cluster_wait_acquire();
     }
 }
 

@@ -171,3 +171,21 @@ def test_init_is_idempotent():
     tp = lib()
     tp.tpar_init(torch.cuda.current_device())
     tp.tpar_init(torch.cuda.current_device())
+
+
+def test_cluster_exchange_never_times_out():
+    """Every cluster-split call completes its exchange: the device error word
+    (set when a bounded wait expires) stays clear across plans and row
+    striding."""
+    tp = lib()
+    dev = torch.cuda.current_device()
+    tp.tpar_device_error(dev)  # clear
+    w = synth.DECODE_70B.with_(T=12)
+    d = to_device(synth.make_inputs(w))
+    for split in (2, 4, 8, 16):
+        for rows in (12, 5, 1):
+            plan = tp.TparPlan(kernel=1, split=split, threads=-(-(-(-1024 // split)) // 32) * 32,
+                               vec_per_thread=1, grid_rows=rows)
+            tp.fused_rmsnorm(d["partials"], d["residual"], d["gamma"], w.eps, plan=plan)
+    torch.cuda.synchronize()
+    assert tp.tpar_device_error(dev) == 0
