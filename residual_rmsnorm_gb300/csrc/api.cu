@@ -330,17 +330,20 @@ tpar_status plan_impl(int64_t T, int64_t d, int n_ranks, int sm_count, uint32_t 
     int split = 1;
     if (!(flags & TPAR_FORCE_ROW)) {
         // Latency path. A CTA that owns a whole row pulls (N+1)*2d bytes
-        // through one SM; when that is large and the rows are few, split each
-        // row over a thread-block cluster so that every CTA pulls about
-        // kClusterSliceBytes (measured on GB300: one 147 KB row per CTA costs
-        // ~0.6 us more than 8 CTAs of 18 KB plus the cluster exchange, while
-        // for rows <= ~80 KB or T > 16 the exchange costs more than it saves).
-        constexpr int64_t kClusterRowBytes = 96 * 1024;
-        constexpr int64_t kClusterSliceBytes = 16 * 1024;
-        constexpr int64_t kClusterMaxRows = 16;
+        // through one SM (~120 GB/s per SM measured on GB300); the cluster
+        // exchange of partial sums costs ~0.45 us. Split rows over a cluster
+        // when the rows are few and long enough to win that back: at T <= 2
+        // rows of >= 48 KB into ~8 KB slices, at T <= 32 rows of >= 96 KB
+        // into ~16 KB slices (measured: N=8, d=8192, T=8 runs 2.68 us split
+        // 8 ways vs 3.37 us whole; d=4096 at T=8 stays whole, 2.50 us).
         const int64_t row_bytes = static_cast<int64_t>(n_ranks + 1) * d * 2;
-        if (T <= kClusterMaxRows && row_bytes >= kClusterRowBytes) {
-            while (split < 16 && row_bytes / (2 * split) >= kClusterSliceBytes && T * (2 * split) <= sm_count &&
+        int64_t slice_target = 0;
+        if (T <= 2 && row_bytes >= 48 * 1024)
+            slice_target = 8 * 1024;
+        else if (T <= 32 && row_bytes >= 96 * 1024)
+            slice_target = 16 * 1024;
+        if (slice_target > 0) {
+            while (split < 16 && row_bytes / (2 * split) >= slice_target && T * (2 * split) <= 2 * sm_count &&
                    nvec / (2 * split) >= 32)
                 split *= 2;
         }

@@ -187,24 +187,24 @@ def test_planner_covers_every_row(tp, sm):
                 s += s & 1
                 assert p.threads * p.vec_per_thread >= s
                 assert s >= 32 or p.split == 2
-                assert T * 2 <= sm and T <= 16  # rows are split only while SMs would idle
+                assert T <= 32 and T * p.split <= 2 * sm  # rows are split only when few
             else:
                 assert p.split == 1 and p.threads * p.vec_per_thread >= nvec
             assert 1 <= p.grid_rows <= min(T, 65535)
 
 
 def test_planner_choices_for_the_pages_shapes(tp):
-    # decode, 73 KB rows (N=8, d=4096): one CTA of 512 threads per row
+    # decode, 73 KB rows (N=8, d=4096): whole rows at T=8, 8-way split at T=1
     p = tp.tpar_plan_launch(8, 4096, 8, 152)
     assert (p.kernel, p.split, p.threads, p.vec_per_thread) == (0, 1, 512, 1)
-    # decode, 147 KB rows (N=8, d=8192), few tokens: rows split over clusters
+    assert tp.tpar_plan_launch(1, 4096, 8, 152).split == 8
+    # decode, 147 KB rows (N=8, d=8192): rows split over clusters up to T=32
     p = tp.tpar_plan_launch(1, 8192, 8, 152)
-    assert (p.kernel, p.split, p.threads) == (1, 8, 128)
-    p = tp.tpar_plan_launch(8, 8192, 8, 152)
-    assert (p.kernel, p.split) == (1, 8)
-    p = tp.tpar_plan_launch(16, 8192, 8, 152)
-    assert (p.kernel, p.split) == (1, 8)
-    assert tp.tpar_plan_launch(32, 8192, 8, 152).kernel == 0
+    assert (p.kernel, p.split, p.threads) == (1, 16, 64)
+    for T in (4, 8, 16, 32):
+        p = tp.tpar_plan_launch(T, 8192, 8, 152)
+        assert (p.kernel, p.split, p.threads) == (1, 8, 128), T
+    assert tp.tpar_plan_launch(64, 8192, 8, 152).kernel == 0
     # prefill: one CTA of 1024 threads per row
     p = tp.tpar_plan_launch(4096, 8192, 8, 152)
     assert (p.kernel, p.split, p.threads, p.vec_per_thread) == (0, 1, 1024, 1)
