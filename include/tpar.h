@@ -68,12 +68,15 @@ typedef void* tpar_stream_t;
 #define TPAR_NO_PDL 0x8u        /* plain stream ordering, no PDL attribute    */
 #define TPAR_DRY_RUN 0x10u      /* check the arguments (and a given plan) on
                                    the host, launch nothing, touch no GPU     */
+#define TPAR_FORCE_STREAM 0x20u /* persistent TMA-fed kernel (bandwidth path) */
 
-/* Launch plan of the fused kernel. kernel: 0 = row kernel, 1 = cluster-split
- * rows. split: CTAs per row (the cluster size, 1 for the row kernel).
- * threads: threads per CTA. vec_per_thread: 16-byte vectors of a row each
- * thread owns (1, 2, 4 or 8). grid_rows: CTAs (clusters) along the rows; each
- * strides over rows t = blockIdx.y, blockIdx.y + grid_rows, ... */
+/* Launch plan of the fused kernel. kernel: 0 = row kernel (one CTA per row),
+ * 1 = cluster-split rows, 2 = persistent TMA-fed stream kernel. split: CTAs
+ * per row (the cluster size; 1 otherwise). threads: threads per CTA (for the
+ * stream kernel: consumer threads, plus one producer warp). vec_per_thread:
+ * 16-byte vectors of a row each (consumer) thread owns (1, 2, 4 or 8).
+ * grid_rows: CTAs (clusters) along the rows; each strides over rows
+ * t = b, b + grid_rows, ... */
 typedef struct tpar_plan {
     int32_t kernel;
     int32_t split;
@@ -135,7 +138,8 @@ tpar_status tpar_fused_rmsnorm(const void* const* partials, int n_ranks, const v
  *          on the device); quantisation happens in the same single pass, and
  *          out_norm may be NULL. A g that is not positive and finite gives
  *          all-zero scales and signed-zero codes.
- *          TPAR_FORCE_ROW / TPAR_FORCE_CLUSTER: pick the kernel; TPAR_NO_PDL.
+ *          TPAR_FORCE_ROW / TPAR_FORCE_CLUSTER / TPAR_FORCE_STREAM: pick the
+ *          kernel (at most one); TPAR_NO_PDL.
  *   plan   NULL for the automatic plan, else a complete plan to launch
  *          (validated: TPAR_ERR_INVALID_ARG if it does not cover a row).
  *   workspace  NULL for the device workspace, else a caller-owned device
@@ -184,7 +188,7 @@ tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* co
 /*
  * tpar_plan_launch -- the launch plan the fused entry points would use for
  * (T, d, n_ranks) on a GPU with sm_count SMs, honouring TPAR_FORCE_ROW /
- * TPAR_FORCE_CLUSTER. Host-only: touches no GPU.
+ * TPAR_FORCE_CLUSTER / TPAR_FORCE_STREAM. Host-only: touches no GPU.
  */
 tpar_status tpar_plan_launch(int64_t T, int64_t d, int n_ranks, int sm_count, uint32_t flags,
                              tpar_plan* out);

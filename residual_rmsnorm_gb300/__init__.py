@@ -13,6 +13,7 @@ from __future__ import annotations
 from ._abi import (  # noqa: F401
     TPAR_FORCE_CLUSTER,
     TPAR_FORCE_ROW,
+    TPAR_FORCE_STREAM,
     TPAR_GSCALE_GIVEN,
     TPAR_MAX_HIDDEN,
     TPAR_MAX_RANKS,

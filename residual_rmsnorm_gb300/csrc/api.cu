@@ -12,6 +12,7 @@
 
 #include "dispatch.h"
 #include "kernels.cuh"
+#include "stream.cuh"
 
 namespace {
 
@@ -182,6 +183,22 @@ cudaError_t launch(const void* fn, dim3 grid, dim3 block, void* arg, cudaStream_
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+int forced_kernels(uint32_t flags)
+{
+    return ((flags & TPAR_FORCE_ROW) != 0) + ((flags & TPAR_FORCE_CLUSTER) != 0) +
+           ((flags & TPAR_FORCE_STREAM) != 0);
+}
+
+// Ring depth of the stream kernel for rows of row_bytes: ~192 KB of shared
+// memory in flight per SM, at least 2 stages.
+int stream_stages(int64_t row_bytes)
+{
+    int64_t s = (192 * 1024) / row_bytes;
+    if (s > 48)
+        s = 48;
+    return static_cast<int>(s < 2 ? 2 : s);
+}
+
 int pow2_at_least(int64_t n)
 {
     int p = 1;
@@ -201,6 +218,17 @@ int slice_for(int nvec, int split)
 tpar_status check_plan(const tpar_plan& p, int64_t d, int n_ranks)
 {
     const int nvec = static_cast<int>(d / 8);
+    if (p.kernel == 2) {
+        // stream kernel: `threads` consumer threads + one producer warp
+        const int v = p.vec_per_thread;
+        if (p.split != 1 || p.threads < 32 || p.threads > 512 || p.threads % 32 != 0)
+            return TPAR_ERR_INVALID_ARG;
+        if (v != 1 && v != 2 && v != 4 && v != 8)
+            return TPAR_ERR_INVALID_ARG;
+        if (static_cast<int64_t>(p.threads) * v < nvec || p.grid_rows < 1 || p.grid_rows > kMaxGridY)
+            return TPAR_ERR_INVALID_ARG;
+        return TPAR_OK;
+    }
     if (p.kernel != 0 && p.kernel != 1)
         return TPAR_ERR_INVALID_ARG;
     if (p.kernel == 0 && p.split != 1)
@@ -253,7 +281,7 @@ tpar_status validate(const Call& c, bool unfused)
         return TPAR_ERR_INVALID_ARG;
     if (!std::isfinite(c.eps) || c.eps < 0.0f)
         return TPAR_ERR_INVALID_ARG;
-    if ((c.flags & TPAR_FORCE_ROW) && (c.flags & TPAR_FORCE_CLUSTER))
+    if (forced_kernels(c.flags) > 1)
         return TPAR_ERR_INVALID_ARG;
     // An empty batch is a no-op: its tensors may be NULL (empty allocations).
     if (c.T == 0)
@@ -324,10 +352,23 @@ tpar_status plan_impl(int64_t T, int64_t d, int n_ranks, int sm_count, uint32_t 
         return TPAR_ERR_INVALID_ARG;
     if (d > TPAR_MAX_HIDDEN)
         return TPAR_ERR_UNSUPPORTED;
-    if ((flags & TPAR_FORCE_ROW) && (flags & TPAR_FORCE_CLUSTER))
+    if (forced_kernels(flags) > 1)
         return TPAR_ERR_INVALID_ARG;
     const int nvec = static_cast<int>(d / 8);
     int split = 1;
+    const bool stream_ok = d >= 2048;  // rows of >= 4 KB keep the TMA ring deep
+    if ((flags & TPAR_FORCE_STREAM) ||
+        (!(flags & (TPAR_FORCE_ROW | TPAR_FORCE_CLUSTER)) && stream_ok && T >= 2 * static_cast<int64_t>(sm_count))) {
+        // Bandwidth path: one persistent CTA per SM, fed by TMA bulk copies.
+        tpar_plan p;
+        p.kernel = 2;
+        p.split = 1;
+        p.threads = static_cast<int>(std::min<int64_t>(512, ceil_div(nvec, 32) * 32));
+        p.vec_per_thread = pow2_at_least(ceil_div(nvec, p.threads));
+        p.grid_rows = std::max<int64_t>(1, std::min<int64_t>(T, sm_count));
+        *out = p;
+        return check_plan(p, d, n_ranks);
+    }
     if (!(flags & TPAR_FORCE_ROW)) {
         // Latency path. A CTA that owns a whole row pulls (N+1)*2d bytes
         // through one SM (~120 GB/s per SM measured on GB300); the cluster
@@ -393,8 +434,41 @@ const void* fused_kernel(int qmode, int nr, int vpt, bool cluster)
     }
 }
 
+tpar_status launch_stream(const FusedArgs& a, int qmode, const tpar_plan& p, cudaStream_t stream, bool pdl)
+{
+    const int nr = tpar::rank_bound(a.n_ranks);
+    const void* fn = tpar::stream_kernel_for(qmode, nr, p.vec_per_thread);
+    if (!fn)
+        return TPAR_ERR_UNSUPPORTED;
+    const int64_t row_bytes = static_cast<int64_t>(a.nvec) * 16;
+    tpar::StreamArgs sa;
+    sa.f = a;
+    sa.f.err = device_error_word();
+    sa.stages = stream_stages(row_bytes);
+    sa.consumers = p.threads;
+    const size_t smem = static_cast<size_t>(sa.stages) * row_bytes + 16u * sa.stages;
+    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
+        return TPAR_ERR_CUDA;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(static_cast<unsigned>(p.grid_rows));
+    cfg.blockDim = dim3(static_cast<unsigned>(p.threads + 32));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at.val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = pdl ? 1 : 0;
+    void* args[1] = {&sa};
+    return cudaLaunchKernelExC(&cfg, fn, args) == cudaSuccess ? TPAR_OK : TPAR_ERR_CUDA;
+}
+
 tpar_status launch_fused(const FusedArgs& a, int qmode, const tpar_plan& p, cudaStream_t stream, bool pdl)
 {
+    if (p.kernel == 2)
+        return launch_stream(a, qmode, p, stream, pdl);
     const int nr = tpar::rank_bound(a.n_ranks);
     const void* fn = fused_kernel(qmode, nr, p.vec_per_thread, p.kernel == 1);
     if (!fn)

@@ -13,6 +13,10 @@ const void* fused_kernel_q0(int nr, int vpt, bool cluster);
 const void* fused_kernel_q1(int nr, int vpt, bool cluster);
 const void* fused_kernel_q2(int nr, int vpt, bool cluster);
 
+// TMA-fed bandwidth kernel (stream.cuh) for quantisation mode q, rank bound
+// nr and vpt vectors per consumer thread.
+const void* stream_kernel_for(int qmode, int nr, int vpt);
+
 const void* reduce_kernel_for(int nr);
 const void* residual_add_kernel_ptr();
 const void* quantize_kernel_for(bool dynamic);

@@ -50,6 +50,74 @@ struct FusedArgs {
     float inv_d;
 };
 
+// Normalise one 16-byte vector of a row (global vector index gv) and emit
+// its outputs: out_norm, and either the NVFP4 codes and scale (given global
+// scale; a 16-element block is this lane's vector and its neighbour's, so
+// the lane joins the shuffle even when `valid` is false) or the running
+// |out_norm| maximum (dynamic scale).
+template <int QMODE>
+__device__ __forceinline__ void emit_vector(const FusedArgs& a, bool valid, int64_t gv, const float h[8],
+                                            const uint4& gamma8, float rinv, float g_given, float& amax_local)
+{
+    float yq[8];
+    if (valid) {
+        float gm[8];
+        unpack8(gamma8, gm);
+        float y[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            y[e] = h[e] * rinv * gm[e];
+        const uint4 yb = pack8(y);
+        if (a.out_norm)
+            st_v4(a.out_norm + gv, yb);
+        unpack8(yb, yq);  // the emitted bf16 values, as fp32
+    } else {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            yq[e] = 0.0f;
+    }
+    if constexpr (QMODE == kQuantAmax) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            amax_local = fmaxf(amax_local, fabsf(yq[e]));
+    }
+    if constexpr (QMODE == kQuantGiven) {
+        float bmax = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            bmax = fmaxf(bmax, fabsf(yq[e]));
+        bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));
+        if (valid) {
+            uint32_t sbyte;
+            const float inv = nvfp4_block_scale(g_given, bmax, sbyte);
+            float q[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                q[e] = __fmul_rn(yq[e], inv);
+            st_u32(a.codes + gv, e2m1x8_from_f32(q));
+            if ((gv & 1) == 0)
+                st_u8(a.scales + gv / 2, sbyte);
+        }
+    }
+}
+
+// CTA-wide max of a non-negative value folded into the device amax with one
+// atomic (same-address atomics serialise in L2, so one per CTA, not per warp).
+// Called by all `nthreads` threads of a block-wide (or named) barrier group.
+__device__ __forceinline__ void cta_amax_atomic(float v, uint32_t* amax_bits, float* scratch32, int warp,
+                                                int lane, int nwarps)
+{
+    const float m = warp_max(v);
+    if (lane == 0)
+        scratch32[warp] = m;
+    __syncthreads();
+    if (warp == 0) {
+        const float c = warp_max(lane < nwarps ? scratch32[lane] : 0.0f);
+        if (lane == 0 && c > 0.0f)
+            atomicMax(amax_bits, __float_as_uint(c));  // |y| >= 0 orders like its bits
+    }
+}
+
 // Largest CTA a fused-kernel instantiation is built for: wide rows (VPT >= 2),
 // many ranks and the cluster exchange need more than the 64 registers a
 // 1024-thread CTA allows.
@@ -184,71 +252,25 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT, CLUSTER))
         for (int j = 0; j < VPT; ++j) {
             const int v = vbeg + tid + j * static_cast<int>(blockDim.x);
             const bool valid = v < vend;
-            float yq[8];
+            uint4 gm = make_uint4(0u, 0u, 0u, 0u);
             if (valid) {
-                float gm[8];
                 if constexpr (kEarlyGamma)
-                    unpack8(gv[kEarlyGamma ? j : 0], gm);
+                    gm = gv[kEarlyGamma ? j : 0];
                 else
-                    unpack8(ld_reuse(a.gamma + v), gm);
-                float y[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    y[e] = h[j][e] * rinv * gm[e];
-                const uint4 yb = pack8(y);
+                    gm = ld_reuse(a.gamma + v);
                 // The cluster form stores the residual only now: a store
                 // issued before the exchange would delay it (measured); the
                 // bandwidth form gains from issuing it early.
                 if (CLUSTER && a.out_residual)
                     st_v4(a.out_residual + rowv + v, pack8(h[j]));
-                if (a.out_norm)
-                    st_v4(a.out_norm + rowv + v, yb);
-                unpack8(yb, yq);  // the emitted bf16 values, as fp32
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    yq[e] = 0.0f;
             }
-            if constexpr (QMODE == kQuantAmax) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    amax_local = fmaxf(amax_local, fabsf(yq[e]));
-            }
-            if constexpr (QMODE == kQuantGiven) {
-                // 16-element block = this lane's vector + its neighbour's.
-                float bmax = 0.0f;
-#pragma unroll
-                for (int e = 0; e < 8; ++e)
-                    bmax = fmaxf(bmax, fabsf(yq[e]));
-                bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));
-                if (valid) {
-                    uint32_t sbyte;
-                    const float inv = nvfp4_block_scale(g_given, bmax, sbyte);
-                    float q[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e)
-                        q[e] = __fmul_rn(yq[e], inv);
-                    st_u32(a.codes + rowv + v, e2m1x8_from_f32(q));
-                    if ((v & 1) == 0)
-                        st_u8(a.scales + (rowv + v) / 2, sbyte);
-                }
-            }
+            emit_vector<QMODE>(a, valid, rowv + v, h[j], gm, rinv, g_given, amax_local);
         }
     }
 
     if constexpr (QMODE == kQuantAmax) {
-        // One atomic per CTA: same-address atomics serialise in L2, so a
-        // per-warp atomic over thousands of CTAs would dominate the kernel.
         __shared__ float warp_max_sh[32];
-        const float m = warp_max(amax_local);
-        if (lane == 0)
-            warp_max_sh[warp] = m;
-        __syncthreads();
-        if (warp == 0) {
-            const float c = warp_max(lane < nwarps ? warp_max_sh[lane] : 0.0f);
-            if (lane == 0 && c > 0.0f)
-                atomicMax(a.amax_bits, __float_as_uint(c));  // |y| >= 0 orders like its bits
-        }
+        cta_amax_atomic(amax_local, a.amax_bits, warp_max_sh, warp, lane, nwarps);
     }
     if constexpr (CLUSTER) {
         // No CTA leaves before every peer is done with this cluster's rows.

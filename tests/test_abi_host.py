@@ -111,7 +111,8 @@ def test_dry_run_accepts_a_valid_call(tp):
     (dict(codes=BASE + 200 * MB, scales=BASE + 210 * MB), INVALID),
     (dict(d=4104, codes=BASE + 200 * MB, scales=BASE + 210 * MB, g=BASE + 220 * MB), INVALID),  # d % 16
     (dict(flags=0x10 | 0x1), INVALID),  # given scale without NVFP4 outputs
-    (dict(flags=0x10 | 0x2 | 0x4), INVALID),  # both kernels forced
+    (dict(flags=0x10 | 0x2 | 0x4), INVALID),  # two kernels forced
+    (dict(flags=0x10 | 0x2 | 0x20), INVALID),
     (dict(parts=[BASE + 8] + [BASE + r * 4 * MB for r in range(1, 8)]), MISALIGNED),
     (dict(residual=BASE + 64 * MB + 2), MISALIGNED),
     (dict(gamma=BASE + 96 * MB + 4), MISALIGNED),
@@ -148,9 +149,11 @@ def test_user_plan_is_checked(tp):
     P = tp.TparPlan
     good = P(kernel=0, split=1, threads=256, vec_per_thread=2, grid_rows=8)
     assert call(tp, plan=good) == OK
+    assert call(tp, plan=P(kernel=2, split=1, threads=256, vec_per_thread=2, grid_rows=3)) == OK
     for bad in (P(0, 2, 256, 2, 8), P(1, 1, 256, 2, 8), P(0, 1, 100, 2, 8), P(0, 1, 256, 3, 8),
                 P(0, 1, 128, 2, 8), P(0, 1, 1024, 4, 8), P(1, 4, 256, 4, 8), P(0, 1, 256, 2, 0),
-                P(1, 32, 32, 1, 8)):
+                P(1, 32, 32, 1, 8), P(2, 2, 256, 2, 8), P(2, 1, 1024, 1, 8), P(2, 1, 256, 1, 8),
+                P(2, 1, 512, 3, 8)):
         assert call(tp, plan=bad) == INVALID, bad.as_dict()
 
 
@@ -181,6 +184,10 @@ def test_planner_covers_every_row(tp, sm):
             p = tp.tpar_plan_launch(T, d, 8, sm)
             assert p.threads % 32 == 0 and 32 <= p.threads <= 1024
             assert p.vec_per_thread in (1, 2, 4, 8)
+            if p.kernel == 2:
+                assert p.split == 1 and p.threads <= 512 and p.threads * p.vec_per_thread >= nvec
+                assert p.grid_rows == min(T, sm) and T >= 2 * sm and d >= 2048
+                continue
             if p.kernel == 1:
                 assert 2 <= p.split <= 16
                 s = -(-nvec // p.split)
@@ -205,11 +212,15 @@ def test_planner_choices_for_the_pages_shapes(tp):
         p = tp.tpar_plan_launch(T, 8192, 8, 152)
         assert (p.kernel, p.split, p.threads) == (1, 8, 128), T
     assert tp.tpar_plan_launch(64, 8192, 8, 152).kernel == 0
-    # prefill: one CTA of 1024 threads per row
+    # prefill: the persistent TMA-fed kernel, one CTA per SM
     p = tp.tpar_plan_launch(4096, 8192, 8, 152)
-    assert (p.kernel, p.split, p.threads, p.vec_per_thread) == (0, 1, 1024, 1)
-    # more than 8 ranks: CTAs capped at 512 threads
-    p = tp.tpar_plan_launch(4096, 8192, 16, 152)
-    assert (p.threads, p.vec_per_thread) == (512, 2)
+    assert (p.kernel, p.split, p.threads, p.vec_per_thread, p.grid_rows) == (2, 1, 512, 2, 152)
+    assert tp.tpar_plan_launch(4096, 8192, 16, 152).kernel == 2
+    # short rows and mid-size batches: one CTA per row, capped at 512 threads for > 8 ranks
+    p = tp.tpar_plan_launch(200, 8192, 16, 152)
+    assert (p.kernel, p.threads, p.vec_per_thread) == (0, 512, 2)
+    assert tp.tpar_plan_launch(4096, 1024, 8, 152).kernel == 0
+    assert tp.tpar_plan_launch(4096, 8192, 8, 152, tp.TPAR_FORCE_ROW).kernel == 0
+    assert tp.tpar_plan_launch(8, 8192, 8, 152, tp.TPAR_FORCE_STREAM).kernel == 2
     assert tp.tpar_plan_launch(1, 8192, 8, 152, tp.TPAR_FORCE_ROW).kernel == 0
     assert tp.tpar_plan_launch(4096, 4096, 8, 152, tp.TPAR_FORCE_CLUSTER).kernel == 1

@@ -101,11 +101,11 @@ def test_ragged_shapes(n, T, d):
     check(out, ref, w.name)
 
 
-@pytest.mark.parametrize("flags", ["row", "cluster"])
+@pytest.mark.parametrize("flags", ["row", "cluster", "stream"])
 @pytest.mark.parametrize("T,d", [(1, 256), (8, 4096), (32, 8192), (100, 1024), (7, 8200)])
 def test_both_kernels(flags, T, d):
     tp = lib()
-    f = tp.TPAR_FORCE_ROW if flags == "row" else tp.TPAR_FORCE_CLUSTER
+    f = {"row": tp.TPAR_FORCE_ROW, "cluster": tp.TPAR_FORCE_CLUSTER, "stream": tp.TPAR_FORCE_STREAM}[flags]
     w = synth.Workload("paths", 8, T, d, 1e-5, 0.5, seed=T + d)
     _, out, ref = run_full(tp, w, flags=f)
     check(out, ref, f"{flags} T{T} d{d}")
@@ -120,6 +120,10 @@ def test_both_kernels(flags, T, d):
     dict(kernel=1, split=4, threads=128, vec_per_thread=2, grid_rows=64),
     dict(kernel=1, split=8, threads=128, vec_per_thread=1, grid_rows=1),
     dict(kernel=1, split=16, threads=64, vec_per_thread=1, grid_rows=33),
+    dict(kernel=2, split=1, threads=512, vec_per_thread=2, grid_rows=3),
+    dict(kernel=2, split=1, threads=256, vec_per_thread=4, grid_rows=67),
+    dict(kernel=2, split=1, threads=128, vec_per_thread=8, grid_rows=5),
+    dict(kernel=2, split=1, threads=512, vec_per_thread=4, grid_rows=1),
 ])
 def test_explicit_plans_with_row_striding(plan):
     """Every legal plan, including grids smaller than T (rows strided)."""
@@ -173,3 +177,31 @@ def test_degenerate_rows():
     assert_close_to_ref(out["out_residual"], ref["h"], "degenerate h")
     assert_close_to_ref(out["out_norm"], ref["y"], "degenerate y")
     assert torch.all(out["out_norm"][0] == 0)
+
+
+@pytest.mark.parametrize("n,T,d,residual", [(8, 700, 8192, True), (16, 310, 4096, True), (1, 333, 2056, False),
+                                            (3, 64, 32768, True), (8, 5, 2048, True)])
+def test_stream_kernel_shapes(n, T, d, residual):
+    """The TMA-fed kernel on ragged shapes: ring wrap-around over many rows
+    per CTA, deep rings of short rows, 3-stage rings of 64 KB rows."""
+    tp = lib()
+    w = synth.Workload(f"stream N{n} T{T} d{d}", n, T, d, 1e-5, 0.5, seed=n + T + d)
+    _, out, ref = run_full(tp, w, residual=residual, flags=tp.TPAR_FORCE_STREAM)
+    check(out, ref, w.name)
+    assert tp.tpar_device_error(torch.cuda.current_device()) == 0
+
+
+def test_stream_kernel_in_place_and_nvfp4_given():
+    tp = lib()
+    w = synth.NVFP4.with_(T=400, d=4096)
+    inputs = synth.make_inputs(w)
+    dev = to_device(inputs)
+    res = dev["residual"].clone()
+    g = torch.tensor([0.03], dtype=torch.float32, device="cuda")
+    out = tp.fused_rmsnorm(dev["partials"], res, dev["gamma"], w.eps, out_residual=res, nvfp4=True,
+                           global_scale=g, flags=tp.TPAR_FORCE_STREAM)
+    torch.cuda.synchronize()
+    ref = oracle_rows(inputs, slice(None), w.eps)
+    assert_close_to_ref(res, ref["h"], "stream in-place residual")
+    assert_close_to_ref(out["out_norm"], ref["y"], "stream out_norm")
+    assert_nvfp4_bit_exact(out["out_norm"], out["codes"], out["scales"], 0.03, given=0.03, what="stream given")
