@@ -525,7 +525,7 @@ def profile_case(args):
     device = torch.device("cuda", 0)
     tp.tpar_init(0)
     base = {"prefill": synth.PREFILL, "decode8b": synth.DECODE_8B, "decode70b": synth.DECODE_70B,
-            "nvfp4": synth.NVFP4, "unfused": synth.PREFILL}[args.profile]
+            "nvfp4": synth.NVFP4, "unfused": synth.PREFILL, "stream": synth.PREFILL}[args.profile]
     w = base.with_(T=args.T) if args.T else base
     cs = CallSet(w, seed=0, device=device, nvfp4=w.nvfp4)
     st = torch.cuda.current_stream().cuda_stream
@@ -536,7 +536,7 @@ def profile_case(args):
                                     w.T, w.d, reduced.data_ptr(), cs.out_norm.data_ptr(),
                                     cs.out_residual.data_ptr(), 0, 0, 0, 0, st)
         else:
-            cs.call(tp, w, st)
+            cs.call(tp, w, st, flags=tp.TPAR_FORCE_STREAM if args.profile == "stream" else 0)
     torch.cuda.synchronize()
     print(f"profile case done: {w.name} T={w.T}, {args.calls} calls, "
           f"{fused_bytes(w.n_ranks, w.T, w.d, nvfp4=w.nvfp4)} algorithmic bytes per fused call")
@@ -552,7 +552,7 @@ def main(argv=None):
     ap.add_argument("--workload", choices=["decode8b"], default="decode8b")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--profile", choices=["prefill", "decode8b", "decode70b", "nvfp4", "unfused"],
+    ap.add_argument("--profile", choices=["prefill", "decode8b", "decode70b", "nvfp4", "unfused", "stream"],
                     help="run a few eager calls of one shape for an ncu capture, then exit")
     ap.add_argument("--T", type=int, default=0, help="token count for --profile")
     ap.add_argument("--calls", type=int, default=3, help="calls for --profile")

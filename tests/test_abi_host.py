@@ -186,8 +186,7 @@ def test_planner_covers_every_row(tp, sm):
             assert p.vec_per_thread in (1, 2, 4, 8)
             if p.kernel == 2:
                 assert p.split == 1 and p.threads <= 512 and p.threads * p.vec_per_thread >= nvec
-                assert p.grid_rows == min(T, sm) and T >= 2 * sm and d >= 2048
-                continue
+                raise AssertionError("the stream kernel is only planned on request")
             if p.kernel == 1:
                 assert 2 <= p.split <= 16
                 s = -(-nvec // p.split)
@@ -212,10 +211,11 @@ def test_planner_choices_for_the_pages_shapes(tp):
         p = tp.tpar_plan_launch(T, 8192, 8, 152)
         assert (p.kernel, p.split, p.threads) == (1, 8, 128), T
     assert tp.tpar_plan_launch(64, 8192, 8, 152).kernel == 0
-    # prefill: the persistent TMA-fed kernel, one CTA per SM
+    # prefill: one CTA of 1024 threads per row; the TMA-fed kernel on request
     p = tp.tpar_plan_launch(4096, 8192, 8, 152)
+    assert (p.kernel, p.split, p.threads, p.vec_per_thread) == (0, 1, 1024, 1)
+    p = tp.tpar_plan_launch(4096, 8192, 8, 152, tp.TPAR_FORCE_STREAM)
     assert (p.kernel, p.split, p.threads, p.vec_per_thread, p.grid_rows) == (2, 1, 512, 2, 152)
-    assert tp.tpar_plan_launch(4096, 8192, 16, 152).kernel == 2
     # short rows and mid-size batches: one CTA per row, capped at 512 threads for > 8 ranks
     p = tp.tpar_plan_launch(200, 8192, 16, 152)
     assert (p.kernel, p.threads, p.vec_per_thread) == (0, 512, 2)
