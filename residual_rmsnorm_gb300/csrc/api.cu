@@ -12,6 +12,7 @@
 
 #include "dispatch.h"
 #include "kernels.cuh"
+#include "nvfp4_small.cuh"
 #include "stream.cuh"
 
 namespace {
@@ -536,6 +537,55 @@ FusedArgs fused_args(const Call& c)
     return a;
 }
 
+// Shape of the single-launch dynamic-NVFP4 path: one cluster of K CTAs, each
+// owning `slice` vectors (a multiple of 32) of every row, at most 4 items of
+// 16 bytes per thread. Returns false when the tensor does not fit one cluster.
+// T <= kSmallNvfp4Rows: measured faster than phase A + phase B up to there.
+constexpr int64_t kSmallNvfp4Rows = 32;
+
+bool small_nvfp4_shape(int64_t T, int64_t d, int* K, int* slice, int* threads, int* ipt)
+{
+    const int64_t nvec = d / 8;
+    if (T < 1 || T > kSmallNvfp4Rows || T > tpar::kSmallMaxRows)
+        return false;
+    for (int k = 16; k >= 2; k /= 2) {
+        if (nvec % (static_cast<int64_t>(k) * 32) != 0)
+            continue;
+        const int64_t sl = nvec / k;
+        const int64_t items = T * sl;
+        if (items > 4 * 512)
+            return false;
+        int v = 1;
+        while (v < 4 && ceil_div(items, v) > 512)
+            v *= 2;
+        *K = k;
+        *slice = static_cast<int>(sl);
+        *ipt = v;
+        *threads = static_cast<int>(ceil_div(ceil_div(items, v), 32) * 32);
+        return true;
+    }
+    return false;
+}
+
+tpar_status launch_small_nvfp4(const FusedArgs& a, float* gscale, int K, int slice, int threads, int ipt,
+                               cudaStream_t stream, bool pdl)
+{
+    const void* fn = tpar::small_kernel_for(tpar::rank_bound(a.n_ranks), ipt);
+    if (!fn)
+        return TPAR_ERR_UNSUPPORTED;
+    if (K > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        return TPAR_ERR_CUDA;
+    tpar::SmallArgs sa;
+    sa.f = a;
+    sa.f.err = device_error_word();
+    sa.gscale = gscale;
+    sa.slice = slice;
+    return launch(fn, dim3(static_cast<unsigned>(K)), dim3(static_cast<unsigned>(threads)), &sa, stream, K, pdl) ==
+                   cudaSuccess
+               ? TPAR_OK
+               : TPAR_ERR_CUDA;
+}
+
 tpar_status fused_impl(const Call& c, const tpar_plan* user_plan, void* user_ws, cudaStream_t stream)
 {
     tpar_status st = validate(c, false);
@@ -565,6 +615,13 @@ tpar_status fused_impl(const Call& c, const tpar_plan* user_plan, void* user_ws,
         return launch_fused(a, tpar::kQuantNone, p, stream, pdl);
     if (given)
         return launch_fused(a, tpar::kQuantGiven, p, stream, pdl);
+    // Dynamic global scale, few tokens: one cluster owns the whole tensor and
+    // exchanges the amax on chip (one launch, no workspace).
+    int K = 0, slice = 0, threads = 0, ipt = 0;
+    if (!user_plan && forced_kernels(c.flags) == 0 && small_nvfp4_shape(c.T, c.d, &K, &slice, &threads, &ipt)) {
+        a.slice = slice;
+        return launch_small_nvfp4(a, c.gscale, K, slice, threads, ipt, stream, pdl);
+    }
     // Dynamic global scale: phase A (the fused pass, folding |out_norm| into
     // the device amax), then phase B (quantise out_norm, publish g, reset).
     uint32_t* ws = nullptr;

@@ -17,6 +17,10 @@ const void* fused_kernel_q2(int nr, int vpt, bool cluster);
 // nr and vpt vectors per consumer thread.
 const void* stream_kernel_for(int qmode, int nr, int vpt);
 
+// Single-launch dynamic-scale NVFP4 kernel (nvfp4_small.cuh) for rank bound
+// nr and ipt items per thread (1, 2, 4).
+const void* small_kernel_for(int nr, int ipt);
+
 const void* reduce_kernel_for(int nr);
 const void* residual_add_kernel_ptr();
 const void* quantize_kernel_for(bool dynamic);

@@ -1,0 +1,221 @@
+// nvfp4_small.cuh -- single-launch fused epilogue with a dynamic NVFP4
+// global scale, for a few decode tokens.
+//
+// The dynamic scale g = amax(|out_norm|) / (6 * 448) depends on every element
+// of the tensor, so in general it needs two passes (phase A + phase B). When
+// the whole [T, d] tensor fits one thread-block cluster, one launch suffices:
+// CTA k of the cluster owns the vector slice [k*slice, (k+1)*slice) of every
+// row, and the cluster
+//   1. sums the ranks and the residual of all its items (fp32 registers),
+//   2. exchanges each row's partial sum of squares with every peer (st.async
+//      into the peers' shared memory, counted on an mbarrier) and normalises,
+//   3. exchanges its local amax of the emitted bf16 values the same way,
+//   4. quantises its items from registers with the cluster-wide g.
+// No re-read of out_norm, no workspace, no second launch. The arithmetic is
+// the same as the two-pass path ("Deep Dive: AllReduce and AllReduce Fusion
+// in TensorRT-LLM", 6.3 and 6.5): results are bit-identical to it.
+#pragma once
+
+#include "kernels.cuh"
+
+namespace tpar {
+
+constexpr int kSmallMaxRanks = 16;  // cluster size bound
+constexpr int kSmallMaxRows = 32;
+
+struct SmallArgs {
+    FusedArgs f;       // inputs, outputs (out_norm may be null), T, nvec, eps
+    float* gscale;     // output: g
+    int slice;         // vectors per CTA (a multiple of 32); slice * gridDim.x == nvec
+};
+
+template <int NR, int IPT>
+__global__ void __launch_bounds__(512) nvfp4_small_kernel(const __grid_constant__ SmallArgs sa)
+{
+    const FusedArgs& a = sa.f;
+    pdl_wait();
+    pdl_launch_dependents();
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int B = blockDim.x;
+    const int nwarps = B >> 5;
+    const int K = static_cast<int>(gridDim.x);
+    const int k = static_cast<int>(cluster_ctarank());
+    const int slice = sa.slice;
+    const int T = static_cast<int>(a.T);
+    const int items = T * slice;
+    const int vbeg = k * slice;
+
+    __shared__ __align__(8) uint64_t xbar[2];          // [0] row sums, [1] amax
+    __shared__ float xrow[kSmallMaxRanks][kSmallMaxRows];  // [peer][row]
+    __shared__ float xmax[kSmallMaxRanks];             // [peer]
+    __shared__ float wsum[IPT][16];                    // [item group][warp]
+    __shared__ float rinv_sh[kSmallMaxRows];
+    __shared__ float wmax[16];
+
+    if (tid == 0) {
+        mbar_init(smem_addr(&xbar[0]), 1);
+        mbar_init(smem_addr(&xbar[1]), 1);
+        fence_mbar_init_cluster();
+    }
+    cluster_arrive_relaxed();  // matched before the first push
+
+    // ---- 1. rank sum + residual for this thread's items (all loads first)
+    float h[IPT][8];
+    uint4 gm[IPT];
+    float ss[IPT];
+    constexpr int G = (NR >= 16 || IPT == 1) ? 1 : 2;
+#pragma unroll
+    for (int g0 = 0; g0 < IPT; g0 += G) {
+        uint4 x[G][NR];
+        uint4 rv[G];
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+            const int i = tid + (g0 + gg) * B;
+            if (i < items) {
+                const int64_t gv = static_cast<int64_t>(i / slice) * a.nvec + vbeg + i % slice;
+#pragma unroll
+                for (int r = 0; r < NR; ++r)
+                    if (r < a.n_ranks)
+                        x[gg][r] = ld_stream(a.partials[r] + gv);
+                rv[gg] = a.residual ? ld_coherent(a.residual + gv) : make_uint4(0u, 0u, 0u, 0u);
+                gm[g0 + gg] = ld_reuse(a.gamma + vbeg + i % slice);
+            }
+        }
+#pragma unroll
+        for (int gg = 0; gg < G; ++gg) {
+            const int j = g0 + gg;
+            const int i = tid + j * B;
+            ss[j] = 0.0f;
+            if (i < items) {
+                unpack8(x[gg][0], h[j]);
+#pragma unroll
+                for (int r = 1; r < NR; ++r)
+                    if (r < a.n_ranks)
+                        add8(x[gg][r], h[j]);
+                if (a.residual)
+                    add8(rv[gg], h[j]);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    ss[j] = fmaf(h[j][e], h[j][e], ss[j]);
+            }
+        }
+    }
+
+    // ---- per-row CTA partial sums. slice % 32 == 0, so each warp's 32 items
+    // of one item group lie in one row.
+#pragma unroll
+    for (int j = 0; j < IPT; ++j) {
+        const float s = warp_sum(ss[j]);
+        if (lane == 0)
+            wsum[j][warp] = s;
+    }
+    __syncthreads();
+    float row_part = 0.0f;
+    if (tid < T) {
+        for (int i0 = tid * slice; i0 < (tid + 1) * slice; i0 += 32)
+            row_part += wsum[i0 / B][(i0 % B) >> 5];  // fixed order over the row's warps
+    }
+
+    // ---- 2. exchange row partials with every peer; normalise
+    cluster_wait_acquire();  // the peers' mbarriers are initialised
+    const uint32_t bar0 = smem_addr(&xbar[0]);
+    if (tid == 0)
+        mbar_arrive_expect_tx(bar0, 4u * static_cast<uint32_t>(K * T));
+    if (tid < T) {
+        for (int p = 0; p < K; ++p)
+            st_async_f32(cluster_addr(smem_addr(&xrow[k][tid]), static_cast<uint32_t>(p)), row_part,
+                         cluster_addr(bar0, static_cast<uint32_t>(p)));
+    }
+    if (!mbar_wait_parity_bounded(bar0, 0u, 200ull * 1000 * 1000) && a.err && tid == 0)
+        atomicOr(a.err, 4u);
+    if (tid < T) {
+        float tot = 0.0f;
+        for (int p = 0; p < K; ++p)
+            tot += xrow[p][tid];  // fixed order over the cluster: identical in every CTA
+        rinv_sh[tid] = rsqrtf(fmaf(tot, a.inv_d, a.eps));
+    }
+    __syncthreads();
+
+    float amax_local = 0.0f;
+#pragma unroll
+    for (int j = 0; j < IPT; ++j) {
+        const int i = tid + j * B;
+        if (i < items) {
+            const int64_t gv = static_cast<int64_t>(i / slice) * a.nvec + vbeg + i % slice;
+            const float rinv = rinv_sh[i / slice];
+            float gmf[8], y[8];
+            unpack8(gm[j], gmf);
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                y[e] = h[j][e] * rinv * gmf[e];
+            const uint4 yb = pack8(y);
+            if (a.out_residual)
+                st_v4(a.out_residual + gv, pack8(h[j]));
+            if (a.out_norm)
+                st_v4(a.out_norm + gv, yb);
+            unpack8(yb, h[j]);  // h now holds the emitted bf16 values
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                amax_local = fmaxf(amax_local, fabsf(h[j][e]));
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                h[j][e] = 0.0f;
+        }
+    }
+
+    // ---- 3. cluster-wide amax of |out_norm|, then g = amax / 2688
+    {
+        const float m = warp_max(amax_local);
+        if (lane == 0)
+            wmax[warp] = m;
+    }
+    __syncthreads();
+    const uint32_t bar1 = smem_addr(&xbar[1]);
+    if (warp == 0) {
+        const float cm = warp_max(lane < nwarps ? wmax[lane] : 0.0f);
+        if (lane == 0)
+            mbar_arrive_expect_tx(bar1, 4u * static_cast<uint32_t>(K));
+        if (lane < K)
+            st_async_f32(cluster_addr(smem_addr(&xmax[k]), static_cast<uint32_t>(lane)), cm,
+                         cluster_addr(bar1, static_cast<uint32_t>(lane)));
+    }
+    if (!mbar_wait_parity_bounded(bar1, 0u, 200ull * 1000 * 1000) && a.err && tid == 0)
+        atomicOr(a.err, 4u);
+    float amax = 0.0f;
+    for (int p = 0; p < K; ++p)
+        amax = fmaxf(amax, xmax[p]);
+    const float g = __fdiv_rn(amax, 2688.0f);
+    if (k == 0 && tid == 0)
+        *sa.gscale = g;
+    cluster_arrive_relaxed();  // done with the peers; matched at exit
+
+    // ---- 4. quantise this thread's items (a block = the vectors of a lane pair)
+#pragma unroll
+    for (int j = 0; j < IPT; ++j) {
+        const int i = tid + j * B;
+        float bmax = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            bmax = fmaxf(bmax, fabsf(h[j][e]));
+        bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));
+        if (i < items) {
+            const int64_t gv = static_cast<int64_t>(i / slice) * a.nvec + vbeg + i % slice;
+            uint32_t sbyte;
+            const float inv = nvfp4_block_scale(g, bmax, sbyte);
+            float q[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                q[e] = __fmul_rn(h[j][e], inv);
+            st_u32(a.codes + gv, e2m1x8_from_f32(q));
+            if ((gv & 1) == 0)
+                st_u8(a.scales + gv / 2, sbyte);
+        }
+    }
+    cluster_wait_acquire();  // no CTA leaves while a peer may still push to it
+}
+
+}  // namespace tpar

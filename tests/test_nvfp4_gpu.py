@@ -162,3 +162,27 @@ def test_workspace_is_left_zeroed_and_reused():
             assert_nvfp4_bit_exact(out["out_norm"], out["codes"], out["scales"], out["global_scale"],
                                    what=f"call {i}")
         assert int(ws.abs().sum().item()) == 0
+
+
+@pytest.mark.parametrize("T,d,n", [(1, 8192, 4), (3, 8192, 4), (8, 4096, 8), (16, 2048, 2), (32, 8192, 4),
+                                   (7, 1024, 16), (5, 256, 1), (32, 4096, 8)])
+def test_single_launch_dynamic_matches_two_pass(T, d, n):
+    """Few tokens: one cluster owns the tensor and exchanges the amax on chip
+    (one launch). It must give exactly the bits of the two-kernel path, and
+    both are bit-exact against the oracle quantiser on out_norm."""
+    tp = lib()
+    w = synth.NVFP4.with_(T=T, d=d, n_ranks=n, seed=T * 13 + d + n)
+    inputs = synth.make_inputs(w)
+    dev = to_device(inputs)
+    one = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True)
+    two = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True,
+                           flags=tp.TPAR_FORCE_ROW)
+    torch.cuda.synchronize()
+    for k in ("out_norm", "out_residual", "codes", "scales", "global_scale"):
+        assert torch.equal(one[k].view(torch.int16) if one[k].dtype == torch.bfloat16 else one[k],
+                           two[k].view(torch.int16) if two[k].dtype == torch.bfloat16 else two[k]), k
+    ref = oracle_rows(inputs, slice(None), w.eps)
+    assert_close_to_ref(one["out_norm"], ref["y"], "single-launch out_norm")
+    assert_close_to_ref(one["out_residual"], ref["h"], "single-launch out_residual")
+    assert_nvfp4_bit_exact(one["out_norm"], one["codes"], one["scales"], one["global_scale"], what="single")
+    assert tp.tpar_device_error(torch.cuda.current_device()) == 0
