@@ -208,12 +208,12 @@ int pow2_at_least(int64_t n)
     return p;
 }
 
-// Vectors of a row owned by one CTA of a `split`-wide cluster (even, so the
-// two halves of every 16-element NVFP4 block stay in one CTA).
+// Vectors of a row owned by one CTA of a `split`-wide cluster: a multiple of
+// 32, so each CTA owns whole 32-vector groups of the canonical sum of
+// squares (and both halves of every 16-element NVFP4 block).
 int slice_for(int nvec, int split)
 {
-    int64_t s = ceil_div(nvec, split);
-    return static_cast<int>(s + (s & 1));
+    return static_cast<int>(ceil_div(ceil_div(nvec, split), 32) * 32);
 }
 
 tpar_status check_plan(const tpar_plan& p, int64_t d, int n_ranks)

@@ -113,6 +113,20 @@ __device__ __forceinline__ float warp_sum(float v)
     return v;
 }
 
+// The row's sum of squares in the one order every kernel uses, whatever its
+// launch shape: W[w] is the butterfly warp sum over the 16-byte vectors
+// 32w .. 32w+31 (each vector's 8 squares folded left to right with fma);
+// the W are added butterfly-wise in groups of 32 and the groups left to
+// right. Called by a whole warp; every lane returns the same bits. Results
+// therefore do not depend on the CTA shape, the cluster split or T.
+__device__ __forceinline__ float canonical_row_sum(const float* W, int nW, int lane)
+{
+    float tot = 0.0f;
+    for (int g = 0; g < nW; g += 32)
+        tot += warp_sum(g + lane < nW ? W[g + lane] : 0.0f);
+    return tot;
+}
+
 __device__ __forceinline__ float warp_max(float v)
 {
 #pragma unroll

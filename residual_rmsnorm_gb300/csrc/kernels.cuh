@@ -24,6 +24,7 @@
 namespace tpar {
 
 constexpr int kMaxRanks = 16;
+constexpr int kMaxRowWarps = 128;  // 32-vector groups of the widest row (d = 32768)
 
 enum QuantMode : int {
     kQuantNone = 0,     // bf16 outputs only
@@ -143,11 +144,12 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT, CLUSTER))
     const int vbeg = crank * a.slice;
     const int vend = min(vbeg + a.slice, a.nvec);
 
-    __shared__ float warp_ss[2][32];  // per-warp sums of squares, by iteration parity
-    // Cluster exchange: every CTA pushes its row sum of squares into slot
-    // [crank] of every peer (st.async), counted on the peer's mbarrier.
+    // Per-32-vector partial sums of squares W[w] of the row, by row parity.
+    // In the cluster form every CTA pushes its W into the same slots of every
+    // peer (st.async), counted on the peer's mbarrier.
+    __shared__ float wsh[2][kMaxRowWarps];
     __shared__ __align__(8) uint64_t xbar[2];
-    __shared__ float xslot[2][16];
+    const int nW = (a.nvec + 31) >> 5;
     if constexpr (CLUSTER) {
         if (tid == 0) {
             mbar_init(smem_addr(&xbar[0]), 1);
@@ -172,7 +174,7 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT, CLUSTER))
         // after the reduction (wide rows fetch it late to save registers).
         constexpr bool kEarlyGamma = VPT <= 4;
         uint4 gv[kEarlyGamma ? VPT : 1];
-        float ss = 0.0f;
+        float ss[VPT];
 
         // ---- rank sum (fixed order 0..N-1) and residual add.
         // All loads of a group of G vectors are issued before any of them is
@@ -199,6 +201,7 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT, CLUSTER))
             for (int jj = 0; jj < G; ++jj) {
                 const int j = j0 + jj;
                 const int v = vbeg + tid + j * static_cast<int>(blockDim.x);
+                ss[j] = 0.0f;
                 if (v < vend) {
                     unpack8(x[jj][0], h[j]);
 #pragma unroll
@@ -209,7 +212,7 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT, CLUSTER))
                         add8(rv[jj], h[j]);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
-                        ss = fmaf(h[j][e], h[j][e], ss);
+                        ss[j] = fmaf(h[j][e], h[j][e], ss[j]);
                     if (!CLUSTER && a.out_residual)
                         st_v4(a.out_residual + rowv + v, pack8(h[j]));
                 } else {
@@ -220,29 +223,38 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT, CLUSTER))
             }
         }
 
-        // ---- row sum of squares: warp -> CTA -> (cluster)
+        // ---- row sum of squares in the canonical order (canonical_row_sum)
         const int buf = it & 1;
-        ss = warp_sum(ss);
-        if (lane == 0)
-            warp_ss[buf][warp] = ss;
-        __syncthreads();
-        float tot = warp_sum(lane < nwarps ? warp_ss[buf][lane] : 0.0f);
-        if constexpr (CLUSTER) {
+        float tot;
+        if constexpr (!CLUSTER) {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const float s = warp_sum(ss[j]);
+                const int w = (j * static_cast<int>(blockDim.x) + 32 * warp) >> 5;
+                if (lane == 0 && 32 * w < vend)
+                    wsh[buf][w] = s;
+            }
+            __syncthreads();
+            tot = canonical_row_sum(wsh[buf], nW, lane);
+        } else {
             // The previous arrive (set-up, or "done with the last row") must
             // be matched before pushing into the peers' slots.
             cluster_wait_acquire();
-            const int b = it & 1;
             const uint32_t parity = static_cast<uint32_t>(it >> 1) & 1u;
-            const uint32_t bar = smem_addr(&xbar[b]);
+            const uint32_t bar = smem_addr(&xbar[buf]);
             if (tid == 0)
-                mbar_arrive_expect_tx(bar, 4u * static_cast<uint32_t>(split));
-            if (tid < split)
-                st_async_f32(cluster_addr(smem_addr(&xslot[b][crank]), static_cast<uint32_t>(tid)), tot,
-                             cluster_addr(bar, static_cast<uint32_t>(tid)));
+                mbar_arrive_expect_tx(bar, 4u * static_cast<uint32_t>(nW));
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const float s = warp_sum(ss[j]);
+                const int v0 = vbeg + j * static_cast<int>(blockDim.x) + 32 * warp;
+                if (v0 < vend && lane < split)
+                    st_async_f32(cluster_addr(smem_addr(&wsh[buf][v0 >> 5]), static_cast<uint32_t>(lane)), s,
+                                 cluster_addr(bar, static_cast<uint32_t>(lane)));
+            }
             if (!mbar_wait_parity_bounded(bar, parity, 200ull * 1000 * 1000) && a.err && tid == 0)
                 atomicOr(a.err, 1u);
-            // fixed order over the cluster ranks, identical in every CTA
-            tot = warp_sum(lane < split ? xslot[b][lane] : 0.0f);
+            tot = canonical_row_sum(wsh[buf], nW, lane);
             cluster_arrive_relaxed();
         }
         const float rinv = rsqrtf(fmaf(tot, a.inv_d, a.eps));

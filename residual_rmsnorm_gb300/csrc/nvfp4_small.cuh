@@ -7,13 +7,15 @@
 // CTA k of the cluster owns the vector slice [k*slice, (k+1)*slice) of every
 // row, and the cluster
 //   1. sums the ranks and the residual of all its items (fp32 registers),
-//   2. exchanges each row's partial sum of squares with every peer (st.async
-//      into the peers' shared memory, counted on an mbarrier) and normalises,
+//   2. pushes each row's 32-vector partial sums of squares to every peer
+//      (st.async into the peers' shared memory, counted on an mbarrier),
+//      adds them in the canonical order of every kernel and normalises,
 //   3. exchanges its local amax of the emitted bf16 values the same way,
 //   4. quantises its items from registers with the cluster-wide g.
 // No re-read of out_norm, no workspace, no second launch. The arithmetic is
 // the same as the two-pass path ("Deep Dive: AllReduce and AllReduce Fusion
-// in TensorRT-LLM", 6.3 and 6.5): results are bit-identical to it.
+// in TensorRT-LLM", 6.3 and 6.5), in the same order: results are
+// bit-identical to it.
 #pragma once
 
 #include "kernels.cuh"
@@ -48,12 +50,12 @@ __global__ void __launch_bounds__(512) nvfp4_small_kernel(const __grid_constant_
     const int items = T * slice;
     const int vbeg = k * slice;
 
-    __shared__ __align__(8) uint64_t xbar[2];          // [0] row sums, [1] amax
-    __shared__ float xrow[kSmallMaxRanks][kSmallMaxRows];  // [peer][row]
+    __shared__ __align__(8) uint64_t xbar[2];          // [0] row partials, [1] amax
+    __shared__ float xrow[kSmallMaxRows][kMaxRowWarps];  // [row][32-vector group], from all CTAs
     __shared__ float xmax[kSmallMaxRanks];             // [peer]
-    __shared__ float wsum[IPT][16];                    // [item group][warp]
     __shared__ float rinv_sh[kSmallMaxRows];
     __shared__ float wmax[16];
+    const int nW = (a.nvec + 31) >> 5;
 
     if (tid == 0) {
         mbar_init(smem_addr(&xbar[0]), 1);
@@ -104,38 +106,29 @@ __global__ void __launch_bounds__(512) nvfp4_small_kernel(const __grid_constant_
         }
     }
 
-    // ---- per-row CTA partial sums. slice % 32 == 0, so each warp's 32 items
-    // of one item group lie in one row.
-#pragma unroll
-    for (int j = 0; j < IPT; ++j) {
-        const float s = warp_sum(ss[j]);
-        if (lane == 0)
-            wsum[j][warp] = s;
-    }
-    __syncthreads();
-    float row_part = 0.0f;
-    if (tid < T) {
-        for (int i0 = tid * slice; i0 < (tid + 1) * slice; i0 += 32)
-            row_part += wsum[i0 / B][(i0 % B) >> 5];  // fixed order over the row's warps
-    }
-
-    // ---- 2. exchange row partials with every peer; normalise
+    // ---- 2. push every 32-vector partial W (a warp's 32 items lie in one row,
+    // as slice % 32 == 0) into the same slot of every peer; then each CTA sums
+    // each row's W in the canonical order (canonical_row_sum) and normalises.
     cluster_wait_acquire();  // the peers' mbarriers are initialised
     const uint32_t bar0 = smem_addr(&xbar[0]);
     if (tid == 0)
-        mbar_arrive_expect_tx(bar0, 4u * static_cast<uint32_t>(K * T));
-    if (tid < T) {
-        for (int p = 0; p < K; ++p)
-            st_async_f32(cluster_addr(smem_addr(&xrow[k][tid]), static_cast<uint32_t>(p)), row_part,
-                         cluster_addr(bar0, static_cast<uint32_t>(p)));
+        mbar_arrive_expect_tx(bar0, 4u * static_cast<uint32_t>(T * nW));
+#pragma unroll
+    for (int j = 0; j < IPT; ++j) {
+        const float s = warp_sum(ss[j]);
+        const int i0 = j * B + 32 * warp;
+        if (i0 < items && lane < K) {
+            const int w = (vbeg + i0 % slice) >> 5;
+            st_async_f32(cluster_addr(smem_addr(&xrow[i0 / slice][w]), static_cast<uint32_t>(lane)), s,
+                         cluster_addr(bar0, static_cast<uint32_t>(lane)));
+        }
     }
     if (!mbar_wait_parity_bounded(bar0, 0u, 200ull * 1000 * 1000) && a.err && tid == 0)
         atomicOr(a.err, 4u);
-    if (tid < T) {
-        float tot = 0.0f;
-        for (int p = 0; p < K; ++p)
-            tot += xrow[p][tid];  // fixed order over the cluster: identical in every CTA
-        rinv_sh[tid] = rsqrtf(fmaf(tot, a.inv_d, a.eps));
+    for (int r = warp; r < T; r += nwarps) {
+        const float tot = canonical_row_sum(xrow[r], nW, lane);
+        if (lane == 0)
+            rinv_sh[r] = rsqrtf(fmaf(tot, a.inv_d, a.eps));
     }
     __syncthreads();
 

@@ -73,7 +73,7 @@ __global__ void __launch_bounds__(544, 1) stream_rmsnorm_kernel(const __grid_con
     const uint32_t empty0 = smem_addr(bars + S);
     const uint32_t ring0 = smem_addr(ring);
 
-    __shared__ float warp_ss[2][32];
+    __shared__ float wsh[2][kMaxRowWarps];  // per-32-vector partial sums of squares
     __shared__ float warp_mx[32];
     __shared__ int abort_flag;   // set by any thread whose bounded wait expired
     __shared__ int stop_sh[2];   // abort_flag as sampled once per row, for a uniform exit
@@ -187,10 +187,11 @@ __global__ void __launch_bounds__(544, 1) stream_rmsnorm_kernel(const __grid_con
                 ++round;
             }
         }
-        float ss = 0.0f;
+        const int buf = it & 1;
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const int v = c + j * C;
+            float ss = 0.0f;
             if (v < nvec) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
@@ -198,15 +199,15 @@ __global__ void __launch_bounds__(544, 1) stream_rmsnorm_kernel(const __grid_con
                 if (a.out_residual)
                     st_v4(a.out_residual + rowv + v, pack8(h[j]));
             }
+            ss = warp_sum(ss);
+            const int w = (j * C + 32 * cwarp) >> 5;
+            if (lane == 0 && 32 * w < nvec)
+                wsh[buf][w] = ss;
         }
-        const int buf = it & 1;
-        ss = warp_sum(ss);
-        if (lane == 0)
-            warp_ss[buf][cwarp] = ss;
         if (c == 0)
             stop_sh[buf] = *reinterpret_cast<volatile int*>(&abort_flag);
         consumers_sync(C);
-        const float tot = warp_sum(lane < nwarps ? warp_ss[buf][lane] : 0.0f);
+        const float tot = canonical_row_sum(wsh[buf], (nvec + 31) >> 5, lane);
         const float rinv = rsqrtf(fmaf(tot, a.inv_d, a.eps));
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {

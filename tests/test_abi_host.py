@@ -189,8 +189,7 @@ def test_planner_covers_every_row(tp, sm):
                 raise AssertionError("the stream kernel is only planned on request")
             if p.kernel == 1:
                 assert 2 <= p.split <= 16
-                s = -(-nvec // p.split)
-                s += s & 1
+                s = -(-(-(-nvec // p.split)) // 32) * 32
                 assert p.threads * p.vec_per_thread >= s
                 assert s >= 32 or p.split == 2
                 assert T <= 32 and T * p.split <= 2 * sm  # rows are split only when few

@@ -189,3 +189,62 @@ def test_cluster_exchange_never_times_out():
             tp.fused_rmsnorm(d["partials"], d["residual"], d["gamma"], w.eps, plan=plan)
     torch.cuda.synchronize()
     assert tp.tpar_device_error(dev) == 0
+
+
+def _plans(tp, d, T):
+    nvec = d // 8
+    P = tp.TparPlan
+    r32 = lambda x: -(-x // 32) * 32
+    plans = []
+    for thr, vpt in ((1024, 1), (512, 2), (256, 4), (128, 8)):
+        if thr * vpt >= nvec and not (vpt >= 2 and thr > 512):
+            plans.append(P(0, 1, thr, vpt, max(1, T // 3)))
+    for split in (2, 4, 8, 16):
+        sl = r32(-(-nvec // split))
+        for vpt in (1, 2):
+            thr = r32(-(-sl // vpt))
+            if 32 <= thr <= 512:
+                plans.append(P(1, split, thr, vpt, T))
+    for thr, vpt in ((512, 2), (256, 4), (512, 4), (128, 8)):
+        if thr * vpt >= nvec:
+            plans.append(P(2, 1, thr, vpt, max(1, min(T, 5))))
+    return plans
+
+
+@pytest.mark.parametrize("d", [8192, 8200, 4096, 1024])
+def test_bitwise_identical_across_plans_and_batch_sizes(d):
+    """The sum of squares is reduced in one canonical order (32-vector warp
+    sums, then groups), so every launch plan -- whole-row CTAs of any shape,
+    cluster splits, the TMA-fed kernel -- and every batch size gives the
+    same bits (batch invariance)."""
+    tp = lib()
+    T = 40
+    w = synth.PREFILL.with_(T=T, d=d, seed=d)
+    dev = to_device(synth.make_inputs(w))
+    ref = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps)
+    for plan in _plans(tp, d, T):
+        out = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, plan=plan)
+        torch.cuda.synchronize()
+        assert same_bits(out["out_norm"], ref["out_norm"]), plan.as_dict()
+        assert same_bits(out["out_residual"], ref["out_residual"]), plan.as_dict()
+    for t in (0, 17, 39):
+        one = tp.fused_rmsnorm([p[t:t + 1].contiguous() for p in dev["partials"]],
+                               dev["residual"][t:t + 1].contiguous(), dev["gamma"], w.eps)
+        torch.cuda.synchronize()
+        assert same_bits(one["out_norm"][0], ref["out_norm"][t]), t
+    assert tp.tpar_device_error(torch.cuda.current_device()) == 0
+
+
+def test_nvfp4_given_scale_identical_across_plans():
+    tp = lib()
+    T, d = 24, 4096
+    w = synth.NVFP4.with_(T=T, d=d)
+    dev = to_device(synth.make_inputs(w))
+    g = torch.tensor([0.05], dtype=torch.float32, device="cuda")
+    ref = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True, global_scale=g)
+    for plan in _plans(tp, d, T):
+        out = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True,
+                               global_scale=g, plan=plan)
+        torch.cuda.synchronize()
+        assert torch.equal(out["codes"], ref["codes"]) and torch.equal(out["scales"], ref["scales"]), \
+            plan.as_dict()
