@@ -196,7 +196,7 @@ def _plans(tp, d, T):
     P = tp.TparPlan
     r32 = lambda x: -(-x // 32) * 32
     plans = []
-    for thr, vpt in ((1024, 1), (512, 2), (256, 4), (128, 8)):
+    for thr, vpt in ((1024, 1), (512, 2), (256, 4), (128, 8), (512, 4), (256, 8)):
         if thr * vpt >= nvec and not (vpt >= 2 and thr > 512):
             plans.append(P(0, 1, thr, vpt, max(1, T // 3)))
     for split in (2, 4, 8, 16):
