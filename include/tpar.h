@@ -118,7 +118,7 @@ tpar_status tpar_init(int device);
  *                scales [T, d/16] E4M3 bytes, global_scale -> one device fp32.
  *                Here global_scale is an OUTPUT: g = amax(|out_norm|) / 2688
  *                over the whole [T, d] tensor, computed on the device. For
- *                T <= 32 and d a multiple of 512 (or 256, 128 ...) one
+ *                T <= 16 and d a multiple of 512 (or 256, 128 ...) one
  *                thread-block cluster owns the whole tensor and the call is a
  *                single launch; otherwise it is two (the fused pass, then a
  *                quantiser re-reading out_norm). Both give identical bits.

@@ -540,8 +540,10 @@ FusedArgs fused_args(const Call& c)
 // Shape of the single-launch dynamic-NVFP4 path: one cluster of K CTAs, each
 // owning `slice` vectors (a multiple of 32) of every row, at most 4 items of
 // 16 bytes per thread. Returns false when the tensor does not fit one cluster.
-// T <= kSmallNvfp4Rows: measured faster than phase A + phase B up to there.
-constexpr int64_t kSmallNvfp4Rows = 32;
+// T <= kSmallNvfp4Rows: measured faster than phase A + phase B up to there
+// (N=4, d=8192: 2.65 / 3.79 / 5.24 us at T = 1 / 8 / 16 vs 4.48 / 5.42 / 5.52;
+// at T = 32 one cluster is too few SMs, 9.2 vs 5.6 us).
+constexpr int64_t kSmallNvfp4Rows = 16;
 
 bool small_nvfp4_shape(int64_t T, int64_t d, int* K, int* slice, int* threads, int* ipt)
 {
