@@ -374,19 +374,13 @@ tpar_status plan_impl(int64_t T, int64_t d, int n_ranks, int sm_count, uint32_t 
     if (!(flags & TPAR_FORCE_ROW)) {
         // Latency path. A CTA that owns a whole row pulls (N+1)*2d bytes
         // through one SM (~120 GB/s per SM measured on GB300); the cluster
-        // exchange of partial sums costs ~0.45 us. Split rows over a cluster
-        // when the rows are few and long enough to win that back: at T <= 2
-        // rows of >= 48 KB into ~8 KB slices, at T <= 32 rows of >= 96 KB
-        // into ~16 KB slices (measured: N=8, d=8192, T=8 runs 2.68 us split
-        // 8 ways vs 3.37 us whole; d=4096 at T=8 stays whole, 2.50 us).
+        // exchange of the 32-vector partial sums costs ~0.2-0.3 us. Split
+        // rows of >= 64 KB over a cluster while T <= 32, into slices of
+        // >= 10 KB (measured: N=4 d=8192 T=8 2.30 us split 8 ways vs 2.88
+        // whole; N=8 d=8192 T=32 3.16 vs 3.50; N=8 d=4096 T=8 a tie at 2.49).
         const int64_t row_bytes = static_cast<int64_t>(n_ranks + 1) * d * 2;
-        int64_t slice_target = 0;
-        if (T <= 2 && row_bytes >= 48 * 1024)
-            slice_target = 8 * 1024;
-        else if (T <= 32 && row_bytes >= 96 * 1024)
-            slice_target = 16 * 1024;
-        if (slice_target > 0) {
-            while (split < 16 && row_bytes / (2 * split) >= slice_target && T * (2 * split) <= 2 * sm_count &&
+        if (T <= 32 && row_bytes >= 64 * 1024) {
+            while (split < 16 && row_bytes / (2 * split) >= 10 * 1024 && T * (2 * split) <= 2 * sm_count &&
                    nvec / (2 * split) >= 32)
                 split *= 2;
         }

@@ -199,17 +199,17 @@ def test_planner_covers_every_row(tp, sm):
 
 
 def test_planner_choices_for_the_pages_shapes(tp):
-    # decode, 73 KB rows (N=8, d=4096): whole rows at T=8, 8-way split at T=1
+    # decode, 73 KB rows (N=8, d=4096): split 4 ways (18 KB slices)
     p = tp.tpar_plan_launch(8, 4096, 8, 152)
-    assert (p.kernel, p.split, p.threads, p.vec_per_thread) == (0, 1, 512, 1)
-    assert tp.tpar_plan_launch(1, 4096, 8, 152).split == 8
-    # decode, 147 KB rows (N=8, d=8192): rows split over clusters up to T=32
-    p = tp.tpar_plan_launch(1, 8192, 8, 152)
-    assert (p.kernel, p.split, p.threads) == (1, 16, 64)
-    for T in (4, 8, 16, 32):
+    assert (p.kernel, p.split, p.threads, p.vec_per_thread) == (1, 4, 128, 1)
+    # decode, 147 KB rows (N=8, d=8192): split 8 ways up to T=32
+    for T in (1, 4, 8, 16, 32):
         p = tp.tpar_plan_launch(T, 8192, 8, 152)
         assert (p.kernel, p.split, p.threads) == (1, 8, 128), T
     assert tp.tpar_plan_launch(64, 8192, 8, 152).kernel == 0
+    # 82 KB rows (N=4, d=8192): split 8 ways; 25 KB rows (N=2, d=4096): whole
+    assert tp.tpar_plan_launch(8, 8192, 4, 152).split == 8
+    assert tp.tpar_plan_launch(8, 4096, 2, 152).kernel == 0
     # prefill: one CTA of 1024 threads per row; the TMA-fed kernel on request
     p = tp.tpar_plan_launch(4096, 8192, 8, 152)
     assert (p.kernel, p.split, p.threads, p.vec_per_thread) == (0, 1, 1024, 1)
