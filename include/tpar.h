@@ -102,15 +102,17 @@ tpar_status tpar_init(int device);
  *   partials     host array of n_ranks device pointers, each bf16 [T, d]
  *   n_ranks      1 .. TPAR_MAX_RANKS
  *   residual     bf16 [T, d], or NULL for no residual (h = s)
- *   gamma        bf16 [d]
+ *   gamma        bf16 [d] (unused, may be NULL, in the all-reduce-only pattern)
  *   eps          >= 0 and finite; used as this fp32 value
  *   T            rows (tokens), >= 0; T == 0 is a no-op that writes nothing
  *                (then only n_ranks, d, eps and flags are checked, and the
  *                tensor pointers may be NULL)
  *   d            hidden size: 8 <= d <= TPAR_MAX_HIDDEN, d % 8 == 0,
  *                and d % 16 == 0 when NVFP4 output is requested
- *   out_norm     bf16 [T, d]; may be NULL only for NVFP4 with
- *                TPAR_GSCALE_GIVEN (via the _ex entry point)
+ *   out_norm     bf16 [T, d]. NULL with no NVFP4 outputs selects the
+ *                all-reduce-only pattern: out_residual = bf16(sum + residual),
+ *                no norm, gamma may be NULL. NULL with NVFP4 needs
+ *                TPAR_GSCALE_GIVEN (via the _ex entry point).
  *   out_residual bf16 [T, d], or NULL to skip it; may be exactly `residual`
  *                (updated in place) but must not otherwise overlap an input
  *   nvfp4_codes, nvfp4_scales, global_scale

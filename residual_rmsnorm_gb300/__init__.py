@@ -36,10 +36,10 @@ from ._abi import (  # noqa: F401
     tpar_version,
     tpar_workspace_bytes,
 )
-from .ops import fused_rmsnorm, nvfp4_quantize, unfused_rmsnorm  # noqa: F401
+from .ops import allreduce_sum, fused_rmsnorm, nvfp4_quantize, unfused_rmsnorm  # noqa: F401
 
 __all__ = [
-    "fused_rmsnorm", "unfused_rmsnorm", "nvfp4_quantize", "TparError", "TparPlan",
+    "fused_rmsnorm", "unfused_rmsnorm", "nvfp4_quantize", "allreduce_sum", "TparError", "TparPlan",
     "tpar_init", "tpar_fused_rmsnorm", "tpar_fused_rmsnorm_ex", "tpar_unfused_rmsnorm",
     "tpar_nvfp4_quantize", "tpar_unfused_rmsnorm_noalloc", "tpar_plan_launch", "tpar_status_string", "tpar_version",
     "tpar_workspace_bytes", "tpar_device_error", "library", "library_path",

@@ -287,7 +287,7 @@ tpar_status validate(const Call& c, bool unfused)
     // An empty batch is a no-op: its tensors may be NULL (empty allocations).
     if (c.T == 0)
         return TPAR_OK;
-    if (!c.gamma)
+    if (!c.gamma && (c.out_norm || c.codes || unfused))
         return TPAR_ERR_INVALID_ARG;
     for (int r = 0; r < c.n_ranks; ++r)
         if (!c.partials[r])
@@ -301,7 +301,12 @@ tpar_status validate(const Call& c, bool unfused)
         return TPAR_ERR_INVALID_ARG;
     if (!nvfp4 && given)
         return TPAR_ERR_INVALID_ARG;
-    if (!c.out_norm && !(nvfp4 && given && !unfused))
+    // out_norm may be NULL for NVFP4 with a given scale, or (fused entry points,
+    // no quantisation) for the all-reduce-only pattern, which then needs no gamma.
+    const bool sum_only = !unfused && !nvfp4 && !c.out_norm;
+    if (!c.out_norm && !(nvfp4 && given && !unfused) && !sum_only)
+        return TPAR_ERR_INVALID_ARG;
+    if (sum_only && !c.out_residual)
         return TPAR_ERR_INVALID_ARG;
     if (unfused && (!c.out_residual || !c.reduced))
         return TPAR_ERR_INVALID_ARG;
@@ -324,7 +329,8 @@ tpar_status validate(const Call& c, bool unfused)
     const bool in_place = c.out_residual && c.out_residual == c.residual;
     if (!in_place)
         ins[ni++] = Range(c.residual, td2);
-    ins[ni++] = Range(c.gamma, c.d * 2);
+    if (c.gamma)
+        ins[ni++] = Range(c.gamma, c.d * 2);
     if (given)
         ins[ni++] = Range(c.gscale, 4);
     Range outs[6];
@@ -605,6 +611,21 @@ tpar_status fused_impl(const Call& c, const tpar_plan* user_plan, void* user_ws,
     const bool nvfp4 = c.codes != nullptr;
     const bool given = (c.flags & TPAR_GSCALE_GIVEN) != 0;
     const bool pdl = (c.flags & TPAR_NO_PDL) == 0;
+    if (!nvfp4 && !c.out_norm) {
+        // All-reduce only (+ residual): a flat vectorised sum, no norm.
+        ReduceArgs ra;
+        std::memset(&ra, 0, sizeof ra);
+        for (int r = 0; r < c.n_ranks; ++r)
+            ra.partials[r] = static_cast<const uint4*>(c.partials[r]);
+        ra.residual = static_cast<const uint4*>(c.residual);
+        ra.reduced = static_cast<uint4*>(c.out_residual);
+        ra.nvec = c.T * c.d / 8;
+        ra.n_ranks = c.n_ranks;
+        return launch(tpar::reduce_kernel_for(tpar::rank_bound(c.n_ranks)), dim3(flat_grid(ra.nvec, sm)),
+                      dim3(256), &ra, stream, 1, pdl) == cudaSuccess
+                   ? TPAR_OK
+                   : TPAR_ERR_CUDA;
+    }
     FusedArgs a = fused_args(c);
     a.slice = p.kernel == 1 ? slice_for(a.nvec, p.split) : a.nvec;
     if (!nvfp4)

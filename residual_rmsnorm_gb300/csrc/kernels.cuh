@@ -361,12 +361,16 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __grid_consta
 
 struct ReduceArgs {
     const uint4* partials[kMaxRanks];
+    const uint4* residual;  // added after the ranks when not null (may equal `reduced`)
     uint4* reduced;
     int64_t nvec;  // T * d / 8
     int n_ranks;
 };
 
-// K1: reduced = bf16(sum of partials), fixed rank order.
+// reduced = bf16(sum of partials [+ residual]), fixed rank order, one
+// rounding: the unfused path's K1 (no residual) and the all-reduce-only
+// pattern of the fused entry points ("Deep Dive: AllReduce and AllReduce
+// Fusion in TensorRT-LLM", 6.3, pattern kAllReduce).
 template <int NR>
 __global__ void __launch_bounds__(256) reduce_kernel(const __grid_constant__ ReduceArgs a)
 {
@@ -385,6 +389,8 @@ __global__ void __launch_bounds__(256) reduce_kernel(const __grid_constant__ Red
         for (int r = 1; r < NR; ++r)
             if (r < a.n_ranks)
                 add8(x[r], s);
+        if (a.residual)
+            add8(ld_coherent(a.residual + v), s);
         st_v4(a.reduced + v, pack8(s));
     }
 }

@@ -90,6 +90,28 @@ def fused_rmsnorm(partials, residual, gamma, eps: float, *, out_norm=None, out_r
             "global_scale": g}
 
 
+def allreduce_sum(partials, residual=None, *, out=None, flags: int = 0, stream=None):
+    """The all-reduce-only pattern: out = bf16(sum(partials) [+ residual]), one
+    rounding, no norm (``tpar_fused_rmsnorm`` with out_norm = gamma = NULL)."""
+    partials = list(partials)
+    if not partials:
+        raise ValueError("need at least one partial")
+    T, d = partials[0].shape
+    dev = partials[0].device
+    for i, p in enumerate(partials):
+        _check_bf16(f"partials[{i}]", p, (T, d))
+    if residual is not None:
+        _check_bf16("residual", residual, (T, d))
+    out = torch.empty((T, d), dtype=torch.bfloat16, device=dev) if out is None else out
+    _check_bf16("out", out, (T, d))
+    with torch.cuda.device(dev):
+        _abi.tpar_fused_rmsnorm_ex(
+            [p.data_ptr() for p in partials], len(partials),
+            residual.data_ptr() if residual is not None else 0, 0, 0.0, T, d, 0, out.data_ptr(),
+            0, 0, 0, flags, None, 0, _stream_handle(dev, stream))
+    return out
+
+
 def unfused_rmsnorm(partials, residual, gamma, eps: float, *, reduced=None, out_norm=None,
                     out_residual=None, nvfp4: bool = False, global_scale=None, flags: int = 0,
                     stream=None):

@@ -91,6 +91,11 @@ def test_dry_run_accepts_a_valid_call(tp):
     nv = dict(codes=BASE + 200 * MB, scales=BASE + 210 * MB, g=BASE + 220 * MB)
     assert call(tp, **nv) == OK
     assert call(tp, out_norm=0, flags=tp.TPAR_DRY_RUN | tp.TPAR_GSCALE_GIVEN, **nv) == OK
+    # all-reduce only: no norm output, no gamma
+    assert call(tp, out_norm=0, gamma=0) == OK
+    assert call(tp, out_norm=0, gamma=0, residual=0) == OK
+    assert call(tp, out_norm=0, gamma=0, out_residual=0) == INVALID
+    assert call(tp, out_norm=0, gamma=0, out_residual=BASE) == INVALID  # on partial 0
 
 
 @pytest.mark.parametrize("kw,status", [
@@ -106,7 +111,8 @@ def test_dry_run_accepts_a_valid_call(tp):
     (dict(eps=float("inf")), INVALID),
     (dict(eps=float("nan")), INVALID),
     (dict(gamma=0), INVALID),
-    (dict(out_norm=0), INVALID),
+    (dict(out_norm=0, out_residual=0), INVALID),
+    (dict(out_norm=0, codes=BASE + 200 * MB, scales=BASE + 210 * MB, g=BASE + 220 * MB), INVALID),
     (dict(codes=BASE + 200 * MB), INVALID),  # incomplete NVFP4 triple
     (dict(codes=BASE + 200 * MB, scales=BASE + 210 * MB), INVALID),
     (dict(d=4104, codes=BASE + 200 * MB, scales=BASE + 210 * MB, g=BASE + 220 * MB), INVALID),  # d % 16

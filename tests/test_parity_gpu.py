@@ -205,3 +205,25 @@ def test_stream_kernel_in_place_and_nvfp4_given():
     assert_close_to_ref(res, ref["h"], "stream in-place residual")
     assert_close_to_ref(out["out_norm"], ref["y"], "stream out_norm")
     assert_nvfp4_bit_exact(out["out_norm"], out["codes"], out["scales"], 0.03, given=0.03, what="stream given")
+
+
+@pytest.mark.parametrize("n,T,d,residual", [(8, 8, 4096, True), (4, 4096, 8192, False), (3, 5, 24, True),
+                                            (16, 33, 2048, True), (1, 7, 8, False)])
+def test_allreduce_only_pattern(n, T, d, residual):
+    """kAllReduce: out = bf16(sum of the ranks [+ residual]), no norm."""
+    tp = lib()
+    w = synth.Workload(f"allreduce N{n} T{T} d{d}", n, T, d, 1e-5, 0.5, seed=n * 7 + T + d)
+    inputs = synth.make_inputs(w)
+    if not residual:
+        inputs = dict(inputs, residual=None)
+    dev = to_device(inputs)
+    out = tp.allreduce_sum(dev["partials"], dev["residual"])
+    torch.cuda.synchronize()
+    ref = oracle_rows(inputs, slice(None), w.eps, residual=residual)
+    assert_close_to_ref(out, ref["h"], "allreduce-only")
+    # in place on the residual
+    if residual:
+        res = dev["residual"].clone()
+        tp.allreduce_sum(dev["partials"], res, out=res)
+        torch.cuda.synchronize()
+        assert torch.equal(res.view(torch.int16), out.view(torch.int16))
