@@ -78,6 +78,8 @@ def _load():
                                           P, P, P, P]
         lib.orc_nvfp4_quantize.restype = ctypes.c_int
         lib.orc_nvfp4_quantize.argtypes = [P, i64, i64, ctypes.c_int, ctypes.c_float, P, P, P]
+        lib.orc_fp8_quantize.restype = ctypes.c_int
+        lib.orc_fp8_quantize.argtypes = [P, i64, i64, ctypes.c_int, ctypes.c_float, P, P]
         lib.orc_bf16_amax.restype = ctypes.c_float
         lib.orc_bf16_amax.argtypes = [P, i64]
         _lib = lib
@@ -199,6 +201,24 @@ def nvfp4_quantize(x, global_scale: float | None = None):
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return codes, scales, np.float32(g.value)
+
+
+def fp8_quantize(x, scale: float | None = None):
+    """Per-tensor FP8 (E4M3) quantisation of a bf16 [T, d] tensor.
+
+    scale None -> dynamic s = amax / 448; else the given s.
+    Returns (codes uint8 [T, d], s as np.float32).
+    """
+    xb = _u16(x)
+    T, d = xb.shape
+    codes = np.empty((T, d), np.uint8)
+    s = ctypes.c_float(0.0)
+    given = scale is not None
+    rc = _load().orc_fp8_quantize(_ptr(xb), T, d, int(given), ctypes.c_float(scale if given else 0.0),
+                                  _ptr(codes), ctypes.byref(s))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return codes, np.float32(s.value)
 
 
 def bf16_amax(x) -> np.float32:

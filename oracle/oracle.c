@@ -343,3 +343,48 @@ float orc_bf16_amax(const uint16_t* x, int64_t n)
     }
     return amax;
 }
+
+/* ------------------------------------------------------------------------ */
+/* FP8 (E4M3) per-tensor quantiser ([AR] 6.3, patterns                     */
+/* kARResidualRMSNormFP8Quant / ...OutFP8Quant), binary32 arithmetic.       */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * x      : bf16 bits [T, d], the normed output
+ * given  : nonzero -> s = s_in (a calibrated dequantisation scale);
+ *          zero    -> s = amax(|x|) / 448 over the whole tensor
+ * codes  : [T, d] E4M3 bytes: code = E4M3(x * inv), inv = min(1/s, FLT_MAX),
+ *          RNE, saturating to +-448; an s that is not a positive finite number
+ *          gives inv = 0 (signed-zero codes)
+ * s_out  : receives s (may be NULL)
+ */
+int orc_fp8_quantize(const uint16_t* x, int64_t T, int64_t d, int given, float s_in, uint8_t* codes,
+                     float* s_out)
+{
+    if (T < 0 || d < 1 || !x)
+        return -1;
+    float s;
+    if (given) {
+        s = s_in;
+    } else {
+        float amax = 0.0f;
+        for (int64_t k = 0; k < T * d; ++k) {
+            float a = fabsf((float)orc_bf16_to_double(x[k]));
+            if (a > amax)
+                amax = a;
+        }
+        s = amax / 448.0f;
+    }
+    if (s_out)
+        *s_out = s;
+    float inv = 0.0f;
+    if (s > 0.0f && !isinf(s)) {
+        inv = 1.0f / s;
+        if (inv > FLT_MAX)
+            inv = FLT_MAX;
+    }
+    if (codes)
+        for (int64_t k = 0; k < T * d; ++k)
+            codes[k] = orc_e4m3_from_float((float)orc_bf16_to_double(x[k]) * inv);
+    return 0;
+}

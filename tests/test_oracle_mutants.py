@@ -36,6 +36,9 @@ MUTANTS = [
     ("gscale_not_448", "g = amax / 2688.0f;", "g = amax / 6.0f;"),
     ("scale_without_6", "float den6 = 6.0f * g;", "float den6 = g;"),
     ("block_amax_not_abs", "float a = fabsf(xv[i]);", "float a = xv[i];"),
+    ("fp8_scale_not_448", "s = amax / 448.0f;", "s = amax / 256.0f;"),
+    ("fp8_divides_by_inverse", "codes[k] = orc_e4m3_from_float((float)orc_bf16_to_double(x[k]) * inv);",
+     "codes[k] = orc_e4m3_from_float((float)orc_bf16_to_double(x[k]) / (inv > 0.0f ? inv : 1.0f));"),
 ]
 
 

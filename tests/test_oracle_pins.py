@@ -484,3 +484,47 @@ def test_golden_small_case_regression(orc):
     assert codes.tobytes().hex() == gold["nvfp4_codes"]
     assert scales.tobytes().hex() == gold["nvfp4_scales"]
     assert float(g) == gold["nvfp4_global_scale"]
+
+
+# ---------------------------------------------------------------------- FP8
+
+def test_fp8_hand_example(orc):
+    """s = 0.5 given: code = E4M3(2x). 1.5 -> 3.0 = 0x44; -0.25 -> -0.5 = 0xB0;
+    300 -> 600 saturates to 448 = 0x7E; 1.25*2^-10 -> 1.25*2^-9 rounds to the
+    subnormal 2^-9 = 0x01; 2^-10 -> 2^-9 exactly = 0x01; 2^-11 -> 2^-10, a tie
+    between 0 and 2^-9, goes to the even code 0x00; signed zeros keep the sign."""
+    x = bf16_bits_of(np.array([[1.5, -0.25, 300.0, 1.25 * 2 ** -10, 2 ** -10, 2 ** -11, 0.0, -0.0]]))
+    codes, s = orc.fp8_quantize(x, scale=0.5)
+    assert s == 0.5
+    assert list(codes[0]) == [0x44, 0xB0, 0x7E, 0x01, 0x01, 0x00, 0x00, 0x80]
+
+
+def test_fp8_dynamic_scale_and_invariants(orc):
+    rng = np.random.default_rng(21)
+    x = rng.standard_normal((16, 256)) * 3
+    x[rng.random(x.shape) < 0.01] *= 50
+    xb = f32_to_bf16_torch(x.astype(np.float32))
+    xv = orc.bf16_to_float64(xb)
+    codes, s = orc.fp8_quantize(xb)
+    assert s == np.float32(np.float32(np.abs(xv).max()) / np.float32(448.0))
+    t, i = np.unravel_index(np.argmax(np.abs(xv)), xv.shape)
+    assert codes[t, i] & 0x7F == 0x7E  # the tensor maximum maps to +-448
+    assert (codes & 0x7F).max() <= 0x7E  # never the NaN pattern
+    # dequantisation error: half an E4M3 step (relative 2^-4) above 2^-6, else 2^-10
+    deq = orc.e4m3_to_float32(codes).astype(np.float64) * float(s)
+    q = np.abs(xv) / float(s)
+    bound = np.where(q >= 2.0 ** -6, q * 2.0 ** -4, 2.0 ** -10) * float(s) * (1 + 1e-6)
+    assert np.all(np.abs(deq - xv) <= bound)
+    nz = deq != 0
+    assert np.all(np.sign(deq[nz]) == np.sign(xv[nz]))
+    c2, s2 = orc.fp8_quantize(xb, scale=float(s))
+    assert np.array_equal(codes, c2) and s2 == s
+
+
+def test_fp8_degenerate_scales(orc):
+    xb = f32_to_bf16_torch(np.linspace(-3, 3, 32, dtype=np.float32).reshape(2, 16))
+    for s in (0.0, -1.0, float("inf"), float("nan")):
+        codes, _ = orc.fp8_quantize(xb, scale=s)
+        assert np.all((codes & 0x7F) == 0)
+    codes, s = orc.fp8_quantize(np.zeros((2, 8), np.uint16))
+    assert s == 0.0 and not codes.any()
