@@ -192,6 +192,35 @@ tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* co
                                 tpar_stream_t stream);
 
 /*
+ * tpar_fused_rmsnorm_fp8 -- the fused epilogue with per-tensor FP8 (E4M3)
+ * output, the patterns kARResidualRMSNormFP8Quant (out_norm NULL) and
+ * kARResidualRMSNormOutFP8Quant ("Deep Dive ..." 6.3).
+ *   fp8_codes  [T, d] E4M3 bytes
+ *   fp8_scale  one device fp32, the dequantisation scale s (x ~ code * s).
+ *              With TPAR_GSCALE_GIVEN an INPUT (calibrated; one pass, out_norm
+ *              may be NULL); otherwise an OUTPUT, s = amax(|out_norm|) / 448
+ *              over the whole tensor (two kernels, out_norm required, uses the
+ *              device workspace like the dynamic NVFP4 path).
+ *   code = E4M3(bf16(y) * min(1/s, FLT_MAX)), round to nearest even,
+ *   saturating; an s that is not positive and finite gives signed-zero codes.
+ * Other arguments, checks and flags (TPAR_NO_PDL, TPAR_FORCE_ROW,
+ * TPAR_FORCE_CLUSTER, TPAR_DRY_RUN) as tpar_fused_rmsnorm_ex.
+ */
+tpar_status tpar_fused_rmsnorm_fp8(const void* const* partials, int n_ranks, const void* residual,
+                                   const void* gamma, float eps, int64_t T, int64_t d, void* out_norm,
+                                   void* out_residual, uint8_t* fp8_codes, float* fp8_scale,
+                                   uint32_t flags, tpar_stream_t stream);
+
+/*
+ * tpar_fp8_quantize -- per-tensor FP8 (E4M3) quantisation of a bf16 [T, d]
+ * tensor x (d % 8 == 0) into codes [T, d]. With TPAR_GSCALE_GIVEN, *scale is
+ * the input s; otherwise s = amax(|x|) / 448 is computed on the device (two
+ * kernels, device workspace) and written to *scale. Arithmetic as above.
+ */
+tpar_status tpar_fp8_quantize(const void* x, int64_t T, int64_t d, uint8_t* codes, float* scale,
+                              uint32_t flags, tpar_stream_t stream);
+
+/*
  * tpar_plan_launch -- the launch plan the fused entry points would use for
  * (T, d, n_ranks) on a GPU with sm_count SMs, honouring TPAR_FORCE_ROW /
  * TPAR_FORCE_CLUSTER / TPAR_FORCE_STREAM. Host-only: touches no GPU.

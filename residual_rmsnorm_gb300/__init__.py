@@ -25,6 +25,8 @@ from ._abi import (  # noqa: F401
     library_path,
     tpar_fused_rmsnorm,
     tpar_fused_rmsnorm_ex,
+    tpar_fused_rmsnorm_fp8,
+    tpar_fp8_quantize,
     tpar_device_error,
     tpar_init,
     tpar_nvfp4_quantize,
@@ -36,10 +38,12 @@ from ._abi import (  # noqa: F401
     tpar_version,
     tpar_workspace_bytes,
 )
-from .ops import allreduce_sum, fused_rmsnorm, nvfp4_quantize, unfused_rmsnorm  # noqa: F401
+from .ops import (allreduce_sum, fp8_quantize, fused_rmsnorm, fused_rmsnorm_fp8,  # noqa: F401
+                  nvfp4_quantize, unfused_rmsnorm)
 
 __all__ = [
-    "fused_rmsnorm", "unfused_rmsnorm", "nvfp4_quantize", "allreduce_sum", "TparError", "TparPlan",
+    "fused_rmsnorm", "unfused_rmsnorm", "nvfp4_quantize", "allreduce_sum", "fused_rmsnorm_fp8",
+    "fp8_quantize", "tpar_fused_rmsnorm_fp8", "tpar_fp8_quantize", "TparError", "TparPlan",
     "tpar_init", "tpar_fused_rmsnorm", "tpar_fused_rmsnorm_ex", "tpar_unfused_rmsnorm",
     "tpar_nvfp4_quantize", "tpar_unfused_rmsnorm_noalloc", "tpar_plan_launch", "tpar_status_string", "tpar_version",
     "tpar_workspace_bytes", "tpar_device_error", "library", "library_path",

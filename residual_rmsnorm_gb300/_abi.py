@@ -81,6 +81,10 @@ def library() -> ctypes.CDLL:
         lib.tpar_unfused_rmsnorm.restype = i32
         lib.tpar_unfused_rmsnorm_noalloc.argtypes = [P, i32, P, P, f32, i64, i64, P, P, P, P, P, u32, P]
         lib.tpar_unfused_rmsnorm_noalloc.restype = i32
+        lib.tpar_fused_rmsnorm_fp8.argtypes = [P, i32, P, P, f32, i64, i64, P, P, P, P, u32, P]
+        lib.tpar_fused_rmsnorm_fp8.restype = i32
+        lib.tpar_fp8_quantize.argtypes = [P, i64, i64, P, P, u32, P]
+        lib.tpar_fp8_quantize.restype = i32
         lib.tpar_nvfp4_quantize.argtypes = [P, i64, i64, P, P, P, u32, P]
         lib.tpar_nvfp4_quantize.restype = i32
         lib.tpar_plan_launch.argtypes = [i64, i64, i32, i32, u32, ctypes.POINTER(TparPlan)]
@@ -173,6 +177,20 @@ def tpar_nvfp4_quantize(x, T, d, codes, scales, global_scale, flags, stream, che
     st = library().tpar_nvfp4_quantize(_p(x), T, d, _p(codes), _p(scales), _p(global_scale),
                                        flags, _p(stream))
     return _check(st, "tpar_nvfp4_quantize") if check else st
+
+
+def tpar_fused_rmsnorm_fp8(partials, n_ranks, residual, gamma, eps, T, d, out_norm, out_residual,
+                           fp8_codes, fp8_scale, flags, stream, check=True) -> int:
+    arr = _ptr_array(partials)
+    st = library().tpar_fused_rmsnorm_fp8(ctypes.cast(arr, ctypes.c_void_p), n_ranks, _p(residual),
+                                          _p(gamma), eps, T, d, _p(out_norm), _p(out_residual),
+                                          _p(fp8_codes), _p(fp8_scale), flags, _p(stream))
+    return _check(st, "tpar_fused_rmsnorm_fp8") if check else st
+
+
+def tpar_fp8_quantize(x, T, d, codes, scale, flags, stream, check=True) -> int:
+    st = library().tpar_fp8_quantize(_p(x), T, d, _p(codes), _p(scale), flags, _p(stream))
+    return _check(st, "tpar_fp8_quantize") if check else st
 
 
 def tpar_plan_launch(T, d, n_ranks, sm_count, flags=0) -> TparPlan:

@@ -266,7 +266,8 @@ struct Call {
     uint8_t* scales;
     float* gscale;
     uint32_t flags;
-    void* reduced;  // unfused only
+    void* reduced;     // unfused only
+    bool fp8 = false;  // an FP8 output accompanies the bf16 ones (checked by its entry point)
 };
 
 // Host-side checks shared by the fused and unfused entry points.
@@ -287,7 +288,7 @@ tpar_status validate(const Call& c, bool unfused)
     // An empty batch is a no-op: its tensors may be NULL (empty allocations).
     if (c.T == 0)
         return TPAR_OK;
-    if (!c.gamma && (c.out_norm || c.codes || unfused))
+    if (!c.gamma && (c.out_norm || c.codes || c.fp8 || unfused))
         return TPAR_ERR_INVALID_ARG;
     for (int r = 0; r < c.n_ranks; ++r)
         if (!c.partials[r])
@@ -299,12 +300,13 @@ tpar_status validate(const Call& c, bool unfused)
     const bool given = (c.flags & TPAR_GSCALE_GIVEN) != 0;
     if (nvfp4 && c.d % 16 != 0)
         return TPAR_ERR_INVALID_ARG;
-    if (!nvfp4 && given)
+    if (!nvfp4 && !c.fp8 && given)
         return TPAR_ERR_INVALID_ARG;
     // out_norm may be NULL for NVFP4 with a given scale, or (fused entry points,
     // no quantisation) for the all-reduce-only pattern, which then needs no gamma.
-    const bool sum_only = !unfused && !nvfp4 && !c.out_norm;
-    if (!c.out_norm && !(nvfp4 && given && !unfused) && !sum_only)
+    const bool sum_only = !unfused && !nvfp4 && !c.fp8 && !c.out_norm;
+    const bool quant_only = !unfused && (nvfp4 || c.fp8) && given;  // no bf16 norm output needed
+    if (!c.out_norm && !quant_only && !sum_only)
         return TPAR_ERR_INVALID_ARG;
     if (sum_only && !c.out_residual)
         return TPAR_ERR_INVALID_ARG;
@@ -432,6 +434,7 @@ const void* fused_kernel(int qmode, int nr, int vpt, bool cluster)
     case 0: return tpar::fused_kernel_q0(nr, vpt, cluster);
     case 1: return tpar::fused_kernel_q1(nr, vpt, cluster);
     case 2: return tpar::fused_kernel_q2(nr, vpt, cluster);
+    case 3: return tpar::fused_kernel_q3(nr, vpt, cluster);
     default: return nullptr;
     }
 }
@@ -812,6 +815,137 @@ tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* co
     if (st != TPAR_OK && ws)
         cudaMemsetAsync(ws, 0, 8, stream);
     return st;
+}
+
+tpar_status tpar_fused_rmsnorm_fp8(const void* const* partials, int n_ranks, const void* residual,
+                                   const void* gamma, float eps, int64_t T, int64_t d, void* out_norm,
+                                   void* out_residual, uint8_t* fp8_codes, float* fp8_scale, uint32_t flags,
+                                   tpar_stream_t stream_)
+{
+    const bool given = (flags & TPAR_GSCALE_GIVEN) != 0;
+    Call c{partials, n_ranks, residual, gamma, eps, T, d, out_norm, out_residual, nullptr, nullptr, nullptr,
+           flags & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_FORCE_ROW | TPAR_FORCE_CLUSTER), nullptr, true};
+    tpar_status st = validate(c, false);
+    if (st != TPAR_OK)
+        return st;
+    if (T > 0) {
+        if (!fp8_codes || !fp8_scale || !gamma)
+            return TPAR_ERR_INVALID_ARG;
+        if (!out_norm && !given)
+            return TPAR_ERR_INVALID_ARG;  // the dynamic scale re-reads out_norm
+        if (!aligned(fp8_codes, 16) || !aligned(fp8_scale, 4))
+            return TPAR_ERR_MISALIGNED;
+        const int64_t td2 = T * d * 2;
+        const Range rq(fp8_codes, T * d), rs(fp8_scale, 4);
+        const Range others[] = {Range(residual, td2), Range(gamma, d * 2), Range(out_norm, td2),
+                                Range(out_residual, td2)};
+        for (const Range& o : others)
+            if (rq.overlaps(o) || rs.overlaps(o))
+                return TPAR_ERR_INVALID_ARG;
+        for (int r = 0; r < n_ranks; ++r)
+            if (rq.overlaps(Range(partials[r], td2)) || rs.overlaps(Range(partials[r], td2)))
+                return TPAR_ERR_INVALID_ARG;
+        if (rq.overlaps(rs))
+            return TPAR_ERR_INVALID_ARG;
+    }
+    if ((flags & TPAR_DRY_RUN) || T == 0)
+        return TPAR_OK;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    int sm = 0;
+    if ((st = current_sm_count(&sm)) != TPAR_OK)
+        return st;
+    tpar_plan p;
+    if ((st = plan_impl(T, d, n_ranks, sm, c.flags, &p)) != TPAR_OK)
+        return st;
+    const bool pdl = (flags & TPAR_NO_PDL) == 0;
+    FusedArgs a = fused_args(c);
+    a.slice = p.kernel == 1 ? slice_for(a.nvec, p.split) : a.nvec;
+    if (given) {
+        a.q8 = reinterpret_cast<uint2*>(fp8_codes);
+        a.gscale = fp8_scale;
+        return launch_fused(a, tpar::kQuantFp8Given, p, stream, pdl);
+    }
+    uint32_t* ws = nullptr;
+    if ((st = workspace_for(nullptr, stream, &ws)) != TPAR_OK)
+        return st;
+    a.amax_bits = ws;
+    if ((st = launch_fused(a, tpar::kQuantAmax, p, stream, pdl)) != TPAR_OK)
+        return st;
+    tpar::Fp8Args f;
+    f.x = static_cast<const uint4*>(out_norm);
+    f.codes = reinterpret_cast<uint2*>(fp8_codes);
+    f.scale = fp8_scale;
+    f.ws = ws;
+    f.nvec = T * d / 8;
+    if (launch(tpar::fp8_quantize_kernel_for(true), dim3(flat_grid(f.nvec, sm)), dim3(256), &f, stream, 1, pdl) !=
+        cudaSuccess) {
+        cudaMemsetAsync(ws, 0, 8, stream);
+        return TPAR_ERR_CUDA;
+    }
+    return TPAR_OK;
+}
+
+tpar_status tpar_fp8_quantize(const void* x, int64_t T, int64_t d, uint8_t* codes, float* scale, uint32_t flags,
+                              tpar_stream_t stream_)
+{
+    if (T < 0 || d < 8 || d % 8 != 0)
+        return TPAR_ERR_INVALID_ARG;
+    if (d > TPAR_MAX_HIDDEN)
+        return TPAR_ERR_UNSUPPORTED;
+    if (T > (INT64_MAX / 4) / d)
+        return TPAR_ERR_INVALID_ARG;
+    if (T == 0)
+        return TPAR_OK;
+    if (!x || !codes || !scale)
+        return TPAR_ERR_INVALID_ARG;
+    if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(scale, 4))
+        return TPAR_ERR_MISALIGNED;
+    Range rx(x, T * d * 2), rc(codes, T * d), rs(scale, 4);
+    if (rc.overlaps(rx) || rs.overlaps(rx) || rc.overlaps(rs))
+        return TPAR_ERR_INVALID_ARG;
+    if (flags & TPAR_DRY_RUN)
+        return TPAR_OK;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+    const bool pdl = (flags & TPAR_NO_PDL) == 0;
+    const bool given = (flags & TPAR_GSCALE_GIVEN) != 0;
+    int sm = 0;
+    tpar_status st = current_sm_count(&sm);
+    if (st != TPAR_OK)
+        return st;
+    const int64_t nvec = T * d / 8;
+    uint32_t* ws = nullptr;
+    if (!given) {
+        if ((st = workspace_for(nullptr, stream, &ws)) != TPAR_OK)
+            return st;
+        const uint4* xv = static_cast<const uint4*>(x);
+        int64_t n = nvec;
+        void* args[3] = {&xv, &n, &ws};
+        cudaLaunchConfig_t cfg;
+        std::memset(&cfg, 0, sizeof cfg);
+        cfg.gridDim = dim3(flat_grid(nvec, sm));
+        cfg.blockDim = dim3(256);
+        cfg.stream = stream;
+        cudaLaunchAttribute at;
+        at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        at.val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = &at;
+        cfg.numAttrs = pdl ? 1 : 0;
+        if (cudaLaunchKernelExC(&cfg, tpar::amax_kernel_ptr(), args) != cudaSuccess)
+            return TPAR_ERR_CUDA;
+    }
+    tpar::Fp8Args f;
+    f.x = static_cast<const uint4*>(x);
+    f.codes = reinterpret_cast<uint2*>(codes);
+    f.scale = scale;
+    f.ws = ws;
+    f.nvec = nvec;
+    if (launch(tpar::fp8_quantize_kernel_for(!given), dim3(flat_grid(nvec, sm)), dim3(256), &f, stream, 1, pdl) !=
+        cudaSuccess) {
+        if (ws)
+            cudaMemsetAsync(ws, 0, 8, stream);
+        return TPAR_ERR_CUDA;
+    }
+    return TPAR_OK;
 }
 
 tpar_status tpar_plan_launch(int64_t T, int64_t d, int n_ranks, int sm_count, uint32_t flags, tpar_plan* out)

@@ -297,6 +297,29 @@ __device__ __forceinline__ uint32_t e2m1x8_from_f32(const float q[8])
     return out;
 }
 
+// Eight binary32 -> eight E4M3 bytes (round to nearest even, saturating to
+// +-448), element k in byte k.
+__device__ __forceinline__ uint2 e4m3x8_from_f32(const float q[8])
+{
+    uint16_t p0, p1, p2, p3;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(p0) : "f"(q[1]), "f"(q[0]));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(p1) : "f"(q[3]), "f"(q[2]));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(p2) : "f"(q[5]), "f"(q[4]));
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(p3) : "f"(q[7]), "f"(q[6]));
+    return make_uint2(static_cast<uint32_t>(p0) | (static_cast<uint32_t>(p1) << 16),
+                      static_cast<uint32_t>(p2) | (static_cast<uint32_t>(p3) << 16));
+}
+
+// Element multiplier of per-tensor FP8 for a dequantisation scale s:
+// min(1/s, FLT_MAX), or 0 when s is not a positive finite number (IEEE
+// division, round to nearest even).
+__device__ __forceinline__ float fp8_inverse_scale(float s)
+{
+    if (!(s > 0.0f) || !(s <= 3.402823466e38f))
+        return 0.0f;
+    return fminf(__fdiv_rn(1.0f, s), 3.402823466e38f);
+}
+
 // The per-block scale of NVFP4 for a given global scale g and block maximum
 // |x|: writes the E4M3 scale byte and returns the element multiplier
 // inv = min(1 / (s * g), FLT_MAX), or 0 when the scale byte is 0 or g is not

@@ -12,6 +12,7 @@ namespace tpar {
 const void* fused_kernel_q0(int nr, int vpt, bool cluster);
 const void* fused_kernel_q1(int nr, int vpt, bool cluster);
 const void* fused_kernel_q2(int nr, int vpt, bool cluster);
+const void* fused_kernel_q3(int nr, int vpt, bool cluster);
 
 // TMA-fed bandwidth kernel (stream.cuh) for quantisation mode q, rank bound
 // nr and vpt vectors per consumer thread.
@@ -25,6 +26,7 @@ const void* reduce_kernel_for(int nr);
 const void* residual_add_kernel_ptr();
 const void* quantize_kernel_for(bool dynamic);
 const void* amax_kernel_ptr();
+const void* fp8_quantize_kernel_for(bool dynamic);
 
 // Largest CTA the fused kernel for rank bound nr, vpt vectors per thread and
 // the row (cluster = false) or cluster form is compiled for (mirrors

@@ -30,6 +30,7 @@ enum QuantMode : int {
     kQuantNone = 0,     // bf16 outputs only
     kQuantGiven = 1,    // NVFP4 with a caller-given global scale, same pass
     kQuantAmax = 2,     // dynamic scale, phase A: fold |bf16(y)| into a device max
+    kQuantFp8Given = 3, // per-tensor FP8 (E4M3) with a caller-given scale, same pass
 };
 
 struct FusedArgs {
@@ -40,6 +41,7 @@ struct FusedArgs {
     uint4* out_residual;               // bf16 [T, d] or null
     uint32_t* codes;                   // [T, d/2] bytes = one word per input vector
     uint8_t* scales;                   // [T, d/16]
+    uint2* q8;                         // FP8 codes [T, d] = 8 bytes per input vector
     const float* gscale;               // given g (kQuantGiven)
     uint32_t* amax_bits;               // running max of |out_norm| bits (kQuantAmax)
     uint32_t* err;                     // device error word (bounded wait expired) or null
@@ -81,6 +83,16 @@ __device__ __forceinline__ void emit_vector(const FusedArgs& a, bool valid, int6
 #pragma unroll
         for (int e = 0; e < 8; ++e)
             amax_local = fmaxf(amax_local, fabsf(yq[e]));
+    }
+    if constexpr (QMODE == kQuantFp8Given) {
+        if (valid) {
+            float q[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                q[e] = __fmul_rn(yq[e], g_given);  // g_given holds 1/s here
+            const uint2 c = e4m3x8_from_f32(q);
+            asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(a.q8 + gv), "r"(c.x), "r"(c.y) : "memory");
+        }
     }
     if constexpr (QMODE == kQuantGiven) {
         float bmax = 0.0f;
@@ -164,6 +176,8 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT, CLUSTER))
     float g_given = 0.0f;
     if constexpr (QMODE == kQuantGiven)
         g_given = *a.gscale;
+    if constexpr (QMODE == kQuantFp8Given)
+        g_given = fp8_inverse_scale(*a.gscale);
     float amax_local = 0.0f;
 
     int it = 0;
@@ -354,6 +368,56 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __grid_consta
             q[e] = __fmul_rn(x[e], inv);
         st_v2(a.codes + 2 * b, e2m1x8_from_f32(q), e2m1x8_from_f32(q + 8));
         st_u8(a.scales + b, sbyte);
+    }
+}
+
+// Per-tensor FP8 quantiser (phase B of the dynamic-scale FP8 path, and the
+// standalone quantiser): one 16-byte vector per thread per iteration. In
+// dynamic mode s = amax / 448 comes from the workspace and the last CTA to
+// have read it zeroes the workspace; with a given scale s is *scale.
+struct Fp8Args {
+    const uint4* x;    // bf16 [T, d] as T*d/8 vectors
+    uint2* codes;      // [T, d] E4M3 bytes, 8 per vector
+    float* scale;      // given: input; dynamic: output
+    uint32_t* ws;      // dynamic: ws[0] = amax bits, ws[1] = completion counter
+    int64_t nvec;
+};
+
+template <bool DYNAMIC>
+__global__ void __launch_bounds__(256) fp8_quantize_kernel(const __grid_constant__ Fp8Args a)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    __shared__ float inv_sh;
+    if (threadIdx.x == 0) {
+        float s;
+        if constexpr (DYNAMIC) {
+            const uint32_t bits = *reinterpret_cast<volatile uint32_t*>(a.ws);
+            s = __fdiv_rn(__uint_as_float(bits), 448.0f);
+            if (blockIdx.x == 0)
+                *a.scale = s;
+            __threadfence();
+            const uint32_t done = atomicAdd(a.ws + 1, 1u);
+            if (done == gridDim.x - 1) {
+                a.ws[0] = 0u;
+                a.ws[1] = 0u;
+            }
+        } else {
+            s = *a.scale;
+        }
+        inv_sh = fp8_inverse_scale(s);
+    }
+    __syncthreads();
+    const float inv = inv_sh;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < a.nvec; v += stride) {
+        float x[8];
+        unpack8(ld_stream(a.x + v), x);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            x[e] = __fmul_rn(x[e], inv);
+        const uint2 c = e4m3x8_from_f32(x);
+        asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(a.codes + v), "r"(c.x), "r"(c.y) : "memory");
     }
 }
 

@@ -63,4 +63,10 @@ const void* quantize_kernel_for(bool dynamic)
 
 const void* amax_kernel_ptr() { return reinterpret_cast<const void*>(&amax_kernel); }
 
+const void* fp8_quantize_kernel_for(bool dynamic)
+{
+    return dynamic ? reinterpret_cast<const void*>(&fp8_quantize_kernel<true>)
+                   : reinterpret_cast<const void*>(&fp8_quantize_kernel<false>);
+}
+
 }  // namespace tpar

@@ -155,3 +155,49 @@ def nvfp4_quantize(x, global_scale: torch.Tensor | None = None, flags: int = 0, 
         _abi.tpar_nvfp4_quantize(x.data_ptr(), T, d, codes.data_ptr(), scales.data_ptr(),
                                  g.data_ptr(), flags, _stream_handle(x.device, stream))
     return codes, scales, g
+
+
+def fused_rmsnorm_fp8(partials, residual, gamma, eps: float, *, scale: torch.Tensor | None = None,
+                      emit_norm: bool = True, out_residual=None, flags: int = 0, stream=None):
+    """sum + residual -> RMSNorm -> per-tensor FP8 (E4M3). ``scale`` (a 1-element
+    fp32 tensor) given: calibrated single pass; None: s = amax/448 computed.
+    Returns dict(out_norm, out_residual, codes uint8 [T, d], scale)."""
+    partials = list(partials)
+    T, d = partials[0].shape
+    dev = partials[0].device
+    for i, p in enumerate(partials):
+        _check_bf16(f"partials[{i}]", p, (T, d))
+    if residual is not None:
+        _check_bf16("residual", residual, (T, d))
+    _check_bf16("gamma", gamma, (d,))
+    out_norm = torch.empty((T, d), dtype=torch.bfloat16, device=dev) if (emit_norm or scale is None) else None
+    out_residual = torch.empty((T, d), dtype=torch.bfloat16, device=dev) if out_residual is None else out_residual
+    codes = torch.empty((T, d), dtype=torch.uint8, device=dev)
+    if scale is None:
+        s = torch.empty((1,), dtype=torch.float32, device=dev)
+    else:
+        s = scale
+        flags |= _abi.TPAR_GSCALE_GIVEN
+    with torch.cuda.device(dev):
+        _abi.tpar_fused_rmsnorm_fp8(
+            [p.data_ptr() for p in partials], len(partials),
+            residual.data_ptr() if residual is not None else 0, gamma.data_ptr(), float(eps), T, d,
+            out_norm.data_ptr() if out_norm is not None else 0, out_residual.data_ptr(), codes.data_ptr(),
+            s.data_ptr(), flags, _stream_handle(dev, stream))
+    return {"out_norm": out_norm, "out_residual": out_residual, "codes": codes, "scale": s}
+
+
+def fp8_quantize(x, scale: torch.Tensor | None = None, flags: int = 0, stream=None):
+    """Per-tensor FP8 (E4M3) quantisation of a bf16 [T, d] CUDA tensor -> (codes, scale)."""
+    _check_bf16("x", x)
+    T, d = x.shape
+    codes = torch.empty((T, d), dtype=torch.uint8, device=x.device)
+    if scale is None:
+        s = torch.empty((1,), dtype=torch.float32, device=x.device)
+    else:
+        s = scale
+        flags |= _abi.TPAR_GSCALE_GIVEN
+    with torch.cuda.device(x.device):
+        _abi.tpar_fp8_quantize(x.data_ptr(), T, d, codes.data_ptr(), s.data_ptr(), flags,
+                               _stream_handle(x.device, stream))
+    return codes, s

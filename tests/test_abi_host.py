@@ -229,3 +229,22 @@ def test_planner_choices_for_the_pages_shapes(tp):
     assert tp.tpar_plan_launch(8, 8192, 8, 152, tp.TPAR_FORCE_STREAM).kernel == 2
     assert tp.tpar_plan_launch(1, 8192, 8, 152, tp.TPAR_FORCE_ROW).kernel == 0
     assert tp.tpar_plan_launch(4096, 4096, 8, 152, tp.TPAR_FORCE_CLUSTER).kernel == 1
+
+
+def test_fp8_entry_point_checks(tp):
+    parts = [BASE + r * 4 * MB for r in range(4)]
+    f = lambda out_norm=BASE + 128 * MB, out_res=BASE + 160 * MB, codes=BASE + 200 * MB, sc=BASE + 240 * MB, \
+        flags=tp.TPAR_DRY_RUN, d=4096, gamma=BASE + 96 * MB: tp.tpar_fused_rmsnorm_fp8(
+            parts, 4, BASE + 64 * MB, gamma, 1e-5, 8, d, out_norm, out_res, codes, sc, flags, 0, check=False)
+    assert f() == OK
+    assert f(out_norm=0) == INVALID  # dynamic scale re-reads out_norm
+    assert f(out_norm=0, flags=tp.TPAR_DRY_RUN | tp.TPAR_GSCALE_GIVEN) == OK
+    assert f(out_norm=0, out_res=0, flags=tp.TPAR_DRY_RUN | tp.TPAR_GSCALE_GIVEN) == OK
+    assert f(codes=0) == INVALID and f(sc=0) == INVALID and f(gamma=0) == INVALID
+    assert f(codes=BASE + 200 * MB + 8) == MISALIGNED
+    assert f(codes=BASE + 128 * MB) == INVALID  # on out_norm
+    assert f(sc=BASE + 200 * MB + 64) == INVALID  # inside the codes
+    assert f(d=12) == INVALID
+    q = lambda x=BASE, c=BASE + 64 * MB, s=BASE + 80 * MB, d=4096: tp.tpar_fp8_quantize(
+        x, 8, d, c, s, tp.TPAR_DRY_RUN, 0, check=False)
+    assert q() == OK and q(c=BASE + 1024) == INVALID and q(d=12) == INVALID and q(x=BASE + 4) == MISALIGNED

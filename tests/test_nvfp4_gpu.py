@@ -186,3 +186,56 @@ def test_single_launch_dynamic_matches_two_pass(T, d, n):
     assert_close_to_ref(one["out_residual"], ref["h"], "single-launch out_residual")
     assert_nvfp4_bit_exact(one["out_norm"], one["codes"], one["scales"], one["global_scale"], what="single")
     assert tp.tpar_device_error(torch.cuda.current_device()) == 0
+
+
+
+# ---------------------------------------------------------------------- FP8
+
+@pytest.mark.parametrize("dynamic", [True, False])
+@pytest.mark.parametrize("T,d", [(1, 16), (7, 264), (64, 4096), (300, 8192)])
+def test_fp8_standalone_quantiser(dynamic, T, d):
+    tp = lib()
+    x = synth.random_bf16((T, d), 2.0, seed=T + d)
+    s_in = None if dynamic else torch.tensor([0.0123], dtype=torch.float32, device="cuda")
+    codes, s = tp.fp8_quantize(x.cuda(), scale=s_in)
+    torch.cuda.synchronize()
+    oc, os_ = oracle.fp8_quantize(synth.bits(x), scale=None if dynamic else float(np.float32(0.0123)))
+    assert np.float32(s.item()) == os_
+    assert np.array_equal(codes.cpu().numpy(), oc)
+
+
+def test_fp8_specials_and_degenerate_scales():
+    tp = lib()
+    vals = np.array([0.0, -0.0, 1e-30, -1e-30, 3e-39, 1e30, -1e30, 3.3e38, 1.0, -1.0, 448.0, -600.0,
+                     2 ** -10, 2 ** -11, -(2 ** -11), 5.0], np.float64)
+    x = oracle.bf16_from_float64(np.tile(vals, (2, 2)))
+    for s in (1.0, 1e-20, 1e20, 3e-39, 0.0, -2.0, float("inf"), float("nan")):
+        codes, s_out = tp.fp8_quantize(synth.from_bits(x, "cuda"),
+                                       scale=torch.tensor([s], dtype=torch.float32, device="cuda"))
+        torch.cuda.synchronize()
+        oc, _ = oracle.fp8_quantize(x, scale=s)
+        assert np.array_equal(codes.cpu().numpy(), oc), s
+
+
+@pytest.mark.parametrize("T", [1, 8, 333, 4096])
+@pytest.mark.parametrize("given", [False, True])
+def test_fused_fp8(T, given):
+    tp = lib()
+    w = synth.PREFILL.with_(T=T, d=8192 if T < 4096 else 4096)
+    inputs = synth.make_inputs(w)
+    dev = to_device(inputs)
+    s = torch.tensor([0.02], dtype=torch.float32, device="cuda") if given else None
+    out = tp.fused_rmsnorm_fp8(dev["partials"], dev["residual"], dev["gamma"], w.eps, scale=s)
+    torch.cuda.synchronize()
+    rows = np.arange(T) if T <= 64 else np.unique(np.random.default_rng(T).choice(T, 40, replace=False))
+    ref = oracle_rows(inputs, rows, w.eps)
+    assert_close_to_ref(out["out_norm"][rows], ref["y"], "fp8 path out_norm")
+    assert_close_to_ref(out["out_residual"][rows], ref["h"], "fp8 path out_residual")
+    oc, os_ = oracle.fp8_quantize(synth.bits(out["out_norm"]), scale=0.02 if given else None)
+    assert np.float32(out["scale"].item()) == os_
+    assert np.array_equal(out["codes"].cpu().numpy(), oc)
+    if given:  # without the bf16 norm output: the same codes
+        o2 = tp.fused_rmsnorm_fp8(dev["partials"], dev["residual"], dev["gamma"], w.eps, scale=s,
+                                  emit_norm=False)
+        torch.cuda.synchronize()
+        assert o2["out_norm"] is None and torch.equal(o2["codes"], out["codes"])
