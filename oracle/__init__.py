@@ -73,6 +73,15 @@ def _load():
         for name in ("orc_bf16_from_double_n", "orc_e4m3_from_float_n", "orc_e2m1_from_float_n"):
             getattr(lib, name).restype = None
             getattr(lib, name).argtypes = [P, P, i64]
+        lib.orc_f16_from_double_n.restype = None
+        lib.orc_f16_from_double_n.argtypes = [P, P, i64]
+        lib.orc_fused_rmsnorm_dt.restype = ctypes.c_int
+        lib.orc_fused_rmsnorm_dt.argtypes = [P, ctypes.c_int, P, P, ctypes.c_float, i64, i64, ctypes.c_int,
+                                             P, P, P, P]
+        lib.orc_nvfp4_quantize_dt.restype = ctypes.c_int
+        lib.orc_nvfp4_quantize_dt.argtypes = [P, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_float, P, P, P]
+        lib.orc_fp8_quantize_dt.restype = ctypes.c_int
+        lib.orc_fp8_quantize_dt.argtypes = [P, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_float, P, P]
         lib.orc_fused_rmsnorm.restype = ctypes.c_int
         lib.orc_fused_rmsnorm.argtypes = [P, ctypes.c_int, P, P, ctypes.c_float, i64, i64,
                                           P, P, P, P]
@@ -113,6 +122,26 @@ def bf16_from_float64(x) -> np.ndarray:
     return out
 
 
+def f16_to_float64(bits) -> np.ndarray:
+    """Decode IEEE binary16 bit patterns (exact)."""
+    return _u16(bits).view(np.float16).astype(np.float64)
+
+
+def f16_from_float64(x) -> np.ndarray:
+    """Round fp64 values to binary16 (nearest, ties to even), as uint16 bits."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().orc_f16_from_double_n(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+DTYPES = {"bf16": 0, "fp16": 1}
+
+
+def to_float64(bits, dtype: str = "bf16") -> np.ndarray:
+    return bf16_to_float64(bits) if dtype == "bf16" else f16_to_float64(bits)
+
+
 def e4m3_from_float32(x) -> np.ndarray:
     """binary32 -> E4M3 bytes, nearest-even, saturating at +-448."""
     x = np.ascontiguousarray(x, dtype=np.float32)
@@ -145,7 +174,7 @@ def e2m1_to_float32(codes) -> np.ndarray:
 
 # ---------------------------------------------------------------- the method
 
-def fused_rmsnorm(partials, residual, gamma, eps: float, want_ref: bool = True):
+def fused_rmsnorm(partials, residual, gamma, eps: float, want_ref: bool = True, dtype: str = "bf16"):
     """Rank sum -> residual add -> RMSNorm on bf16 bit-pattern arrays.
 
     partials : list of n uint16 arrays [T, d]; residual: uint16 [T, d] or None;
@@ -171,9 +200,9 @@ def fused_rmsnorm(partials, residual, gamma, eps: float, want_ref: bool = True):
     out_n = np.empty((T, d), np.uint16)
     h = np.empty((T, d), np.float64) if want_ref else None
     y = np.empty((T, d), np.float64) if want_ref else None
-    rc = _load().orc_fused_rmsnorm(ctypes.cast(arr, ctypes.c_void_p), len(parts), _ptr(res),
-                                   _ptr(g), ctypes.c_float(eps), T, d, _ptr(h), _ptr(y),
-                                   _ptr(out_r), _ptr(out_n))
+    rc = _load().orc_fused_rmsnorm_dt(ctypes.cast(arr, ctypes.c_void_p), len(parts), _ptr(res),
+                                      _ptr(g), ctypes.c_float(eps), T, d, DTYPES[dtype], _ptr(h), _ptr(y),
+                                      _ptr(out_r), _ptr(out_n))
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     out = {"out_residual": out_r, "out_norm": out_n}
@@ -183,7 +212,7 @@ def fused_rmsnorm(partials, residual, gamma, eps: float, want_ref: bool = True):
     return out
 
 
-def nvfp4_quantize(x, global_scale: float | None = None):
+def nvfp4_quantize(x, global_scale: float | None = None, dtype: str = "bf16"):
     """NVFP4 quantisation of a bf16 [T, d] tensor (d % 16 == 0).
 
     global_scale None -> dynamic g = amax / (6 * 448); else the given g.
@@ -195,15 +224,15 @@ def nvfp4_quantize(x, global_scale: float | None = None):
     scales = np.empty((T, d // 16), np.uint8)
     g = ctypes.c_float(0.0)
     given = global_scale is not None
-    rc = _load().orc_nvfp4_quantize(_ptr(xb), T, d, int(given),
-                                    ctypes.c_float(global_scale if given else 0.0),
-                                    _ptr(codes), _ptr(scales), ctypes.byref(g))
+    rc = _load().orc_nvfp4_quantize_dt(_ptr(xb), T, d, DTYPES[dtype], int(given),
+                                       ctypes.c_float(global_scale if given else 0.0),
+                                       _ptr(codes), _ptr(scales), ctypes.byref(g))
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return codes, scales, np.float32(g.value)
 
 
-def fp8_quantize(x, scale: float | None = None):
+def fp8_quantize(x, scale: float | None = None, dtype: str = "bf16"):
     """Per-tensor FP8 (E4M3) quantisation of a bf16 [T, d] tensor.
 
     scale None -> dynamic s = amax / 448; else the given s.
@@ -214,8 +243,8 @@ def fp8_quantize(x, scale: float | None = None):
     codes = np.empty((T, d), np.uint8)
     s = ctypes.c_float(0.0)
     given = scale is not None
-    rc = _load().orc_fp8_quantize(_ptr(xb), T, d, int(given), ctypes.c_float(scale if given else 0.0),
-                                  _ptr(codes), ctypes.byref(s))
+    rc = _load().orc_fp8_quantize_dt(_ptr(xb), T, d, DTYPES[dtype], int(given),
+                                     ctypes.c_float(scale if given else 0.0), _ptr(codes), ctypes.byref(s))
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return codes, np.float32(s.value)

@@ -80,6 +80,59 @@ uint16_t orc_bf16_from_double(double x)
     return (uint16_t)(sign | (uint16_t)(u >> 16));
 }
 
+/* IEEE binary16: 1 sign, 5 exponent bits (bias 15), 10 fraction bits,
+ * subnormals below 2^-14 (spacing 2^-24), largest finite 65504. */
+double orc_f16_to_double(uint16_t h)
+{
+    int s = (h >> 15) & 1, e = (h >> 10) & 0x1F, m = h & 0x3FF;
+    double v;
+    if (e == 31)
+        v = m ? NAN : INFINITY;
+    else if (e == 0)
+        v = ldexp((double)m, -24);
+    else
+        v = ldexp(1.0 + m / 1024.0, e - 15);
+    return s ? -v : v;
+}
+
+/* Round a double straight to binary16, nearest, ties to even; overflow to
+ * infinity (same scale-and-rint method as orc_bf16_from_double). */
+uint16_t orc_f16_from_double(double x)
+{
+    uint16_t sign = signbit(x) ? 0x8000u : 0u;
+    if (isnan(x))
+        return 0x7E00u;
+    double a = fabs(x);
+    if (a == 0.0)
+        return sign;
+    if (isinf(a) || a >= 65520.0) /* 65520 = halfway to 2^16: rounds to inf */
+        return (uint16_t)(sign | 0x7C00u);
+    int e;
+    frexp(a, &e); /* a in [2^(e-1), 2^e) */
+    int qexp = (e - 1) - 10;
+    if (qexp < -24)
+        qexp = -24;
+    double q = ldexp(1.0, qexp);
+    double r = rint(a / q) * q; /* <= 65504 here */
+    if (r < 0x1p-14)
+        return (uint16_t)(sign | (uint16_t)(r / 0x1p-24)); /* subnormal (or 2^-14 exactly below) */
+    int er;
+    double f = frexp(r, &er); /* r = 2f * 2^(er-1), 2f in [1, 2) */
+    int m = (int)((2.0 * f - 1.0) * 1024.0);
+    return (uint16_t)(sign | (uint16_t)(((er - 1 + 15) << 10) | m));
+}
+
+/* Element decode / encode of the tensors' dtype: 0 = bf16, 1 = fp16. */
+static double elem_to_double(uint16_t v, int dtype)
+{
+    return dtype ? orc_f16_to_double(v) : orc_bf16_to_double(v);
+}
+
+static uint16_t elem_from_double(double x, int dtype)
+{
+    return dtype ? orc_f16_from_double(x) : orc_bf16_from_double(x);
+}
+
 /* E4M3 (OCP FP8): 1 sign, 4 exponent bits (bias 7), 3 mantissa bits,
  * subnormals at exponent field 0, S.1111.111 is NaN, no infinities,
  * largest finite 448. */
@@ -184,6 +237,11 @@ void orc_bf16_from_double_n(const double* x, uint16_t* out, int64_t n)
     for (int64_t i = 0; i < n; ++i)
         out[i] = orc_bf16_from_double(x[i]);
 }
+void orc_f16_from_double_n(const double* x, uint16_t* out, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = orc_f16_from_double(x[i]);
+}
 void orc_e4m3_from_float_n(const float* x, uint8_t* out, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i)
@@ -210,9 +268,23 @@ void orc_e2m1_from_float_n(const float* x, uint8_t* out, int64_t n)
  * out_norm  : bf16 bits [T, d] or NULL -- bf16_rne(y)
  * Returns 0, or -1 on a bad argument.
  */
+int orc_fused_rmsnorm_dt(const uint16_t* const* partials, int n, const uint16_t* residual,
+                         const uint16_t* gamma, float eps, int64_t T, int64_t d, int dtype,
+                         double* h_ref, double* y_ref, uint16_t* out_res, uint16_t* out_norm);
+
 int orc_fused_rmsnorm(const uint16_t* const* partials, int n, const uint16_t* residual,
                       const uint16_t* gamma, float eps, int64_t T, int64_t d, double* h_ref,
                       double* y_ref, uint16_t* out_res, uint16_t* out_norm)
+{
+    return orc_fused_rmsnorm_dt(partials, n, residual, gamma, eps, T, d, 0, h_ref, y_ref, out_res,
+                                out_norm);
+}
+
+/* As orc_fused_rmsnorm, for tensors of dtype 0 (bf16) or 1 (fp16): every
+ * input is decoded and every output rounded in that format. */
+int orc_fused_rmsnorm_dt(const uint16_t* const* partials, int n, const uint16_t* residual,
+                         const uint16_t* gamma, float eps, int64_t T, int64_t d, int dtype,
+                         double* h_ref, double* y_ref, uint16_t* out_res, uint16_t* out_norm)
 {
     if (n < 1 || T < 0 || d < 1 || !partials || !gamma)
         return -1;
@@ -223,12 +295,12 @@ int orc_fused_rmsnorm(const uint16_t* const* partials, int n, const uint16_t* re
         for (int64_t i = 0; i < d; ++i) {
             double s = 0.0;
             for (int r = 0; r < n; ++r)
-                s += orc_bf16_to_double(partials[r][row + i]);
-            double h = residual ? s + orc_bf16_to_double(residual[row + i]) : s;
+                s += elem_to_double(partials[r][row + i], dtype);
+            double h = residual ? s + elem_to_double(residual[row + i], dtype) : s;
             if (h_ref)
                 h_ref[row + i] = h;
             if (out_res)
-                out_res[row + i] = orc_bf16_from_double(h);
+                out_res[row + i] = elem_from_double(h, dtype);
             sumsq += h * h;
         }
         /* 4: mean square over the hidden dimension */
@@ -238,13 +310,13 @@ int orc_fused_rmsnorm(const uint16_t* const* partials, int n, const uint16_t* re
         for (int64_t i = 0; i < d; ++i) {
             double s = 0.0;
             for (int r = 0; r < n; ++r)
-                s += orc_bf16_to_double(partials[r][row + i]);
-            double h = residual ? s + orc_bf16_to_double(residual[row + i]) : s;
-            double y = h / denom * orc_bf16_to_double(gamma[i]);
+                s += elem_to_double(partials[r][row + i], dtype);
+            double h = residual ? s + elem_to_double(residual[row + i], dtype) : s;
+            double y = h / denom * elem_to_double(gamma[i], dtype);
             if (y_ref)
                 y_ref[row + i] = y;
             if (out_norm)
-                out_norm[row + i] = orc_bf16_from_double(y);
+                out_norm[row + i] = elem_from_double(y, dtype);
         }
     }
     return 0;
@@ -272,8 +344,18 @@ int orc_fused_rmsnorm(const uint16_t* const* partials, int n, const uint16_t* re
  * A g that is not a positive finite number makes every scale 0 and every
  * code a signed zero.
  */
+int orc_nvfp4_quantize_dt(const uint16_t* x, int64_t T, int64_t d, int dtype, int given, float g_in,
+                          uint8_t* codes, uint8_t* scales, float* g_out);
+
 int orc_nvfp4_quantize(const uint16_t* x, int64_t T, int64_t d, int given, float g_in,
                        uint8_t* codes, uint8_t* scales, float* g_out)
+{
+    return orc_nvfp4_quantize_dt(x, T, d, 0, given, g_in, codes, scales, g_out);
+}
+
+/* As orc_nvfp4_quantize for x of dtype 0 (bf16) or 1 (fp16). */
+int orc_nvfp4_quantize_dt(const uint16_t* x, int64_t T, int64_t d, int dtype, int given, float g_in,
+                          uint8_t* codes, uint8_t* scales, float* g_out)
 {
     if (T < 0 || d < 16 || d % 16 != 0 || !x)
         return -1;
@@ -283,7 +365,7 @@ int orc_nvfp4_quantize(const uint16_t* x, int64_t T, int64_t d, int given, float
     } else {
         float amax = 0.0f;
         for (int64_t k = 0; k < T * d; ++k) {
-            float a = fabsf((float)orc_bf16_to_double(x[k]));
+            float a = fabsf((float)elem_to_double(x[k], dtype));
             if (a > amax)
                 amax = a;
         }
@@ -298,7 +380,7 @@ int orc_nvfp4_quantize(const uint16_t* x, int64_t T, int64_t d, int given, float
             float xv[16];
             float amax_b = 0.0f;
             for (int i = 0; i < 16; ++i) {
-                xv[i] = (float)orc_bf16_to_double(xb[i]);
+                xv[i] = (float)elem_to_double(xb[i], dtype);
                 float a = fabsf(xv[i]);
                 if (a > amax_b)
                     amax_b = a;
@@ -358,8 +440,18 @@ float orc_bf16_amax(const uint16_t* x, int64_t n)
  *          gives inv = 0 (signed-zero codes)
  * s_out  : receives s (may be NULL)
  */
+int orc_fp8_quantize_dt(const uint16_t* x, int64_t T, int64_t d, int dtype, int given, float s_in,
+                        uint8_t* codes, float* s_out);
+
 int orc_fp8_quantize(const uint16_t* x, int64_t T, int64_t d, int given, float s_in, uint8_t* codes,
                      float* s_out)
+{
+    return orc_fp8_quantize_dt(x, T, d, 0, given, s_in, codes, s_out);
+}
+
+/* As orc_fp8_quantize for x of dtype 0 (bf16) or 1 (fp16). */
+int orc_fp8_quantize_dt(const uint16_t* x, int64_t T, int64_t d, int dtype, int given, float s_in,
+                        uint8_t* codes, float* s_out)
 {
     if (T < 0 || d < 1 || !x)
         return -1;
@@ -369,7 +461,7 @@ int orc_fp8_quantize(const uint16_t* x, int64_t T, int64_t d, int given, float s
     } else {
         float amax = 0.0f;
         for (int64_t k = 0; k < T * d; ++k) {
-            float a = fabsf((float)orc_bf16_to_double(x[k]));
+            float a = fabsf((float)elem_to_double(x[k], dtype));
             if (a > amax)
                 amax = a;
         }
@@ -385,6 +477,6 @@ int orc_fp8_quantize(const uint16_t* x, int64_t T, int64_t d, int given, float s
     }
     if (codes)
         for (int64_t k = 0; k < T * d; ++k)
-            codes[k] = orc_e4m3_from_float((float)orc_bf16_to_double(x[k]) * inv);
+            codes[k] = orc_e4m3_from_float((float)elem_to_double(x[k], dtype) * inv);
     return 0;
 }

@@ -37,6 +37,8 @@ MUTANTS = [
     ("scale_without_6", "float den6 = 6.0f * g;", "float den6 = g;"),
     ("block_amax_not_abs", "float a = fabsf(xv[i]);", "float a = xv[i];"),
     ("fp8_scale_not_448", "s = amax / 448.0f;", "s = amax / 256.0f;"),
+    ("f16_truncates", "    double r = rint(a / q) * q; /* <= 65504 here */", "    double r = floor(a / q) * q;"),
+    ("f16_wrong_bias", "(uint16_t)(((er - 1 + 15) << 10) | m)", "(uint16_t)(((er - 1 + 14) << 10) | m)"),
     ("fp8_divides_by_inverse", "codes[k] = orc_e4m3_from_float((float)orc_bf16_to_double(x[k]) * inv);",
      "codes[k] = orc_e4m3_from_float((float)orc_bf16_to_double(x[k]) / (inv > 0.0f ? inv : 1.0f));"),
 ]

@@ -528,3 +528,54 @@ def test_fp8_degenerate_scales(orc):
         assert np.all((codes & 0x7F) == 0)
     codes, s = orc.fp8_quantize(np.zeros((2, 8), np.uint16))
     assert s == 0.0 and not codes.any()
+
+
+# ---------------------------------------------------------------------- fp16
+
+def test_f16_rounding_matches_numpy(orc):
+    """numpy's float64 -> float16 conversion is a correctly rounded library routine."""
+    rng = np.random.default_rng(31)
+    x = np.concatenate([
+        rng.standard_normal(20000),
+        rng.standard_normal(20000) * np.exp2(rng.integers(-30, 17, 20000)),
+        np.array([0.0, -0.0, 65504.0, 65519.99, 65520.0, 65536.0, 1e6, 2.0 ** -24, 2.0 ** -25,
+                  3 * 2.0 ** -26, 2.0 ** -14, (1 - 2 ** -11) * 2.0 ** -14]),
+    ])
+    codes = np.arange(0, 0x7C00, dtype=np.uint16)
+    vals = codes.view(np.float16).astype(np.float64)
+    ties = (vals[1:] + vals[:-1]) / 2  # every midpoint between neighbours
+    x = np.concatenate([x, ties, -ties])
+    with np.errstate(over="ignore"):  # overflow to infinity is part of the check
+        want = x.astype(np.float16).view(np.uint16)
+    assert np.array_equal(orc.f16_from_float64(x), want)
+
+
+def test_f16_decode_all_codes(orc):
+    codes = np.arange(0, 65536, dtype=np.uint32).astype(np.uint16)
+    got = orc.f16_to_float64(codes)
+    want = codes.view(np.float16).astype(np.float64)
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    assert np.array_equal(got[ok], want[ok])
+
+
+def test_fp16_fused_closed_form_and_library_case(orc):
+    """fp16 tensors: constant row closed form, and N=1 without residual is
+    torch.nn.functional.rms_norm on the decoded fp16 input."""
+    d, c, eps = 64, 3.0, 0.5
+    f16 = lambda v: np.asarray(v, np.float16).view(np.uint16)
+    out = orc.fused_rmsnorm([f16(np.full((2, d), c / 2)), f16(np.full((2, d), c / 2))], None,
+                            f16(np.ones(d)), eps, dtype="fp16")
+    assert np.allclose(out["y"], c / math.sqrt(c * c + float(np.float32(eps))), rtol=1e-15)
+    assert np.array_equal(out["out_norm"], orc.f16_from_float64(out["y"]))
+    rng = np.random.default_rng(32)
+    x = f16(rng.standard_normal((4, 128)))
+    g = f16(1 + 0.1 * rng.standard_normal(128))
+    o = orc.fused_rmsnorm([x], None, g, 1e-5, dtype="fp16")
+    want = torch.nn.functional.rms_norm(torch.from_numpy(x.view(np.float16).astype(np.float64)), (128,),
+                                        weight=torch.from_numpy(g.view(np.float16).astype(np.float64)),
+                                        eps=float(np.float32(1e-5))).numpy()
+    assert np.allclose(o["y"], want, rtol=1e-12, atol=1e-15)
+    # the quantisers decode fp16 input exactly
+    codes, s = orc.fp8_quantize(f16([[448.0, -1.0]]), dtype="fp16")
+    assert s == 1.0 and list(codes[0]) == [0x7E, 0xB8]
