@@ -21,7 +21,9 @@
  *
  * Conventions for every entry point:
  *   - Tensors are row-major and contiguous: [T, d] bf16 (2 bytes per element),
- *     gamma [d] bf16, codes [T, d/2] bytes, scales [T, d/16] bytes.
+ *     gamma [d] bf16, codes [T, d/2] bytes, scales [T, d/16] bytes. With the
+ *     TPAR_DTYPE_FP16 flag (every entry point that takes flags) the bf16
+ *     tensors are IEEE binary16 instead; everything else is unchanged.
  *   - Pointers to tensors are DEVICE pointers; `partials` itself is a HOST
  *     array holding n_ranks device pointers. The caller owns every buffer; no
  *     entry point allocates or frees per call.
@@ -69,6 +71,8 @@ typedef void* tpar_stream_t;
 #define TPAR_DRY_RUN 0x10u      /* check the arguments (and a given plan) on
                                    the host, launch nothing, touch no GPU     */
 #define TPAR_FORCE_STREAM 0x20u /* persistent TMA-fed kernel (bandwidth path) */
+#define TPAR_DTYPE_FP16 0x40u   /* every [T, d] tensor and gamma is IEEE binary16
+                                   instead of bf16 (accumulation stays fp32) */
 
 /* Launch plan of the fused kernel. kernel: 0 = row kernel (one CTA per row),
  * 1 = cluster-split rows, 2 = persistent TMA-fed stream kernel. split: CTAs

@@ -14,6 +14,7 @@ from ._abi import (  # noqa: F401
     TPAR_FORCE_CLUSTER,
     TPAR_FORCE_ROW,
     TPAR_FORCE_STREAM,
+    TPAR_DTYPE_FP16,
     TPAR_GSCALE_GIVEN,
     TPAR_MAX_HIDDEN,
     TPAR_MAX_RANKS,

@@ -22,6 +22,7 @@ TPAR_FORCE_CLUSTER = 0x4
 TPAR_NO_PDL = 0x8
 TPAR_DRY_RUN = 0x10
 TPAR_FORCE_STREAM = 0x20
+TPAR_DTYPE_FP16 = 0x40
 
 _STATUS = {
     0: "TPAR_OK", 1: "TPAR_ERR_INVALID_ARG", 2: "TPAR_ERR_MISALIGNED",

@@ -502,7 +502,7 @@ unsigned flat_grid(int64_t nvec, int sm_count)
 
 tpar_status launch_quantize(const void* x, int64_t T, int64_t d, uint8_t* codes, uint8_t* scales,
                             float* gscale, uint32_t* ws, bool dynamic, int sm_count, cudaStream_t stream,
-                            bool pdl)
+                            bool pdl, bool f16)
 {
     QuantArgs q;
     q.x = static_cast<const uint4*>(x);
@@ -511,6 +511,7 @@ tpar_status launch_quantize(const void* x, int64_t T, int64_t d, uint8_t* codes,
     q.gscale = gscale;
     q.ws = ws;
     q.nvec = T * d / 8;
+    q.f16 = f16;
     const unsigned grid = flat_grid(q.nvec / 2, sm_count);  // one thread per 16-element block
     if (launch(tpar::quantize_kernel_for(dynamic), dim3(grid), dim3(256), &q, stream, 1, pdl) != cudaSuccess)
         return TPAR_ERR_CUDA;
@@ -537,6 +538,7 @@ FusedArgs fused_args(const Call& c)
     a.slice = a.nvec;
     a.eps = c.eps;
     a.inv_d = 1.0f / static_cast<float>(c.d);
+    a.f16 = (c.flags & TPAR_DTYPE_FP16) != 0;
     return a;
 }
 
@@ -624,6 +626,7 @@ tpar_status fused_impl(const Call& c, const tpar_plan* user_plan, void* user_ws,
         ra.reduced = static_cast<uint4*>(c.out_residual);
         ra.nvec = c.T * c.d / 8;
         ra.n_ranks = c.n_ranks;
+        ra.f16 = (c.flags & TPAR_DTYPE_FP16) != 0;
         return launch(tpar::reduce_kernel_for(tpar::rank_bound(c.n_ranks)), dim3(flat_grid(ra.nvec, sm)),
                       dim3(256), &ra, stream, 1, pdl) == cudaSuccess
                    ? TPAR_OK
@@ -652,7 +655,7 @@ tpar_status fused_impl(const Call& c, const tpar_plan* user_plan, void* user_ws,
     a.scales = nullptr;
     if ((st = launch_fused(a, tpar::kQuantAmax, p, stream, pdl)) != TPAR_OK)
         return st;
-    st = launch_quantize(c.out_norm, c.T, c.d, c.codes, c.scales, c.gscale, ws, true, sm, stream, pdl);
+    st = launch_quantize(c.out_norm, c.T, c.d, c.codes, c.scales, c.gscale, ws, true, sm, stream, pdl, a.f16);
     if (st != TPAR_OK)
         cudaMemsetAsync(ws, 0, 8, stream);  // leave the workspace zeroed
     return st;
@@ -692,7 +695,7 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
                                  uint32_t flags, tpar_stream_t stream_)
 {
     Call c{partials, n_ranks, residual, gamma, eps, T, d, out_norm, out_residual,
-           nvfp4_codes, nvfp4_scales, global_scale, flags & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL), reduced};
+           nvfp4_codes, nvfp4_scales, global_scale, flags & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_DTYPE_FP16), reduced};
     tpar_status st = validate(c, true);
     if (st != TPAR_OK || (flags & TPAR_DRY_RUN))
         return st;
@@ -718,6 +721,7 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
     ra.reduced = static_cast<uint4*>(reduced);
     ra.nvec = nvec;
     ra.n_ranks = n_ranks;
+    ra.f16 = (flags & TPAR_DTYPE_FP16) != 0;
     if (launch(tpar::reduce_kernel_for(tpar::rank_bound(n_ranks)), dim3(flat_grid(nvec, sm)), dim3(256), &ra,
                stream, 1, pdl) != cudaSuccess)
         return TPAR_ERR_CUDA;
@@ -727,7 +731,8 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
         const uint4* res = static_cast<const uint4*>(residual);
         uint4* outr = static_cast<uint4*>(out_residual);
         int64_t n = nvec;
-        void* args[4] = {&red, &res, &outr, &n};
+        bool f16 = (flags & TPAR_DTYPE_FP16) != 0;
+        void* args[5] = {&red, &res, &outr, &n, &f16};
         cudaLaunchConfig_t cfg;
         std::memset(&cfg, 0, sizeof cfg);
         cfg.gridDim = dim3(flat_grid(nvec, sm));
@@ -744,7 +749,7 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
     // K3: out_norm = RMSNorm(out_residual) (+ amax for a dynamic NVFP4 scale)
     const void* k3_in[1] = {out_residual};
     Call k3{k3_in, 1, nullptr, gamma, eps, T, d, out_norm, nullptr, nullptr, nullptr, nullptr,
-            TPAR_FORCE_ROW, nullptr};
+            TPAR_FORCE_ROW | (flags & TPAR_DTYPE_FP16), nullptr};
     FusedArgs a = fused_args(k3);
     a.amax_bits = ws;
     tpar_plan p;
@@ -756,7 +761,7 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
     // K4: the separate NVFP4 quantiser
     if (nvfp4) {
         st = launch_quantize(out_norm, T, d, nvfp4_codes, nvfp4_scales, global_scale, ws, !given, sm, stream,
-                             pdl);
+                             pdl, (flags & TPAR_DTYPE_FP16) != 0);
         if (st != TPAR_OK && ws)
             cudaMemsetAsync(ws, 0, 8, stream);
     }
@@ -797,7 +802,8 @@ tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* co
             return st;
         const uint4* xv = static_cast<const uint4*>(x);
         int64_t nvec = T * d / 8;
-        void* args[3] = {&xv, &nvec, &ws};
+        bool f16 = (flags & TPAR_DTYPE_FP16) != 0;
+        void* args[4] = {&xv, &nvec, &ws, &f16};
         cudaLaunchConfig_t cfg;
         std::memset(&cfg, 0, sizeof cfg);
         cfg.gridDim = dim3(flat_grid(nvec, sm));
@@ -811,7 +817,8 @@ tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* co
         if (cudaLaunchKernelExC(&cfg, tpar::amax_kernel_ptr(), args) != cudaSuccess)
             return TPAR_ERR_CUDA;
     }
-    st = launch_quantize(x, T, d, codes, scales, global_scale, ws, !given, sm, stream, pdl);
+    st = launch_quantize(x, T, d, codes, scales, global_scale, ws, !given, sm, stream, pdl,
+                         (flags & TPAR_DTYPE_FP16) != 0);
     if (st != TPAR_OK && ws)
         cudaMemsetAsync(ws, 0, 8, stream);
     return st;
@@ -824,7 +831,8 @@ tpar_status tpar_fused_rmsnorm_fp8(const void* const* partials, int n_ranks, con
 {
     const bool given = (flags & TPAR_GSCALE_GIVEN) != 0;
     Call c{partials, n_ranks, residual, gamma, eps, T, d, out_norm, out_residual, nullptr, nullptr, nullptr,
-           flags & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_FORCE_ROW | TPAR_FORCE_CLUSTER), nullptr, true};
+           flags & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_FORCE_ROW | TPAR_FORCE_CLUSTER | TPAR_DTYPE_FP16), nullptr,
+           true};
     tpar_status st = validate(c, false);
     if (st != TPAR_OK)
         return st;
@@ -877,6 +885,7 @@ tpar_status tpar_fused_rmsnorm_fp8(const void* const* partials, int n_ranks, con
     f.scale = fp8_scale;
     f.ws = ws;
     f.nvec = T * d / 8;
+    f.f16 = a.f16;
     if (launch(tpar::fp8_quantize_kernel_for(true), dim3(flat_grid(f.nvec, sm)), dim3(256), &f, stream, 1, pdl) !=
         cudaSuccess) {
         cudaMemsetAsync(ws, 0, 8, stream);
@@ -919,7 +928,8 @@ tpar_status tpar_fp8_quantize(const void* x, int64_t T, int64_t d, uint8_t* code
             return st;
         const uint4* xv = static_cast<const uint4*>(x);
         int64_t n = nvec;
-        void* args[3] = {&xv, &n, &ws};
+        bool f16 = (flags & TPAR_DTYPE_FP16) != 0;
+        void* args[4] = {&xv, &n, &ws, &f16};
         cudaLaunchConfig_t cfg;
         std::memset(&cfg, 0, sizeof cfg);
         cfg.gridDim = dim3(flat_grid(nvec, sm));
@@ -939,6 +949,7 @@ tpar_status tpar_fp8_quantize(const void* x, int64_t T, int64_t d, uint8_t* code
     f.scale = scale;
     f.ws = ws;
     f.nvec = nvec;
+    f.f16 = (flags & TPAR_DTYPE_FP16) != 0;
     if (launch(tpar::fp8_quantize_kernel_for(!given), dim3(flat_grid(nvec, sm)), dim3(256), &f, stream, 1, pdl) !=
         cudaSuccess) {
         if (ws)
@@ -1048,7 +1059,7 @@ extern "C" tpar_status tpar_unfused_rmsnorm_noalloc(const void* const* partials,
 {
     if (T > 0 && d > 0 && T > kNoAllocMaxElems / d)
         return TPAR_ERR_SCRATCH_TOO_SMALL;
-    const uint32_t fl = flags & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_DRY_RUN);
+    const uint32_t fl = flags & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_DRY_RUN | TPAR_DTYPE_FP16);
     const bool dry = (fl & TPAR_DRY_RUN) != 0;
     unsigned char* scratch = nullptr;
     if (!dry && T > 0) {
@@ -1060,7 +1071,7 @@ extern "C" tpar_status tpar_unfused_rmsnorm_noalloc(const void* const* partials,
     void* reduced = scratch ? static_cast<void*>(scratch + kNoAllocHeaderBytes)
                             : reinterpret_cast<void*>(static_cast<uintptr_t>(kNoAllocHeaderBytes));
     Call c{partials, n_ranks, residual, gamma, eps, T, d, out_norm, out_residual,
-           nvfp4_codes, nvfp4_scales, global_scale, fl & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL), reduced};
+           nvfp4_codes, nvfp4_scales, global_scale, fl & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_DTYPE_FP16), reduced};
     tpar_status st = validate(c, true);
     if (st != TPAR_OK || dry || T == 0)
         return st;
@@ -1088,6 +1099,7 @@ extern "C" tpar_status tpar_unfused_rmsnorm_noalloc(const void* const* partials,
     ra.reduced = static_cast<uint4*>(reduced);
     ra.nvec = nvec;
     ra.n_ranks = n_ranks;
+    ra.f16 = (flags & TPAR_DTYPE_FP16) != 0;
     if (launch(tpar::reduce_kernel_for(tpar::rank_bound(n_ranks)), dim3(flat_grid(nvec, sm)), dim3(256), &ra,
                stream, 1, pdl) != cudaSuccess)
         return TPAR_ERR_CUDA;
@@ -1097,7 +1109,8 @@ extern "C" tpar_status tpar_unfused_rmsnorm_noalloc(const void* const* partials,
         const uint4* res = static_cast<const uint4*>(residual);
         uint4* outr = static_cast<uint4*>(out_residual);
         int64_t n = nvec;
-        void* args[4] = {&red, &res, &outr, &n};
+        bool f16 = (flags & TPAR_DTYPE_FP16) != 0;
+        void* args[5] = {&red, &res, &outr, &n, &f16};
         cudaLaunchConfig_t cfg;
         std::memset(&cfg, 0, sizeof cfg);
         cfg.gridDim = dim3(flat_grid(nvec, sm));
@@ -1114,7 +1127,7 @@ extern "C" tpar_status tpar_unfused_rmsnorm_noalloc(const void* const* partials,
     // K3: out_norm = RMSNorm(out_residual) (+ amax for a dynamic NVFP4 scale)
     const void* k3_in[1] = {out_residual};
     Call k3{k3_in, 1, nullptr, gamma, eps, T, d, out_norm, nullptr, nullptr, nullptr, nullptr,
-            TPAR_FORCE_ROW, nullptr};
+            TPAR_FORCE_ROW | (flags & TPAR_DTYPE_FP16), nullptr};
     FusedArgs a = fused_args(k3);
     a.amax_bits = (nvfp4 && !given) ? ws : nullptr;
     tpar_plan p;
@@ -1126,6 +1139,6 @@ extern "C" tpar_status tpar_unfused_rmsnorm_noalloc(const void* const* partials,
     // K4: the separate NVFP4 quantiser
     if (nvfp4)
         st = launch_quantize(out_norm, T, d, nvfp4_codes, nvfp4_scales, global_scale, given ? nullptr : ws,
-                             !given, sm, stream, pdl);
+                             !given, sm, stream, pdl, (fl & TPAR_DTYPE_FP16) != 0);
     return st;
 }

@@ -101,6 +101,46 @@ __device__ __forceinline__ uint4 pack8(const float f[8])
                       pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
 }
 
+// The same for a 16-byte vector of 8 elements of either storage type: bf16
+// (f16 = false) or IEEE binary16 (f16 = true). The flag is uniform per
+// launch, so the branch costs one predicate.
+__device__ __forceinline__ void unpack8_dt(const uint4& v, float f[8], bool f16)
+{
+    if (!f16) {
+        unpack8(v, f);
+        return;
+    }
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const float2 p = __half22float2(*reinterpret_cast<const __half2*>(&w[k]));
+        f[2 * k] = p.x;
+        f[2 * k + 1] = p.y;
+    }
+}
+
+__device__ __forceinline__ void add8_dt(const uint4& v, float f[8], bool f16)
+{
+    float t[8];
+    unpack8_dt(v, t, f16);
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+        f[e] += t[e];
+}
+
+__device__ __forceinline__ uint4 pack8_dt(const float f[8], bool f16)
+{
+    if (!f16)
+        return pack8(f);
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const __half2 h = __floats2half2_rn(f[2 * k], f[2 * k + 1]);
+        w[k] = *reinterpret_cast<const uint32_t*>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 // ---------------------------------------------------------------- reductions
 
 // Butterfly all-reduce over the warp. Every lane ends with the same bits

@@ -174,9 +174,9 @@ __global__ void __launch_bounds__(544, 1) stream_rmsnorm_kernel(const __grid_con
                 if (v < nvec) {
                     const uint4 x = stage[v];
                     if (src == 0)
-                        unpack8(x, h[j]);
+                        unpack8_dt(x, h[j], a.f16);
                     else
-                        add8(x, h[j]);
+                        add8_dt(x, h[j], a.f16);
                 }
             }
             __syncwarp();
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(544, 1) stream_rmsnorm_kernel(const __grid_con
                 for (int e = 0; e < 8; ++e)
                     ss = fmaf(h[j][e], h[j][e], ss);
                 if (a.out_residual)
-                    st_v4(a.out_residual + rowv + v, pack8(h[j]));
+                    st_v4(a.out_residual + rowv + v, pack8_dt(h[j], a.f16));
             }
             ss = warp_sum(ss);
             const int w = (j * C + 32 * cwarp) >> 5;

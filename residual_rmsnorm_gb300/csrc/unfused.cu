@@ -7,7 +7,7 @@
 namespace tpar {
 
 // amax of |x| over a bf16 tensor into ws[0] (for the standalone quantiser).
-__global__ void __launch_bounds__(256) amax_kernel(const uint4* x, int64_t nvec, uint32_t* ws)
+__global__ void __launch_bounds__(256) amax_kernel(const uint4* x, int64_t nvec, uint32_t* ws, bool f16)
 {
     pdl_wait();
     pdl_launch_dependents();
@@ -15,7 +15,7 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint4* x, int64_t nvec,
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec; v += stride) {
         float f[8];
-        unpack8(ld_stream(x + v), f);
+        unpack8_dt(ld_stream(x + v), f, f16);
 #pragma unroll
         for (int e = 0; e < 8; ++e)
             m = fmaxf(m, fabsf(f[e]));
@@ -27,17 +27,17 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint4* x, int64_t nvec,
 
 // K2: out_residual = bf16(reduced + residual) (a copy when residual is null).
 __global__ void __launch_bounds__(256) residual_add_kernel(const uint4* reduced, const uint4* residual,
-                                                           uint4* out_residual, int64_t nvec)
+                                                           uint4* out_residual, int64_t nvec, bool f16)
 {
     pdl_wait();
     pdl_launch_dependents();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec; v += stride) {
         float s[8];
-        unpack8(ld_stream(reduced + v), s);
+        unpack8_dt(ld_stream(reduced + v), s, f16);
         if (residual)
-            add8(ld_coherent(residual + v), s);
-        st_v4(out_residual + v, pack8(s));
+            add8_dt(ld_coherent(residual + v), s, f16);
+        st_v4(out_residual + v, pack8_dt(s, f16));
     }
 }
 

@@ -1,8 +1,9 @@
 """PyTorch-tensor front end of the C ABI (marshalling only).
 
 PyTorch supplies device memory and the current CUDA stream; every step of the
-epilogue runs in libtpar.so. Tensors must be CUDA, contiguous, bf16 (gamma
-too) and 16-byte aligned, as include/tpar.h requires.
+epilogue runs in libtpar.so. Tensors must be CUDA, contiguous and 16-byte
+aligned, as include/tpar.h requires, and all of one element type: bf16, or
+fp16 for the whole call (then TPAR_DTYPE_FP16 is passed).
 """
 from __future__ import annotations
 
@@ -11,13 +12,19 @@ import torch
 from . import _abi
 
 
-def _check_bf16(name, t, shape=None):
+_DTYPES = (torch.bfloat16, torch.float16)
+
+
+def _check_bf16(name, t, shape=None, dtype=None):
+    """A CUDA, contiguous tensor of the call's element type (bf16, or fp16 for
+    the whole call), of the given shape."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
     if t.device.type != "cuda":
         raise ValueError(f"{name} must live on a CUDA device (no CPU path exists)")
-    if t.dtype != torch.bfloat16:
-        raise TypeError(f"{name} must be bf16, got {t.dtype}")
+    want = dtype if dtype is not None else t.dtype
+    if t.dtype not in _DTYPES or t.dtype != want:
+        raise TypeError(f"{name} must be {want if dtype is not None else 'bf16 or fp16'}, got {t.dtype}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
     if shape is not None and tuple(t.shape) != tuple(shape):
@@ -61,18 +68,21 @@ def fused_rmsnorm(partials, residual, gamma, eps: float, *, out_norm=None, out_r
         raise ValueError("need at least one partial")
     T, d = partials[0].shape
     dev = partials[0].device
+    dt = partials[0].dtype
+    if dt == torch.float16:
+        flags |= _abi.TPAR_DTYPE_FP16
     for i, p in enumerate(partials):
-        _check_bf16(f"partials[{i}]", p, (T, d))
+        _check_bf16(f"partials[{i}]", p, (T, d), dt)
     if residual is not None:
-        _check_bf16("residual", residual, (T, d))
-    _check_bf16("gamma", gamma, (d,))
+        _check_bf16("residual", residual, (T, d), dt)
+    _check_bf16("gamma", gamma, (d,), dt)
     if out_norm is None and (emit_norm or not nvfp4 or global_scale is None):
-        out_norm = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+        out_norm = torch.empty((T, d), dtype=dt, device=dev)
     if out_norm is not None:
-        _check_bf16("out_norm", out_norm, (T, d))
+        _check_bf16("out_norm", out_norm, (T, d), dt)
     if out_residual is None:
-        out_residual = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
-    _check_bf16("out_residual", out_residual, (T, d))
+        out_residual = torch.empty((T, d), dtype=dt, device=dev)
+    _check_bf16("out_residual", out_residual, (T, d), dt)
     codes = scales = g = None
     if nvfp4:
         codes, scales, g, given = _nvfp4_outputs(T, d, dev, global_scale)
@@ -98,12 +108,15 @@ def allreduce_sum(partials, residual=None, *, out=None, flags: int = 0, stream=N
         raise ValueError("need at least one partial")
     T, d = partials[0].shape
     dev = partials[0].device
+    dt = partials[0].dtype
+    if dt == torch.float16:
+        flags |= _abi.TPAR_DTYPE_FP16
     for i, p in enumerate(partials):
-        _check_bf16(f"partials[{i}]", p, (T, d))
+        _check_bf16(f"partials[{i}]", p, (T, d), dt)
     if residual is not None:
-        _check_bf16("residual", residual, (T, d))
-    out = torch.empty((T, d), dtype=torch.bfloat16, device=dev) if out is None else out
-    _check_bf16("out", out, (T, d))
+        _check_bf16("residual", residual, (T, d), dt)
+    out = torch.empty((T, d), dtype=dt, device=dev) if out is None else out
+    _check_bf16("out", out, (T, d), dt)
     with torch.cuda.device(dev):
         _abi.tpar_fused_rmsnorm_ex(
             [p.data_ptr() for p in partials], len(partials),
@@ -119,14 +132,17 @@ def unfused_rmsnorm(partials, residual, gamma, eps: float, *, reduced=None, out_
     partials = list(partials)
     T, d = partials[0].shape
     dev = partials[0].device
+    dt = partials[0].dtype
+    if dt == torch.float16:
+        flags |= _abi.TPAR_DTYPE_FP16
     for i, p in enumerate(partials):
-        _check_bf16(f"partials[{i}]", p, (T, d))
+        _check_bf16(f"partials[{i}]", p, (T, d), dt)
     if residual is not None:
-        _check_bf16("residual", residual, (T, d))
-    _check_bf16("gamma", gamma, (d,))
-    reduced = torch.empty((T, d), dtype=torch.bfloat16, device=dev) if reduced is None else reduced
-    out_norm = torch.empty((T, d), dtype=torch.bfloat16, device=dev) if out_norm is None else out_norm
-    out_residual = (torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+        _check_bf16("residual", residual, (T, d), dt)
+    _check_bf16("gamma", gamma, (d,), dt)
+    reduced = torch.empty((T, d), dtype=dt, device=dev) if reduced is None else reduced
+    out_norm = torch.empty((T, d), dtype=dt, device=dev) if out_norm is None else out_norm
+    out_residual = (torch.empty((T, d), dtype=dt, device=dev)
                     if out_residual is None else out_residual)
     codes = scales = g = None
     if nvfp4:
@@ -148,6 +164,8 @@ def nvfp4_quantize(x, global_scale: torch.Tensor | None = None, flags: int = 0, 
     """NVFP4 quantisation of a bf16 [T, d] CUDA tensor -> (codes, scales, global_scale)."""
     _check_bf16("x", x)
     T, d = x.shape
+    if x.dtype == torch.float16:
+        flags |= _abi.TPAR_DTYPE_FP16
     codes, scales, g, given = _nvfp4_outputs(T, d, x.device, global_scale)
     if given:
         flags |= _abi.TPAR_GSCALE_GIVEN
@@ -165,13 +183,16 @@ def fused_rmsnorm_fp8(partials, residual, gamma, eps: float, *, scale: torch.Ten
     partials = list(partials)
     T, d = partials[0].shape
     dev = partials[0].device
+    dt = partials[0].dtype
+    if dt == torch.float16:
+        flags |= _abi.TPAR_DTYPE_FP16
     for i, p in enumerate(partials):
-        _check_bf16(f"partials[{i}]", p, (T, d))
+        _check_bf16(f"partials[{i}]", p, (T, d), dt)
     if residual is not None:
-        _check_bf16("residual", residual, (T, d))
-    _check_bf16("gamma", gamma, (d,))
-    out_norm = torch.empty((T, d), dtype=torch.bfloat16, device=dev) if (emit_norm or scale is None) else None
-    out_residual = torch.empty((T, d), dtype=torch.bfloat16, device=dev) if out_residual is None else out_residual
+        _check_bf16("residual", residual, (T, d), dt)
+    _check_bf16("gamma", gamma, (d,), dt)
+    out_norm = torch.empty((T, d), dtype=dt, device=dev) if (emit_norm or scale is None) else None
+    out_residual = torch.empty((T, d), dtype=dt, device=dev) if out_residual is None else out_residual
     codes = torch.empty((T, d), dtype=torch.uint8, device=dev)
     if scale is None:
         s = torch.empty((1,), dtype=torch.float32, device=dev)
@@ -191,6 +212,8 @@ def fp8_quantize(x, scale: torch.Tensor | None = None, flags: int = 0, stream=No
     """Per-tensor FP8 (E4M3) quantisation of a bf16 [T, d] CUDA tensor -> (codes, scale)."""
     _check_bf16("x", x)
     T, d = x.shape
+    if x.dtype == torch.float16:
+        flags |= _abi.TPAR_DTYPE_FP16
     codes = torch.empty((T, d), dtype=torch.uint8, device=x.device)
     if scale is None:
         s = torch.empty((1,), dtype=torch.float32, device=x.device)

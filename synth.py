@@ -66,10 +66,11 @@ NVFP4_TS = tuple(2 ** k for k in range(15))  # 1 .. 16384
 
 
 def make_inputs(w: Workload, device: str | torch.device = "cpu", T: int | None = None,
-                n_ranks: int | None = None, seed: int | None = None):
-    """Draw the bf16 inputs of ``w`` (optionally overriding T / N / seed).
+                n_ranks: int | None = None, seed: int | None = None, dtype=torch.bfloat16):
+    """Draw the inputs of ``w`` (optionally overriding T / N / seed), rounded
+    once to ``dtype`` (bf16, or fp16).
 
-    Returns dict(partials=[N x bf16 [T, d]], residual=bf16 [T, d], gamma=bf16 [d]).
+    Returns dict(partials=[N x [T, d]], residual=[T, d], gamma=[d]).
     """
     T = w.T if T is None else T
     n = w.n_ranks if n_ranks is None else n_ranks
@@ -90,23 +91,23 @@ def make_inputs(w: Workload, device: str | torch.device = "cpu", T: int | None =
                 flat = p.view(-1)
                 flat[idx] = flat[idx] * w.outlier_scale
     return {
-        "partials": [p.to(torch.bfloat16) for p in raw],
-        "residual": res.to(torch.bfloat16),
-        "gamma": gamma.to(torch.bfloat16),
+        "partials": [p.to(dtype) for p in raw],
+        "residual": res.to(dtype),
+        "gamma": gamma.to(dtype),
     }
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
-    """bf16 tensor (any device) -> numpy uint16 bit patterns."""
-    if t.dtype != torch.bfloat16:
-        raise TypeError("expected a bf16 tensor")
+    """bf16 or fp16 tensor (any device) -> numpy uint16 bit patterns."""
+    if t.dtype not in (torch.bfloat16, torch.float16):
+        raise TypeError("expected a bf16 or fp16 tensor")
     return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
 
 
-def from_bits(a: np.ndarray, device="cpu") -> torch.Tensor:
-    """numpy uint16 bit patterns -> bf16 tensor."""
+def from_bits(a: np.ndarray, device="cpu", dtype=torch.bfloat16) -> torch.Tensor:
+    """numpy uint16 bit patterns -> bf16 (or fp16) tensor."""
     a = np.ascontiguousarray(a, dtype=np.uint16)
-    return torch.from_numpy(a.view(np.int16).copy()).view(torch.bfloat16).to(device)
+    return torch.from_numpy(a.view(np.int16).copy()).view(dtype).to(device)
 
 
 def random_bf16(shape, std: float, seed: int, device="cpu") -> torch.Tensor:

@@ -25,8 +25,12 @@ def lib():
     return tp
 
 
+def dtype_name(t: torch.Tensor) -> str:
+    return "fp16" if t.dtype == torch.float16 else "bf16"
+
+
 def assert_close_to_ref(got_bf16: torch.Tensor, ref64: np.ndarray, what: str, extra=None):
-    got = oracle.bf16_to_float64(synth.bits(got_bf16))
+    got = oracle.to_float64(synth.bits(got_bf16), dtype_name(got_bf16))
     assert got.shape == ref64.shape, (got.shape, ref64.shape)
     err = np.abs(got - ref64)
     bound = RTOL * np.abs(ref64) + ATOL
@@ -40,11 +44,13 @@ def assert_close_to_ref(got_bf16: torch.Tensor, ref64: np.ndarray, what: str, ex
 
 
 def oracle_rows(inputs, rows, eps, residual=True):
-    """Oracle outputs for the selected rows (rows are independent)."""
+    """Oracle outputs for the selected rows (rows are independent), in the
+    inputs' element type."""
     sel = lambda t: synth.bits(t[rows])
     parts = [sel(p) for p in inputs["partials"]]
     res = sel(inputs["residual"]) if residual and inputs.get("residual") is not None else None
-    return oracle.fused_rmsnorm(parts, res, synth.bits(inputs["gamma"]), eps)
+    return oracle.fused_rmsnorm(parts, res, synth.bits(inputs["gamma"]), eps,
+                                dtype=dtype_name(inputs["gamma"]))
 
 
 def to_device(inputs, dev="cuda"):
@@ -54,8 +60,8 @@ def to_device(inputs, dev="cuda"):
 
 
 def assert_nvfp4_bit_exact(out_norm: torch.Tensor, codes, scales, g, given=None, what="nvfp4"):
-    """The oracle quantiser run on the kernel's own bf16 normed tensor."""
-    oc, os_, og = oracle.nvfp4_quantize(synth.bits(out_norm), global_scale=given)
+    """The oracle quantiser run on the kernel's own normed tensor."""
+    oc, os_, og = oracle.nvfp4_quantize(synth.bits(out_norm), global_scale=given, dtype=dtype_name(out_norm))
     gc = codes.cpu().numpy()
     gs = scales.cpu().numpy()
     gg = np.float32(g.item()) if isinstance(g, torch.Tensor) else np.float32(g)
@@ -76,9 +82,10 @@ def assert_nvfp4_bit_exact(out_norm: torch.Tensor, codes, scales, g, given=None,
 # bound per element: 2^-8 * sum_r |P_r| for h, and the same times
 # |gamma| / sqrt(ms + eps) for y.
 def unfused_extra_tolerance(inputs, ref, eps):
-    s_abs = sum(np.abs(oracle.bf16_to_float64(synth.bits(p))) for p in inputs["partials"])
-    eh = 2.0 ** -8 * s_abs
-    gam = np.abs(oracle.bf16_to_float64(synth.bits(inputs["gamma"])))
+    dt = dtype_name(inputs["gamma"])
+    s_abs = sum(np.abs(oracle.to_float64(synth.bits(p), dt)) for p in inputs["partials"])
+    eh = (2.0 ** -8 if dt == "bf16" else 2.0 ** -11) * s_abs
+    gam = np.abs(oracle.to_float64(synth.bits(inputs["gamma"]), dt))
     ms = np.mean(ref["h"] ** 2, axis=1, keepdims=True)
     ey = eh * gam[None, :] / np.sqrt(ms + float(np.float32(eps))) * 1.01
     return eh, ey

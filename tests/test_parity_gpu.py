@@ -227,3 +227,50 @@ def test_allreduce_only_pattern(n, T, d, residual):
         tp.allreduce_sum(dev["partials"], res, out=res)
         torch.cuda.synchronize()
         assert torch.equal(res.view(torch.int16), out.view(torch.int16))
+
+
+
+# ---------------------------------------------------------------------- fp16
+
+@pytest.mark.parametrize("kind", ["auto", "row", "cluster", "stream"])
+@pytest.mark.parametrize("n,T,d", [(8, 8, 4096), (4, 1, 8192), (8, 300, 8192), (3, 5, 24), (16, 33, 2056)])
+def test_fp16_epilogue(kind, n, T, d):
+    """IEEE binary16 tensors (TPAR_DTYPE_FP16): same path, fp32 arithmetic."""
+    tp = lib()
+    flags = {"auto": 0, "row": tp.TPAR_FORCE_ROW, "cluster": tp.TPAR_FORCE_CLUSTER,
+             "stream": tp.TPAR_FORCE_STREAM}[kind]
+    if kind == "cluster" and d < 64:
+        pytest.skip("rows too short to split")
+    w = synth.Workload(f"fp16 N{n} T{T} d{d}", n, T, d, 1e-5, 0.5, seed=n + T + d)
+    inputs = synth.make_inputs(w, dtype=torch.float16)
+    dev = to_device(inputs)
+    out = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, flags=flags)
+    torch.cuda.synchronize()
+    assert out["out_norm"].dtype == torch.float16
+    ref = oracle_rows(inputs, slice(None), w.eps)
+    assert_close_to_ref(out["out_residual"], ref["h"], f"{w.name} {kind} out_residual")
+    assert_close_to_ref(out["out_norm"], ref["y"], f"{w.name} {kind} out_norm")
+
+
+def test_fp16_quantised_outputs_and_unfused():
+    tp = lib()
+    for T in (4, 200):
+        w = synth.NVFP4.with_(T=T, d=4096)
+        inputs = synth.make_inputs(w, dtype=torch.float16)
+        dev = to_device(inputs)
+        o = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True)
+        torch.cuda.synchronize()
+        assert_nvfp4_bit_exact(o["out_norm"], o["codes"], o["scales"], o["global_scale"], what=f"fp16 T{T}")
+        f = tp.fused_rmsnorm_fp8(dev["partials"], dev["residual"], dev["gamma"], w.eps)
+        torch.cuda.synchronize()
+        oc, os_ = oracle.fp8_quantize(synth.bits(f["out_norm"]), dtype="fp16")
+        assert np.array_equal(f["codes"].cpu().numpy(), oc) and np.float32(f["scale"].item()) == os_
+        u = tp.unfused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps)
+        torch.cuda.synchronize()
+        ref = oracle_rows(inputs, slice(None), w.eps)
+        from gpu_helpers import unfused_extra_tolerance
+        eh, ey = unfused_extra_tolerance(inputs, ref, w.eps)
+        assert_close_to_ref(u["out_norm"], ref["y"], "fp16 unfused", extra=ey)
+        s = tp.allreduce_sum(dev["partials"], dev["residual"])
+        torch.cuda.synchronize()
+        assert_close_to_ref(s, ref["h"], "fp16 allreduce")
