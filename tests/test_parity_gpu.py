@@ -274,3 +274,31 @@ def test_fp16_quantised_outputs_and_unfused():
         s = tp.allreduce_sum(dev["partials"], dev["residual"])
         torch.cuda.synchronize()
         assert_close_to_ref(s, ref["h"], "fp16 allreduce")
+
+
+@pytest.mark.parametrize("kind", ["auto", "stream", "nvfp4", "fp8"])
+def test_more_rows_than_one_grid_dimension(kind):
+    """T = 70000 > 65535: row kernels stride over rows beyond the grid's
+    y-dimension limit; the quantised paths cover the same rows."""
+    tp = lib()
+    w = synth.Workload("many rows", 2, 70000, 64, 1e-6, 1.0, seed=11)
+    inputs = synth.make_inputs(w)
+    dev = to_device(inputs)
+    rows = np.array([0, 1, 65534, 65535, 65536, 69999])
+    ref = oracle_rows(inputs, rows, w.eps)
+    if kind in ("auto", "stream"):
+        out = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps,
+                               flags=tp.TPAR_FORCE_STREAM if kind == "stream" else 0)
+        torch.cuda.synchronize()
+        assert_close_to_ref(out["out_norm"][rows], ref["y"], f"{kind} out_norm")
+        assert_close_to_ref(out["out_residual"][rows], ref["h"], f"{kind} out_residual")
+    elif kind == "nvfp4":
+        out = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True)
+        torch.cuda.synchronize()
+        assert_close_to_ref(out["out_norm"][rows], ref["y"], "nvfp4 out_norm")
+        assert_nvfp4_bit_exact(out["out_norm"], out["codes"], out["scales"], out["global_scale"], what="70000")
+    else:
+        out = tp.fused_rmsnorm_fp8(dev["partials"], dev["residual"], dev["gamma"], w.eps)
+        torch.cuda.synchronize()
+        oc, os_ = oracle.fp8_quantize(synth.bits(out["out_norm"]))
+        assert np.array_equal(out["codes"].cpu().numpy(), oc) and np.float32(out["scale"].item()) == os_
