@@ -18,7 +18,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libtpar.so")
-SOURCES = ["api.cu", "kernels_q0.cu", "kernels_q1.cu", "kernels_q2.cu", "kernels_q3.cu", "kernels_stream.cu", "kernels_small.cu", "unfused.cu"]
+SOURCES = ["api.cu"] + [f"kernels_q{q}_{t}.cu" for q in range(4) for t in ("bf16", "fp16")] + [
+    "kernels_stream_bf16.cu", "kernels_stream_fp16.cu", "kernels_small.cu", "unfused.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

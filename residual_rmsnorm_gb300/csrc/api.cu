@@ -428,21 +428,10 @@ tpar_status plan_impl(int64_t T, int64_t d, int n_ranks, int sm_count, uint32_t 
     return check_plan(p, d, n_ranks);
 }
 
-const void* fused_kernel(int qmode, int nr, int vpt, bool cluster)
-{
-    switch (qmode) {
-    case 0: return tpar::fused_kernel_q0(nr, vpt, cluster);
-    case 1: return tpar::fused_kernel_q1(nr, vpt, cluster);
-    case 2: return tpar::fused_kernel_q2(nr, vpt, cluster);
-    case 3: return tpar::fused_kernel_q3(nr, vpt, cluster);
-    default: return nullptr;
-    }
-}
-
 tpar_status launch_stream(const FusedArgs& a, int qmode, const tpar_plan& p, cudaStream_t stream, bool pdl)
 {
     const int nr = tpar::rank_bound(a.n_ranks);
-    const void* fn = tpar::stream_kernel_for(qmode, nr, p.vec_per_thread);
+    const void* fn = tpar::stream_kernel_for(qmode, nr, p.vec_per_thread, a.f16);
     if (!fn)
         return TPAR_ERR_UNSUPPORTED;
     const int64_t row_bytes = static_cast<int64_t>(a.nvec) * 16;
@@ -475,7 +464,7 @@ tpar_status launch_fused(const FusedArgs& a, int qmode, const tpar_plan& p, cuda
     if (p.kernel == 2)
         return launch_stream(a, qmode, p, stream, pdl);
     const int nr = tpar::rank_bound(a.n_ranks);
-    const void* fn = fused_kernel(qmode, nr, p.vec_per_thread, p.kernel == 1);
+    const void* fn = tpar::fused_kernel_for(qmode, nr, p.vec_per_thread, p.kernel == 1, a.f16);
     if (!fn)
         return TPAR_ERR_UNSUPPORTED;
     if (p.kernel == 1 && p.split > 8) {
@@ -513,7 +502,7 @@ tpar_status launch_quantize(const void* x, int64_t T, int64_t d, uint8_t* codes,
     q.nvec = T * d / 8;
     q.f16 = f16;
     const unsigned grid = flat_grid(q.nvec / 2, sm_count);  // one thread per 16-element block
-    if (launch(tpar::quantize_kernel_for(dynamic), dim3(grid), dim3(256), &q, stream, 1, pdl) != cudaSuccess)
+    if (launch(tpar::quantize_kernel_for(dynamic, f16), dim3(grid), dim3(256), &q, stream, 1, pdl) != cudaSuccess)
         return TPAR_ERR_CUDA;
     return TPAR_OK;
 }
@@ -577,7 +566,7 @@ bool small_nvfp4_shape(int64_t T, int64_t d, int* K, int* slice, int* threads, i
 tpar_status launch_small_nvfp4(const FusedArgs& a, float* gscale, int K, int slice, int threads, int ipt,
                                cudaStream_t stream, bool pdl)
 {
-    const void* fn = tpar::small_kernel_for(tpar::rank_bound(a.n_ranks), ipt);
+    const void* fn = tpar::small_kernel_for(tpar::rank_bound(a.n_ranks), ipt, a.f16);
     if (!fn)
         return TPAR_ERR_UNSUPPORTED;
     if (K > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
@@ -627,7 +616,7 @@ tpar_status fused_impl(const Call& c, const tpar_plan* user_plan, void* user_ws,
         ra.nvec = c.T * c.d / 8;
         ra.n_ranks = c.n_ranks;
         ra.f16 = (c.flags & TPAR_DTYPE_FP16) != 0;
-        return launch(tpar::reduce_kernel_for(tpar::rank_bound(c.n_ranks)), dim3(flat_grid(ra.nvec, sm)),
+        return launch(tpar::reduce_kernel_for(tpar::rank_bound(c.n_ranks), ra.f16), dim3(flat_grid(ra.nvec, sm)),
                       dim3(256), &ra, stream, 1, pdl) == cudaSuccess
                    ? TPAR_OK
                    : TPAR_ERR_CUDA;
@@ -722,7 +711,7 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
     ra.nvec = nvec;
     ra.n_ranks = n_ranks;
     ra.f16 = (flags & TPAR_DTYPE_FP16) != 0;
-    if (launch(tpar::reduce_kernel_for(tpar::rank_bound(n_ranks)), dim3(flat_grid(nvec, sm)), dim3(256), &ra,
+    if (launch(tpar::reduce_kernel_for(tpar::rank_bound(n_ranks), ra.f16), dim3(flat_grid(nvec, sm)), dim3(256), &ra,
                stream, 1, pdl) != cudaSuccess)
         return TPAR_ERR_CUDA;
     // K2: out_residual = bf16(reduced + residual)
@@ -731,8 +720,7 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
         const uint4* res = static_cast<const uint4*>(residual);
         uint4* outr = static_cast<uint4*>(out_residual);
         int64_t n = nvec;
-        bool f16 = (flags & TPAR_DTYPE_FP16) != 0;
-        void* args[5] = {&red, &res, &outr, &n, &f16};
+        void* args[4] = {&red, &res, &outr, &n};
         cudaLaunchConfig_t cfg;
         std::memset(&cfg, 0, sizeof cfg);
         cfg.gridDim = dim3(flat_grid(nvec, sm));
@@ -743,7 +731,7 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
         at.val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = &at;
         cfg.numAttrs = pdl ? 1 : 0;
-        if (cudaLaunchKernelExC(&cfg, tpar::residual_add_kernel_ptr(), args) != cudaSuccess)
+        if (cudaLaunchKernelExC(&cfg, tpar::residual_add_kernel_ptr((flags & TPAR_DTYPE_FP16) != 0), args) != cudaSuccess)
             return TPAR_ERR_CUDA;
     }
     // K3: out_norm = RMSNorm(out_residual) (+ amax for a dynamic NVFP4 scale)
@@ -802,8 +790,7 @@ tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* co
             return st;
         const uint4* xv = static_cast<const uint4*>(x);
         int64_t nvec = T * d / 8;
-        bool f16 = (flags & TPAR_DTYPE_FP16) != 0;
-        void* args[4] = {&xv, &nvec, &ws, &f16};
+        void* args[3] = {&xv, &nvec, &ws};
         cudaLaunchConfig_t cfg;
         std::memset(&cfg, 0, sizeof cfg);
         cfg.gridDim = dim3(flat_grid(nvec, sm));
@@ -814,7 +801,7 @@ tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* co
         at.val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = &at;
         cfg.numAttrs = pdl ? 1 : 0;
-        if (cudaLaunchKernelExC(&cfg, tpar::amax_kernel_ptr(), args) != cudaSuccess)
+        if (cudaLaunchKernelExC(&cfg, tpar::amax_kernel_ptr((flags & TPAR_DTYPE_FP16) != 0), args) != cudaSuccess)
             return TPAR_ERR_CUDA;
     }
     st = launch_quantize(x, T, d, codes, scales, global_scale, ws, !given, sm, stream, pdl,
@@ -886,7 +873,7 @@ tpar_status tpar_fused_rmsnorm_fp8(const void* const* partials, int n_ranks, con
     f.ws = ws;
     f.nvec = T * d / 8;
     f.f16 = a.f16;
-    if (launch(tpar::fp8_quantize_kernel_for(true), dim3(flat_grid(f.nvec, sm)), dim3(256), &f, stream, 1, pdl) !=
+    if (launch(tpar::fp8_quantize_kernel_for(true, f.f16), dim3(flat_grid(f.nvec, sm)), dim3(256), &f, stream, 1, pdl) !=
         cudaSuccess) {
         cudaMemsetAsync(ws, 0, 8, stream);
         return TPAR_ERR_CUDA;
@@ -928,8 +915,7 @@ tpar_status tpar_fp8_quantize(const void* x, int64_t T, int64_t d, uint8_t* code
             return st;
         const uint4* xv = static_cast<const uint4*>(x);
         int64_t n = nvec;
-        bool f16 = (flags & TPAR_DTYPE_FP16) != 0;
-        void* args[4] = {&xv, &n, &ws, &f16};
+        void* args[3] = {&xv, &n, &ws};
         cudaLaunchConfig_t cfg;
         std::memset(&cfg, 0, sizeof cfg);
         cfg.gridDim = dim3(flat_grid(nvec, sm));
@@ -940,7 +926,7 @@ tpar_status tpar_fp8_quantize(const void* x, int64_t T, int64_t d, uint8_t* code
         at.val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = &at;
         cfg.numAttrs = pdl ? 1 : 0;
-        if (cudaLaunchKernelExC(&cfg, tpar::amax_kernel_ptr(), args) != cudaSuccess)
+        if (cudaLaunchKernelExC(&cfg, tpar::amax_kernel_ptr((flags & TPAR_DTYPE_FP16) != 0), args) != cudaSuccess)
             return TPAR_ERR_CUDA;
     }
     tpar::Fp8Args f;
@@ -950,7 +936,7 @@ tpar_status tpar_fp8_quantize(const void* x, int64_t T, int64_t d, uint8_t* code
     f.ws = ws;
     f.nvec = nvec;
     f.f16 = (flags & TPAR_DTYPE_FP16) != 0;
-    if (launch(tpar::fp8_quantize_kernel_for(!given), dim3(flat_grid(nvec, sm)), dim3(256), &f, stream, 1, pdl) !=
+    if (launch(tpar::fp8_quantize_kernel_for(!given, f.f16), dim3(flat_grid(nvec, sm)), dim3(256), &f, stream, 1, pdl) !=
         cudaSuccess) {
         if (ws)
             cudaMemsetAsync(ws, 0, 8, stream);
@@ -1100,7 +1086,7 @@ extern "C" tpar_status tpar_unfused_rmsnorm_noalloc(const void* const* partials,
     ra.nvec = nvec;
     ra.n_ranks = n_ranks;
     ra.f16 = (flags & TPAR_DTYPE_FP16) != 0;
-    if (launch(tpar::reduce_kernel_for(tpar::rank_bound(n_ranks)), dim3(flat_grid(nvec, sm)), dim3(256), &ra,
+    if (launch(tpar::reduce_kernel_for(tpar::rank_bound(n_ranks), ra.f16), dim3(flat_grid(nvec, sm)), dim3(256), &ra,
                stream, 1, pdl) != cudaSuccess)
         return TPAR_ERR_CUDA;
     // K2: out_residual = bf16(reduced + residual)
@@ -1109,8 +1095,7 @@ extern "C" tpar_status tpar_unfused_rmsnorm_noalloc(const void* const* partials,
         const uint4* res = static_cast<const uint4*>(residual);
         uint4* outr = static_cast<uint4*>(out_residual);
         int64_t n = nvec;
-        bool f16 = (flags & TPAR_DTYPE_FP16) != 0;
-        void* args[5] = {&red, &res, &outr, &n, &f16};
+        void* args[4] = {&red, &res, &outr, &n};
         cudaLaunchConfig_t cfg;
         std::memset(&cfg, 0, sizeof cfg);
         cfg.gridDim = dim3(flat_grid(nvec, sm));
@@ -1121,7 +1106,7 @@ extern "C" tpar_status tpar_unfused_rmsnorm_noalloc(const void* const* partials,
         at.val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = &at;
         cfg.numAttrs = pdl ? 1 : 0;
-        if (cudaLaunchKernelExC(&cfg, tpar::residual_add_kernel_ptr(), args) != cudaSuccess)
+        if (cudaLaunchKernelExC(&cfg, tpar::residual_add_kernel_ptr((flags & TPAR_DTYPE_FP16) != 0), args) != cudaSuccess)
             return TPAR_ERR_CUDA;
     }
     // K3: out_norm = RMSNorm(out_residual) (+ amax for a dynamic NVFP4 scale)

@@ -6,27 +6,48 @@
 
 namespace tpar {
 
-// Fused kernel for quantisation mode q (0 none, 1 given scale, 2 dynamic
-// amax), rank bound nr (1, 2, 4, 8, 16), vectors per thread vpt (1, 2, 4, 8;
-// the cluster form only 1, 2). Returns null for a combination not built.
-const void* fused_kernel_q0(int nr, int vpt, bool cluster);
-const void* fused_kernel_q1(int nr, int vpt, bool cluster);
-const void* fused_kernel_q2(int nr, int vpt, bool cluster);
-const void* fused_kernel_q3(int nr, int vpt, bool cluster);
+// Fused kernel for quantisation mode q (0 none, 1 NVFP4 given scale, 2
+// dynamic amax, 3 FP8 given scale), rank bound nr (1, 2, 4, 8, 16), vectors
+// per thread vpt (1, 2, 4, 8; the cluster form only 1, 2) and element type.
+// Returns null for a combination not built.
+const void* fused_kernel_q0_bf16(int nr, int vpt, bool cluster);
+const void* fused_kernel_q1_bf16(int nr, int vpt, bool cluster);
+const void* fused_kernel_q2_bf16(int nr, int vpt, bool cluster);
+const void* fused_kernel_q3_bf16(int nr, int vpt, bool cluster);
+const void* fused_kernel_q0_fp16(int nr, int vpt, bool cluster);
+const void* fused_kernel_q1_fp16(int nr, int vpt, bool cluster);
+const void* fused_kernel_q2_fp16(int nr, int vpt, bool cluster);
+const void* fused_kernel_q3_fp16(int nr, int vpt, bool cluster);
 
-// TMA-fed bandwidth kernel (stream.cuh) for quantisation mode q, rank bound
-// nr and vpt vectors per consumer thread.
-const void* stream_kernel_for(int qmode, int nr, int vpt);
+inline const void* fused_kernel_for(int q, int nr, int vpt, bool cluster, bool f16)
+{
+    switch (q) {
+    case 0: return f16 ? fused_kernel_q0_fp16(nr, vpt, cluster) : fused_kernel_q0_bf16(nr, vpt, cluster);
+    case 1: return f16 ? fused_kernel_q1_fp16(nr, vpt, cluster) : fused_kernel_q1_bf16(nr, vpt, cluster);
+    case 2: return f16 ? fused_kernel_q2_fp16(nr, vpt, cluster) : fused_kernel_q2_bf16(nr, vpt, cluster);
+    case 3: return f16 ? fused_kernel_q3_fp16(nr, vpt, cluster) : fused_kernel_q3_bf16(nr, vpt, cluster);
+    default: return nullptr;
+    }
+}
+
+// TMA-fed bandwidth kernel (stream.cuh) for quantisation mode q (0-2), rank
+// bound nr and vpt vectors per consumer thread.
+const void* stream_kernel_bf16(int qmode, int nr, int vpt);
+const void* stream_kernel_fp16(int qmode, int nr, int vpt);
+inline const void* stream_kernel_for(int qmode, int nr, int vpt, bool f16)
+{
+    return f16 ? stream_kernel_fp16(qmode, nr, vpt) : stream_kernel_bf16(qmode, nr, vpt);
+}
 
 // Single-launch dynamic-scale NVFP4 kernel (nvfp4_small.cuh) for rank bound
 // nr and ipt items per thread (1, 2, 4).
-const void* small_kernel_for(int nr, int ipt);
+const void* small_kernel_for(int nr, int ipt, bool f16);
 
-const void* reduce_kernel_for(int nr);
-const void* residual_add_kernel_ptr();
-const void* quantize_kernel_for(bool dynamic);
-const void* amax_kernel_ptr();
-const void* fp8_quantize_kernel_for(bool dynamic);
+const void* reduce_kernel_for(int nr, bool f16);
+const void* residual_add_kernel_ptr(bool f16);
+const void* quantize_kernel_for(bool dynamic, bool f16);
+const void* amax_kernel_ptr(bool f16);
+const void* fp8_quantize_kernel_for(bool dynamic, bool f16);
 
 // Largest CTA the fused kernel for rank bound nr, vpt vectors per thread and
 // the row (cluster = false) or cluster form is compiled for (mirrors

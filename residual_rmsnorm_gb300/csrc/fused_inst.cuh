@@ -1,0 +1,44 @@
+// fused_inst.cuh -- the switch from runtime (rank bound, vectors per thread,
+// cluster form) to a fused-kernel instantiation. Each kernels_q<Q>_<dtype>.cu
+// expands it for one quantisation mode Q and one element type, so the build
+// compiles the modes and types in parallel.
+#pragma once
+
+#include "dispatch.h"
+#include "kernels.cuh"
+
+namespace tpar {
+
+template <int NR, int Q, bool F16>
+const void* fused_pick_vpt(int vpt, bool cluster)
+{
+    if (cluster) {
+        switch (vpt) {
+        case 1: return reinterpret_cast<const void*>(&fused_rmsnorm_kernel<NR, 1, true, Q, F16>);
+        case 2: return reinterpret_cast<const void*>(&fused_rmsnorm_kernel<NR, 2, true, Q, F16>);
+        default: return nullptr;
+        }
+    }
+    switch (vpt) {
+    case 1: return reinterpret_cast<const void*>(&fused_rmsnorm_kernel<NR, 1, false, Q, F16>);
+    case 2: return reinterpret_cast<const void*>(&fused_rmsnorm_kernel<NR, 2, false, Q, F16>);
+    case 4: return reinterpret_cast<const void*>(&fused_rmsnorm_kernel<NR, 4, false, Q, F16>);
+    case 8: return reinterpret_cast<const void*>(&fused_rmsnorm_kernel<NR, 8, false, Q, F16>);
+    default: return nullptr;
+    }
+}
+
+template <int Q, bool F16>
+const void* fused_pick(int nr, int vpt, bool cluster)
+{
+    switch (nr) {
+    case 1: return fused_pick_vpt<1, Q, F16>(vpt, cluster);
+    case 2: return fused_pick_vpt<2, Q, F16>(vpt, cluster);
+    case 4: return fused_pick_vpt<4, Q, F16>(vpt, cluster);
+    case 8: return fused_pick_vpt<8, Q, F16>(vpt, cluster);
+    case 16: return fused_pick_vpt<16, Q, F16>(vpt, cluster);
+    default: return nullptr;
+    }
+}
+
+}  // namespace tpar

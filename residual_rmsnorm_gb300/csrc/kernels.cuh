@@ -46,7 +46,7 @@ struct FusedArgs {
     uint32_t* amax_bits;               // running max of |out_norm| bits (kQuantAmax)
     uint32_t* err;                     // device error word (bounded wait expired) or null
     int64_t T;
-    bool f16;                          // tensors are IEEE binary16 (else bf16)
+    bool f16;                          // host: tensors are binary16 (picks the F16 instantiation)
     int n_ranks;
     int nvec;   // d / 8
     int slice;  // vectors per CTA along a row (even); nvec for the row kernel
@@ -59,22 +59,22 @@ struct FusedArgs {
 // scale; a 16-element block is this lane's vector and its neighbour's, so
 // the lane joins the shuffle even when `valid` is false) or the running
 // |out_norm| maximum (dynamic scale).
-template <int QMODE>
+template <int QMODE, bool F16>
 __device__ __forceinline__ void emit_vector(const FusedArgs& a, bool valid, int64_t gv, const float h[8],
                                             const uint4& gamma8, float rinv, float g_given, float& amax_local)
 {
     float yq[8];
     if (valid) {
         float gm[8];
-        unpack8_dt(gamma8, gm, a.f16);
+        unpack8_dt(gamma8, gm, F16);
         float y[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e)
             y[e] = h[e] * rinv * gm[e];
-        const uint4 yb = pack8_dt(y, a.f16);
+        const uint4 yb = pack8_dt(y, F16);
         if (a.out_norm)
             st_v4(a.out_norm + gv, yb);
-        unpack8_dt(yb, yq, a.f16);  // the emitted values, as fp32
+        unpack8_dt(yb, yq, F16);  // the emitted values, as fp32
     } else {
 #pragma unroll
         for (int e = 0; e < 8; ++e)
@@ -140,7 +140,7 @@ constexpr int fused_max_threads(int nr, int vpt, bool cluster)
     return (vpt >= 2 || nr >= 16 || cluster) ? 512 : 1024;
 }
 
-template <int NR, int VPT, bool CLUSTER, int QMODE>
+template <int NR, int VPT, bool CLUSTER, int QMODE, bool F16>
 __global__ void __launch_bounds__(fused_max_threads(NR, VPT, CLUSTER))
     fused_rmsnorm_kernel(const __grid_constant__ FusedArgs a)
 {
@@ -218,18 +218,18 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT, CLUSTER))
                 const int v = vbeg + tid + j * static_cast<int>(blockDim.x);
                 ss[j] = 0.0f;
                 if (v < vend) {
-                    unpack8_dt(x[jj][0], h[j], a.f16);
+                    unpack8_dt(x[jj][0], h[j], F16);
 #pragma unroll
                     for (int r = 1; r < NR; ++r)
                         if (r < a.n_ranks)
-                            add8_dt(x[jj][r], h[j], a.f16);
+                            add8_dt(x[jj][r], h[j], F16);
                     if (a.residual)
-                        add8_dt(rv[jj], h[j], a.f16);
+                        add8_dt(rv[jj], h[j], F16);
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         ss[j] = fmaf(h[j][e], h[j][e], ss[j]);
                     if (!CLUSTER && a.out_residual)
-                        st_v4(a.out_residual + rowv + v, pack8_dt(h[j], a.f16));
+                        st_v4(a.out_residual + rowv + v, pack8_dt(h[j], F16));
                 } else {
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
@@ -289,9 +289,9 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT, CLUSTER))
                 // issued before the exchange would delay it (measured); the
                 // bandwidth form gains from issuing it early.
                 if (CLUSTER && a.out_residual)
-                    st_v4(a.out_residual + rowv + v, pack8_dt(h[j], a.f16));
+                    st_v4(a.out_residual + rowv + v, pack8_dt(h[j], F16));
             }
-            emit_vector<QMODE>(a, valid, rowv + v, h[j], gm, rinv, g_given, amax_local);
+            emit_vector<QMODE, F16>(a, valid, rowv + v, h[j], gm, rinv, g_given, amax_local);
         }
     }
 
@@ -314,7 +314,7 @@ struct QuantArgs {
     float* gscale;       // given: input; dynamic: output
     uint32_t* ws;        // dynamic: ws[0] = amax bits, ws[1] = completion counter
     int64_t nvec;        // T * d / 8 (even)
-    bool f16;            // x is IEEE binary16 (else bf16)
+    bool f16;            // host: x is binary16 (picks the F16 instantiation)
 };
 
 // One thread owns one 16-element block (two consecutive 16-byte vectors) per
@@ -322,7 +322,7 @@ struct QuantArgs {
 // round trip) runs once per block. In dynamic mode g = amax / 2688 is read
 // from the workspace; the last CTA to have read it zeroes the workspace for
 // the next call (no CTA waits on another).
-template <bool DYNAMIC>
+template <bool DYNAMIC, bool F16>
 __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __grid_constant__ QuantArgs a)
 {
     pdl_wait();
@@ -356,8 +356,8 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __grid_consta
         // the two halves of the block; the second load hits the lines the
         // first brought into L1
         float x[16];
-        unpack8_dt(ld_reuse(a.x + 2 * b), x, a.f16);
-        unpack8_dt(ld_reuse(a.x + 2 * b + 1), x + 8, a.f16);
+        unpack8_dt(ld_reuse(a.x + 2 * b), x, F16);
+        unpack8_dt(ld_reuse(a.x + 2 * b + 1), x + 8, F16);
         float bmax = 0.0f;
 #pragma unroll
         for (int e = 0; e < 16; ++e)
@@ -383,10 +383,10 @@ struct Fp8Args {
     float* scale;      // given: input; dynamic: output
     uint32_t* ws;      // dynamic: ws[0] = amax bits, ws[1] = completion counter
     int64_t nvec;
-    bool f16;          // x is IEEE binary16 (else bf16)
+    bool f16;          // host: x is binary16 (picks the F16 instantiation)
 };
 
-template <bool DYNAMIC>
+template <bool DYNAMIC, bool F16>
 __global__ void __launch_bounds__(256) fp8_quantize_kernel(const __grid_constant__ Fp8Args a)
 {
     pdl_wait();
@@ -415,7 +415,7 @@ __global__ void __launch_bounds__(256) fp8_quantize_kernel(const __grid_constant
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < a.nvec; v += stride) {
         float x[8];
-        unpack8_dt(ld_stream(a.x + v), x, a.f16);
+        unpack8_dt(ld_stream(a.x + v), x, F16);
 #pragma unroll
         for (int e = 0; e < 8; ++e)
             x[e] = __fmul_rn(x[e], inv);
@@ -432,14 +432,14 @@ struct ReduceArgs {
     uint4* reduced;
     int64_t nvec;  // T * d / 8
     int n_ranks;
-    bool f16;      // tensors are IEEE binary16 (else bf16)
+    bool f16;      // host: tensors are binary16 (picks the F16 instantiation)
 };
 
 // reduced = bf16(sum of partials [+ residual]), fixed rank order, one
 // rounding: the unfused path's K1 (no residual) and the all-reduce-only
 // pattern of the fused entry points ("Deep Dive: AllReduce and AllReduce
 // Fusion in TensorRT-LLM", 6.3, pattern kAllReduce).
-template <int NR>
+template <int NR, bool F16>
 __global__ void __launch_bounds__(256) reduce_kernel(const __grid_constant__ ReduceArgs a)
 {
     pdl_wait();
@@ -452,14 +452,14 @@ __global__ void __launch_bounds__(256) reduce_kernel(const __grid_constant__ Red
             if (r < a.n_ranks)
                 x[r] = ld_stream(a.partials[r] + v);
         float s[8];
-        unpack8_dt(x[0], s, a.f16);
+        unpack8_dt(x[0], s, F16);
 #pragma unroll
         for (int r = 1; r < NR; ++r)
             if (r < a.n_ranks)
-                add8_dt(x[r], s, a.f16);
+                add8_dt(x[r], s, F16);
         if (a.residual)
-            add8_dt(ld_coherent(a.residual + v), s, a.f16);
-        st_v4(a.reduced + v, pack8_dt(s, a.f16));
+            add8_dt(ld_coherent(a.residual + v), s, F16);
+        st_v4(a.reduced + v, pack8_dt(s, F16));
     }
 }
 

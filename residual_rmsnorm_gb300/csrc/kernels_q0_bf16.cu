@@ -1,0 +1,10 @@
+// kernels_q0_bf16.cu -- fused-kernel instantiations for quantisation mode
+// 0 (0: bf16/fp16 outputs only, 1: NVFP4 with a given global scale,
+// 2: dynamic-scale phase A, 3: FP8 with a given scale) and bf16 tensors.
+#include "fused_inst.cuh"
+
+namespace tpar {
+
+const void* fused_kernel_q0_bf16(int nr, int vpt, bool cluster) { return fused_pick<0, false>(nr, vpt, cluster); }
+
+}  // namespace tpar

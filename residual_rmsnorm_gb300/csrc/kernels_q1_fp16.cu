@@ -1,0 +1,10 @@
+// kernels_q1_fp16.cu -- fused-kernel instantiations for quantisation mode
+// 1 (0: bf16/fp16 outputs only, 1: NVFP4 with a given global scale,
+// 2: dynamic-scale phase A, 3: FP8 with a given scale) and fp16 tensors.
+#include "fused_inst.cuh"
+
+namespace tpar {
+
+const void* fused_kernel_q1_fp16(int nr, int vpt, bool cluster) { return fused_pick<1, true>(nr, vpt, cluster); }
+
+}  // namespace tpar

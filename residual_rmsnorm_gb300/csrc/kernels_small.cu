@@ -6,28 +6,34 @@
 namespace tpar {
 
 namespace {
-template <int NR>
+template <int NR, bool F16>
 const void* pick_small(int ipt)
 {
     switch (ipt) {
-    case 1: return reinterpret_cast<const void*>(&nvfp4_small_kernel<NR, 1>);
-    case 2: return reinterpret_cast<const void*>(&nvfp4_small_kernel<NR, 2>);
-    case 4: return reinterpret_cast<const void*>(&nvfp4_small_kernel<NR, 4>);
+    case 1: return reinterpret_cast<const void*>(&nvfp4_small_kernel<NR, 1, F16>);
+    case 2: return reinterpret_cast<const void*>(&nvfp4_small_kernel<NR, 2, F16>);
+    case 4: return reinterpret_cast<const void*>(&nvfp4_small_kernel<NR, 4, F16>);
+    default: return nullptr;
+    }
+}
+
+template <bool F16>
+const void* pick_small_nr(int nr, int ipt)
+{
+    switch (nr) {
+    case 1: return pick_small<1, F16>(ipt);
+    case 2: return pick_small<2, F16>(ipt);
+    case 4: return pick_small<4, F16>(ipt);
+    case 8: return pick_small<8, F16>(ipt);
+    case 16: return pick_small<16, F16>(ipt);
     default: return nullptr;
     }
 }
 }  // namespace
 
-const void* small_kernel_for(int nr, int ipt)
+const void* small_kernel_for(int nr, int ipt, bool f16)
 {
-    switch (nr) {
-    case 1: return pick_small<1>(ipt);
-    case 2: return pick_small<2>(ipt);
-    case 4: return pick_small<4>(ipt);
-    case 8: return pick_small<8>(ipt);
-    case 16: return pick_small<16>(ipt);
-    default: return nullptr;
-    }
+    return f16 ? pick_small_nr<true>(nr, ipt) : pick_small_nr<false>(nr, ipt);
 }
 
 }  // namespace tpar

@@ -1,0 +1,45 @@
+// kernels_stream_bf16.cu -- instantiations of the TMA-fed bandwidth kernel
+// (stream.cuh) for bf16 tensors.
+#include "dispatch.h"
+#include "stream.cuh"
+
+namespace tpar {
+
+namespace {
+template <int NR, int Q>
+const void* pick_stream(int vpt)
+{
+    switch (vpt) {
+    case 1: return reinterpret_cast<const void*>(&stream_rmsnorm_kernel<NR, 1, Q, false>);
+    case 2: return reinterpret_cast<const void*>(&stream_rmsnorm_kernel<NR, 2, Q, false>);
+    case 4: return reinterpret_cast<const void*>(&stream_rmsnorm_kernel<NR, 4, Q, false>);
+    case 8: return reinterpret_cast<const void*>(&stream_rmsnorm_kernel<NR, 8, Q, false>);
+    default: return nullptr;
+    }
+}
+
+template <int Q>
+const void* pick_stream_nr(int nr, int vpt)
+{
+    switch (nr) {
+    case 1: return pick_stream<1, Q>(vpt);
+    case 2: return pick_stream<2, Q>(vpt);
+    case 4: return pick_stream<4, Q>(vpt);
+    case 8: return pick_stream<8, Q>(vpt);
+    case 16: return pick_stream<16, Q>(vpt);
+    default: return nullptr;
+    }
+}
+}  // namespace
+
+const void* stream_kernel_bf16(int qmode, int nr, int vpt)
+{
+    switch (qmode) {
+    case 0: return pick_stream_nr<0>(nr, vpt);
+    case 1: return pick_stream_nr<1>(nr, vpt);
+    case 2: return pick_stream_nr<2>(nr, vpt);
+    default: return nullptr;  // FP8 output is not built into the stream kernel
+    }
+}
+
+}  // namespace tpar

@@ -31,7 +31,7 @@ struct SmallArgs {
     int slice;         // vectors per CTA (a multiple of 32); slice * gridDim.x == nvec
 };
 
-template <int NR, int IPT>
+template <int NR, int IPT, bool F16>
 __global__ void __launch_bounds__(512) nvfp4_small_kernel(const __grid_constant__ SmallArgs sa)
 {
     const FusedArgs& a = sa.f;
@@ -92,13 +92,13 @@ __global__ void __launch_bounds__(512) nvfp4_small_kernel(const __grid_constant_
             const int i = tid + j * B;
             ss[j] = 0.0f;
             if (i < items) {
-                unpack8_dt(x[gg][0], h[j], a.f16);
+                unpack8_dt(x[gg][0], h[j], F16);
 #pragma unroll
                 for (int r = 1; r < NR; ++r)
                     if (r < a.n_ranks)
-                        add8_dt(x[gg][r], h[j], a.f16);
+                        add8_dt(x[gg][r], h[j], F16);
                 if (a.residual)
-                    add8_dt(rv[gg], h[j], a.f16);
+                    add8_dt(rv[gg], h[j], F16);
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
                     ss[j] = fmaf(h[j][e], h[j][e], ss[j]);
@@ -140,16 +140,16 @@ __global__ void __launch_bounds__(512) nvfp4_small_kernel(const __grid_constant_
             const int64_t gv = static_cast<int64_t>(i / slice) * a.nvec + vbeg + i % slice;
             const float rinv = rinv_sh[i / slice];
             float gmf[8], y[8];
-            unpack8_dt(gm[j], gmf, a.f16);
+            unpack8_dt(gm[j], gmf, F16);
 #pragma unroll
             for (int e = 0; e < 8; ++e)
                 y[e] = h[j][e] * rinv * gmf[e];
-            const uint4 yb = pack8_dt(y, a.f16);
+            const uint4 yb = pack8_dt(y, F16);
             if (a.out_residual)
-                st_v4(a.out_residual + gv, pack8_dt(h[j], a.f16));
+                st_v4(a.out_residual + gv, pack8_dt(h[j], F16));
             if (a.out_norm)
                 st_v4(a.out_norm + gv, yb);
-            unpack8_dt(yb, h[j], a.f16);  // h now holds the emitted values
+            unpack8_dt(yb, h[j], F16);  // h now holds the emitted values
 #pragma unroll
             for (int e = 0; e < 8; ++e)
                 amax_local = fmaxf(amax_local, fabsf(h[j][e]));

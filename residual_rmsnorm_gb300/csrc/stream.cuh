@@ -52,7 +52,7 @@ __device__ __forceinline__ void consumers_sync(int nthreads)
 
 constexpr uint64_t kStreamWaitNs = 500ull * 1000 * 1000;
 
-template <int NR, int VPT, int QMODE>
+template <int NR, int VPT, int QMODE, bool F16>
 __global__ void __launch_bounds__(544, 1) stream_rmsnorm_kernel(const __grid_constant__ StreamArgs sa)
 {
     extern __shared__ __align__(128) unsigned char ring[];
@@ -174,9 +174,9 @@ __global__ void __launch_bounds__(544, 1) stream_rmsnorm_kernel(const __grid_con
                 if (v < nvec) {
                     const uint4 x = stage[v];
                     if (src == 0)
-                        unpack8_dt(x, h[j], a.f16);
+                        unpack8_dt(x, h[j], F16);
                     else
-                        add8_dt(x, h[j], a.f16);
+                        add8_dt(x, h[j], F16);
                 }
             }
             __syncwarp();
@@ -197,7 +197,7 @@ __global__ void __launch_bounds__(544, 1) stream_rmsnorm_kernel(const __grid_con
                 for (int e = 0; e < 8; ++e)
                     ss = fmaf(h[j][e], h[j][e], ss);
                 if (a.out_residual)
-                    st_v4(a.out_residual + rowv + v, pack8_dt(h[j], a.f16));
+                    st_v4(a.out_residual + rowv + v, pack8_dt(h[j], F16));
             }
             ss = warp_sum(ss);
             const int w = (j * C + 32 * cwarp) >> 5;
@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(544, 1) stream_rmsnorm_kernel(const __grid_con
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const int v = c + j * C;
-            emit_vector<QMODE>(a, v < nvec, rowv + v, h[j], gam[j], rinv, g_given, amax_local);
+            emit_vector<QMODE, F16>(a, v < nvec, rowv + v, h[j], gam[j], rinv, g_given, amax_local);
         }
         if (stop_sh[buf])
             break;  // the same sample for every consumer: all leave together

@@ -7,7 +7,8 @@
 namespace tpar {
 
 // amax of |x| over a bf16 tensor into ws[0] (for the standalone quantiser).
-__global__ void __launch_bounds__(256) amax_kernel(const uint4* x, int64_t nvec, uint32_t* ws, bool f16)
+template <bool F16>
+__global__ void __launch_bounds__(256) amax_kernel(const uint4* x, int64_t nvec, uint32_t* ws)
 {
     pdl_wait();
     pdl_launch_dependents();
@@ -15,7 +16,7 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint4* x, int64_t nvec,
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec; v += stride) {
         float f[8];
-        unpack8_dt(ld_stream(x + v), f, f16);
+        unpack8_dt(ld_stream(x + v), f, F16);
 #pragma unroll
         for (int e = 0; e < 8; ++e)
             m = fmaxf(m, fabsf(f[e]));
@@ -26,47 +27,71 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint4* x, int64_t nvec,
 }
 
 // K2: out_residual = bf16(reduced + residual) (a copy when residual is null).
+template <bool F16>
 __global__ void __launch_bounds__(256) residual_add_kernel(const uint4* reduced, const uint4* residual,
-                                                           uint4* out_residual, int64_t nvec, bool f16)
+                                                           uint4* out_residual, int64_t nvec)
 {
     pdl_wait();
     pdl_launch_dependents();
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < nvec; v += stride) {
         float s[8];
-        unpack8_dt(ld_stream(reduced + v), s, f16);
+        unpack8_dt(ld_stream(reduced + v), s, F16);
         if (residual)
-            add8_dt(ld_coherent(residual + v), s, f16);
-        st_v4(out_residual + v, pack8_dt(s, f16));
+            add8_dt(ld_coherent(residual + v), s, F16);
+        st_v4(out_residual + v, pack8_dt(s, F16));
     }
 }
 
-const void* reduce_kernel_for(int nr)
+const void* reduce_kernel_for(int nr, bool f16)
 {
+    if (f16) {
+        switch (nr) {
+        case 1: return reinterpret_cast<const void*>(&reduce_kernel<1, true>);
+        case 2: return reinterpret_cast<const void*>(&reduce_kernel<2, true>);
+        case 4: return reinterpret_cast<const void*>(&reduce_kernel<4, true>);
+        case 8: return reinterpret_cast<const void*>(&reduce_kernel<8, true>);
+        case 16: return reinterpret_cast<const void*>(&reduce_kernel<16, true>);
+        default: return nullptr;
+        }
+    }
     switch (nr) {
-    case 1: return reinterpret_cast<const void*>(&reduce_kernel<1>);
-    case 2: return reinterpret_cast<const void*>(&reduce_kernel<2>);
-    case 4: return reinterpret_cast<const void*>(&reduce_kernel<4>);
-    case 8: return reinterpret_cast<const void*>(&reduce_kernel<8>);
-    case 16: return reinterpret_cast<const void*>(&reduce_kernel<16>);
+    case 1: return reinterpret_cast<const void*>(&reduce_kernel<1, false>);
+    case 2: return reinterpret_cast<const void*>(&reduce_kernel<2, false>);
+    case 4: return reinterpret_cast<const void*>(&reduce_kernel<4, false>);
+    case 8: return reinterpret_cast<const void*>(&reduce_kernel<8, false>);
+    case 16: return reinterpret_cast<const void*>(&reduce_kernel<16, false>);
     default: return nullptr;
     }
 }
 
-const void* residual_add_kernel_ptr() { return reinterpret_cast<const void*>(&residual_add_kernel); }
-
-const void* quantize_kernel_for(bool dynamic)
+const void* residual_add_kernel_ptr(bool f16)
 {
-    return dynamic ? reinterpret_cast<const void*>(&nvfp4_quantize_kernel<true>)
-                   : reinterpret_cast<const void*>(&nvfp4_quantize_kernel<false>);
+    return f16 ? reinterpret_cast<const void*>(&residual_add_kernel<true>)
+               : reinterpret_cast<const void*>(&residual_add_kernel<false>);
 }
 
-const void* amax_kernel_ptr() { return reinterpret_cast<const void*>(&amax_kernel); }
-
-const void* fp8_quantize_kernel_for(bool dynamic)
+const void* quantize_kernel_for(bool dynamic, bool f16)
 {
-    return dynamic ? reinterpret_cast<const void*>(&fp8_quantize_kernel<true>)
-                   : reinterpret_cast<const void*>(&fp8_quantize_kernel<false>);
+    if (f16)
+        return dynamic ? reinterpret_cast<const void*>(&nvfp4_quantize_kernel<true, true>)
+                       : reinterpret_cast<const void*>(&nvfp4_quantize_kernel<false, true>);
+    return dynamic ? reinterpret_cast<const void*>(&nvfp4_quantize_kernel<true, false>)
+                   : reinterpret_cast<const void*>(&nvfp4_quantize_kernel<false, false>);
+}
+
+const void* amax_kernel_ptr(bool f16)
+{
+    return f16 ? reinterpret_cast<const void*>(&amax_kernel<true>) : reinterpret_cast<const void*>(&amax_kernel<false>);
+}
+
+const void* fp8_quantize_kernel_for(bool dynamic, bool f16)
+{
+    if (f16)
+        return dynamic ? reinterpret_cast<const void*>(&fp8_quantize_kernel<true, true>)
+                       : reinterpret_cast<const void*>(&fp8_quantize_kernel<false, true>);
+    return dynamic ? reinterpret_cast<const void*>(&fp8_quantize_kernel<true, false>)
+                   : reinterpret_cast<const void*>(&fp8_quantize_kernel<false, false>);
 }
 
 }  // namespace tpar
