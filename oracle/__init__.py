@@ -89,6 +89,8 @@ def _load():
         lib.orc_nvfp4_quantize.argtypes = [P, i64, i64, ctypes.c_int, ctypes.c_float, P, P, P]
         lib.orc_fp8_quantize.restype = ctypes.c_int
         lib.orc_fp8_quantize.argtypes = [P, i64, i64, ctypes.c_int, ctypes.c_float, P, P]
+        lib.orc_nvfp4_scales_128x4.restype = ctypes.c_int
+        lib.orc_nvfp4_scales_128x4.argtypes = [P, i64, i64, P]
         lib.orc_bf16_amax.restype = ctypes.c_float
         lib.orc_bf16_amax.argtypes = [P, i64]
         _lib = lib
@@ -230,6 +232,26 @@ def nvfp4_quantize(x, global_scale: float | None = None, dtype: str = "bf16"):
     if rc != 0:
         raise ValueError("oracle rejected the arguments")
     return codes, scales, np.float32(g.value)
+
+
+def padded_rows_128(T: int) -> int:
+    """Rows of the 128x4 tiled scale layout: T rounded up to a multiple of 128."""
+    return (T + 127) // 128 * 128
+
+
+def nvfp4_scales_128x4(scales, fill: int = 0):
+    """Row-major NVFP4 scales [T, kb] (kb % 4 == 0) -> the 128x4 tiled layout
+    block-scaled GEMMs read (cuBLAS documentation, "1D Block Scaling Factors
+    Layout"): a flat uint8 array of padded_rows_128(T) * kb bytes whose
+    padding-row entries hold ``fill``.
+    """
+    s = np.ascontiguousarray(scales, dtype=np.uint8)
+    T, kb = s.shape
+    out = np.full(padded_rows_128(T) * kb, fill, np.uint8)
+    rc = _load().orc_nvfp4_scales_128x4(_ptr(s), T, kb, _ptr(out))
+    if rc != 0:
+        raise ValueError("oracle rejected the arguments")
+    return out
 
 
 def fp8_quantize(x, scale: float | None = None, dtype: str = "bf16"):

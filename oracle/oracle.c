@@ -414,6 +414,42 @@ int orc_nvfp4_quantize_dt(const uint16_t* x, int64_t T, int64_t d, int dtype, in
     return 0;
 }
 
+/* ------------------------------------------------------------------------ */
+/* NVFP4 scales in the 128x4 tiled layout that block-scaled GEMMs read.     */
+/* ------------------------------------------------------------------------ */
+
+/*
+ * The pages name only "NVFP4". The layout below is the public one that
+ * Blackwell block-scaled matrix multiplies read the 16-element-block scales
+ * of an operand in (cuBLAS documentation, "1D Block Scaling Factors Layout"):
+ *   - the [T, kb] scale matrix (kb = d / 16, a multiple of 4) is cut into
+ *     tiles of 128 rows x 4 scale columns; rows are padded up to a multiple
+ *     of 128, so the array holds ceil(T / 128) * 128 * kb bytes;
+ *   - tiles follow one another row-major (all column tiles of rows 0..127,
+ *     then of rows 128..255, ...), 512 bytes each;
+ *   - inside a tile, the 512 bytes are 32 lines of 16: line j holds the
+ *     4 scales of tile rows j, j + 32, j + 64, j + 96, in that order, each
+ *     as 4 consecutive bytes (its 4 columns).
+ * So scale (t, c) sits at
+ *   tile   = (t / 128) * (kb / 4) + c / 4
+ *   offset = tile * 512 + (t % 32) * 16 + ((t % 128) / 32) * 4 + c % 4.
+ * Only the T * kb entries of real rows are written; padding rows of `out`
+ * are left as the caller filled them.
+ */
+int orc_nvfp4_scales_128x4(const uint8_t* scales, int64_t T, int64_t kb, uint8_t* out)
+{
+    if (T < 0 || kb < 4 || kb % 4 != 0 || !scales || !out)
+        return -1;
+    for (int64_t t = 0; t < T; ++t) {
+        for (int64_t c = 0; c < kb; ++c) {
+            int64_t tile = (t / 128) * (kb / 4) + c / 4;
+            int64_t off = tile * 512 + (t % 32) * 16 + ((t % 128) / 32) * 4 + c % 4;
+            out[off] = scales[t * kb + c];
+        }
+    }
+    return 0;
+}
+
 /* Absolute maximum of a bf16 tensor, as the binary32 bit pattern. */
 float orc_bf16_amax(const uint16_t* x, int64_t n)
 {

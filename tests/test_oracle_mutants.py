@@ -18,12 +18,12 @@ MUTANTS = [
     ("mean_as_sum", "double ms = sumsq / (double)d;", "double ms = sumsq;"),
     ("eps_outside_sqrt", "double denom = sqrt(ms + (double)eps);", "double denom = sqrt(ms) + (double)eps;"),
     ("eps_dropped", "double denom = sqrt(ms + (double)eps);", "double denom = sqrt(ms);"),
-    ("last_rank_dropped", "for (int r = 0; r < n; ++r)\n                s += orc_bf16_to_double(partials[r][row + i]);\n            double h = residual ? s + orc_bf16_to_double(residual[row + i]) : s;\n            if (h_ref)",
-     "for (int r = 0; r < n - 1; ++r)\n                s += orc_bf16_to_double(partials[r][row + i]);\n            double h = residual ? s + orc_bf16_to_double(residual[row + i]) : s;\n            if (h_ref)"),
-    ("residual_dropped", "double h = residual ? s + orc_bf16_to_double(residual[row + i]) : s;\n            if (h_ref)",
+    ("last_rank_dropped", "for (int r = 0; r < n; ++r)\n                s += elem_to_double(partials[r][row + i], dtype);\n            double h = residual ? s + elem_to_double(residual[row + i], dtype) : s;\n            if (h_ref)",
+     "for (int r = 0; r < n - 1; ++r)\n                s += elem_to_double(partials[r][row + i], dtype);\n            double h = residual ? s + elem_to_double(residual[row + i], dtype) : s;\n            if (h_ref)"),
+    ("residual_dropped", "double h = residual ? s + elem_to_double(residual[row + i], dtype) : s;\n            if (h_ref)",
      "double h = s;\n            if (h_ref)"),
-    ("gamma_reversed", "orc_bf16_to_double(gamma[i])", "orc_bf16_to_double(gamma[d - 1 - i])"),
-    ("gamma_dropped", "double y = h / denom * orc_bf16_to_double(gamma[i]);", "double y = h / denom;"),
+    ("gamma_reversed", "elem_to_double(gamma[i], dtype)", "elem_to_double(gamma[d - 1 - i], dtype)"),
+    ("gamma_dropped", "double y = h / denom * elem_to_double(gamma[i], dtype);", "double y = h / denom;"),
     ("bf16_truncates", "double r = rint(a / q) * q;\n    if (r >= 0x1p128)", "double r = floor(a / q) * q;\n    if (r >= 0x1p128)"),
     ("bf16_ties_away", "double r = rint(a / q) * q;\n    if (r >= 0x1p128)", "double r = round(a / q) * q;\n    if (r >= 0x1p128)"),
     ("e4m3_wrong_bias", "return (uint8_t)(((ub + 7) << 3) | m);", "return (uint8_t)(((ub + 8) << 3) | m);"),
@@ -39,8 +39,12 @@ MUTANTS = [
     ("fp8_scale_not_448", "s = amax / 448.0f;", "s = amax / 256.0f;"),
     ("f16_truncates", "    double r = rint(a / q) * q; /* <= 65504 here */", "    double r = floor(a / q) * q;"),
     ("f16_wrong_bias", "(uint16_t)(((er - 1 + 15) << 10) | m)", "(uint16_t)(((er - 1 + 14) << 10) | m)"),
-    ("fp8_divides_by_inverse", "codes[k] = orc_e4m3_from_float((float)orc_bf16_to_double(x[k]) * inv);",
-     "codes[k] = orc_e4m3_from_float((float)orc_bf16_to_double(x[k]) / (inv > 0.0f ? inv : 1.0f));"),
+    ("fp8_divides_by_inverse", "codes[k] = orc_e4m3_from_float((float)elem_to_double(x[k], dtype) * inv);",
+     "codes[k] = orc_e4m3_from_float((float)elem_to_double(x[k], dtype) / (inv > 0.0f ? inv : 1.0f));"),
+    ("sf_row_strides_swapped", "int64_t off = tile * 512 + (t % 32) * 16 + ((t % 128) / 32) * 4 + c % 4;",
+     "int64_t off = tile * 512 + (t % 32) * 4 + ((t % 128) / 32) * 16 + c % 4;"),
+    ("sf_tiles_column_major", "int64_t tile = (t / 128) * (kb / 4) + c / 4;",
+     "int64_t tile = (c / 4) * ((T + 127) / 128) + t / 128;"),
 ]
 
 

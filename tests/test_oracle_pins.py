@@ -579,3 +579,61 @@ def test_fp16_fused_closed_form_and_library_case(orc):
     # the quantisers decode fp16 input exactly
     codes, s = orc.fp8_quantize(f16([[448.0, -1.0]]), dtype="fp16")
     assert s == 1.0 and list(codes[0]) == [0x7E, 0xB8]
+
+
+# ---------------------------------------------------------------- 128x4 scale layout
+
+def _scales_128x4_by_tiles(s: np.ndarray, fill: int) -> np.ndarray:
+    """The tile picture, independently of any index formula: pad the rows to
+    a multiple of 128, view row t = 128 i + 32 a + b and column c = 4 j + k as
+    [i, a, b, j, k], and lay the bytes out as [i, j, b, a, k]."""
+    T, kb = s.shape
+    Tp = (T + 127) // 128 * 128
+    p = np.full((Tp, kb), fill, np.uint8)
+    p[:T] = s
+    return p.reshape(Tp // 128, 4, 32, kb // 4, 4).transpose(0, 3, 2, 1, 4).reshape(-1)
+
+
+def test_scales_128x4_hand_worked_positions(orc):
+    with open(os.path.join(GOLDEN, "nvfp4_scales_128x4.json")) as f:
+        gold = json.load(f)
+    for case in gold["cases"]:
+        T, kb = case["T"], case["kb"]
+        # a distinct byte per (t, c) where the case is small enough to allow it
+        rng = np.random.default_rng(T * 31 + kb)
+        s = rng.integers(0, 256, size=(T, kb), dtype=np.uint8)
+        out = orc.nvfp4_scales_128x4(s, fill=0)
+        assert out.size == case["size"]
+        for t, c, off in case["positions"]:
+            assert out[off] == s[t, c], (T, kb, t, c, off)
+
+
+@pytest.mark.parametrize("T,kb", [(1, 4), (5, 8), (127, 4), (128, 8), (129, 12), (300, 16), (513, 512)])
+def test_scales_128x4_matches_tile_picture(orc, T, kb):
+    rng = np.random.default_rng(T + 1000 * kb)
+    s = rng.integers(0, 256, size=(T, kb), dtype=np.uint8)
+    got = orc.nvfp4_scales_128x4(s, fill=0xAB)
+    np.testing.assert_array_equal(got, _scales_128x4_by_tiles(s, 0xAB))
+
+
+def test_scales_128x4_is_a_permutation_with_untouched_padding(orc):
+    """Every real (t, c) lands on its own byte; the bytes of padding rows are
+    exactly those left with the fill value."""
+    T, kb = 200, 8
+    ids = np.arange(T * kb, dtype=np.int64)
+    # two byte planes carry the 11-bit index of each entry
+    lo = orc.nvfp4_scales_128x4((ids & 0xFF).astype(np.uint8).reshape(T, kb), fill=0xFF)
+    hi = orc.nvfp4_scales_128x4((ids >> 8).astype(np.uint8).reshape(T, kb), fill=0xFF)
+    code = lo.astype(np.int64) | (hi.astype(np.int64) << 8)
+    real = code[code != 0xFFFF]
+    assert np.array_equal(np.sort(real), ids)
+    assert (code == 0xFFFF).sum() == (256 - T) * kb
+    # a padding row's entries: rows 200..255 of tile row 1
+    pad = np.zeros((T, kb), np.uint8)
+    pos = orc.nvfp4_scales_128x4(pad, fill=0x5A)
+    assert (pos == 0x5A).sum() == (256 - T) * kb
+
+
+def test_scales_128x4_rejects_ragged_columns(orc):
+    with pytest.raises(ValueError):
+        orc.nvfp4_scales_128x4(np.zeros((4, 6), np.uint8))
