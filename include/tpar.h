@@ -73,6 +73,25 @@ typedef void* tpar_stream_t;
 #define TPAR_FORCE_STREAM 0x20u /* persistent TMA-fed kernel (bandwidth path) */
 #define TPAR_DTYPE_FP16 0x40u   /* every [T, d] tensor and gamma is IEEE binary16
                                    instead of bf16 (accumulation stays fp32) */
+#define TPAR_SCALES_128X4 0x80u /* NVFP4 scales in the 128x4 tiled layout that
+                                   block-scaled GEMMs read, see below         */
+
+/*
+ * TPAR_SCALES_128X4 (NVFP4 outputs only; d % 64 == 0). The pages name only
+ * "NVFP4"; this layout is the public one in which Blackwell block-scaled
+ * matrix multiplies read an operand's 16-element-block scales (cuBLAS
+ * documentation, "1D Block Scaling Factors Layout"). The [T, d/16] scale
+ * matrix is cut into tiles of 128 rows x 4 blocks; rows are padded to a
+ * multiple of 128, so the scales buffer holds TPAR_SCALES_128X4_BYTES(T, d)
+ * bytes. Tiles follow one another row-major, 512 bytes each; inside a tile,
+ * row t's 4 scale bytes start at (t % 32) * 16 + ((t % 128) / 32) * 4. So
+ * the scale of row t, block c sits at
+ *   ((t / 128) * (d / 64) + c / 4) * 512 + (t % 32) * 16 + ((t % 128) / 32) * 4 + c % 4.
+ * Only the T * d/16 entries of real rows are written; the bytes of padding
+ * rows are never touched (zero them once if the consumer needs them
+ * defined). Codes and the global scale are unchanged.
+ */
+#define TPAR_SCALES_128X4_BYTES(T, d) ((((int64_t)(T) + 127) / 128) * 128 * ((int64_t)(d) / 16))
 
 /* Launch plan of the fused kernel. kernel: 0 = row kernel (one CTA per row),
  * 1 = cluster-split rows, 2 = persistent TMA-fed stream kernel. split: CTAs
@@ -149,7 +168,10 @@ tpar_status tpar_fused_rmsnorm(const void* const* partials, int n_ranks, const v
  *          out_norm may be NULL. A g that is not positive and finite gives
  *          all-zero scales and signed-zero codes.
  *          TPAR_FORCE_ROW / TPAR_FORCE_CLUSTER / TPAR_FORCE_STREAM: pick the
- *          kernel (at most one); TPAR_NO_PDL.
+ *          kernel (at most one); TPAR_NO_PDL. TPAR_SCALES_128X4: nvfp4_scales
+ *          in the 128x4 tiled GEMM layout (NVFP4 outputs required, d % 64
+ *          == 0, buffer of TPAR_SCALES_128X4_BYTES(T, d) bytes, none of
+ *          which may overlap another tensor); TPAR_ERR_INVALID_ARG otherwise.
  *   plan   NULL for the automatic plan, else a complete plan to launch
  *          (validated: TPAR_ERR_INVALID_ARG if it does not cover a row).
  *   workspace  NULL for the device workspace, else a caller-owned device
@@ -173,7 +195,8 @@ tpar_status tpar_fused_rmsnorm_ex(const void* const* partials, int n_ranks, cons
  *   reduced      caller scratch, bf16 [T, d], must not overlap anything else
  *   out_residual required here (the norm reads it back)
  *   out_norm     required
- *   flags        TPAR_GSCALE_GIVEN, TPAR_NO_PDL
+ *   flags        TPAR_GSCALE_GIVEN, TPAR_NO_PDL, TPAR_SCALES_128X4 (as in
+ *                tpar_fused_rmsnorm_ex)
  * Other arguments as tpar_fused_rmsnorm.
  */
 tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const void* residual,
@@ -189,7 +212,9 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
  * amax(|x|) / 2688 is computed on the device (two kernels, using the device
  * workspace) and written to *global_scale. Per block: s = E4M3(amax_b/(6g)),
  * inv = min(1/(s g), FLT_MAX) (0 when s is 0), code = E2M1(x * inv); all
- * binary32, round to nearest even, saturating.
+ * binary32, round to nearest even, saturating. TPAR_SCALES_128X4 writes the
+ * scales in the 128x4 tiled GEMM layout (d % 64 == 0, buffer of
+ * TPAR_SCALES_128X4_BYTES(T, d) bytes).
  */
 tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* codes,
                                 uint8_t* scales, float* global_scale, uint32_t flags,
@@ -208,7 +233,8 @@ tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* co
  *   code = E4M3(bf16(y) * min(1/s, FLT_MAX)), round to nearest even,
  *   saturating; an s that is not positive and finite gives signed-zero codes.
  * Other arguments, checks and flags (TPAR_NO_PDL, TPAR_FORCE_ROW,
- * TPAR_FORCE_CLUSTER, TPAR_DRY_RUN) as tpar_fused_rmsnorm_ex.
+ * TPAR_FORCE_CLUSTER, TPAR_DRY_RUN) as tpar_fused_rmsnorm_ex;
+ * TPAR_SCALES_128X4 (an NVFP4 layout) is TPAR_ERR_INVALID_ARG here.
  */
 tpar_status tpar_fused_rmsnorm_fp8(const void* const* partials, int n_ranks, const void* residual,
                                    const void* gamma, float eps, int64_t T, int64_t d, void* out_norm,
@@ -220,6 +246,7 @@ tpar_status tpar_fused_rmsnorm_fp8(const void* const* partials, int n_ranks, con
  * tensor x (d % 8 == 0) into codes [T, d]. With TPAR_GSCALE_GIVEN, *scale is
  * the input s; otherwise s = amax(|x|) / 448 is computed on the device (two
  * kernels, device workspace) and written to *scale. Arithmetic as above.
+ * TPAR_SCALES_128X4 is TPAR_ERR_INVALID_ARG here.
  */
 tpar_status tpar_fp8_quantize(const void* x, int64_t T, int64_t d, uint8_t* codes, float* scale,
                               uint32_t flags, tpar_stream_t stream);

@@ -20,10 +20,12 @@ from ._abi import (  # noqa: F401
     TPAR_MAX_RANKS,
     TPAR_NO_PDL,
     TPAR_DRY_RUN,
+    TPAR_SCALES_128X4,
     TparError,
     TparPlan,
     library,
     library_path,
+    scales_128x4_bytes,
     tpar_fused_rmsnorm,
     tpar_fused_rmsnorm_ex,
     tpar_fused_rmsnorm_fp8,

@@ -23,6 +23,13 @@ TPAR_NO_PDL = 0x8
 TPAR_DRY_RUN = 0x10
 TPAR_FORCE_STREAM = 0x20
 TPAR_DTYPE_FP16 = 0x40
+TPAR_SCALES_128X4 = 0x80
+
+
+def scales_128x4_bytes(T: int, d: int) -> int:
+    """TPAR_SCALES_128X4_BYTES: the scales buffer of the 128x4 tiled layout."""
+    return (T + 127) // 128 * 128 * (d // 16)
+
 
 _STATUS = {
     0: "TPAR_OK", 1: "TPAR_ERR_INVALID_ARG", 2: "TPAR_ERR_MISALIGNED",

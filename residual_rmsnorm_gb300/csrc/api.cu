@@ -270,6 +270,15 @@ struct Call {
     bool fp8 = false;  // an FP8 output accompanies the bf16 ones (checked by its entry point)
 };
 
+// Bytes the NVFP4 scales occupy: [T, d/16], or the padded 128x4 tiles.
+int64_t scale_bytes(int64_t T, int64_t d, uint32_t flags)
+{
+    return (flags & TPAR_SCALES_128X4) ? TPAR_SCALES_128X4_BYTES(T, d) : T * (d / 16);
+}
+
+// Column tiles of the 128x4 layout (0 = row-major scales).
+int scale_tiles(int64_t d, uint32_t flags) { return (flags & TPAR_SCALES_128X4) ? static_cast<int>(d / 64) : 0; }
+
 // Host-side checks shared by the fused and unfused entry points.
 tpar_status validate(const Call& c, bool unfused)
 {
@@ -285,6 +294,8 @@ tpar_status validate(const Call& c, bool unfused)
         return TPAR_ERR_INVALID_ARG;
     if (forced_kernels(c.flags) > 1)
         return TPAR_ERR_INVALID_ARG;
+    if ((c.flags & TPAR_SCALES_128X4) && (c.fp8 || c.d % 64 != 0))
+        return TPAR_ERR_INVALID_ARG;
     // An empty batch is a no-op: its tensors may be NULL (empty allocations).
     if (c.T == 0)
         return TPAR_OK;
@@ -299,6 +310,8 @@ tpar_status validate(const Call& c, bool unfused)
     const bool nvfp4 = nq == 3;
     const bool given = (c.flags & TPAR_GSCALE_GIVEN) != 0;
     if (nvfp4 && c.d % 16 != 0)
+        return TPAR_ERR_INVALID_ARG;
+    if ((c.flags & TPAR_SCALES_128X4) && !nvfp4)
         return TPAR_ERR_INVALID_ARG;
     if (!nvfp4 && !c.fp8 && given)
         return TPAR_ERR_INVALID_ARG;
@@ -340,7 +353,7 @@ tpar_status validate(const Call& c, bool unfused)
     outs[no++] = Range(c.out_norm, td2);
     outs[no++] = Range(c.out_residual, td2);
     outs[no++] = Range(c.codes, c.T * c.d / 2);
-    outs[no++] = Range(c.scales, c.T * c.d / 16);
+    outs[no++] = Range(c.scales, scale_bytes(c.T, c.d, c.flags));
     if (nvfp4 && !given)
         outs[no++] = Range(c.gscale, 4);
     outs[no++] = Range(c.reduced, td2);
@@ -491,7 +504,7 @@ unsigned flat_grid(int64_t nvec, int sm_count)
 
 tpar_status launch_quantize(const void* x, int64_t T, int64_t d, uint8_t* codes, uint8_t* scales,
                             float* gscale, uint32_t* ws, bool dynamic, int sm_count, cudaStream_t stream,
-                            bool pdl, bool f16)
+                            bool pdl, bool f16, int sf_tiles)
 {
     QuantArgs q;
     q.x = static_cast<const uint4*>(x);
@@ -501,6 +514,8 @@ tpar_status launch_quantize(const void* x, int64_t T, int64_t d, uint8_t* codes,
     q.ws = ws;
     q.nvec = T * d / 8;
     q.f16 = f16;
+    q.kb = static_cast<int>(d / 16);
+    q.sf_tiles = sf_tiles;
     const unsigned grid = flat_grid(q.nvec / 2, sm_count);  // one thread per 16-element block
     if (launch(tpar::quantize_kernel_for(dynamic, f16), dim3(grid), dim3(256), &q, stream, 1, pdl) != cudaSuccess)
         return TPAR_ERR_CUDA;
@@ -528,6 +543,7 @@ FusedArgs fused_args(const Call& c)
     a.eps = c.eps;
     a.inv_d = 1.0f / static_cast<float>(c.d);
     a.f16 = (c.flags & TPAR_DTYPE_FP16) != 0;
+    a.sf_tiles = scale_tiles(c.d, c.flags);
     return a;
 }
 
@@ -644,7 +660,8 @@ tpar_status fused_impl(const Call& c, const tpar_plan* user_plan, void* user_ws,
     a.scales = nullptr;
     if ((st = launch_fused(a, tpar::kQuantAmax, p, stream, pdl)) != TPAR_OK)
         return st;
-    st = launch_quantize(c.out_norm, c.T, c.d, c.codes, c.scales, c.gscale, ws, true, sm, stream, pdl, a.f16);
+    st = launch_quantize(c.out_norm, c.T, c.d, c.codes, c.scales, c.gscale, ws, true, sm, stream, pdl, a.f16,
+                         a.sf_tiles);
     if (st != TPAR_OK)
         cudaMemsetAsync(ws, 0, 8, stream);  // leave the workspace zeroed
     return st;
@@ -684,7 +701,8 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
                                  uint32_t flags, tpar_stream_t stream_)
 {
     Call c{partials, n_ranks, residual, gamma, eps, T, d, out_norm, out_residual,
-           nvfp4_codes, nvfp4_scales, global_scale, flags & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_DTYPE_FP16), reduced};
+           nvfp4_codes, nvfp4_scales, global_scale,
+           flags & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_DTYPE_FP16 | TPAR_SCALES_128X4), reduced};
     tpar_status st = validate(c, true);
     if (st != TPAR_OK || (flags & TPAR_DRY_RUN))
         return st;
@@ -749,7 +767,7 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
     // K4: the separate NVFP4 quantiser
     if (nvfp4) {
         st = launch_quantize(out_norm, T, d, nvfp4_codes, nvfp4_scales, global_scale, ws, !given, sm, stream,
-                             pdl, (flags & TPAR_DTYPE_FP16) != 0);
+                             pdl, (flags & TPAR_DTYPE_FP16) != 0, scale_tiles(d, flags));
         if (st != TPAR_OK && ws)
             cudaMemsetAsync(ws, 0, 8, stream);
     }
@@ -765,6 +783,8 @@ tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* co
         return TPAR_ERR_UNSUPPORTED;
     if (T > (INT64_MAX / 4) / d)
         return TPAR_ERR_INVALID_ARG;
+    if ((flags & TPAR_SCALES_128X4) && d % 64 != 0)
+        return TPAR_ERR_INVALID_ARG;
     if (T == 0)
         return TPAR_OK;  // empty batch: a no-op, tensors may be NULL
     if (!x || !codes || !scales || !global_scale)
@@ -772,7 +792,7 @@ tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* co
     if (!aligned(x, 16) || !aligned(codes, 16) || !aligned(scales, 16) || !aligned(global_scale, 4))
         return TPAR_ERR_MISALIGNED;
     const bool given = (flags & TPAR_GSCALE_GIVEN) != 0;
-    Range rx(x, T * d * 2), rc(codes, T * d / 2), rs(scales, T * d / 16), rg(global_scale, 4);
+    Range rx(x, T * d * 2), rc(codes, T * d / 2), rs(scales, scale_bytes(T, d, flags)), rg(global_scale, 4);
     if (rc.overlaps(rx) || rs.overlaps(rx) || rc.overlaps(rs) || rg.overlaps(rx) || rg.overlaps(rc) ||
         rg.overlaps(rs))
         return TPAR_ERR_INVALID_ARG;
@@ -805,7 +825,7 @@ tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* co
             return TPAR_ERR_CUDA;
     }
     st = launch_quantize(x, T, d, codes, scales, global_scale, ws, !given, sm, stream, pdl,
-                         (flags & TPAR_DTYPE_FP16) != 0);
+                         (flags & TPAR_DTYPE_FP16) != 0, scale_tiles(d, flags));
     if (st != TPAR_OK && ws)
         cudaMemsetAsync(ws, 0, 8, stream);
     return st;
@@ -818,8 +838,9 @@ tpar_status tpar_fused_rmsnorm_fp8(const void* const* partials, int n_ranks, con
 {
     const bool given = (flags & TPAR_GSCALE_GIVEN) != 0;
     Call c{partials, n_ranks, residual, gamma, eps, T, d, out_norm, out_residual, nullptr, nullptr, nullptr,
-           flags & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_FORCE_ROW | TPAR_FORCE_CLUSTER | TPAR_DTYPE_FP16), nullptr,
-           true};
+           flags & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_FORCE_ROW | TPAR_FORCE_CLUSTER | TPAR_DTYPE_FP16 |
+                    TPAR_SCALES_128X4),
+           nullptr, true};
     tpar_status st = validate(c, false);
     if (st != TPAR_OK)
         return st;
@@ -888,7 +909,7 @@ tpar_status tpar_fp8_quantize(const void* x, int64_t T, int64_t d, uint8_t* code
         return TPAR_ERR_INVALID_ARG;
     if (d > TPAR_MAX_HIDDEN)
         return TPAR_ERR_UNSUPPORTED;
-    if (T > (INT64_MAX / 4) / d)
+    if (T > (INT64_MAX / 4) / d || (flags & TPAR_SCALES_128X4))
         return TPAR_ERR_INVALID_ARG;
     if (T == 0)
         return TPAR_OK;
@@ -1124,6 +1145,6 @@ extern "C" tpar_status tpar_unfused_rmsnorm_noalloc(const void* const* partials,
     // K4: the separate NVFP4 quantiser
     if (nvfp4)
         st = launch_quantize(out_norm, T, d, nvfp4_codes, nvfp4_scales, global_scale, given ? nullptr : ws,
-                             !given, sm, stream, pdl, (fl & TPAR_DTYPE_FP16) != 0);
+                             !given, sm, stream, pdl, (fl & TPAR_DTYPE_FP16) != 0, 0);
     return st;
 }

@@ -40,7 +40,7 @@ struct FusedArgs {
     uint4* out_norm;                   // bf16 [T, d] or null
     uint4* out_residual;               // bf16 [T, d] or null
     uint32_t* codes;                   // [T, d/2] bytes = one word per input vector
-    uint8_t* scales;                   // [T, d/16]
+    uint8_t* scales;                   // [T, d/16] row-major, or 128x4 tiles (sf_tiles)
     uint2* q8;                         // FP8 codes [T, d] = 8 bytes per input vector
     const float* gscale;               // given g (kQuantGiven)
     uint32_t* amax_bits;               // running max of |out_norm| bits (kQuantAmax)
@@ -52,7 +52,24 @@ struct FusedArgs {
     int slice;  // vectors per CTA along a row (even); nvec for the row kernel
     float eps;
     float inv_d;
+    int sf_tiles;  // 0: scales row-major; else the 128x4 tiled layout with d/64 column tiles
 };
+
+// Byte offset of the scale of row t, 16-element block c in the 128x4 tiled
+// layout that block-scaled GEMMs read (cuBLAS documentation, "1D Block
+// Scaling Factors Layout"): tiles of 128 rows x 4 blocks, 512 bytes each,
+// row-major over tiles (col_tiles = d / 64 per 128 rows); inside a tile,
+// row t's 4 bytes start at (t % 32) * 16 + ((t % 128) / 32) * 4.
+__device__ __forceinline__ int64_t scale_offset_128x4(int64_t t, int c, int col_tiles)
+{
+    return ((t >> 7) * col_tiles + (c >> 2)) * 512 + ((t & 31) << 4) + (((t >> 5) & 3) << 2) + (c & 3);
+}
+
+// Where the scale of block `b` (= gv / 2, row t, vector v of the row) goes.
+__device__ __forceinline__ int64_t scale_index(int sf_tiles, int64_t b, int64_t t, int v)
+{
+    return sf_tiles ? scale_offset_128x4(t, v >> 1, sf_tiles) : b;
+}
 
 // Normalise one 16-byte vector of a row (global vector index gv) and emit
 // its outputs: out_norm, and either the NVFP4 codes and scale (given global
@@ -60,7 +77,7 @@ struct FusedArgs {
 // the lane joins the shuffle even when `valid` is false) or the running
 // |out_norm| maximum (dynamic scale).
 template <int QMODE, bool F16>
-__device__ __forceinline__ void emit_vector(const FusedArgs& a, bool valid, int64_t gv, const float h[8],
+__device__ __forceinline__ void emit_vector(const FusedArgs& a, bool valid, int64_t gv, int64_t t, int v, const float h[8],
                                             const uint4& gamma8, float rinv, float g_given, float& amax_local)
 {
     float yq[8];
@@ -110,7 +127,7 @@ __device__ __forceinline__ void emit_vector(const FusedArgs& a, bool valid, int6
                 q[e] = __fmul_rn(yq[e], inv);
             st_u32(a.codes + gv, e2m1x8_from_f32(q));
             if ((gv & 1) == 0)
-                st_u8(a.scales + gv / 2, sbyte);
+                st_u8(a.scales + scale_index(a.sf_tiles, gv >> 1, t, v), sbyte);
         }
     }
 }
@@ -291,7 +308,7 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT, CLUSTER))
                 if (CLUSTER && a.out_residual)
                     st_v4(a.out_residual + rowv + v, pack8_dt(h[j], F16));
             }
-            emit_vector<QMODE, F16>(a, valid, rowv + v, h[j], gm, rinv, g_given, amax_local);
+            emit_vector<QMODE, F16>(a, valid, rowv + v, t, v, h[j], gm, rinv, g_given, amax_local);
         }
     }
 
@@ -315,6 +332,8 @@ struct QuantArgs {
     uint32_t* ws;        // dynamic: ws[0] = amax bits, ws[1] = completion counter
     int64_t nvec;        // T * d / 8 (even)
     bool f16;            // host: x is binary16 (picks the F16 instantiation)
+    int kb;              // blocks per row, d / 16
+    int sf_tiles;        // 0: scales row-major; else 128x4 tiles, d / 64 per 128 rows
 };
 
 // One thread owns one 16-element block (two consecutive 16-byte vectors) per
@@ -369,7 +388,12 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __grid_consta
         for (int e = 0; e < 16; ++e)
             q[e] = __fmul_rn(x[e], inv);
         st_v2(a.codes + 2 * b, e2m1x8_from_f32(q), e2m1x8_from_f32(q + 8));
-        st_u8(a.scales + b, sbyte);
+        int64_t si = b;
+        if (a.sf_tiles) {
+            const int64_t t = b / a.kb;
+            si = scale_offset_128x4(t, static_cast<int>(b - t * a.kb), a.sf_tiles);
+        }
+        st_u8(a.scales + si, sbyte);
     }
 }
 

@@ -196,7 +196,9 @@ __global__ void __launch_bounds__(512) nvfp4_small_kernel(const __grid_constant_
             bmax = fmaxf(bmax, fabsf(h[j][e]));
         bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));
         if (i < items) {
-            const int64_t gv = static_cast<int64_t>(i / slice) * a.nvec + vbeg + i % slice;
+            const int t = i / slice;
+            const int v = vbeg + i % slice;
+            const int64_t gv = static_cast<int64_t>(t) * a.nvec + v;
             uint32_t sbyte;
             const float inv = nvfp4_block_scale(g, bmax, sbyte);
             float q[8];
@@ -205,7 +207,7 @@ __global__ void __launch_bounds__(512) nvfp4_small_kernel(const __grid_constant_
                 q[e] = __fmul_rn(h[j][e], inv);
             st_u32(a.codes + gv, e2m1x8_from_f32(q));
             if ((gv & 1) == 0)
-                st_u8(a.scales + gv / 2, sbyte);
+                st_u8(a.scales + scale_index(a.sf_tiles, gv >> 1, t, v), sbyte);
         }
     }
     cluster_wait_acquire();  // no CTA leaves while a peer may still push to it

@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(544, 1) stream_rmsnorm_kernel(const __grid_con
 #pragma unroll
         for (int j = 0; j < VPT; ++j) {
             const int v = c + j * C;
-            emit_vector<QMODE, F16>(a, v < nvec, rowv + v, h[j], gam[j], rinv, g_given, amax_local);
+            emit_vector<QMODE, F16>(a, v < nvec, rowv + v, t, v, h[j], gam[j], rinv, g_given, amax_local);
         }
         if (stop_sh[buf])
             break;  // the same sample for every consumer: all leave together

@@ -36,9 +36,13 @@ def _stream_handle(device, stream):
     return s.cuda_stream
 
 
-def _nvfp4_outputs(T, d, device, global_scale):
+def _nvfp4_outputs(T, d, device, global_scale, scales_128x4=False):
     codes = torch.empty((T, d // 2), dtype=torch.uint8, device=device)
-    scales = torch.empty((T, d // 16), dtype=torch.uint8, device=device)
+    if scales_128x4:
+        # the 128x4 tiled GEMM layout, flat; padding rows stay zero
+        scales = torch.zeros((_abi.scales_128x4_bytes(T, d),), dtype=torch.uint8, device=device)
+    else:
+        scales = torch.empty((T, d // 16), dtype=torch.uint8, device=device)
     if global_scale is None:
         g = torch.empty((1,), dtype=torch.float32, device=device)
         given = False
@@ -52,15 +56,17 @@ def _nvfp4_outputs(T, d, device, global_scale):
 
 def fused_rmsnorm(partials, residual, gamma, eps: float, *, out_norm=None, out_residual=None,
                   nvfp4: bool = False, global_scale: torch.Tensor | None = None,
-                  emit_norm: bool = True, flags: int = 0, plan: _abi.TparPlan | None = None,
-                  workspace: torch.Tensor | None = None, stream=None):
+                  emit_norm: bool = True, scales_128x4: bool = False, flags: int = 0,
+                  plan: _abi.TparPlan | None = None, workspace: torch.Tensor | None = None, stream=None):
     """sum(partials) + residual -> RMSNorm(gamma, eps) [-> NVFP4], one fused pass.
 
     partials: list of N bf16 [T, d] CUDA tensors; residual: bf16 [T, d] or None;
     gamma: bf16 [d]. With ``nvfp4=True`` also returns E2M1 codes [T, d/2],
     E4M3 scales [T, d/16] and the global scale; ``global_scale`` given (a
     1-element fp32 tensor) selects the calibrated single-pass mode, in which
-    ``emit_norm=False`` skips the bf16 normed output.
+    ``emit_norm=False`` skips the bf16 normed output. ``scales_128x4=True``
+    returns the scales flat, in the 128x4 tiled layout block-scaled GEMMs
+    read (TPAR_SCALES_128X4; d % 64 == 0; padding rows zero).
     Returns dict(out_norm, out_residual, codes, scales, global_scale).
     """
     partials = list(partials)
@@ -85,9 +91,11 @@ def fused_rmsnorm(partials, residual, gamma, eps: float, *, out_norm=None, out_r
     _check_bf16("out_residual", out_residual, (T, d), dt)
     codes = scales = g = None
     if nvfp4:
-        codes, scales, g, given = _nvfp4_outputs(T, d, dev, global_scale)
+        codes, scales, g, given = _nvfp4_outputs(T, d, dev, global_scale, scales_128x4)
         if given:
             flags |= _abi.TPAR_GSCALE_GIVEN
+        if scales_128x4:
+            flags |= _abi.TPAR_SCALES_128X4
     with torch.cuda.device(dev):
         _abi.tpar_fused_rmsnorm_ex(
             [p.data_ptr() for p in partials], len(partials),
@@ -126,8 +134,8 @@ def allreduce_sum(partials, residual=None, *, out=None, flags: int = 0, stream=N
 
 
 def unfused_rmsnorm(partials, residual, gamma, eps: float, *, reduced=None, out_norm=None,
-                    out_residual=None, nvfp4: bool = False, global_scale=None, flags: int = 0,
-                    stream=None):
+                    out_residual=None, nvfp4: bool = False, global_scale=None, scales_128x4: bool = False,
+                    flags: int = 0, stream=None):
     """The same epilogue as separate kernels through HBM (the comparison baseline)."""
     partials = list(partials)
     T, d = partials[0].shape
@@ -146,9 +154,11 @@ def unfused_rmsnorm(partials, residual, gamma, eps: float, *, reduced=None, out_
                     if out_residual is None else out_residual)
     codes = scales = g = None
     if nvfp4:
-        codes, scales, g, given = _nvfp4_outputs(T, d, dev, global_scale)
+        codes, scales, g, given = _nvfp4_outputs(T, d, dev, global_scale, scales_128x4)
         if given:
             flags |= _abi.TPAR_GSCALE_GIVEN
+        if scales_128x4:
+            flags |= _abi.TPAR_SCALES_128X4
     with torch.cuda.device(dev):
         _abi.tpar_unfused_rmsnorm(
             [p.data_ptr() for p in partials], len(partials),
@@ -160,15 +170,19 @@ def unfused_rmsnorm(partials, residual, gamma, eps: float, *, reduced=None, out_
             "global_scale": g, "reduced": reduced}
 
 
-def nvfp4_quantize(x, global_scale: torch.Tensor | None = None, flags: int = 0, stream=None):
-    """NVFP4 quantisation of a bf16 [T, d] CUDA tensor -> (codes, scales, global_scale)."""
+def nvfp4_quantize(x, global_scale: torch.Tensor | None = None, scales_128x4: bool = False, flags: int = 0,
+                   stream=None):
+    """NVFP4 quantisation of a bf16 [T, d] CUDA tensor -> (codes, scales, global_scale).
+    ``scales_128x4=True``: scales flat in the 128x4 tiled GEMM layout."""
     _check_bf16("x", x)
     T, d = x.shape
     if x.dtype == torch.float16:
         flags |= _abi.TPAR_DTYPE_FP16
-    codes, scales, g, given = _nvfp4_outputs(T, d, x.device, global_scale)
+    codes, scales, g, given = _nvfp4_outputs(T, d, x.device, global_scale, scales_128x4)
     if given:
         flags |= _abi.TPAR_GSCALE_GIVEN
+    if scales_128x4:
+        flags |= _abi.TPAR_SCALES_128X4
     with torch.cuda.device(x.device):
         _abi.tpar_nvfp4_quantize(x.data_ptr(), T, d, codes.data_ptr(), scales.data_ptr(),
                                  g.data_ptr(), flags, _stream_handle(x.device, stream))

@@ -59,9 +59,14 @@ def to_device(inputs, dev="cuda"):
             "gamma": inputs["gamma"].to(dev)}
 
 
-def assert_nvfp4_bit_exact(out_norm: torch.Tensor, codes, scales, g, given=None, what="nvfp4"):
-    """The oracle quantiser run on the kernel's own normed tensor."""
+def assert_nvfp4_bit_exact(out_norm: torch.Tensor, codes, scales, g, given=None, what="nvfp4",
+                           scales_128x4=False, sf_fill=0):
+    """The oracle quantiser run on the kernel's own normed tensor. With
+    ``scales_128x4`` the kernel's scales are the flat 128x4 tiled layout,
+    whose padding rows must still hold ``sf_fill``."""
     oc, os_, og = oracle.nvfp4_quantize(synth.bits(out_norm), global_scale=given, dtype=dtype_name(out_norm))
+    if scales_128x4:
+        os_ = oracle.nvfp4_scales_128x4(os_, fill=sf_fill)
     gc = codes.cpu().numpy()
     gs = scales.cpu().numpy()
     gg = np.float32(g.item()) if isinstance(g, torch.Tensor) else np.float32(g)

@@ -248,3 +248,37 @@ def test_fp8_entry_point_checks(tp):
     q = lambda x=BASE, c=BASE + 64 * MB, s=BASE + 80 * MB, d=4096: tp.tpar_fp8_quantize(
         x, 8, d, c, s, tp.TPAR_DRY_RUN, 0, check=False)
     assert q() == OK and q(c=BASE + 1024) == INVALID and q(d=12) == INVALID and q(x=BASE + 4) == MISALIGNED
+
+
+def test_scales_128x4_checks(tp):
+    """TPAR_SCALES_128X4: NVFP4 outputs only, d % 64 == 0, and the overlap
+    rules count the padded buffer of TPAR_SCALES_128X4_BYTES(T, d) bytes."""
+    S = tp.TPAR_SCALES_128X4
+    D = tp.TPAR_DRY_RUN
+    nv = dict(codes=BASE + 200 * MB, scales=BASE + 240 * MB, g=BASE + 250 * MB)
+    assert tp.scales_128x4_bytes(1, 4096) == 128 * 256
+    assert tp.scales_128x4_bytes(129, 64) == 256 * 4
+    assert call(tp, flags=D | S, **nv) == OK
+    assert call(tp, flags=D | S, T=333, d=8192, **nv) == OK
+    assert call(tp, flags=D | S) == INVALID              # no NVFP4 outputs
+    assert call(tp, flags=D | S, d=4112, **nv) == INVALID  # d % 64 != 0
+    assert call(tp, flags=D, d=4112, **nv) == OK          # row-major scales take d % 16
+    # T = 8, d = 4096: row-major scales are 2 KiB, the tiled ones 32 KiB
+    after_linear = dict(nv, g=BASE + 240 * MB + 4096)
+    assert call(tp, flags=D, **after_linear) == OK
+    assert call(tp, flags=D | S, **after_linear) == INVALID
+    # the same rules on the unfused and standalone quantiser entry points
+    parts = [BASE + r * 4 * MB for r in range(4)]
+    u = lambda fl, d=4096, g=BASE + 250 * MB: tp.tpar_unfused_rmsnorm(
+        parts, 4, BASE + 64 * MB, BASE + 96 * MB, 1e-5, 8, d, BASE + 300 * MB, BASE + 128 * MB,
+        BASE + 160 * MB, BASE + 200 * MB, BASE + 240 * MB, g, fl, 0, check=False)
+    assert u(D | S) == OK and u(D | S, d=4112) == INVALID and u(D | S, g=BASE + 240 * MB + 4096) == INVALID
+    q = lambda fl, d=4096, g=BASE + 90 * MB: tp.tpar_nvfp4_quantize(BASE, 8, d, BASE + 64 * MB, BASE + 80 * MB, g,
+                                                                     fl, 0, check=False)
+    assert q(D | S) == OK and q(D | S, d=4112) == INVALID and q(D | S, g=BASE + 80 * MB + 4096) == INVALID
+    assert q(D, g=BASE + 80 * MB + 4096) == OK
+    # FP8 outputs have no block scales
+    f = tp.tpar_fused_rmsnorm_fp8(parts, 4, BASE + 64 * MB, BASE + 96 * MB, 1e-5, 8, 4096, BASE + 128 * MB,
+                                  BASE + 160 * MB, BASE + 200 * MB, BASE + 240 * MB, D | S, 0, check=False)
+    assert f == INVALID
+    assert tp.tpar_fp8_quantize(BASE, 8, 4096, BASE + 64 * MB, BASE + 80 * MB, D | S, 0, check=False) == INVALID

@@ -239,3 +239,95 @@ def test_fused_fp8(T, given):
                                   emit_norm=False)
         torch.cuda.synchronize()
         assert o2["out_norm"] is None and torch.equal(o2["codes"], out["codes"])
+
+
+# ---------------------------------------------------------------- 128x4 tiled scales
+# TPAR_SCALES_128X4: the scales in the tiled layout block-scaled GEMMs read
+# (cuBLAS documentation, "1D Block Scaling Factors Layout"). Codes and g are
+# unchanged; the scale bytes must equal the oracle's tiling of its own
+# row-major scales, and padding rows must be left untouched.
+
+@pytest.mark.parametrize("dynamic", [True, False])
+@pytest.mark.parametrize("T,d", [(1, 64), (127, 192), (128, 4096), (129, 8192), (300, 1024)])
+def test_scales_128x4_standalone_quantiser(dynamic, T, d):
+    tp = lib()
+    xb = synth.bits(synth.random_bf16((T, d), 1.0, seed=7 * T + d))
+    g = None if dynamic else float(np.float32(0.0371))
+    gs = None if dynamic else torch.tensor([g], dtype=torch.float32, device="cuda")
+    codes, scales, gout = tp.nvfp4_quantize(synth.from_bits(xb, "cuda"), global_scale=gs, scales_128x4=True)
+    torch.cuda.synchronize()
+    oc, os_, og = oracle.nvfp4_quantize(xb, global_scale=g)
+    assert scales.numel() == tp.scales_128x4_bytes(T, d)
+    assert np.array_equal(codes.cpu().numpy(), oc)
+    assert np.array_equal(scales.cpu().numpy(), oracle.nvfp4_scales_128x4(os_, fill=0))
+    assert np.float32(gout.item()) == og
+
+
+# (name, T, d, n_ranks, given g, flags, dtype)
+_TILED_CASES = [
+    ("given_row", 333, 4096, 4, True, "FORCE_ROW", torch.bfloat16),
+    ("given_cluster", 8, 8192, 8, True, "FORCE_CLUSTER", torch.bfloat16),
+    ("given_stream", 200, 2048, 4, True, "FORCE_STREAM", torch.bfloat16),
+    ("dynamic_single_launch", 8, 8192, 4, False, None, torch.bfloat16),
+    ("dynamic_single_launch_T16", 16, 4096, 2, False, None, torch.bfloat16),
+    ("dynamic_cluster_two_pass", 24, 8192, 8, False, None, torch.bfloat16),
+    ("dynamic_row_two_pass", 333, 8192, 4, False, None, torch.bfloat16),
+    ("dynamic_two_pass_fp16", 130, 1024, 4, False, None, torch.float16),
+]
+
+
+@pytest.mark.parametrize("name,T,d,n,given,force,dt", _TILED_CASES, ids=[c[0] for c in _TILED_CASES])
+def test_scales_128x4_fused_paths(name, T, d, n, given, force, dt):
+    tp = lib()
+    w = synth.NVFP4.with_(d=d, n_ranks=n)
+    inputs = synth.make_inputs(w, "cuda", T=T, seed=T + d, dtype=dt)
+    gs = torch.tensor([0.0123], dtype=torch.float32, device="cuda") if given else None
+    flags = getattr(tp, "TPAR_" + force) if force else 0
+    out = tp.fused_rmsnorm(inputs["partials"], inputs["residual"], inputs["gamma"], w.eps, nvfp4=True,
+                           global_scale=gs, scales_128x4=True, flags=flags)
+    torch.cuda.synchronize()
+    assert out["scales"].numel() == tp.scales_128x4_bytes(T, d)
+    assert_nvfp4_bit_exact(out["out_norm"], out["codes"], out["scales"], out["global_scale"],
+                           given=float(np.float32(0.0123)) if given else None, what=name, scales_128x4=True)
+    # the bf16 outputs are those of the row-major call
+    ref = tp.fused_rmsnorm(inputs["partials"], inputs["residual"], inputs["gamma"], w.eps, nvfp4=True,
+                           global_scale=gs, flags=flags)
+    torch.cuda.synchronize()
+    assert torch.equal(out["out_norm"], ref["out_norm"]) and torch.equal(out["codes"], ref["codes"])
+    assert np.array_equal(oracle.nvfp4_scales_128x4(ref["scales"].cpu().numpy()), out["scales"].cpu().numpy())
+
+
+@pytest.mark.parametrize("given", [False, True])
+def test_scales_128x4_unfused(given):
+    tp = lib()
+    T, d = 150, 1024
+    w = synth.NVFP4.with_(d=d)
+    inputs = synth.make_inputs(w, "cuda", T=T, seed=5)
+    gs = torch.tensor([0.02], dtype=torch.float32, device="cuda") if given else None
+    out = tp.unfused_rmsnorm(inputs["partials"], inputs["residual"], inputs["gamma"], w.eps, nvfp4=True,
+                             global_scale=gs, scales_128x4=True)
+    torch.cuda.synchronize()
+    assert_nvfp4_bit_exact(out["out_norm"], out["codes"], out["scales"], out["global_scale"],
+                           given=float(np.float32(0.02)) if given else None, what="unfused", scales_128x4=True)
+
+
+@pytest.mark.parametrize("flags", ["auto", "FORCE_ROW", "FORCE_CLUSTER"])
+def test_scales_128x4_padding_rows_untouched(flags):
+    """Through the C ABI with a scales buffer pre-filled with 0xA5: only the
+    T * d/16 real entries change (single launch, two-pass and cluster forms)."""
+    tp = lib()
+    T, d = 5, 256
+    inputs = synth.make_inputs(synth.SMALL, "cuda", T=T)
+    dev = "cuda"
+    out_norm = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    out_res = torch.empty((T, d), dtype=torch.bfloat16, device=dev)
+    codes = torch.empty((T, d // 2), dtype=torch.uint8, device=dev)
+    scales = torch.full((tp.scales_128x4_bytes(T, d),), 0xA5, dtype=torch.uint8, device=dev)
+    g = torch.empty(1, dtype=torch.float32, device=dev)
+    fl = tp.TPAR_SCALES_128X4 | (0 if flags == "auto" else getattr(tp, "TPAR_" + flags))
+    tp.tpar_fused_rmsnorm_ex([p.data_ptr() for p in inputs["partials"]], len(inputs["partials"]),
+                             inputs["residual"].data_ptr(), inputs["gamma"].data_ptr(), synth.SMALL.eps, T, d,
+                             out_norm.data_ptr(), out_res.data_ptr(), codes.data_ptr(), scales.data_ptr(),
+                             g.data_ptr(), fl, None, 0, torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert_nvfp4_bit_exact(out_norm, codes, scales, g, what=f"padding {flags}", scales_128x4=True, sf_fill=0xA5)
