@@ -313,6 +313,31 @@ def measure_sweep(torch, tp, device):
     del cs, reduced
     torch.cuda.empty_cache()
 
+    # prefill T sweep, N=8 d=8192: the automatic plan (the prefetching row
+    # kernel once T exceeds the SM count) against one CTA per row without
+    # prefetch; eager calls rotating over input sets totalling > 2x L2
+    rows = []
+    for T in (128, 160, 256, 512, 1024, 2048, 4096):
+        w = synth.PREFILL.with_(T=T)
+        b = fused_bytes(w.n_ranks, T, w.d)
+        n_sets = min(8, n_sets_for(b, l2_bytes(torch)))
+        sets = [CallSet(w, seed=i, device=device) for i in range(n_sets)]
+        k = [0]
+
+        def rot(flags, sets=sets, w=w):
+            sets[k[0] % len(sets)].call(tp, w, st.cuda_stream, flags=flags)
+            k[0] += 1
+
+        us_auto = ev_time(lambda: rot(0), reps=24)
+        us_row = ev_time(lambda: rot(tp.TPAR_FORCE_ROW), reps=24)
+        plan = tp.tpar_plan_launch(T, w.d, w.n_ranks, torch.cuda.get_device_properties(device).multi_processor_count)
+        rows.append({"N": 8, "T": T, "d": w.d, "auto_kernel": plan.kernel, "auto_us": round(us_auto, 2),
+                     "row_us": round(us_row, 2), "auto_frac_of_measured_hbm": round(b / us_auto / 1e3 / peak, 4),
+                     "row_frac_of_measured_hbm": round(b / us_row / 1e3 / peak, 4)})
+        del sets
+        torch.cuda.empty_cache()
+    out["prefill_T_sweep_N8_d8192"] = rows
+
     # NVFP4: N=4, d=8192, dynamic global scale, T = 1 .. 16384
     rows = []
     for T in synth.NVFP4_TS:
@@ -525,7 +550,8 @@ def profile_case(args):
     device = torch.device("cuda", 0)
     tp.tpar_init(0)
     base = {"prefill": synth.PREFILL, "decode8b": synth.DECODE_8B, "decode70b": synth.DECODE_70B,
-            "nvfp4": synth.NVFP4, "unfused": synth.PREFILL, "stream": synth.PREFILL}[args.profile]
+            "nvfp4": synth.NVFP4, "unfused": synth.PREFILL, "stream": synth.PREFILL,
+            "row": synth.PREFILL}[args.profile]
     w = base.with_(T=args.T) if args.T else base
     cs = CallSet(w, seed=0, device=device, nvfp4=w.nvfp4)
     st = torch.cuda.current_stream().cuda_stream
@@ -536,7 +562,7 @@ def profile_case(args):
                                     w.T, w.d, reduced.data_ptr(), cs.out_norm.data_ptr(),
                                     cs.out_residual.data_ptr(), 0, 0, 0, 0, st)
         else:
-            cs.call(tp, w, st, flags=tp.TPAR_FORCE_STREAM if args.profile == "stream" else 0)
+            cs.call(tp, w, st, flags={"stream": tp.TPAR_FORCE_STREAM, "row": tp.TPAR_FORCE_ROW}.get(args.profile, 0))
     torch.cuda.synchronize()
     print(f"profile case done: {w.name} T={w.T}, {args.calls} calls, "
           f"{fused_bytes(w.n_ranks, w.T, w.d, nvfp4=w.nvfp4)} algorithmic bytes per fused call")
@@ -552,7 +578,7 @@ def main(argv=None):
     ap.add_argument("--workload", choices=["decode8b"], default="decode8b")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--profile", choices=["prefill", "decode8b", "decode70b", "nvfp4", "unfused", "stream"],
+    ap.add_argument("--profile", choices=["prefill", "decode8b", "decode70b", "nvfp4", "unfused", "stream", "row"],
                     help="run a few eager calls of one shape for an ncu capture, then exit")
     ap.add_argument("--T", type=int, default=0, help="token count for --profile")
     ap.add_argument("--calls", type=int, default=3, help="calls for --profile")

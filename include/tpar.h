@@ -94,7 +94,10 @@ typedef void* tpar_stream_t;
 #define TPAR_SCALES_128X4_BYTES(T, d) ((((int64_t)(T) + 127) / 128) * 128 * ((int64_t)(d) / 16))
 
 /* Launch plan of the fused kernel. kernel: 0 = row kernel (one CTA per row),
- * 1 = cluster-split rows, 2 = persistent TMA-fed stream kernel. split: CTAs
+ * 1 = cluster-split rows, 2 = persistent TMA-fed stream kernel, 3 = persistent
+ * row kernel with the next rows prefetched into shared memory (cp.async; the
+ * automatic choice when T exceeds 1.5x the SM count, 2048 <= d <= 16384 and
+ * a row of every source fits 200 KB; vec_per_thread 1 or 2). split: CTAs
  * per row (the cluster size; 1 otherwise). threads: threads per CTA (for the
  * stream kernel: consumer threads, plus one producer warp). vec_per_thread:
  * 16-byte vectors of a row each (consumer) thread owns (1, 2, 4 or 8).
@@ -168,7 +171,8 @@ tpar_status tpar_fused_rmsnorm(const void* const* partials, int n_ranks, const v
  *          out_norm may be NULL. A g that is not positive and finite gives
  *          all-zero scales and signed-zero codes.
  *          TPAR_FORCE_ROW / TPAR_FORCE_CLUSTER / TPAR_FORCE_STREAM: pick the
- *          kernel (at most one); TPAR_NO_PDL. TPAR_SCALES_128X4: nvfp4_scales
+ *          kernel (at most one; TPAR_FORCE_ROW = kernel 0, one CTA per row
+ *          without prefetch); TPAR_NO_PDL. TPAR_SCALES_128X4: nvfp4_scales
  *          in the 128x4 tiled GEMM layout (NVFP4 outputs required, d % 64
  *          == 0, buffer of TPAR_SCALES_128X4_BYTES(T, d) bytes, none of
  *          which may overlap another tensor); TPAR_ERR_INVALID_ARG otherwise.

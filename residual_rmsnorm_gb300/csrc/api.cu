@@ -13,6 +13,7 @@
 #include "dispatch.h"
 #include "kernels.cuh"
 #include "nvfp4_small.cuh"
+#include "rows.cuh"
 #include "stream.cuh"
 
 namespace {
@@ -154,13 +155,13 @@ tpar_status current_sm_count(int* sm)
 }
 
 cudaError_t launch(const void* fn, dim3 grid, dim3 block, void* arg, cudaStream_t stream, int cluster_x,
-                   bool pdl)
+                   bool pdl, size_t smem = 0)
 {
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
     cfg.gridDim = grid;
     cfg.blockDim = block;
-    cfg.dynamicSmemBytes = 0;
+    cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
     cudaLaunchAttribute attrs[2];
     unsigned na = 0;
@@ -200,6 +201,42 @@ int stream_stages(int64_t row_bytes)
     return static_cast<int>(s < 2 ? 2 : s);
 }
 
+// Rows in flight per CTA of the prefetching row kernel (rows.cuh) for rows of
+// d elements from nsrc sources: as many stages of nsrc * d * 2 bytes as fit
+// the shared-memory budget, at most kRowsMaxStages; 0 if one does not fit.
+int rows_stages(int64_t d, int nsrc)
+{
+    const int64_t stage = static_cast<int64_t>(nsrc) * d * 2;
+    const int64_t s = stage > 0 ? tpar::kRowsSmemBudget / stage : 0;
+    return static_cast<int>(std::min<int64_t>(s, tpar::kRowsMaxStages));
+}
+
+// cudaFuncSetAttribute once per (kernel, attribute, value): a host call,
+// kept off the per-call path.
+cudaError_t set_attr_once(const void* fn, cudaFuncAttribute attr, int value)
+{
+    struct Entry {
+        int device;
+        const void* fn;
+        cudaFuncAttribute attr;
+        int value;
+    };
+    static std::mutex mu;
+    static Entry done[128];
+    static int used = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return cudaFuncSetAttribute(fn, attr, value);
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (done[i].device == dev && done[i].fn == fn && done[i].attr == attr && done[i].value == value)
+            return cudaSuccess;
+    const cudaError_t e = cudaFuncSetAttribute(fn, attr, value);
+    if (e == cudaSuccess && used < 128)
+        done[used++] = Entry{dev, fn, attr, value};
+    return e;
+}
+
 int pow2_at_least(int64_t n)
 {
     int p = 1;
@@ -228,6 +265,20 @@ tpar_status check_plan(const tpar_plan& p, int64_t d, int n_ranks)
             return TPAR_ERR_INVALID_ARG;
         if (static_cast<int64_t>(p.threads) * v < nvec || p.grid_rows < 1 || p.grid_rows > kMaxGridY)
             return TPAR_ERR_INVALID_ARG;
+        return TPAR_OK;
+    }
+    if (p.kernel == 3) {
+        // prefetching row kernel: rows of <= 2 vectors per thread, a ring
+        // stage (every partial and the residual) within the smem budget
+        const int v = p.vec_per_thread;
+        if (p.split != 1 || p.threads < 32 || p.threads > 1024 || p.threads % 32 != 0)
+            return TPAR_ERR_INVALID_ARG;
+        if (v < 1 || v > tpar::kRowsMaxVpt || (v & (v - 1)) != 0)
+            return TPAR_ERR_INVALID_ARG;
+        if (static_cast<int64_t>(p.threads) * v < nvec || p.grid_rows < 1 || p.grid_rows > kMaxGridY)
+            return TPAR_ERR_INVALID_ARG;
+        if (rows_stages(d, n_ranks + 1) < 1)
+            return TPAR_ERR_UNSUPPORTED;
         return TPAR_OK;
     }
     if (p.kernel != 0 && p.kernel != 1)
@@ -428,6 +479,23 @@ tpar_status plan_impl(int64_t T, int64_t d, int n_ranks, int sm_count, uint32_t 
         while (split < 16 && slice_for(nvec, split) > 2 * tpar::fused_thread_cap(nr, 2, true))
             split *= 2;
     }
+    if (split == 1 && !(flags & TPAR_FORCE_ROW) && 2 * T > 3 * static_cast<int64_t>(sm_count) && nvec >= 256 &&
+        nvec <= 1024 * tpar::kRowsMaxVpt && rows_stages(d, n_ranks + 1) >= 1) {
+        // Bandwidth path: rows of >= 2048 elements, T > 1.5x the SM count.
+        // One persistent CTA per SM with the next rows in flight as cp.async
+        // copies (rows.cuh). Measured on GB300, N=8 d=8192: 111.7 vs 113.3 us
+        // at T=4096, 30.4 vs 32.4 at T=1024, 10.6 vs 10.7 at T=256 and 9.5 vs
+        // 9.0 at T=160 (one CTA per row wins below ~1.5 rows per SM); N=4
+        // T=16384 dynamic NVFP4 346 vs 364 us.
+        tpar_plan p;
+        p.kernel = 3;
+        p.split = 1;
+        p.vec_per_thread = nvec <= 1024 ? 1 : 2;
+        p.threads = static_cast<int>(ceil_div(ceil_div(nvec, p.vec_per_thread), 32) * 32);
+        p.grid_rows = std::min<int64_t>(T, std::min<int64_t>(sm_count, kMaxGridY));
+        *out = p;
+        return check_plan(p, d, n_ranks);
+    }
     tpar_plan p;
     // Row kernels stride over rows with at most 8 CTAs per SM in the grid:
     // as fast as one CTA per row (measured), and it bounds the per-CTA
@@ -454,8 +522,7 @@ tpar_status launch_stream(const FusedArgs& a, int qmode, const tpar_plan& p, cud
     sa.stages = stream_stages(row_bytes);
     sa.consumers = p.threads;
     const size_t smem = static_cast<size_t>(sa.stages) * row_bytes + 16u * sa.stages;
-    if (cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-        cudaSuccess)
+    if (set_attr_once(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
         return TPAR_ERR_CUDA;
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
@@ -472,16 +539,42 @@ tpar_status launch_stream(const FusedArgs& a, int qmode, const tpar_plan& p, cud
     return cudaLaunchKernelExC(&cfg, fn, args) == cudaSuccess ? TPAR_OK : TPAR_ERR_CUDA;
 }
 
+tpar_status launch_rows(const FusedArgs& a, int qmode, const tpar_plan& p, cudaStream_t stream, bool pdl)
+{
+    const int nr = tpar::rank_bound(a.n_ranks);
+    const void* fn = tpar::rows_kernel_for(qmode, nr, p.vec_per_thread, a.f16);
+    if (!fn)
+        return TPAR_ERR_UNSUPPORTED;
+    const int nsrc = a.n_ranks + (a.residual ? 1 : 0);
+    const int64_t d = static_cast<int64_t>(a.nvec) * 8;
+    const int stages = rows_stages(d, nsrc);
+    if (stages < 1)
+        return TPAR_ERR_UNSUPPORTED;
+    if (set_attr_once(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, tpar::kRowsSmemBudget) != cudaSuccess)
+        return TPAR_ERR_CUDA;
+    tpar::RowsArgs ra;
+    ra.f = a;
+    ra.f.err = device_error_word();
+    ra.stages = stages;
+    const size_t smem = std::max<size_t>(static_cast<size_t>(stages) * nsrc * d * 2, tpar::kRowsSmemFloor);
+    return launch(fn, dim3(static_cast<unsigned>(p.grid_rows)), dim3(static_cast<unsigned>(p.threads)), &ra, stream,
+                  1, pdl, smem) == cudaSuccess
+               ? TPAR_OK
+               : TPAR_ERR_CUDA;
+}
+
 tpar_status launch_fused(const FusedArgs& a, int qmode, const tpar_plan& p, cudaStream_t stream, bool pdl)
 {
     if (p.kernel == 2)
         return launch_stream(a, qmode, p, stream, pdl);
+    if (p.kernel == 3)
+        return launch_rows(a, qmode, p, stream, pdl);
     const int nr = tpar::rank_bound(a.n_ranks);
     const void* fn = tpar::fused_kernel_for(qmode, nr, p.vec_per_thread, p.kernel == 1, a.f16);
     if (!fn)
         return TPAR_ERR_UNSUPPORTED;
     if (p.kernel == 1 && p.split > 8) {
-        if (cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        if (set_attr_once(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
             return TPAR_ERR_CUDA;
     }
     FusedArgs args = a;
@@ -493,10 +586,43 @@ tpar_status launch_fused(const FusedArgs& a, int qmode, const tpar_plan& p, cuda
     return TPAR_OK;
 }
 
-unsigned flat_grid(int64_t nvec, int sm_count)
+// CTAs of 256 threads that fit on one SM at once for kernel `fn` (from the
+// occupancy calculator, queried once per kernel; a host-side query that
+// enqueues nothing, so it may run during graph capture).
+int resident_ctas(const void* fn)
 {
-    int64_t blocks = ceil_div(nvec, 256);
-    int64_t cap = static_cast<int64_t>(sm_count) * 8;
+    static std::mutex mu;
+    static const void* keys[64];
+    static int devs[64];
+    static int vals[64];
+    static int used = 0;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (keys[i] == fn && devs[i] == dev)
+            return vals[i];
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, fn, 256, 0) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        return 4;
+    }
+    if (used < 64) {
+        keys[used] = fn;
+        devs[used] = dev;
+        vals[used++] = n;
+    }
+    return n;
+}
+
+// Grid of a flat grid-stride kernel over `items` work items, `per_thread`
+// of them per thread and loop iteration: one full wave of resident CTAs at
+// most, so every CTA runs from the start (a partial second wave would leave
+// SMs idle at the end while the first wave's CTAs hold equal shares).
+unsigned flat_grid(int64_t items, int sm_count, const void* fn, int per_thread = 1)
+{
+    int64_t blocks = ceil_div(items, 256 * static_cast<int64_t>(per_thread));
+    const int64_t cap = static_cast<int64_t>(sm_count) * resident_ctas(fn);
     if (blocks > cap)
         blocks = cap;
     return static_cast<unsigned>(blocks < 1 ? 1 : blocks);
@@ -516,8 +642,9 @@ tpar_status launch_quantize(const void* x, int64_t T, int64_t d, uint8_t* codes,
     q.f16 = f16;
     q.kb = static_cast<int>(d / 16);
     q.sf_tiles = sf_tiles;
-    const unsigned grid = flat_grid(q.nvec / 2, sm_count);  // one thread per 16-element block
-    if (launch(tpar::quantize_kernel_for(dynamic, f16), dim3(grid), dim3(256), &q, stream, 1, pdl) != cudaSuccess)
+    const void* fn = tpar::quantize_kernel_for(dynamic, f16);
+    const unsigned grid = flat_grid(q.nvec / 2, sm_count, fn, 2);  // two 16-element blocks per thread
+    if (launch(fn, dim3(grid), dim3(256), &q, stream, 1, pdl) != cudaSuccess)
         return TPAR_ERR_CUDA;
     return TPAR_OK;
 }
@@ -585,7 +712,7 @@ tpar_status launch_small_nvfp4(const FusedArgs& a, float* gscale, int K, int sli
     const void* fn = tpar::small_kernel_for(tpar::rank_bound(a.n_ranks), ipt, a.f16);
     if (!fn)
         return TPAR_ERR_UNSUPPORTED;
-    if (K > 8 && cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+    if (K > 8 && set_attr_once(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
         return TPAR_ERR_CUDA;
     tpar::SmallArgs sa;
     sa.f = a;
@@ -632,8 +759,8 @@ tpar_status fused_impl(const Call& c, const tpar_plan* user_plan, void* user_ws,
         ra.nvec = c.T * c.d / 8;
         ra.n_ranks = c.n_ranks;
         ra.f16 = (c.flags & TPAR_DTYPE_FP16) != 0;
-        return launch(tpar::reduce_kernel_for(tpar::rank_bound(c.n_ranks), ra.f16), dim3(flat_grid(ra.nvec, sm)),
-                      dim3(256), &ra, stream, 1, pdl) == cudaSuccess
+        const void* fn = tpar::reduce_kernel_for(tpar::rank_bound(c.n_ranks), ra.f16);
+        return launch(fn, dim3(flat_grid(ra.nvec, sm, fn)), dim3(256), &ra, stream, 1, pdl) == cudaSuccess
                    ? TPAR_OK
                    : TPAR_ERR_CUDA;
     }
@@ -729,8 +856,8 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
     ra.nvec = nvec;
     ra.n_ranks = n_ranks;
     ra.f16 = (flags & TPAR_DTYPE_FP16) != 0;
-    if (launch(tpar::reduce_kernel_for(tpar::rank_bound(n_ranks), ra.f16), dim3(flat_grid(nvec, sm)), dim3(256), &ra,
-               stream, 1, pdl) != cudaSuccess)
+    const void* k1 = tpar::reduce_kernel_for(tpar::rank_bound(n_ranks), ra.f16);
+    if (launch(k1, dim3(flat_grid(nvec, sm, k1)), dim3(256), &ra, stream, 1, pdl) != cudaSuccess)
         return TPAR_ERR_CUDA;
     // K2: out_residual = bf16(reduced + residual)
     {
@@ -741,7 +868,8 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
         void* args[4] = {&red, &res, &outr, &n};
         cudaLaunchConfig_t cfg;
         std::memset(&cfg, 0, sizeof cfg);
-        cfg.gridDim = dim3(flat_grid(nvec, sm));
+        const void* k2 = tpar::residual_add_kernel_ptr((flags & TPAR_DTYPE_FP16) != 0);
+        cfg.gridDim = dim3(flat_grid(nvec, sm, k2));
         cfg.blockDim = dim3(256);
         cfg.stream = stream;
         cudaLaunchAttribute at;
@@ -749,7 +877,7 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
         at.val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = &at;
         cfg.numAttrs = pdl ? 1 : 0;
-        if (cudaLaunchKernelExC(&cfg, tpar::residual_add_kernel_ptr((flags & TPAR_DTYPE_FP16) != 0), args) != cudaSuccess)
+        if (cudaLaunchKernelExC(&cfg, k2, args) != cudaSuccess)
             return TPAR_ERR_CUDA;
     }
     // K3: out_norm = RMSNorm(out_residual) (+ amax for a dynamic NVFP4 scale)
@@ -758,8 +886,8 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
             TPAR_FORCE_ROW | (flags & TPAR_DTYPE_FP16), nullptr};
     FusedArgs a = fused_args(k3);
     a.amax_bits = ws;
-    tpar_plan p;
-    if ((st = plan_impl(T, d, 1, sm, TPAR_FORCE_ROW, &p)) != TPAR_OK)
+    tpar_plan p;  // the norm kernel the fused path would pick for one source
+    if ((st = plan_impl(T, d, 1, sm, 0u, &p)) != TPAR_OK)
         return st;
     if ((st = launch_fused(a, (nvfp4 && !given) ? tpar::kQuantAmax : tpar::kQuantNone, p, stream, pdl)) !=
         TPAR_OK)
@@ -813,7 +941,8 @@ tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* co
         void* args[3] = {&xv, &nvec, &ws};
         cudaLaunchConfig_t cfg;
         std::memset(&cfg, 0, sizeof cfg);
-        cfg.gridDim = dim3(flat_grid(nvec, sm));
+        const void* ka = tpar::amax_kernel_ptr((flags & TPAR_DTYPE_FP16) != 0);
+        cfg.gridDim = dim3(flat_grid(nvec, sm, ka));
         cfg.blockDim = dim3(256);
         cfg.stream = stream;
         cudaLaunchAttribute at;
@@ -821,7 +950,7 @@ tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* co
         at.val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = &at;
         cfg.numAttrs = pdl ? 1 : 0;
-        if (cudaLaunchKernelExC(&cfg, tpar::amax_kernel_ptr((flags & TPAR_DTYPE_FP16) != 0), args) != cudaSuccess)
+        if (cudaLaunchKernelExC(&cfg, ka, args) != cudaSuccess)
             return TPAR_ERR_CUDA;
     }
     st = launch_quantize(x, T, d, codes, scales, global_scale, ws, !given, sm, stream, pdl,
@@ -894,8 +1023,8 @@ tpar_status tpar_fused_rmsnorm_fp8(const void* const* partials, int n_ranks, con
     f.ws = ws;
     f.nvec = T * d / 8;
     f.f16 = a.f16;
-    if (launch(tpar::fp8_quantize_kernel_for(true, f.f16), dim3(flat_grid(f.nvec, sm)), dim3(256), &f, stream, 1, pdl) !=
-        cudaSuccess) {
+    const void* kq = tpar::fp8_quantize_kernel_for(true, f.f16);
+    if (launch(kq, dim3(flat_grid(f.nvec, sm, kq, 2)), dim3(256), &f, stream, 1, pdl) != cudaSuccess) {
         cudaMemsetAsync(ws, 0, 8, stream);
         return TPAR_ERR_CUDA;
     }
@@ -939,7 +1068,8 @@ tpar_status tpar_fp8_quantize(const void* x, int64_t T, int64_t d, uint8_t* code
         void* args[3] = {&xv, &n, &ws};
         cudaLaunchConfig_t cfg;
         std::memset(&cfg, 0, sizeof cfg);
-        cfg.gridDim = dim3(flat_grid(nvec, sm));
+        const void* ka = tpar::amax_kernel_ptr((flags & TPAR_DTYPE_FP16) != 0);
+        cfg.gridDim = dim3(flat_grid(nvec, sm, ka));
         cfg.blockDim = dim3(256);
         cfg.stream = stream;
         cudaLaunchAttribute at;
@@ -947,7 +1077,7 @@ tpar_status tpar_fp8_quantize(const void* x, int64_t T, int64_t d, uint8_t* code
         at.val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = &at;
         cfg.numAttrs = pdl ? 1 : 0;
-        if (cudaLaunchKernelExC(&cfg, tpar::amax_kernel_ptr((flags & TPAR_DTYPE_FP16) != 0), args) != cudaSuccess)
+        if (cudaLaunchKernelExC(&cfg, ka, args) != cudaSuccess)
             return TPAR_ERR_CUDA;
     }
     tpar::Fp8Args f;
@@ -957,8 +1087,8 @@ tpar_status tpar_fp8_quantize(const void* x, int64_t T, int64_t d, uint8_t* code
     f.ws = ws;
     f.nvec = nvec;
     f.f16 = (flags & TPAR_DTYPE_FP16) != 0;
-    if (launch(tpar::fp8_quantize_kernel_for(!given, f.f16), dim3(flat_grid(nvec, sm)), dim3(256), &f, stream, 1, pdl) !=
-        cudaSuccess) {
+    const void* kq = tpar::fp8_quantize_kernel_for(!given, f.f16);
+    if (launch(kq, dim3(flat_grid(nvec, sm, kq, 2)), dim3(256), &f, stream, 1, pdl) != cudaSuccess) {
         if (ws)
             cudaMemsetAsync(ws, 0, 8, stream);
         return TPAR_ERR_CUDA;
@@ -1107,8 +1237,8 @@ extern "C" tpar_status tpar_unfused_rmsnorm_noalloc(const void* const* partials,
     ra.nvec = nvec;
     ra.n_ranks = n_ranks;
     ra.f16 = (flags & TPAR_DTYPE_FP16) != 0;
-    if (launch(tpar::reduce_kernel_for(tpar::rank_bound(n_ranks), ra.f16), dim3(flat_grid(nvec, sm)), dim3(256), &ra,
-               stream, 1, pdl) != cudaSuccess)
+    const void* k1 = tpar::reduce_kernel_for(tpar::rank_bound(n_ranks), ra.f16);
+    if (launch(k1, dim3(flat_grid(nvec, sm, k1)), dim3(256), &ra, stream, 1, pdl) != cudaSuccess)
         return TPAR_ERR_CUDA;
     // K2: out_residual = bf16(reduced + residual)
     {
@@ -1119,7 +1249,8 @@ extern "C" tpar_status tpar_unfused_rmsnorm_noalloc(const void* const* partials,
         void* args[4] = {&red, &res, &outr, &n};
         cudaLaunchConfig_t cfg;
         std::memset(&cfg, 0, sizeof cfg);
-        cfg.gridDim = dim3(flat_grid(nvec, sm));
+        const void* k2 = tpar::residual_add_kernel_ptr((flags & TPAR_DTYPE_FP16) != 0);
+        cfg.gridDim = dim3(flat_grid(nvec, sm, k2));
         cfg.blockDim = dim3(256);
         cfg.stream = stream;
         cudaLaunchAttribute at;
@@ -1127,7 +1258,7 @@ extern "C" tpar_status tpar_unfused_rmsnorm_noalloc(const void* const* partials,
         at.val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = &at;
         cfg.numAttrs = pdl ? 1 : 0;
-        if (cudaLaunchKernelExC(&cfg, tpar::residual_add_kernel_ptr((flags & TPAR_DTYPE_FP16) != 0), args) != cudaSuccess)
+        if (cudaLaunchKernelExC(&cfg, k2, args) != cudaSuccess)
             return TPAR_ERR_CUDA;
     }
     // K3: out_norm = RMSNorm(out_residual) (+ amax for a dynamic NVFP4 scale)

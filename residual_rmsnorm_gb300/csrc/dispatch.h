@@ -1,5 +1,6 @@
 // dispatch.h -- host-side lookup of kernel instantiations (compiled in
-// kernels_q0.cu, kernels_q1.cu, kernels_q2.cu and unfused.cu).
+// kernels_q<Q>_<dtype>.cu, kernels_stream_<dtype>.cu, kernels_small.cu and
+// unfused.cu).
 #pragma once
 
 #include <cstdint>
@@ -26,6 +27,28 @@ inline const void* fused_kernel_for(int q, int nr, int vpt, bool cluster, bool f
     case 1: return f16 ? fused_kernel_q1_fp16(nr, vpt, cluster) : fused_kernel_q1_bf16(nr, vpt, cluster);
     case 2: return f16 ? fused_kernel_q2_fp16(nr, vpt, cluster) : fused_kernel_q2_bf16(nr, vpt, cluster);
     case 3: return f16 ? fused_kernel_q3_fp16(nr, vpt, cluster) : fused_kernel_q3_bf16(nr, vpt, cluster);
+    default: return nullptr;
+    }
+}
+
+// Prefetching bandwidth kernel (rows.cuh) for quantisation mode q (0-3),
+// rank bound nr and vpt (1, 2) vectors per thread.
+const void* rows_kernel_q0_bf16(int nr, int vpt);
+const void* rows_kernel_q1_bf16(int nr, int vpt);
+const void* rows_kernel_q2_bf16(int nr, int vpt);
+const void* rows_kernel_q3_bf16(int nr, int vpt);
+const void* rows_kernel_q0_fp16(int nr, int vpt);
+const void* rows_kernel_q1_fp16(int nr, int vpt);
+const void* rows_kernel_q2_fp16(int nr, int vpt);
+const void* rows_kernel_q3_fp16(int nr, int vpt);
+
+inline const void* rows_kernel_for(int q, int nr, int vpt, bool f16)
+{
+    switch (q) {
+    case 0: return f16 ? rows_kernel_q0_fp16(nr, vpt) : rows_kernel_q0_bf16(nr, vpt);
+    case 1: return f16 ? rows_kernel_q1_fp16(nr, vpt) : rows_kernel_q1_bf16(nr, vpt);
+    case 2: return f16 ? rows_kernel_q2_fp16(nr, vpt) : rows_kernel_q2_bf16(nr, vpt);
+    case 3: return f16 ? rows_kernel_q3_fp16(nr, vpt) : rows_kernel_q3_bf16(nr, vpt);
     default: return nullptr;
     }
 }

@@ -336,11 +336,41 @@ struct QuantArgs {
     int sf_tiles;        // 0: scales row-major; else 128x4 tiles, d / 64 per 128 rows
 };
 
-// One thread owns one 16-element block (two consecutive 16-byte vectors) per
-// iteration, so the block-scale arithmetic (two IEEE divisions and the E4M3
-// round trip) runs once per block. In dynamic mode g = amax / 2688 is read
-// from the workspace; the last CTA to have read it zeroes the workspace for
-// the next call (no CTA waits on another).
+// Quantise one 16-element block b (the 16-byte vectors 2b and 2b + 1) with
+// global scale g: block scale, codes and scale byte.
+template <bool F16>
+__device__ __forceinline__ void quantize_block(const QuantArgs& a, float g, int64_t b, const uint4& lo,
+                                               const uint4& hi)
+{
+    float x[16];
+    unpack8_dt(lo, x, F16);
+    unpack8_dt(hi, x + 8, F16);
+    float bmax = 0.0f;
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+        bmax = fmaxf(bmax, fabsf(x[e]));
+    uint32_t sbyte;
+    const float inv = nvfp4_block_scale(g, bmax, sbyte);
+    float q[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+        q[e] = __fmul_rn(x[e], inv);
+    st_v2(a.codes + 2 * b, e2m1x8_from_f32(q), e2m1x8_from_f32(q + 8));
+    int64_t si = b;
+    if (a.sf_tiles) {
+        const int64_t t = b / a.kb;
+        si = scale_offset_128x4(t, static_cast<int>(b - t * a.kb), a.sf_tiles);
+    }
+    st_u8(a.scales + si, sbyte);
+}
+
+// A thread owns two 16-element blocks per iteration (b and b + stride; the
+// four 16-byte loads issued before either is used), so the block-scale
+// arithmetic (two IEEE divisions and the E4M3 round trip) runs once per
+// block. The first iteration's loads go out before the global scale is
+// known. In dynamic mode thread 0 of each CTA reads amax from the workspace
+// (g = amax / 2688) and, after its own blocks, counts the CTA as done; the
+// last CTA zeroes the workspace for the next call (no CTA waits on another).
 template <bool DYNAMIC, bool F16>
 __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __grid_constant__ QuantArgs a)
 {
@@ -348,57 +378,55 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __grid_consta
     pdl_launch_dependents();
 
     __shared__ float g_sh;
-    if constexpr (DYNAMIC) {
-        if (threadIdx.x == 0) {
-            const uint32_t bits = *reinterpret_cast<volatile uint32_t*>(a.ws);
-            const float g = __fdiv_rn(__uint_as_float(bits), 2688.0f);
-            g_sh = g;
+    if (threadIdx.x == 0) {
+        float g;
+        if constexpr (DYNAMIC) {
+            g = __fdiv_rn(__uint_as_float(*reinterpret_cast<volatile uint32_t*>(a.ws)), 2688.0f);
             if (blockIdx.x == 0)
                 *a.gscale = g;
+        } else {
+            g = *a.gscale;
+        }
+        g_sh = g;
+    }
+    const int64_t nblocks = a.nvec / 2;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    uint4 v[2][2];
+    auto load_pair = [&](int64_t b0) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const int64_t bu = b0 + u * stride;
+            if (bu < nblocks) {
+                // the second load hits the lines the first brought into L1
+                v[u][0] = ld_reuse(a.x + 2 * bu);
+                v[u][1] = ld_reuse(a.x + 2 * bu + 1);
+            }
+        }
+    };
+    load_pair(b);
+    __syncthreads();
+    const float g = g_sh;
+    while (b < nblocks) {
+        quantize_block<F16>(a, g, b, v[0][0], v[0][1]);
+        if (b + stride < nblocks)
+            quantize_block<F16>(a, g, b + stride, v[1][0], v[1][1]);
+        b += 2 * stride;
+        load_pair(b);
+    }
+    if constexpr (DYNAMIC) {
+        if (threadIdx.x == 0) {
             __threadfence();
-            const uint32_t done = atomicAdd(a.ws + 1, 1u);
-            if (done == gridDim.x - 1) {
+            if (atomicAdd(a.ws + 1, 1u) == gridDim.x - 1) {
                 a.ws[0] = 0u;
                 a.ws[1] = 0u;
             }
         }
-    } else {
-        if (threadIdx.x == 0)
-            g_sh = *a.gscale;
-    }
-    __syncthreads();
-    const float g = g_sh;
-
-    const int64_t nblocks = a.nvec / 2;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t b = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; b < nblocks; b += stride) {
-        // the two halves of the block; the second load hits the lines the
-        // first brought into L1
-        float x[16];
-        unpack8_dt(ld_reuse(a.x + 2 * b), x, F16);
-        unpack8_dt(ld_reuse(a.x + 2 * b + 1), x + 8, F16);
-        float bmax = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-            bmax = fmaxf(bmax, fabsf(x[e]));
-        uint32_t sbyte;
-        const float inv = nvfp4_block_scale(g, bmax, sbyte);
-        float q[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e)
-            q[e] = __fmul_rn(x[e], inv);
-        st_v2(a.codes + 2 * b, e2m1x8_from_f32(q), e2m1x8_from_f32(q + 8));
-        int64_t si = b;
-        if (a.sf_tiles) {
-            const int64_t t = b / a.kb;
-            si = scale_offset_128x4(t, static_cast<int>(b - t * a.kb), a.sf_tiles);
-        }
-        st_u8(a.scales + si, sbyte);
     }
 }
 
 // Per-tensor FP8 quantiser (phase B of the dynamic-scale FP8 path, and the
-// standalone quantiser): one 16-byte vector per thread per iteration. In
+// standalone quantiser): two 16-byte vectors per thread per iteration. In
 // dynamic mode s = amax / 448 comes from the workspace and the last CTA to
 // have read it zeroes the workspace; with a given scale s is *scale.
 struct Fp8Args {
@@ -419,32 +447,54 @@ __global__ void __launch_bounds__(256) fp8_quantize_kernel(const __grid_constant
     if (threadIdx.x == 0) {
         float s;
         if constexpr (DYNAMIC) {
-            const uint32_t bits = *reinterpret_cast<volatile uint32_t*>(a.ws);
-            s = __fdiv_rn(__uint_as_float(bits), 448.0f);
+            s = __fdiv_rn(__uint_as_float(*reinterpret_cast<volatile uint32_t*>(a.ws)), 448.0f);
             if (blockIdx.x == 0)
                 *a.scale = s;
-            __threadfence();
-            const uint32_t done = atomicAdd(a.ws + 1, 1u);
-            if (done == gridDim.x - 1) {
-                a.ws[0] = 0u;
-                a.ws[1] = 0u;
-            }
         } else {
             s = *a.scale;
         }
         inv_sh = fp8_inverse_scale(s);
     }
+    // two vectors per thread and iteration (v and v + stride), loads first;
+    // the first iteration's loads go out before the scale is known
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    uint4 xv[2];
+    auto load_pair = [&](int64_t v0) {
+#pragma unroll
+        for (int u = 0; u < 2; ++u)
+            if (v0 + u * stride < a.nvec)
+                xv[u] = ld_stream(a.x + v0 + u * stride);
+    };
+    load_pair(v);
     __syncthreads();
     const float inv = inv_sh;
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; v < a.nvec; v += stride) {
-        float x[8];
-        unpack8_dt(ld_stream(a.x + v), x, F16);
+    while (v < a.nvec) {
 #pragma unroll
-        for (int e = 0; e < 8; ++e)
-            x[e] = __fmul_rn(x[e], inv);
-        const uint2 c = e4m3x8_from_f32(x);
-        asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(a.codes + v), "r"(c.x), "r"(c.y) : "memory");
+        for (int u = 0; u < 2; ++u) {
+            const int64_t vu = v + u * stride;
+            if (vu < a.nvec) {
+                float x[8];
+                unpack8_dt(xv[u], x, F16);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    x[e] = __fmul_rn(x[e], inv);
+                const uint2 c = e4m3x8_from_f32(x);
+                asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(a.codes + vu), "r"(c.x), "r"(c.y) : "memory");
+            }
+        }
+        v += 2 * stride;
+        load_pair(v);
+    }
+    if constexpr (DYNAMIC) {
+        // thread 0 read the workspace above; count the CTA, the last resets
+        if (threadIdx.x == 0) {
+            __threadfence();
+            if (atomicAdd(a.ws + 1, 1u) == gridDim.x - 1) {
+                a.ws[0] = 0u;
+                a.ws[1] = 0u;
+            }
+        }
     }
 }
 

@@ -1,0 +1,187 @@
+// rows.cuh -- the bandwidth form of the fused epilogue, with the next rows
+// prefetched into shared memory.
+//
+// Same arithmetic, in the same order, as fused_rmsnorm_kernel ("Deep Dive:
+// AllReduce and AllReduce Fusion in TensorRT-LLM", 6.3 Inside the Fused
+// Kernel: rank sum, residual add, store residual_out, RMSNorm with gamma,
+// store norm_out, optional quantisation), for many rows:
+//   * one CTA per SM strides over rows t = blockIdx.x, + gridDim.x, ...;
+//   * the rows of its next S iterations are always in flight as cp.async
+//     copies into a ring of S shared-memory stages (stage = the row of every
+//     partial and of the residual);
+//   * each thread copies exactly the 16-byte vectors it later reads (its
+//     vectors v = tid + j * blockDim.x of every source), so its own
+//     cp.async.wait_group is all the synchronisation the data needs; the one
+//     CTA barrier per row is the sum of squares, as in the row form.
+// A CTA that loads a row only when it starts the row holds its SM's loads
+// in flight up to the row's barrier and then leaves HBM idle while it
+// reduces, normalises and stores; here the next rows' copies are already
+// outstanding during that time. The row's partial sums of squares follow the
+// canonical order of every kernel (canonical_row_sum), so the results are
+// bit-identical to the row and cluster forms.
+#pragma once
+
+#include "kernels.cuh"
+
+namespace tpar {
+
+struct RowsArgs {
+    FusedArgs f;  // pointers, sizes, epilogue outputs (slice unused)
+    int stages;   // S, rows in flight per CTA (1..kRowsMaxStages)
+};
+
+constexpr int kRowsMaxStages = 4;
+constexpr int kRowsMaxVpt = 2;                // vectors per thread: d <= 16384
+constexpr int kRowsSmemBudget = 200 * 1024;  // bytes of ring per CTA
+// Dynamic shared memory a CTA asks for at least: more than half of an SM's
+// 228 KB, so that two CTAs of this persistent kernel never share an SM (the
+// grid is one CTA per SM; with PDL the CTAs are placed while the previous
+// kernel drains, and two on one SM would leave another SM without one).
+constexpr int kRowsSmemFloor = 116 * 1024;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src)
+{
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+
+// Wait until at most `pending` (0..3) of this thread's newest copy groups are
+// still in flight.
+__device__ __forceinline__ void cp_async_wait_pending(int pending)
+{
+    switch (pending) {
+    case 0: asm volatile("cp.async.wait_group 0;" ::: "memory"); break;
+    case 1: asm volatile("cp.async.wait_group 1;" ::: "memory"); break;
+    case 2: asm volatile("cp.async.wait_group 2;" ::: "memory"); break;
+    default: asm volatile("cp.async.wait_group 3;" ::: "memory"); break;
+    }
+}
+
+template <int NR, int VPT, int QMODE, bool F16>
+__global__ void __launch_bounds__(1024) rows_prefetch_kernel(const __grid_constant__ RowsArgs ra)
+{
+    extern __shared__ __align__(16) uint4 rows_ring[];  // [S][nsrc][nvec]
+    const FusedArgs& a = ra.f;
+    pdl_wait();
+    pdl_launch_dependents();
+
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int nwarps = blockDim.x >> 5;
+    const int B = static_cast<int>(blockDim.x);
+    const int nvec = a.nvec;
+    const int S = ra.stages;
+    const int nsrc = a.n_ranks + (a.residual ? 1 : 0);
+    const int64_t G = gridDim.x;
+    const int nW = (nvec + 31) >> 5;
+    __shared__ float wsh[2][kMaxRowWarps];  // per-32-vector partial sums of squares, by row parity
+
+    // copy this thread's vectors of row t (every source) into stage s
+    auto prefetch = [&](int64_t t, int s) {
+        if (t < a.T) {
+            const int64_t rowv = t * static_cast<int64_t>(nvec);
+            const uint32_t st = smem_addr(rows_ring + static_cast<size_t>(s) * nsrc * nvec);
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int v = tid + j * B;
+                if (v < nvec) {
+#pragma unroll
+                    for (int r = 0; r < NR; ++r)
+                        if (r < a.n_ranks)
+                            cp_async16(st + 16u * static_cast<uint32_t>(r * nvec + v), a.partials[r] + rowv + v);
+                    if (a.residual)
+                        cp_async16(st + 16u * static_cast<uint32_t>(a.n_ranks * nvec + v), a.residual + rowv + v);
+                }
+            }
+        }
+        cp_async_commit();  // one group per call, empty past the last row
+    };
+    for (int s = 0; s < S; ++s)
+        prefetch(blockIdx.x + s * G, s);
+
+    float g_given = 0.0f;
+    if constexpr (QMODE == kQuantGiven)
+        g_given = *a.gscale;
+    if constexpr (QMODE == kQuantFp8Given)
+        g_given = fp8_inverse_scale(*a.gscale);
+    uint4 gam[VPT];
+#pragma unroll
+    for (int j = 0; j < VPT; ++j) {
+        const int v = tid + j * B;
+        gam[j] = v < nvec ? ld_reuse(a.gamma + v) : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float amax_local = 0.0f;
+
+    int it = 0;
+    for (int64_t t = blockIdx.x; t < a.T; t += G, ++it) {
+        const int s = it % S;
+        const int64_t rowv = t * static_cast<int64_t>(nvec);
+        cp_async_wait_pending(S - 1);  // this thread's copies of row t have landed
+        const uint4* st = rows_ring + static_cast<size_t>(s) * nsrc * nvec;
+
+        // ---- rank sum (fixed order 0..N-1) and residual add, from the stage
+        float h[VPT][8];
+        float ss[VPT];
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int v = tid + j * B;
+            ss[j] = 0.0f;
+            if (v < nvec) {
+                unpack8_dt(st[v], h[j], F16);
+#pragma unroll
+                for (int r = 1; r < NR; ++r)
+                    if (r < a.n_ranks)
+                        add8_dt(st[r * nvec + v], h[j], F16);
+                if (a.residual)
+                    add8_dt(st[a.n_ranks * nvec + v], h[j], F16);
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    ss[j] = fmaf(h[j][e], h[j][e], ss[j]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    h[j][e] = 0.0f;
+            }
+        }
+        // this thread's slots of stage s are free: start row t + S * G
+        prefetch(t + S * G, s);
+        if (a.out_residual) {
+#pragma unroll
+            for (int j = 0; j < VPT; ++j) {
+                const int v = tid + j * B;
+                if (v < nvec)
+                    st_v4(a.out_residual + rowv + v, pack8_dt(h[j], F16));
+            }
+        }
+
+        // ---- row sum of squares in the canonical order (canonical_row_sum)
+        const int buf = it & 1;
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const float sj = warp_sum(ss[j]);
+            const int w = (j * B + 32 * warp) >> 5;
+            if (lane == 0 && 32 * w < nvec)
+                wsh[buf][w] = sj;
+        }
+        __syncthreads();
+        const float tot = canonical_row_sum(wsh[buf], nW, lane);
+        const float rinv = rsqrtf(fmaf(tot, a.inv_d, a.eps));
+
+        // ---- normalise, scale by gamma, store; optional quantisation
+#pragma unroll
+        for (int j = 0; j < VPT; ++j) {
+            const int v = tid + j * B;
+            emit_vector<QMODE, F16>(a, v < nvec, rowv + v, t, v, h[j], gam[j], rinv, g_given, amax_local);
+        }
+    }
+    cp_async_wait_pending(0);  // no copy of ours is outstanding at exit
+
+    if constexpr (QMODE == kQuantAmax) {
+        __shared__ float warp_max_sh[32];
+        cta_amax_atomic(amax_local, a.amax_bits, warp_max_sh, warp, lane, nwarps);
+    }
+}
+
+}  // namespace tpar

@@ -161,6 +161,17 @@ def test_user_plan_is_checked(tp):
                 P(1, 32, 32, 1, 8), P(2, 2, 256, 2, 8), P(2, 1, 1024, 1, 8), P(2, 1, 256, 1, 8),
                 P(2, 1, 512, 3, 8)):
         assert call(tp, plan=bad) == INVALID, bad.as_dict()
+    # the prefetching row kernel (kernel 3): <= 2 vectors per thread, split 1
+    assert call(tp, plan=P(3, 1, 512, 1, 152)) == OK
+    assert call(tp, plan=P(3, 1, 256, 2, 7)) == OK
+    for bad in (P(3, 2, 512, 1, 152), P(3, 1, 256, 1, 152), P(3, 1, 128, 4, 152), P(3, 1, 512, 1, 0),
+                P(3, 1, 500, 1, 152), P(4, 1, 512, 1, 152)):
+        assert call(tp, plan=bad) == INVALID, bad.as_dict()
+    # a row of all 9 sources (288 KB at d = 16384) does not fit the ring
+    parts16 = [BASE + r * 8 * MB for r in range(8)]
+    assert call(tp, parts=parts16, d=16384, residual=BASE + 64 * MB, gamma=BASE + 100 * MB,
+                out_norm=BASE + 128 * MB, out_residual=BASE + 192 * MB, T=8,
+                plan=P(3, 1, 1024, 2, 152)) == UNSUPPORTED
 
 
 def test_unfused_and_quantize_checks(tp):
@@ -193,7 +204,11 @@ def test_planner_covers_every_row(tp, sm):
             if p.kernel == 2:
                 assert p.split == 1 and p.threads <= 512 and p.threads * p.vec_per_thread >= nvec
                 raise AssertionError("the stream kernel is only planned on request")
-            if p.kernel == 1:
+            if p.kernel == 3:
+                assert 2 * T > 3 * sm and nvec >= 256 and p.split == 1 and p.vec_per_thread in (1, 2)
+                assert p.threads * p.vec_per_thread >= nvec and p.grid_rows == sm
+                assert (8 + 1) * d * 2 <= 200 * 1024  # a row of every source fits one stage
+            elif p.kernel == 1:
                 assert 2 <= p.split <= 16
                 s = -(-(-(-nvec // p.split)) // 32) * 32
                 assert p.threads * p.vec_per_thread >= s
@@ -216,15 +231,26 @@ def test_planner_choices_for_the_pages_shapes(tp):
     # 82 KB rows (N=4, d=8192): split 8 ways; 25 KB rows (N=2, d=4096): whole
     assert tp.tpar_plan_launch(8, 8192, 4, 152).split == 8
     assert tp.tpar_plan_launch(8, 4096, 2, 152).kernel == 0
-    # prefill: one CTA of 1024 threads per row; the TMA-fed kernel on request
+    # prefill: one persistent CTA of 1024 threads per SM with the next rows
+    # prefetched; the TMA-fed kernel on request
     p = tp.tpar_plan_launch(4096, 8192, 8, 152)
-    assert (p.kernel, p.split, p.threads, p.vec_per_thread) == (0, 1, 1024, 1)
+    assert (p.kernel, p.split, p.threads, p.vec_per_thread, p.grid_rows) == (3, 1, 1024, 1, 152)
+    p = tp.tpar_plan_launch(16384, 8192, 4, 148)
+    assert (p.kernel, p.threads, p.vec_per_thread, p.grid_rows) == (3, 1024, 1, 148)
+    p = tp.tpar_plan_launch(4096, 16384, 4, 152)
+    assert (p.kernel, p.threads, p.vec_per_thread) == (3, 1024, 2)
+    # no prefetch where a row of every source outgrows the ring, or T <= SMs
+    assert tp.tpar_plan_launch(4096, 16384, 8, 152).kernel == 0
+    assert tp.tpar_plan_launch(4096, 32768, 1, 152).kernel == 0
+    assert tp.tpar_plan_launch(228, 8192, 8, 152).kernel == 0
+    assert tp.tpar_plan_launch(229, 8192, 8, 152).kernel == 3
+    assert tp.tpar_plan_launch(4096, 1024, 8, 152).kernel == 0  # rows of 128 vectors
     p = tp.tpar_plan_launch(4096, 8192, 8, 152, tp.TPAR_FORCE_STREAM)
     assert (p.kernel, p.split, p.threads, p.vec_per_thread, p.grid_rows) == (2, 1, 512, 2, 152)
     # short rows and mid-size batches: one CTA per row, capped at 512 threads for > 8 ranks
     p = tp.tpar_plan_launch(200, 8192, 16, 152)
     assert (p.kernel, p.threads, p.vec_per_thread) == (0, 512, 2)
-    assert tp.tpar_plan_launch(4096, 1024, 8, 152).kernel == 0
+    assert tp.tpar_plan_launch(4096, 2048, 8, 152).kernel == 3
     assert tp.tpar_plan_launch(4096, 8192, 8, 152, tp.TPAR_FORCE_ROW).kernel == 0
     assert tp.tpar_plan_launch(8, 8192, 8, 152, tp.TPAR_FORCE_STREAM).kernel == 2
     assert tp.tpar_plan_launch(1, 8192, 8, 152, tp.TPAR_FORCE_ROW).kernel == 0

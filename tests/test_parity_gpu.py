@@ -302,3 +302,83 @@ def test_more_rows_than_one_grid_dimension(kind):
         torch.cuda.synchronize()
         oc, os_ = oracle.fp8_quantize(synth.bits(out["out_norm"]))
         assert np.array_equal(out["codes"].cpu().numpy(), oc) and np.float32(out["scale"].item()) == os_
+
+
+# ------------------------------------------------- prefetching row kernel (plan kernel 3)
+
+def _rows_plan(tp, d, grid):
+    nvec = d // 8
+    vpt = 1 if nvec <= 1024 else 2
+    threads = -(-(-(-nvec // vpt)) // 32) * 32
+    return tp.TparPlan(kernel=3, split=1, threads=threads, vec_per_thread=vpt, grid_rows=grid)
+
+
+@pytest.mark.parametrize("n,T,d,residual,grid", [
+    (8, 700, 8192, True, 152),   # 1 stage of 144 KB; rows wrap the ring many times
+    (8, 500, 4096, True, 19),    # 2 stages, 27 rows per CTA
+    (3, 401, 8192, True, 152),   # 3 stages of 64 KB
+    (4, 999, 1024, False, 7),    # 4 stages, no residual, 143 rows per CTA
+    (16, 300, 2048, True, 152),  # 16 ranks
+    (2, 333, 16384, True, 152),  # 2 vectors per thread
+    (5, 160, 8200, True, 152),   # 1025 vectors: 2 per thread, a ragged last warp
+    (1, 153, 8, False, 152),     # one vector per row
+    (7, 37, 4096, True, 64),     # fewer rows than CTAs
+])
+def test_prefetch_row_kernel_shapes(n, T, d, residual, grid):
+    """Every ring depth and row shape; results equal the row kernel's bits."""
+    tp = lib()
+    w = synth.Workload(f"rows N{n} T{T} d{d}", n, T, d, 1e-5, 0.5, seed=n * 3 + T + d)
+    inputs, out, ref = run_full(tp, w, residual=residual, plan=_rows_plan(tp, d, grid))
+    check(out, ref, w.name)
+    dev = to_device(inputs if residual else dict(inputs, residual=None))
+    row = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, flags=tp.TPAR_FORCE_ROW)
+    torch.cuda.synchronize()
+    assert torch.equal(out["out_norm"].view(torch.int16), row["out_norm"].view(torch.int16))
+    assert torch.equal(out["out_residual"].view(torch.int16), row["out_residual"].view(torch.int16))
+
+
+@pytest.mark.parametrize("mode", ["nvfp4_given", "nvfp4_dynamic", "nvfp4_128x4", "fp8_given", "fp8_dynamic",
+                                  "fp16_nvfp4"])
+def test_prefetch_row_kernel_quantised(mode):
+    """The automatic plan at T > SMs is the prefetching kernel; every
+    quantised output mode through it, bit-exact against the oracle quantiser."""
+    tp = lib()
+    T, d, n = 600, 4096, 4
+    assert tp.tpar_plan_launch(T, d, n, torch.cuda.get_device_properties(0).multi_processor_count).kernel == 3
+    dt = torch.float16 if mode.startswith("fp16") else torch.bfloat16
+    w = synth.NVFP4.with_(T=T, d=d, n_ranks=n)
+    inputs = synth.make_inputs(w, dtype=dt)
+    dev = to_device(inputs)
+    rows = np.array([0, 1, 151, 152, 300, T - 1])
+    ref = oracle_rows(inputs, rows, w.eps)
+    g = torch.tensor([0.04], dtype=torch.float32, device="cuda")
+    if mode.startswith("fp8"):
+        out = tp.fused_rmsnorm_fp8(dev["partials"], dev["residual"], dev["gamma"], w.eps,
+                                   scale=g if mode == "fp8_given" else None)
+        torch.cuda.synchronize()
+        oc, os_ = oracle.fp8_quantize(synth.bits(out["out_norm"]), scale=0.04 if mode == "fp8_given" else None)
+        assert np.array_equal(out["codes"].cpu().numpy(), oc) and np.float32(out["scale"].item()) == os_
+    else:
+        given = mode == "nvfp4_given"
+        out = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True,
+                               global_scale=g if given else None, scales_128x4=mode == "nvfp4_128x4")
+        torch.cuda.synchronize()
+        assert_nvfp4_bit_exact(out["out_norm"], out["codes"], out["scales"], out["global_scale"],
+                               given=float(np.float32(0.04)) if given else None, what=mode,
+                               scales_128x4=mode == "nvfp4_128x4")
+    assert_close_to_ref(out["out_norm"][rows], ref["y"], f"{mode} out_norm")
+    assert_close_to_ref(out["out_residual"][rows], ref["h"], f"{mode} out_residual")
+
+
+def test_prefetch_row_kernel_in_place_residual():
+    tp = lib()
+    w = synth.Workload("rows in place", 8, 777, 2048, 1e-5, 0.5, seed=21)
+    inputs = synth.make_inputs(w)
+    dev = to_device(inputs)
+    res = dev["residual"].clone()
+    out = tp.fused_rmsnorm(dev["partials"], res, dev["gamma"], w.eps, out_residual=res,
+                           plan=_rows_plan(tp, w.d, 152))
+    torch.cuda.synchronize()
+    ref = oracle_rows(inputs, slice(None), w.eps)
+    assert_close_to_ref(res, ref["h"], "rows in-place residual")
+    assert_close_to_ref(out["out_norm"], ref["y"], "rows in-place out_norm")

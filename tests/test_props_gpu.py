@@ -208,6 +208,11 @@ def _plans(tp, d, T):
     for thr, vpt in ((512, 2), (256, 4), (512, 4), (128, 8)):
         if thr * vpt >= nvec:
             plans.append(P(2, 1, thr, vpt, max(1, min(T, 5))))
+    for vpt in (1, 2):  # the prefetching row kernel, one CTA or a few
+        thr = r32(-(-nvec // vpt))
+        if thr <= 1024:
+            plans.append(P(3, 1, thr, vpt, 1))
+            plans.append(P(3, 1, thr, vpt, max(1, T // 5)))
     return plans
 
 
@@ -216,7 +221,7 @@ def test_bitwise_identical_across_plans_and_batch_sizes(d):
     """The sum of squares is reduced in one canonical order (32-vector warp
     sums, then groups), so every launch plan -- whole-row CTAs of any shape,
     cluster splits, the TMA-fed kernel -- and every batch size gives the
-    same bits (batch invariance)."""
+    same bits (batch invariance); the prefetching row kernel included."""
     tp = lib()
     T = 40
     w = synth.PREFILL.with_(T=T, d=d, seed=d)
