@@ -75,6 +75,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
     os.replace(tmp, LIB)
+    for obj, _ in results:  # every build recompiles all units: keep only the library
+        os.remove(obj)
     if verbose:
         print("built", LIB)
     return LIB

@@ -32,11 +32,15 @@ def dtype_name(t: torch.Tensor) -> str:
 def assert_close_to_ref(got_bf16: torch.Tensor, ref64: np.ndarray, what: str, extra=None):
     got = oracle.to_float64(synth.bits(got_bf16), dtype_name(got_bf16))
     assert got.shape == ref64.shape, (got.shape, ref64.shape)
-    err = np.abs(got - ref64)
-    bound = RTOL * np.abs(ref64) + ATOL
-    if extra is not None:
-        bound = bound + extra
-    bad = err > bound
+    with np.errstate(invalid="ignore"):
+        err = np.abs(got - ref64)
+        bound = RTOL * np.abs(ref64) + ATOL
+        if extra is not None:
+            bound = bound + extra
+        # within the bound (false for any NaN), or NaN exactly where the
+        # reference is NaN, or the same infinity
+        ok = (err <= bound) | (np.isnan(got) & np.isnan(ref64)) | (np.isinf(got) & (got == ref64))
+    bad = ~ok
     if bad.any():
         idx = np.argwhere(bad)[:5]
         raise AssertionError(f"{what}: {int(bad.sum())} of {bad.size} elements out of tolerance; "

@@ -382,3 +382,36 @@ def test_prefetch_row_kernel_in_place_residual():
     ref = oracle_rows(inputs, slice(None), w.eps)
     assert_close_to_ref(res, ref["h"], "rows in-place residual")
     assert_close_to_ref(out["out_norm"], ref["y"], "rows in-place out_norm")
+
+
+@pytest.mark.parametrize("kind", ["auto", "row", "cluster", "rows_prefetch"])
+def test_special_values_propagate_like_the_oracle(kind):
+    """Inf and NaN inputs follow IEEE arithmetic as in the oracle: a row with
+    an infinite element has ms = inf, so its finite elements normalise to 0
+    and the infinite one to NaN (inf * 0); a NaN poisons its whole row;
+    other rows are untouched. (Rows whose sum of squares overflows fp32,
+    |h| ~ 1e19 and up, are outside the fp32 arithmetic of the method and not
+    compared with the fp64 oracle.)"""
+    tp = lib()
+    T, d, n = 240, 2048, 3
+    w = synth.Workload("specials", n, T, d, 1e-5, 0.5, seed=77)
+    inputs = synth.make_inputs(w)
+    p0 = inputs["partials"][0].clone()
+    p0[3, 5] = float("inf")
+    p0[7, 100] = float("-inf")
+    p0[11, 2000] = float("nan")
+    inputs = dict(inputs, partials=[p0] + inputs["partials"][1:])
+    flags = {"auto": 0, "row": tp.TPAR_FORCE_ROW, "cluster": tp.TPAR_FORCE_CLUSTER}.get(kind, 0)
+    plan = None
+    if kind == "rows_prefetch":
+        plan = tp.TparPlan(kernel=3, split=1, threads=256, vec_per_thread=1, grid_rows=152)
+    dev = to_device(inputs)
+    out = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, flags=flags, plan=plan)
+    torch.cuda.synchronize()
+    ref = oracle_rows(inputs, slice(None), w.eps)
+    assert np.isnan(ref["y"][11]).all() and np.isnan(ref["y"][3, 5]) and ref["y"][3, 6] == 0
+    assert_close_to_ref(out["out_residual"], ref["h"], f"{kind} specials out_residual")
+    assert_close_to_ref(out["out_norm"], ref["y"], f"{kind} specials out_norm")
+    got_h = oracle.to_float64(synth.bits(out["out_residual"]))
+    assert got_h[3, 5] == np.inf and got_h[7, 100] == -np.inf and np.isnan(got_h[11, 2000])
+    assert np.isfinite(oracle.to_float64(synth.bits(out["out_norm"]))[[0, 1, 2, 4, 239]]).all()
