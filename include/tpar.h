@@ -24,9 +24,15 @@
  *     gamma [d] bf16, codes [T, d/2] bytes, scales [T, d/16] bytes. With the
  *     TPAR_DTYPE_FP16 flag (every entry point that takes flags) the bf16
  *     tensors are IEEE binary16 instead; everything else is unchanged.
- *   - Pointers to tensors are DEVICE pointers; `partials` itself is a HOST
- *     array holding n_ranks device pointers. The caller owns every buffer; no
- *     entry point allocates or frees per call.
+ *   - Pointers to tensors are addresses the device can access: device
+ *     memory, or page-locked host memory mapped into the device's address
+ *     space (cudaHostAlloc / cudaHostRegister; under unified addressing the
+ *     host pointer itself). Host-resident tensors are read and written by
+ *     the kernels directly over the CPU-GPU link (on GB300, NVLink-C2C):
+ *     no staging copy, results visible on the host once the stream reaches
+ *     the call's end. `partials` itself is a HOST array holding n_ranks such
+ *     pointers. The caller owns every buffer; no entry point allocates or
+ *     frees per call.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = the legacy
  *     default stream): no host synchronisation, no memcpy, no allocation.
  *     They may be captured in a CUDA graph once tpar_init() has run for the

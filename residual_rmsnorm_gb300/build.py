@@ -8,6 +8,7 @@ No fast-math: the NVFP4 scale arithmetic must round exactly as IEEE binary32.
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import os
 import shutil
 import subprocess
@@ -49,10 +50,20 @@ def _needs_rebuild() -> bool:
 
 
 def build(force: bool = False, verbose: bool = False) -> str:
-    """Compile and link libtpar.so; returns its path. Raises on failure."""
+    """Compile and link libtpar.so; returns its path. Raises on failure.
+    Processes that build at the same time take turns (a file lock); the
+    ones that wait find the library up to date."""
     if not force and not _needs_rebuild():
         return LIB
     os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, ".lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        if not force and not _needs_rebuild():
+            return LIB
+        return _build_locked(verbose)
+
+
+def _build_locked(verbose: bool) -> str:
     cc = nvcc()
 
     def compile_one(src: str) -> tuple[str, str]:

@@ -1,9 +1,12 @@
 """PyTorch-tensor front end of the C ABI (marshalling only).
 
 PyTorch supplies device memory and the current CUDA stream; every step of the
-epilogue runs in libtpar.so. Tensors must be CUDA, contiguous and 16-byte
-aligned, as include/tpar.h requires, and all of one element type: bf16, or
-fp16 for the whole call (then TPAR_DTYPE_FP16 is passed).
+epilogue runs in libtpar.so. Tensors must be contiguous and 16-byte aligned,
+as include/tpar.h requires, and all of one element type: bf16, or fp16 for
+the whole call (then TPAR_DTYPE_FP16 is passed). They live on the CUDA
+device, or in page-locked (pinned) host memory, which the kernels read and
+write in place over the CPU-GPU link; outputs this module allocates are on
+the CUDA device of the first device tensor (else the current device).
 """
 from __future__ import annotations
 
@@ -20,8 +23,8 @@ def _check_bf16(name, t, shape=None, dtype=None):
     the whole call), of the given shape."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.device.type != "cuda":
-        raise ValueError(f"{name} must live on a CUDA device (no CPU path exists)")
+    if t.device.type != "cuda" and not (t.device.type == "cpu" and t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory (no CPU compute path exists)")
     want = dtype if dtype is not None else t.dtype
     if t.dtype not in _DTYPES or t.dtype != want:
         raise TypeError(f"{name} must be {want if dtype is not None else 'bf16 or fp16'}, got {t.dtype}")
@@ -34,6 +37,15 @@ def _check_bf16(name, t, shape=None, dtype=None):
 def _stream_handle(device, stream):
     s = stream if stream is not None else torch.cuda.current_stream(device)
     return s.cuda_stream
+
+
+def _device_of(*tensors) -> torch.device:
+    """The CUDA device a call runs on: that of the first CUDA tensor, else
+    the current device (every tensor in pinned host memory)."""
+    for t in tensors:
+        if isinstance(t, torch.Tensor) and t.device.type == "cuda":
+            return t.device
+    return torch.device("cuda", torch.cuda.current_device())
 
 
 def _nvfp4_outputs(T, d, device, global_scale, scales_128x4=False):
@@ -73,7 +85,7 @@ def fused_rmsnorm(partials, residual, gamma, eps: float, *, out_norm=None, out_r
     if not partials:
         raise ValueError("need at least one partial")
     T, d = partials[0].shape
-    dev = partials[0].device
+    dev = _device_of(*partials, residual, gamma)
     dt = partials[0].dtype
     if dt == torch.float16:
         flags |= _abi.TPAR_DTYPE_FP16
@@ -115,7 +127,7 @@ def allreduce_sum(partials, residual=None, *, out=None, flags: int = 0, stream=N
     if not partials:
         raise ValueError("need at least one partial")
     T, d = partials[0].shape
-    dev = partials[0].device
+    dev = _device_of(*partials, residual)
     dt = partials[0].dtype
     if dt == torch.float16:
         flags |= _abi.TPAR_DTYPE_FP16
@@ -139,7 +151,7 @@ def unfused_rmsnorm(partials, residual, gamma, eps: float, *, reduced=None, out_
     """The same epilogue as separate kernels through HBM (the comparison baseline)."""
     partials = list(partials)
     T, d = partials[0].shape
-    dev = partials[0].device
+    dev = _device_of(*partials, residual, gamma)
     dt = partials[0].dtype
     if dt == torch.float16:
         flags |= _abi.TPAR_DTYPE_FP16
@@ -178,14 +190,15 @@ def nvfp4_quantize(x, global_scale: torch.Tensor | None = None, scales_128x4: bo
     T, d = x.shape
     if x.dtype == torch.float16:
         flags |= _abi.TPAR_DTYPE_FP16
-    codes, scales, g, given = _nvfp4_outputs(T, d, x.device, global_scale, scales_128x4)
+    dev = _device_of(x)
+    codes, scales, g, given = _nvfp4_outputs(T, d, dev, global_scale, scales_128x4)
     if given:
         flags |= _abi.TPAR_GSCALE_GIVEN
     if scales_128x4:
         flags |= _abi.TPAR_SCALES_128X4
-    with torch.cuda.device(x.device):
+    with torch.cuda.device(dev):
         _abi.tpar_nvfp4_quantize(x.data_ptr(), T, d, codes.data_ptr(), scales.data_ptr(),
-                                 g.data_ptr(), flags, _stream_handle(x.device, stream))
+                                 g.data_ptr(), flags, _stream_handle(dev, stream))
     return codes, scales, g
 
 
@@ -196,7 +209,7 @@ def fused_rmsnorm_fp8(partials, residual, gamma, eps: float, *, scale: torch.Ten
     Returns dict(out_norm, out_residual, codes uint8 [T, d], scale)."""
     partials = list(partials)
     T, d = partials[0].shape
-    dev = partials[0].device
+    dev = _device_of(*partials, residual, gamma)
     dt = partials[0].dtype
     if dt == torch.float16:
         flags |= _abi.TPAR_DTYPE_FP16
@@ -228,13 +241,14 @@ def fp8_quantize(x, scale: torch.Tensor | None = None, flags: int = 0, stream=No
     T, d = x.shape
     if x.dtype == torch.float16:
         flags |= _abi.TPAR_DTYPE_FP16
-    codes = torch.empty((T, d), dtype=torch.uint8, device=x.device)
+    dev = _device_of(x)
+    codes = torch.empty((T, d), dtype=torch.uint8, device=dev)
     if scale is None:
-        s = torch.empty((1,), dtype=torch.float32, device=x.device)
+        s = torch.empty((1,), dtype=torch.float32, device=dev)
     else:
         s = scale
         flags |= _abi.TPAR_GSCALE_GIVEN
-    with torch.cuda.device(x.device):
+    with torch.cuda.device(dev):
         _abi.tpar_fp8_quantize(x.data_ptr(), T, d, codes.data_ptr(), s.data_ptr(), flags,
-                               _stream_handle(x.device, stream))
+                               _stream_handle(dev, stream))
     return codes, s

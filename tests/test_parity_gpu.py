@@ -415,3 +415,35 @@ def test_special_values_propagate_like_the_oracle(kind):
     got_h = oracle.to_float64(synth.bits(out["out_residual"]))
     assert got_h[3, 5] == np.inf and got_h[7, 100] == -np.inf and np.isnan(got_h[11, 2000])
     assert np.isfinite(oracle.to_float64(synth.bits(out["out_norm"]))[[0, 1, 2, 4, 239]]).all()
+
+
+@pytest.mark.parametrize("case,n,T,d", [("decode_cluster", 8, 8, 4096), ("rows_prefetch", 4, 400, 2048),
+                                        ("nvfp4_dynamic_single_launch", 4, 8, 8192), ("nvfp4_given", 4, 300, 4096),
+                                        ("row", 2, 100, 1024)])
+def test_host_resident_tensors(case, n, T, d):
+    """Inputs and outputs in pinned host memory: the kernels read and write
+    them in place over the CPU-GPU link (no staging copy). The results are
+    the bits of the same call on device memory, within tolerance of the
+    oracle."""
+    tp = lib()
+    w = synth.Workload(f"host {case}", n, T, d, 1e-5, 0.5, seed=T + d + n)
+    inputs = synth.make_inputs(w)
+    hp = [p.pin_memory() for p in inputs["partials"]]
+    hr, hg = inputs["residual"].pin_memory(), inputs["gamma"].pin_memory()
+    on = torch.empty((T, d), dtype=torch.bfloat16).pin_memory()
+    orr = torch.empty((T, d), dtype=torch.bfloat16).pin_memory()
+    nvfp4 = case.startswith("nvfp4")
+    gs = torch.tensor([0.02], dtype=torch.float32, device="cuda") if case == "nvfp4_given" else None
+    h = tp.fused_rmsnorm(hp, hr, hg, w.eps, out_norm=on, out_residual=orr, nvfp4=nvfp4, global_scale=gs)
+    torch.cuda.synchronize()
+    dev = to_device(inputs)
+    dd = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=nvfp4, global_scale=gs)
+    torch.cuda.synchronize()
+    assert torch.equal(on.view(torch.int16), dd["out_norm"].cpu().view(torch.int16))
+    assert torch.equal(orr.view(torch.int16), dd["out_residual"].cpu().view(torch.int16))
+    if nvfp4:
+        assert torch.equal(h["codes"], dd["codes"]) and torch.equal(h["scales"], dd["scales"])
+        assert h["global_scale"].item() == dd["global_scale"].item()
+    ref = oracle_rows(inputs, slice(None), w.eps)
+    assert_close_to_ref(orr, ref["h"], f"{case} host out_residual")
+    assert_close_to_ref(on, ref["y"], f"{case} host out_norm")
