@@ -81,6 +81,26 @@ typedef void* tpar_stream_t;
                                    instead of bf16 (accumulation stays fp32) */
 #define TPAR_SCALES_128X4 0x80u /* NVFP4 scales in the 128x4 tiled layout that
                                    block-scaled GEMMs read, see below         */
+#define TPAR_DEBUG_SHRINK 0x100u /* debug builds only (tpar_debug_build() == 1),
+                                   fused entry points and tpar_nvfp4_quantize:
+                                   check [T, d] accesses against one vector
+                                   fewer than the tensor holds, so the last
+                                   vector's accesses are reported and skipped
+                                   (a self-test of the index checks); release
+                                   builds return TPAR_ERR_UNSUPPORTED, the
+                                   unfused and FP8-quantiser entry points
+                                   TPAR_ERR_INVALID_ARG                       */
+
+/* Bits of the device error word (tpar_device_error). */
+#define TPAR_DEVERR_CLUSTER_WAIT 0x1u /* a bounded wait of the cluster-split
+                                         kernel's exchange expired            */
+#define TPAR_DEVERR_STREAM_WAIT 0x2u  /* a bounded ring wait of the TMA-fed
+                                         kernel expired                       */
+#define TPAR_DEVERR_SMALL_WAIT 0x4u   /* a bounded exchange wait of the
+                                         single-launch NVFP4 kernel expired   */
+#define TPAR_DEVERR_INDEX 0x8u        /* debug builds: a computed index failed
+                                         its bounds check; the access was
+                                         skipped                              */
 
 /*
  * TPAR_SCALES_128X4 (NVFP4 outputs only; d % 64 == 0). The pages name only
@@ -271,12 +291,21 @@ tpar_status tpar_plan_launch(int64_t T, int64_t d, int n_ranks, int sm_count, ui
 
 /*
  * tpar_device_error -- read and clear the device's error word (kept in the
- * tpar_init workspace; 0 when tpar_init never ran for `device`). Bit 0: a
- * bounded wait inside the cluster-split kernel expired, so that call's
- * outputs are wrong. Synchronises the device; a diagnostic, not for the hot
- * path.
+ * tpar_init workspace; 0 when tpar_init never ran for `device`): an OR of
+ * TPAR_DEVERR_* bits. Any bit set means some call since the last read
+ * produced wrong outputs (a bounded wait gave up, or in a debug build an
+ * index check skipped an access). Synchronises the device; a diagnostic,
+ * not for the hot path.
  */
 tpar_status tpar_device_error(int device, uint32_t* code);
+
+/*
+ * tpar_debug_build -- 1 if this library was compiled with -DTPAR_DEBUG: every
+ * computed global and shared-memory index of the fused kernels is checked
+ * against its buffer before the access, and one out of range sets
+ * TPAR_DEVERR_INDEX and skips the access (no trap, no fault); 0 otherwise.
+ */
+int tpar_debug_build(void);
 
 /* Bytes of a caller-owned workspace for tpar_fused_rmsnorm_ex. */
 int64_t tpar_workspace_bytes(void);

@@ -24,6 +24,11 @@ TPAR_DRY_RUN = 0x10
 TPAR_FORCE_STREAM = 0x20
 TPAR_DTYPE_FP16 = 0x40
 TPAR_SCALES_128X4 = 0x80
+TPAR_DEBUG_SHRINK = 0x100
+TPAR_DEVERR_CLUSTER_WAIT = 0x1
+TPAR_DEVERR_STREAM_WAIT = 0x2
+TPAR_DEVERR_SMALL_WAIT = 0x4
+TPAR_DEVERR_INDEX = 0x8
 
 
 def scales_128x4_bytes(T: int, d: int) -> int:
@@ -42,6 +47,10 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 
 
 def library_path() -> str:
+    """libtpar.so, or the index-checking debug build libtpar_debug.so when
+    the environment sets TPAR_DEBUG=1 (read once, when the library loads)."""
+    if os.environ.get("TPAR_DEBUG") == "1":
+        return os.path.join(_HERE, "_build_debug", "libtpar_debug.so")
     return os.path.join(_HERE, "_build", "libtpar.so")
 
 
@@ -97,6 +106,8 @@ def library() -> ctypes.CDLL:
         lib.tpar_nvfp4_quantize.restype = i32
         lib.tpar_plan_launch.argtypes = [i64, i64, i32, i32, u32, ctypes.POINTER(TparPlan)]
         lib.tpar_plan_launch.restype = i32
+        lib.tpar_debug_build.argtypes = []
+        lib.tpar_debug_build.restype = i32
         lib.tpar_device_error.argtypes = [i32, ctypes.POINTER(ctypes.c_uint32)]
         lib.tpar_device_error.restype = i32
         lib.tpar_workspace_bytes.argtypes = []
@@ -209,7 +220,7 @@ def tpar_plan_launch(T, d, n_ranks, sm_count, flags=0) -> TparPlan:
 
 
 def tpar_device_error(device: int) -> int:
-    """Read and clear the device error word (0: no bounded wait expired)."""
+    """Read and clear the device error word: an OR of TPAR_DEVERR_* bits (0: none)."""
     code = ctypes.c_uint32(0)
     _check(library().tpar_device_error(device, ctypes.byref(code)), "tpar_device_error")
     return int(code.value)
@@ -225,3 +236,8 @@ def tpar_status_string(status: int) -> str:
 
 def tpar_version() -> int:
     return int(library().tpar_version())
+
+
+def tpar_debug_build() -> bool:
+    """True for the index-checking debug build (TPAR_DEBUG=1)."""
+    return bool(library().tpar_debug_build())

@@ -25,6 +25,18 @@ using tpar::ReduceArgs;
 constexpr int kMaxDevices = 64;
 constexpr int64_t kWorkspaceBytes = 256;
 constexpr int64_t kMaxGridY = 65535;
+#ifdef TPAR_DEBUG
+constexpr bool kDebugBuild = true;   // kernels check their indices (TPAR_IN_RANGE)
+#else
+constexpr bool kDebugBuild = false;
+#endif
+
+// The extent the debug index checks allow for a [T, d] tensor: T * d / 8
+// vectors, one fewer under the TPAR_DEBUG_SHRINK self-test.
+int64_t checked_vectors(int64_t T, int64_t d, uint32_t flags)
+{
+    return T * (d / 8) - ((flags & TPAR_DEBUG_SHRINK) ? 1 : 0);
+}
 
 struct DeviceState {
     int sm_count = 0;          // 0 until queried
@@ -347,6 +359,12 @@ tpar_status validate(const Call& c, bool unfused)
         return TPAR_ERR_INVALID_ARG;
     if ((c.flags & TPAR_SCALES_128X4) && (c.fp8 || c.d % 64 != 0))
         return TPAR_ERR_INVALID_ARG;
+    if (c.flags & TPAR_DEBUG_SHRINK) {
+        if (unfused)
+            return TPAR_ERR_INVALID_ARG;
+        if (!kDebugBuild)
+            return TPAR_ERR_UNSUPPORTED;
+    }
     // An empty batch is a no-op: its tensors may be NULL (empty allocations).
     if (c.T == 0)
         return TPAR_OK;
@@ -630,8 +648,10 @@ unsigned flat_grid(int64_t items, int sm_count, const void* fn, int per_thread =
 
 tpar_status launch_quantize(const void* x, int64_t T, int64_t d, uint8_t* codes, uint8_t* scales,
                             float* gscale, uint32_t* ws, bool dynamic, int sm_count, cudaStream_t stream,
-                            bool pdl, bool f16, int sf_tiles)
+                            bool pdl, uint32_t flags)
 {
+    const bool f16 = (flags & TPAR_DTYPE_FP16) != 0;
+    const int sf_tiles = scale_tiles(d, flags);
     QuantArgs q;
     q.x = static_cast<const uint4*>(x);
     q.codes = reinterpret_cast<uint32_t*>(codes);
@@ -642,6 +662,9 @@ tpar_status launch_quantize(const void* x, int64_t T, int64_t d, uint8_t* codes,
     q.f16 = f16;
     q.kb = static_cast<int>(d / 16);
     q.sf_tiles = sf_tiles;
+    q.err = device_error_word();
+    q.n_vec_total = checked_vectors(T, d, flags);
+    q.n_scales = scale_bytes(T, d, flags);
     const void* fn = tpar::quantize_kernel_for(dynamic, f16);
     const unsigned grid = flat_grid(q.nvec / 2, sm_count, fn, 2);  // two 16-element blocks per thread
     if (launch(fn, dim3(grid), dim3(256), &q, stream, 1, pdl) != cudaSuccess)
@@ -671,6 +694,8 @@ FusedArgs fused_args(const Call& c)
     a.inv_d = 1.0f / static_cast<float>(c.d);
     a.f16 = (c.flags & TPAR_DTYPE_FP16) != 0;
     a.sf_tiles = scale_tiles(c.d, c.flags);
+    a.n_vec_total = checked_vectors(c.T, c.d, c.flags);
+    a.n_scales = scale_bytes(c.T, c.d, c.flags);
     return a;
 }
 
@@ -787,8 +812,7 @@ tpar_status fused_impl(const Call& c, const tpar_plan* user_plan, void* user_ws,
     a.scales = nullptr;
     if ((st = launch_fused(a, tpar::kQuantAmax, p, stream, pdl)) != TPAR_OK)
         return st;
-    st = launch_quantize(c.out_norm, c.T, c.d, c.codes, c.scales, c.gscale, ws, true, sm, stream, pdl, a.f16,
-                         a.sf_tiles);
+    st = launch_quantize(c.out_norm, c.T, c.d, c.codes, c.scales, c.gscale, ws, true, sm, stream, pdl, c.flags);
     if (st != TPAR_OK)
         cudaMemsetAsync(ws, 0, 8, stream);  // leave the workspace zeroed
     return st;
@@ -829,7 +853,8 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
 {
     Call c{partials, n_ranks, residual, gamma, eps, T, d, out_norm, out_residual,
            nvfp4_codes, nvfp4_scales, global_scale,
-           flags & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_DTYPE_FP16 | TPAR_SCALES_128X4), reduced};
+           flags & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_DTYPE_FP16 | TPAR_SCALES_128X4 | TPAR_DEBUG_SHRINK),
+           reduced};
     tpar_status st = validate(c, true);
     if (st != TPAR_OK || (flags & TPAR_DRY_RUN))
         return st;
@@ -895,7 +920,7 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
     // K4: the separate NVFP4 quantiser
     if (nvfp4) {
         st = launch_quantize(out_norm, T, d, nvfp4_codes, nvfp4_scales, global_scale, ws, !given, sm, stream,
-                             pdl, (flags & TPAR_DTYPE_FP16) != 0, scale_tiles(d, flags));
+                             pdl, c.flags);
         if (st != TPAR_OK && ws)
             cudaMemsetAsync(ws, 0, 8, stream);
     }
@@ -913,6 +938,8 @@ tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* co
         return TPAR_ERR_INVALID_ARG;
     if ((flags & TPAR_SCALES_128X4) && d % 64 != 0)
         return TPAR_ERR_INVALID_ARG;
+    if ((flags & TPAR_DEBUG_SHRINK) && !kDebugBuild)
+        return TPAR_ERR_UNSUPPORTED;
     if (T == 0)
         return TPAR_OK;  // empty batch: a no-op, tensors may be NULL
     if (!x || !codes || !scales || !global_scale)
@@ -953,8 +980,7 @@ tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* co
         if (cudaLaunchKernelExC(&cfg, ka, args) != cudaSuccess)
             return TPAR_ERR_CUDA;
     }
-    st = launch_quantize(x, T, d, codes, scales, global_scale, ws, !given, sm, stream, pdl,
-                         (flags & TPAR_DTYPE_FP16) != 0, scale_tiles(d, flags));
+    st = launch_quantize(x, T, d, codes, scales, global_scale, ws, !given, sm, stream, pdl, flags);
     if (st != TPAR_OK && ws)
         cudaMemsetAsync(ws, 0, 8, stream);
     return st;
@@ -968,7 +994,7 @@ tpar_status tpar_fused_rmsnorm_fp8(const void* const* partials, int n_ranks, con
     const bool given = (flags & TPAR_GSCALE_GIVEN) != 0;
     Call c{partials, n_ranks, residual, gamma, eps, T, d, out_norm, out_residual, nullptr, nullptr, nullptr,
            flags & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_FORCE_ROW | TPAR_FORCE_CLUSTER | TPAR_DTYPE_FP16 |
-                    TPAR_SCALES_128X4),
+                    TPAR_SCALES_128X4 | TPAR_DEBUG_SHRINK),
            nullptr, true};
     tpar_status st = validate(c, false);
     if (st != TPAR_OK)
@@ -1038,7 +1064,7 @@ tpar_status tpar_fp8_quantize(const void* x, int64_t T, int64_t d, uint8_t* code
         return TPAR_ERR_INVALID_ARG;
     if (d > TPAR_MAX_HIDDEN)
         return TPAR_ERR_UNSUPPORTED;
-    if (T > (INT64_MAX / 4) / d || (flags & TPAR_SCALES_128X4))
+    if (T > (INT64_MAX / 4) / d || (flags & (TPAR_SCALES_128X4 | TPAR_DEBUG_SHRINK)))
         return TPAR_ERR_INVALID_ARG;
     if (T == 0)
         return TPAR_OK;
@@ -1145,6 +1171,8 @@ const char* tpar_status_string(tpar_status s)
 }
 
 int tpar_version(void) { return 100; }
+
+int tpar_debug_build(void) { return kDebugBuild ? 1 : 0; }
 
 }  // extern "C"
 
@@ -1276,6 +1304,6 @@ extern "C" tpar_status tpar_unfused_rmsnorm_noalloc(const void* const* partials,
     // K4: the separate NVFP4 quantiser
     if (nvfp4)
         st = launch_quantize(out_norm, T, d, nvfp4_codes, nvfp4_scales, global_scale, given ? nullptr : ws,
-                             !given, sm, stream, pdl, (fl & TPAR_DTYPE_FP16) != 0, 0);
+                             !given, sm, stream, pdl, fl & TPAR_DTYPE_FP16);
     return st;
 }

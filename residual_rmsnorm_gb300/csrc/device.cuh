@@ -9,7 +9,29 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include "tpar.h"
+
 namespace tpar {
+
+// ---------------------------------------------------------------- debug checks
+
+// Debug builds (-DTPAR_DEBUG) check a computed index against the extent of
+// its buffer before the access: out of range sets TPAR_DEVERR_INDEX in the
+// device error word and the caller skips the access (no trap, no fault, the
+// context stays usable). Release builds compile every check to `true`.
+#ifdef TPAR_DEBUG
+__device__ __forceinline__ bool dbg_in_range(uint32_t* err, int64_t i, int64_t n)
+{
+    if (i >= 0 && i < n)
+        return true;
+    if (err)
+        atomicOr(err, TPAR_DEVERR_INDEX);
+    return false;
+}
+#define TPAR_IN_RANGE(err, i, n) ::tpar::dbg_in_range((err), static_cast<int64_t>(i), static_cast<int64_t>(n))
+#else
+#define TPAR_IN_RANGE(err, i, n) true
+#endif
 
 // ---------------------------------------------------------------- memory
 

@@ -53,6 +53,10 @@ struct FusedArgs {
     float eps;
     float inv_d;
     int sf_tiles;  // 0: scales row-major; else the 128x4 tiled layout with d/64 column tiles
+    // extents checked by debug builds (TPAR_IN_RANGE): 16-byte vectors of a
+    // [T, d] tensor (T * nvec) and scale bytes
+    int64_t n_vec_total;
+    int64_t n_scales;
 };
 
 // Byte offset of the scale of row t, 16-element block c in the 128x4 tiled
@@ -81,6 +85,7 @@ __device__ __forceinline__ void emit_vector(const FusedArgs& a, bool valid, int6
                                             const uint4& gamma8, float rinv, float g_given, float& amax_local)
 {
     float yq[8];
+    const bool in = !valid || TPAR_IN_RANGE(a.err, gv, a.n_vec_total);
     if (valid) {
         float gm[8];
         unpack8_dt(gamma8, gm, F16);
@@ -89,7 +94,7 @@ __device__ __forceinline__ void emit_vector(const FusedArgs& a, bool valid, int6
         for (int e = 0; e < 8; ++e)
             y[e] = h[e] * rinv * gm[e];
         const uint4 yb = pack8_dt(y, F16);
-        if (a.out_norm)
+        if (a.out_norm && in)
             st_v4(a.out_norm + gv, yb);
         unpack8_dt(yb, yq, F16);  // the emitted values, as fp32
     } else {
@@ -109,7 +114,8 @@ __device__ __forceinline__ void emit_vector(const FusedArgs& a, bool valid, int6
             for (int e = 0; e < 8; ++e)
                 q[e] = __fmul_rn(yq[e], g_given);  // g_given holds 1/s here
             const uint2 c = e4m3x8_from_f32(q);
-            asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(a.q8 + gv), "r"(c.x), "r"(c.y) : "memory");
+            if (in)
+                asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(a.q8 + gv), "r"(c.x), "r"(c.y) : "memory");
         }
     }
     if constexpr (QMODE == kQuantGiven) {
@@ -125,9 +131,11 @@ __device__ __forceinline__ void emit_vector(const FusedArgs& a, bool valid, int6
 #pragma unroll
             for (int e = 0; e < 8; ++e)
                 q[e] = __fmul_rn(yq[e], inv);
-            st_u32(a.codes + gv, e2m1x8_from_f32(q));
-            if ((gv & 1) == 0)
-                st_u8(a.scales + scale_index(a.sf_tiles, gv >> 1, t, v), sbyte);
+            if (in)
+                st_u32(a.codes + gv, e2m1x8_from_f32(q));
+            const int64_t si = scale_index(a.sf_tiles, gv >> 1, t, v);
+            if ((gv & 1) == 0 && TPAR_IN_RANGE(a.err, si, a.n_scales))
+                st_u8(a.scales + si, sbyte);
         }
     }
 }
@@ -220,13 +228,15 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT, CLUSTER))
             for (int jj = 0; jj < G; ++jj) {
                 const int v = vbeg + tid + (j0 + jj) * static_cast<int>(blockDim.x);
                 if (v < vend) {
+                    const bool in = TPAR_IN_RANGE(a.err, rowv + v, a.n_vec_total);
 #pragma unroll
                     for (int r = 0; r < NR; ++r)
                         if (r < a.n_ranks)
-                            x[jj][r] = ld_stream(a.partials[r] + rowv + v);
-                    rv[jj] = a.residual ? ld_coherent(a.residual + rowv + v) : make_uint4(0u, 0u, 0u, 0u);
+                            x[jj][r] = in ? ld_stream(a.partials[r] + rowv + v) : make_uint4(0u, 0u, 0u, 0u);
+                    rv[jj] = (a.residual && in) ? ld_coherent(a.residual + rowv + v) : make_uint4(0u, 0u, 0u, 0u);
                     if constexpr (kEarlyGamma)
-                        gv[kEarlyGamma ? j0 + jj : 0] = ld_reuse(a.gamma + v);
+                        gv[kEarlyGamma ? j0 + jj : 0] =
+                            TPAR_IN_RANGE(a.err, v, a.nvec) ? ld_reuse(a.gamma + v) : make_uint4(0u, 0u, 0u, 0u);
                 }
             }
 #pragma unroll
@@ -245,7 +255,7 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT, CLUSTER))
 #pragma unroll
                     for (int e = 0; e < 8; ++e)
                         ss[j] = fmaf(h[j][e], h[j][e], ss[j]);
-                    if (!CLUSTER && a.out_residual)
+                    if (!CLUSTER && a.out_residual && TPAR_IN_RANGE(a.err, rowv + v, a.n_vec_total))
                         st_v4(a.out_residual + rowv + v, pack8_dt(h[j], F16));
                 } else {
 #pragma unroll
@@ -263,7 +273,7 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT, CLUSTER))
             for (int j = 0; j < VPT; ++j) {
                 const float s = warp_sum(ss[j]);
                 const int w = (j * static_cast<int>(blockDim.x) + 32 * warp) >> 5;
-                if (lane == 0 && 32 * w < vend)
+                if (lane == 0 && 32 * w < vend && TPAR_IN_RANGE(a.err, w, kMaxRowWarps))
                     wsh[buf][w] = s;
             }
             __syncthreads();
@@ -280,12 +290,12 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT, CLUSTER))
             for (int j = 0; j < VPT; ++j) {
                 const float s = warp_sum(ss[j]);
                 const int v0 = vbeg + j * static_cast<int>(blockDim.x) + 32 * warp;
-                if (v0 < vend && lane < split)
+                if (v0 < vend && lane < split && TPAR_IN_RANGE(a.err, v0 >> 5, kMaxRowWarps))
                     st_async_f32(cluster_addr(smem_addr(&wsh[buf][v0 >> 5]), static_cast<uint32_t>(lane)), s,
                                  cluster_addr(bar, static_cast<uint32_t>(lane)));
             }
             if (!mbar_wait_parity_bounded(bar, parity, 200ull * 1000 * 1000) && a.err && tid == 0)
-                atomicOr(a.err, 1u);
+                atomicOr(a.err, TPAR_DEVERR_CLUSTER_WAIT);
             tot = canonical_row_sum(wsh[buf], nW, lane);
             cluster_arrive_relaxed();
         }
@@ -300,12 +310,12 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT, CLUSTER))
             if (valid) {
                 if constexpr (kEarlyGamma)
                     gm = gv[kEarlyGamma ? j : 0];
-                else
+                else if (TPAR_IN_RANGE(a.err, v, a.nvec))
                     gm = ld_reuse(a.gamma + v);
                 // The cluster form stores the residual only now: a store
                 // issued before the exchange would delay it (measured); the
                 // bandwidth form gains from issuing it early.
-                if (CLUSTER && a.out_residual)
+                if (CLUSTER && a.out_residual && TPAR_IN_RANGE(a.err, rowv + v, a.n_vec_total))
                     st_v4(a.out_residual + rowv + v, pack8_dt(h[j], F16));
             }
             emit_vector<QMODE, F16>(a, valid, rowv + v, t, v, h[j], gm, rinv, g_given, amax_local);
@@ -334,6 +344,9 @@ struct QuantArgs {
     bool f16;            // host: x is binary16 (picks the F16 instantiation)
     int kb;              // blocks per row, d / 16
     int sf_tiles;        // 0: scales row-major; else 128x4 tiles, d / 64 per 128 rows
+    uint32_t* err;       // device error word (debug index checks) or null
+    int64_t n_vec_total; // extents checked by debug builds: vectors of x, scale bytes
+    int64_t n_scales;
 };
 
 // Quantise one 16-element block b (the 16-byte vectors 2b and 2b + 1) with
@@ -345,6 +358,7 @@ __device__ __forceinline__ void quantize_block(const QuantArgs& a, float g, int6
     float x[16];
     unpack8_dt(lo, x, F16);
     unpack8_dt(hi, x + 8, F16);
+    const bool in = TPAR_IN_RANGE(a.err, 2 * b + 1, a.n_vec_total);
     float bmax = 0.0f;
 #pragma unroll
     for (int e = 0; e < 16; ++e)
@@ -355,13 +369,15 @@ __device__ __forceinline__ void quantize_block(const QuantArgs& a, float g, int6
 #pragma unroll
     for (int e = 0; e < 16; ++e)
         q[e] = __fmul_rn(x[e], inv);
-    st_v2(a.codes + 2 * b, e2m1x8_from_f32(q), e2m1x8_from_f32(q + 8));
+    if (in)
+        st_v2(a.codes + 2 * b, e2m1x8_from_f32(q), e2m1x8_from_f32(q + 8));
     int64_t si = b;
     if (a.sf_tiles) {
         const int64_t t = b / a.kb;
         si = scale_offset_128x4(t, static_cast<int>(b - t * a.kb), a.sf_tiles);
     }
-    st_u8(a.scales + si, sbyte);
+    if (TPAR_IN_RANGE(a.err, si, a.n_scales))
+        st_u8(a.scales + si, sbyte);
 }
 
 // A thread owns two 16-element blocks per iteration (b and b + stride; the
@@ -397,7 +413,7 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __grid_consta
 #pragma unroll
         for (int u = 0; u < 2; ++u) {
             const int64_t bu = b0 + u * stride;
-            if (bu < nblocks) {
+            if (bu < nblocks && TPAR_IN_RANGE(a.err, 2 * bu + 1, a.n_vec_total)) {
                 // the second load hits the lines the first brought into L1
                 v[u][0] = ld_reuse(a.x + 2 * bu);
                 v[u][1] = ld_reuse(a.x + 2 * bu + 1);

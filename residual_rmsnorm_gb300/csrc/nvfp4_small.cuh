@@ -78,12 +78,14 @@ __global__ void __launch_bounds__(512) nvfp4_small_kernel(const __grid_constant_
             const int i = tid + (g0 + gg) * B;
             if (i < items) {
                 const int64_t gv = static_cast<int64_t>(i / slice) * a.nvec + vbeg + i % slice;
+                const bool in = TPAR_IN_RANGE(a.err, gv, a.n_vec_total);
 #pragma unroll
                 for (int r = 0; r < NR; ++r)
                     if (r < a.n_ranks)
-                        x[gg][r] = ld_stream(a.partials[r] + gv);
-                rv[gg] = a.residual ? ld_coherent(a.residual + gv) : make_uint4(0u, 0u, 0u, 0u);
-                gm[g0 + gg] = ld_reuse(a.gamma + vbeg + i % slice);
+                        x[gg][r] = in ? ld_stream(a.partials[r] + gv) : make_uint4(0u, 0u, 0u, 0u);
+                rv[gg] = (a.residual && in) ? ld_coherent(a.residual + gv) : make_uint4(0u, 0u, 0u, 0u);
+                gm[g0 + gg] = TPAR_IN_RANGE(a.err, vbeg + i % slice, a.nvec) ? ld_reuse(a.gamma + vbeg + i % slice)
+                                                                             : make_uint4(0u, 0u, 0u, 0u);
             }
         }
 #pragma unroll
@@ -117,14 +119,15 @@ __global__ void __launch_bounds__(512) nvfp4_small_kernel(const __grid_constant_
     for (int j = 0; j < IPT; ++j) {
         const float s = warp_sum(ss[j]);
         const int i0 = j * B + 32 * warp;
-        if (i0 < items && lane < K) {
+        if (i0 < items && lane < K && TPAR_IN_RANGE(a.err, i0 / slice, kSmallMaxRows) &&
+            TPAR_IN_RANGE(a.err, (vbeg + i0 % slice) >> 5, kMaxRowWarps)) {
             const int w = (vbeg + i0 % slice) >> 5;
             st_async_f32(cluster_addr(smem_addr(&xrow[i0 / slice][w]), static_cast<uint32_t>(lane)), s,
                          cluster_addr(bar0, static_cast<uint32_t>(lane)));
         }
     }
     if (!mbar_wait_parity_bounded(bar0, 0u, 200ull * 1000 * 1000) && a.err && tid == 0)
-        atomicOr(a.err, 4u);
+        atomicOr(a.err, TPAR_DEVERR_SMALL_WAIT);
     for (int r = warp; r < T; r += nwarps) {
         const float tot = canonical_row_sum(xrow[r], nW, lane);
         if (lane == 0)
@@ -145,9 +148,10 @@ __global__ void __launch_bounds__(512) nvfp4_small_kernel(const __grid_constant_
             for (int e = 0; e < 8; ++e)
                 y[e] = h[j][e] * rinv * gmf[e];
             const uint4 yb = pack8_dt(y, F16);
-            if (a.out_residual)
+            const bool in = TPAR_IN_RANGE(a.err, gv, a.n_vec_total);
+            if (a.out_residual && in)
                 st_v4(a.out_residual + gv, pack8_dt(h[j], F16));
-            if (a.out_norm)
+            if (a.out_norm && in)
                 st_v4(a.out_norm + gv, yb);
             unpack8_dt(yb, h[j], F16);  // h now holds the emitted values
 #pragma unroll
@@ -172,12 +176,12 @@ __global__ void __launch_bounds__(512) nvfp4_small_kernel(const __grid_constant_
         const float cm = warp_max(lane < nwarps ? wmax[lane] : 0.0f);
         if (lane == 0)
             mbar_arrive_expect_tx(bar1, 4u * static_cast<uint32_t>(K));
-        if (lane < K)
+        if (lane < K && TPAR_IN_RANGE(a.err, k, kSmallMaxRanks))
             st_async_f32(cluster_addr(smem_addr(&xmax[k]), static_cast<uint32_t>(lane)), cm,
                          cluster_addr(bar1, static_cast<uint32_t>(lane)));
     }
     if (!mbar_wait_parity_bounded(bar1, 0u, 200ull * 1000 * 1000) && a.err && tid == 0)
-        atomicOr(a.err, 4u);
+        atomicOr(a.err, TPAR_DEVERR_SMALL_WAIT);
     float amax = 0.0f;
     for (int p = 0; p < K; ++p)
         amax = fmaxf(amax, xmax[p]);
@@ -205,9 +209,11 @@ __global__ void __launch_bounds__(512) nvfp4_small_kernel(const __grid_constant_
 #pragma unroll
             for (int e = 0; e < 8; ++e)
                 q[e] = __fmul_rn(h[j][e], inv);
-            st_u32(a.codes + gv, e2m1x8_from_f32(q));
-            if ((gv & 1) == 0)
-                st_u8(a.scales + scale_index(a.sf_tiles, gv >> 1, t, v), sbyte);
+            if (TPAR_IN_RANGE(a.err, gv, a.n_vec_total))
+                st_u32(a.codes + gv, e2m1x8_from_f32(q));
+            const int64_t si = scale_index(a.sf_tiles, gv >> 1, t, v);
+            if ((gv & 1) == 0 && TPAR_IN_RANGE(a.err, si, a.n_scales))
+                st_u8(a.scales + si, sbyte);
         }
     }
     cluster_wait_acquire();  // no CTA leaves while a peer may still push to it

@@ -76,6 +76,7 @@ __global__ void __launch_bounds__(1024) rows_prefetch_kernel(const __grid_consta
     const int nsrc = a.n_ranks + (a.residual ? 1 : 0);
     const int64_t G = gridDim.x;
     const int nW = (nvec + 31) >> 5;
+    const int64_t ring_vecs = static_cast<int64_t>(S) * nsrc * nvec;  // extent checked by debug builds
     __shared__ float wsh[2][kMaxRowWarps];  // per-32-vector partial sums of squares, by row parity
 
     // copy this thread's vectors of row t (every source) into stage s
@@ -86,7 +87,8 @@ __global__ void __launch_bounds__(1024) rows_prefetch_kernel(const __grid_consta
 #pragma unroll
             for (int j = 0; j < VPT; ++j) {
                 const int v = tid + j * B;
-                if (v < nvec) {
+                if (v < nvec && TPAR_IN_RANGE(a.err, rowv + v, a.n_vec_total) &&
+                    TPAR_IN_RANGE(a.err, (static_cast<int64_t>(s) * nsrc + nsrc - 1) * nvec + v, ring_vecs)) {
 #pragma unroll
                     for (int r = 0; r < NR; ++r)
                         if (r < a.n_ranks)
@@ -110,7 +112,7 @@ __global__ void __launch_bounds__(1024) rows_prefetch_kernel(const __grid_consta
 #pragma unroll
     for (int j = 0; j < VPT; ++j) {
         const int v = tid + j * B;
-        gam[j] = v < nvec ? ld_reuse(a.gamma + v) : make_uint4(0u, 0u, 0u, 0u);
+        gam[j] = (v < nvec && TPAR_IN_RANGE(a.err, v, a.nvec)) ? ld_reuse(a.gamma + v) : make_uint4(0u, 0u, 0u, 0u);
     }
     float amax_local = 0.0f;
 
@@ -151,7 +153,7 @@ __global__ void __launch_bounds__(1024) rows_prefetch_kernel(const __grid_consta
 #pragma unroll
             for (int j = 0; j < VPT; ++j) {
                 const int v = tid + j * B;
-                if (v < nvec)
+                if (v < nvec && TPAR_IN_RANGE(a.err, rowv + v, a.n_vec_total))
                     st_v4(a.out_residual + rowv + v, pack8_dt(h[j], F16));
             }
         }
@@ -162,7 +164,7 @@ __global__ void __launch_bounds__(1024) rows_prefetch_kernel(const __grid_consta
         for (int j = 0; j < VPT; ++j) {
             const float sj = warp_sum(ss[j]);
             const int w = (j * B + 32 * warp) >> 5;
-            if (lane == 0 && 32 * w < nvec)
+            if (lane == 0 && 32 * w < nvec && TPAR_IN_RANGE(a.err, w, kMaxRowWarps))
                 wsh[buf][w] = sj;
         }
         __syncthreads();

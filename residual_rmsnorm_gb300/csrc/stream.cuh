@@ -103,8 +103,15 @@ __global__ void __launch_bounds__(544, 1) stream_rmsnorm_kernel(const __grid_con
                         break;
                     }
                     const uint4* src = (j < a.n_ranks ? a.partials[j] : a.residual) + t * static_cast<int64_t>(nvec);
-                    mbar_arrive_expect_tx(full, row_bytes);
-                    bulk_g2s(ring0 + static_cast<uint32_t>(s) * row_bytes, src, row_bytes, full);
+                    // debug builds check the row read and the stage written; a
+                    // skipped copy completes its stage by a plain arrive
+                    if (TPAR_IN_RANGE(a.err, t * static_cast<int64_t>(nvec) + nvec - 1, a.n_vec_total) &&
+                        TPAR_IN_RANGE(a.err, s, S)) {
+                        mbar_arrive_expect_tx(full, row_bytes);
+                        bulk_g2s(ring0 + static_cast<uint32_t>(s) * row_bytes, src, row_bytes, full);
+                    } else {
+                        mbar_arrive(full);
+                    }
                     ++issued;
                     if (++s == S) {
                         s = 0;
@@ -116,7 +123,7 @@ __global__ void __launch_bounds__(544, 1) stream_rmsnorm_kernel(const __grid_con
             }
             if (!ok) {
                 if (a.err)
-                    atomicOr(a.err, 2u);
+                    atomicOr(a.err, TPAR_DEVERR_STREAM_WAIT);
                 *reinterpret_cast<volatile int*>(&abort_flag) = 1;
             }
             // Drain: no copy of ours may still be in flight when the CTA exits.
@@ -164,7 +171,7 @@ __global__ void __launch_bounds__(544, 1) stream_rmsnorm_kernel(const __grid_con
             if (ok && !mbar_wait_parity_bounded(full, round & 1u, kStreamWaitNs)) {
                 ok = false;
                 if (a.err && lane == 0)
-                    atomicOr(a.err, 2u);
+                    atomicOr(a.err, TPAR_DEVERR_STREAM_WAIT);
                 *reinterpret_cast<volatile int*>(&abort_flag) = 1;
             }
             const uint4* stage = reinterpret_cast<const uint4*>(ring + static_cast<size_t>(s) * row_bytes);
@@ -196,12 +203,12 @@ __global__ void __launch_bounds__(544, 1) stream_rmsnorm_kernel(const __grid_con
 #pragma unroll
                 for (int e = 0; e < 8; ++e)
                     ss = fmaf(h[j][e], h[j][e], ss);
-                if (a.out_residual)
+                if (a.out_residual && TPAR_IN_RANGE(a.err, rowv + v, a.n_vec_total))
                     st_v4(a.out_residual + rowv + v, pack8_dt(h[j], F16));
             }
             ss = warp_sum(ss);
             const int w = (j * C + 32 * cwarp) >> 5;
-            if (lane == 0 && 32 * w < nvec)
+            if (lane == 0 && 32 * w < nvec && TPAR_IN_RANGE(a.err, w, kMaxRowWarps))
                 wsh[buf][w] = ss;
         }
         if (c == 0)

@@ -1,0 +1,142 @@
+"""Every kernel form through the index-checking debug build (TPAR_DEBUG=1).
+
+Run as a script with TPAR_DEBUG=1 in the environment (tests/test_debug_gpu.py
+does). Each call's computed global and shared-memory indices are checked
+against their buffers inside the kernels; the device error word must stay 0
+and the results must match the oracle. Then the checks check themselves:
+with TPAR_DEBUG_SHRINK the [T, d] extent is one vector short, so the last
+vector's accesses must be reported (TPAR_DEVERR_INDEX) and skipped, leaving
+that vector's outputs untouched while every other row equals a plain call.
+"""
+import os
+import sys
+
+import numpy as np
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, os.path.dirname(HERE))
+sys.path.insert(0, HERE)
+
+import synth  # noqa: E402
+from gpu_helpers import (assert_close_to_ref, assert_nvfp4_bit_exact, lib, oracle_rows,  # noqa: E402
+                         to_device)
+
+
+def expect_clean(tp, what):
+    code = tp.tpar_device_error(torch.cuda.current_device())
+    assert code == 0, f"{what}: device error word {code:#x}"
+
+
+def fused_cases(tp):
+    P = tp.TparPlan
+    g = torch.tensor([0.03], dtype=torch.float32, device="cuda")
+    # name, N, T, d, fused_rmsnorm keyword arguments
+    return [
+        ("row", 8, 37, 8192, dict(flags=tp.TPAR_FORCE_ROW)),
+        ("row vpt8", 3, 9, 32768, dict(flags=tp.TPAR_FORCE_ROW)),
+        ("cluster", 8, 8, 4096, dict()),
+        ("cluster 16", 4, 3, 8192, dict(plan=P(1, 16, 64, 1, 3))),
+        ("rows prefetch", 4, 400, 2048, dict()),
+        ("rows prefetch 4 stages", 2, 301, 2048, dict(plan=P(3, 1, 256, 1, 19))),
+        ("rows prefetch vpt2", 2, 300, 16384, dict()),
+        ("stream", 4, 70, 4096, dict(flags=tp.TPAR_FORCE_STREAM)),
+        ("nvfp4 single launch", 4, 8, 8192, dict(nvfp4=True)),
+        ("nvfp4 two pass", 4, 333, 4096, dict(nvfp4=True)),
+        ("nvfp4 given", 4, 40, 4096, dict(nvfp4=True, global_scale=g)),
+        ("nvfp4 given 128x4", 4, 300, 4096, dict(nvfp4=True, global_scale=g, scales_128x4=True)),
+        ("nvfp4 dynamic 128x4", 2, 7, 8192, dict(nvfp4=True, scales_128x4=True)),
+        ("ragged", 5, 3, 8200, dict()),
+        ("no residual", 3, 260, 2048, dict(residual=None)),
+    ]
+
+
+def run_fused(tp):
+    for name, n, T, d, kw in fused_cases(tp):
+        w = synth.Workload(name, n, T, d, 1e-5, 0.5, seed=T + d + n)
+        inputs = synth.make_inputs(w)
+        residual = True
+        if "residual" in kw:
+            kw = dict(kw)
+            kw.pop("residual")
+            inputs = dict(inputs, residual=None)
+            residual = False
+        dev = to_device(inputs)
+        out = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, **kw)
+        torch.cuda.synchronize()
+        expect_clean(tp, name)
+        rows = np.unique([0, T // 2, T - 1])
+        ref = oracle_rows(inputs, rows, w.eps, residual=residual)
+        assert_close_to_ref(out["out_norm"][rows], ref["y"], name)
+        if kw.get("nvfp4"):
+            given = None if kw.get("global_scale") is None else float(np.float32(0.03))
+            assert_nvfp4_bit_exact(out["out_norm"], out["codes"], out["scales"], out["global_scale"],
+                                   given=given, what=name, scales_128x4=kw.get("scales_128x4", False))
+    # the other entry points
+    w = synth.NVFP4.with_(T=200, d=4096)
+    inputs = synth.make_inputs(w)
+    dev = to_device(inputs)
+    tp.unfused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True)
+    tp.fused_rmsnorm_fp8(dev["partials"], dev["residual"], dev["gamma"], w.eps)
+    tp.allreduce_sum(dev["partials"], dev["residual"])
+    tp.nvfp4_quantize(dev["partials"][0], scales_128x4=True)
+    tp.fp8_quantize(dev["partials"][0])
+    f16 = to_device(synth.make_inputs(w, dtype=torch.float16))
+    tp.fused_rmsnorm(f16["partials"], f16["residual"], f16["gamma"], w.eps, nvfp4=True)
+    torch.cuda.synchronize()
+    expect_clean(tp, "other entry points")
+
+
+def run_shrink(tp):
+    """TPAR_DEBUG_SHRINK: the last vector of the [T, d] tensors is out of the
+    checked extent."""
+    P = tp.TparPlan
+    forms = [("row", dict(flags=tp.TPAR_FORCE_ROW)), ("cluster", dict(flags=tp.TPAR_FORCE_CLUSTER)),
+             ("rows prefetch", dict(plan=P(3, 1, 256, 1, 152))), ("stream", dict(flags=tp.TPAR_FORCE_STREAM)),
+             ("nvfp4 single launch", dict(nvfp4=True)), ("nvfp4 two pass", dict(nvfp4=True, flags=tp.TPAR_FORCE_ROW))]
+    T, d, n = 6, 2048, 4
+    w = synth.Workload("shrink", n, T, d, 1e-5, 0.5, seed=3)
+    dev = to_device(synth.make_inputs(w))
+    for name, kw in forms:
+        kw = dict(kw)
+        base = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, **kw)
+        torch.cuda.synchronize()
+        expect_clean(tp, name + " plain")
+        on = torch.full((T, d), 7.0, dtype=torch.bfloat16, device="cuda")
+        orr = torch.full((T, d), 7.0, dtype=torch.bfloat16, device="cuda")
+        kw["flags"] = kw.get("flags", 0) | tp.TPAR_DEBUG_SHRINK
+        out = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, out_norm=on,
+                               out_residual=orr, **kw)
+        torch.cuda.synchronize()
+        code = tp.tpar_device_error(torch.cuda.current_device())
+        assert code & tp.TPAR_DEVERR_INDEX, f"{name}: the shrunk extent was not reported ({code:#x})"
+        # the last 16-byte vector (8 elements) was never written
+        assert torch.all(on[T - 1, d - 8:] == 7.0) and torch.all(orr[T - 1, d - 8:] == 7.0), name
+        # rows before the last are the plain call's bits
+        assert torch.equal(on[:T - 1].view(torch.int16), base["out_norm"][:T - 1].view(torch.int16)), name
+        assert torch.equal(orr[:T - 1].view(torch.int16), base["out_residual"][:T - 1].view(torch.int16)), name
+        if kw.get("nvfp4"):
+            assert torch.equal(out["codes"][:T - 1], base["codes"][:T - 1]), name
+    # the standalone quantiser: the last vector's codes are skipped
+    x = dev["partials"][0]
+    codes, _, _ = tp.nvfp4_quantize(x)
+    torch.cuda.synchronize()
+    expect_clean(tp, "quantiser plain")
+    c2, _, _ = tp.nvfp4_quantize(x, flags=tp.TPAR_DEBUG_SHRINK)
+    torch.cuda.synchronize()
+    assert tp.tpar_device_error(torch.cuda.current_device()) & tp.TPAR_DEVERR_INDEX
+    assert torch.equal(c2[:T - 1], codes[:T - 1])
+
+
+def main():
+    assert os.environ.get("TPAR_DEBUG") == "1", "run with TPAR_DEBUG=1"
+    tp = lib()
+    assert tp.tpar_debug_build(), "the debug library did not load"
+    expect_clean(tp, "start")
+    run_fused(tp)
+    run_shrink(tp)
+    print("debug checks passed")
+
+
+if __name__ == "__main__":
+    main()

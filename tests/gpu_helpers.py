@@ -17,9 +17,10 @@ def need_gpu():
 
 def lib():
     need_gpu()
+    import os
     import residual_rmsnorm_gb300 as tp
     from residual_rmsnorm_gb300 import build
-    build.build()
+    build.build(debug=os.environ.get("TPAR_DEBUG") == "1")
     tp.library()
     tp.tpar_init(torch.cuda.current_device())
     return tp

@@ -308,3 +308,19 @@ def test_scales_128x4_checks(tp):
                                   BASE + 160 * MB, BASE + 200 * MB, BASE + 240 * MB, D | S, 0, check=False)
     assert f == INVALID
     assert tp.tpar_fp8_quantize(BASE, 8, 4096, BASE + 64 * MB, BASE + 80 * MB, D | S, 0, check=False) == INVALID
+
+
+def test_debug_build_exports_the_same_abi(tp):
+    """libtpar_debug.so (-DTPAR_DEBUG) builds and exports exactly the
+    header's functions; only it reports itself as a debug build, and the
+    release library refuses the debug self-test flag."""
+    from residual_rmsnorm_gb300 import build
+    path = build.build(debug=True)
+    out = subprocess.run(["nm", "-D", "--defined-only", path], capture_output=True, text=True).stdout
+    assert set(re.findall(r" T (tpar_\w+)", out)) == set(declared_functions())
+    dbg = ctypes.CDLL(path)
+    assert dbg.tpar_debug_build() == 1
+    assert tp.tpar_debug_build() is False
+    assert call(tp, flags=tp.TPAR_DRY_RUN | tp.TPAR_DEBUG_SHRINK) == UNSUPPORTED
+    assert tp.tpar_fp8_quantize(BASE, 8, 4096, BASE + 64 * MB, BASE + 80 * MB,
+                                tp.TPAR_DRY_RUN | tp.TPAR_DEBUG_SHRINK, 0, check=False) == INVALID
