@@ -81,6 +81,15 @@ typedef void* tpar_stream_t;
                                    instead of bf16 (accumulation stays fp32) */
 #define TPAR_SCALES_128X4 0x80u /* NVFP4 scales in the 128x4 tiled layout that
                                    block-scaled GEMMs read, see below         */
+#define TPAR_FORCE_GRID 0x200u  /* dynamic-scale NVFP4 in ONE cooperative launch:
+                                   each CTA keeps its rows' emitted values in
+                                   shared memory across a bounded grid barrier
+                                   (no out_norm re-read). Rows of d <= 8192
+                                   with ceil(T / SMs) of them within 200 KB,
+                                   else
+                                   TPAR_ERR_UNSUPPORTED; other calls
+                                   TPAR_ERR_INVALID_ARG. Bit-identical to the
+                                   default path, which measured faster       */
 #define TPAR_DEBUG_SHRINK 0x100u /* debug builds only (tpar_debug_build() == 1),
                                    fused entry points and tpar_nvfp4_quantize:
                                    check [T, d] accesses against one vector
@@ -101,6 +110,8 @@ typedef void* tpar_stream_t;
 #define TPAR_DEVERR_INDEX 0x8u        /* debug builds: a computed index failed
                                          its bounds check; the access was
                                          skipped                              */
+#define TPAR_DEVERR_GRID_WAIT 0x10u   /* the grid barrier of the cooperative
+                                         single-launch NVFP4 kernel timed out */
 
 /*
  * TPAR_SCALES_128X4 (NVFP4 outputs only; d % 64 == 0). The pages name only

@@ -12,6 +12,7 @@ from __future__ import annotations
 
 from ._abi import (  # noqa: F401
     TPAR_FORCE_CLUSTER,
+    TPAR_FORCE_GRID,
     TPAR_FORCE_ROW,
     TPAR_FORCE_STREAM,
     TPAR_DTYPE_FP16,

@@ -24,7 +24,7 @@ LIB = os.path.join(BUILD, "libtpar.so")
 BUILD_DEBUG = os.path.join(HERE, "_build_debug")
 LIB_DEBUG = os.path.join(BUILD_DEBUG, "libtpar_debug.so")
 SOURCES = ["api.cu"] + [f"kernels_q{q}_{t}.cu" for q in range(4) for t in ("bf16", "fp16")] + [
-    "kernels_stream_bf16.cu", "kernels_stream_fp16.cu", "kernels_small.cu", "unfused.cu"]
+    "kernels_stream_bf16.cu", "kernels_stream_fp16.cu", "kernels_small.cu", "kernels_grid.cu", "unfused.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -12,6 +12,7 @@
 
 #include "dispatch.h"
 #include "kernels.cuh"
+#include "nvfp4_grid.cuh"
 #include "nvfp4_small.cuh"
 #include "rows.cuh"
 #include "stream.cuh"
@@ -200,7 +201,7 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 int forced_kernels(uint32_t flags)
 {
     return ((flags & TPAR_FORCE_ROW) != 0) + ((flags & TPAR_FORCE_CLUSTER) != 0) +
-           ((flags & TPAR_FORCE_STREAM) != 0);
+           ((flags & TPAR_FORCE_STREAM) != 0) + ((flags & TPAR_FORCE_GRID) != 0);
 }
 
 // Ring depth of the stream kernel for rows of row_bytes: ~192 KB of shared
@@ -382,6 +383,8 @@ tpar_status validate(const Call& c, bool unfused)
         return TPAR_ERR_INVALID_ARG;
     if ((c.flags & TPAR_SCALES_128X4) && !nvfp4)
         return TPAR_ERR_INVALID_ARG;
+    if ((c.flags & TPAR_FORCE_GRID) && (!nvfp4 || given || unfused))
+        return TPAR_ERR_INVALID_ARG;  // the cooperative path is the dynamic-scale NVFP4 one
     if (!nvfp4 && !c.fp8 && given)
         return TPAR_ERR_INVALID_ARG;
     // out_norm may be NULL for NVFP4 with a given scale, or (fused entry points,
@@ -750,6 +753,97 @@ tpar_status launch_small_nvfp4(const FusedArgs& a, float* gscale, int K, int sli
                : TPAR_ERR_CUDA;
 }
 
+// Shape of the cooperative single-launch dynamic-NVFP4 path (nvfp4_grid.cuh,
+// TPAR_FORCE_GRID): at most one CTA per SM (grid = min(T, SMs)), each
+// buffering its ceil(T / grid) rows of emitted values in shared memory.
+// False when a row needs more than kGridMaxVpt vectors per thread or the
+// rows do not fit the buffer. Not planned automatically: measured slower
+// than phase A + phase B on GB300 at every T from 17 to 1824 except 256
+// (N=4, d=8192, 100-call graphs: 6.70 vs 5.35 us at T=17, 8.46 vs 8.33 at
+// 128, 12.0 vs 12.2 at 256, 29.2 vs 25.0 at 1024, 51.3 vs 40.5 at 1824): a
+// cooperative launch cannot start early under PDL, and its rows get no
+// prefetch.
+bool grid_nvfp4_shape(int64_t T, int64_t d, int n_ranks, int sm_count, int* grid, int* rows, int* threads, int* vpt)
+{
+    const int64_t nvec = d / 8;
+    if (T < 1)
+        return false;
+    const int nr = tpar::rank_bound(n_ranks);
+    int v = 1;
+    while (v <= tpar::kGridMaxVpt && ceil_div(nvec, v) > tpar::fused_thread_cap(nr, v, false))
+        v *= 2;
+    if (v > tpar::kGridMaxVpt)
+        return false;
+    const int64_t g = std::min<int64_t>(T, sm_count);
+    const int64_t r = ceil_div(T, g);
+    if (r * nvec * 16 > tpar::kGridSmemBudget)
+        return false;
+    *grid = static_cast<int>(g);
+    *rows = static_cast<int>(r);
+    *vpt = v;
+    *threads = static_cast<int>(ceil_div(ceil_div(nvec, v), 32) * 32);
+    return true;
+}
+
+// Whether one CTA of `fn` with `threads` threads and the full row buffer
+// fits an SM (checked once per kernel and CTA size): then a grid of at most
+// one CTA per SM is co-resident, as the cooperative launch requires.
+bool grid_kernel_fits(const void* fn, int threads)
+{
+    static std::mutex mu;
+    static const void* keys[64];
+    static int thr[64];
+    static bool vals[64];
+    static int used = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (keys[i] == fn && thr[i] == threads)
+            return vals[i];
+    int occ = 0;
+    const bool ok = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, threads, tpar::kGridSmemBudget) ==
+                        cudaSuccess &&
+                    occ >= 1;
+    if (!ok)
+        cudaGetLastError();
+    if (used < 64) {
+        keys[used] = fn;
+        thr[used] = threads;
+        vals[used++] = ok;
+    }
+    return ok;
+}
+
+tpar_status launch_grid_nvfp4(const FusedArgs& a, float* gscale, uint32_t* ws, int grid, int rows, int threads,
+                              int vpt, cudaStream_t stream)
+{
+    const void* fn = tpar::grid_kernel_for(tpar::rank_bound(a.n_ranks), vpt, a.f16);
+    if (!fn)
+        return TPAR_ERR_UNSUPPORTED;
+    if (set_attr_once(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, tpar::kGridSmemBudget) != cudaSuccess)
+        return TPAR_ERR_CUDA;
+    if (!grid_kernel_fits(fn, threads))
+        return TPAR_ERR_UNSUPPORTED;
+    tpar::GridArgs ga;
+    ga.f = a;
+    ga.f.err = device_error_word();
+    ga.gscale = gscale;
+    ga.ws = ws;
+    ga.rows = rows;
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof cfg);
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(static_cast<unsigned>(threads));
+    cfg.dynamicSmemBytes = static_cast<size_t>(rows) * a.nvec * 16;
+    cfg.stream = stream;
+    cudaLaunchAttribute at;
+    at.id = cudaLaunchAttributeCooperative;  // every CTA resident: the grid barrier can complete
+    at.val.cooperative = 1;
+    cfg.attrs = &at;
+    cfg.numAttrs = 1;
+    void* args[1] = {&ga};
+    return cudaLaunchKernelExC(&cfg, fn, args) == cudaSuccess ? TPAR_OK : TPAR_ERR_CUDA;
+}
+
 tpar_status fused_impl(const Call& c, const tpar_plan* user_plan, void* user_ws, cudaStream_t stream)
 {
     tpar_status st = validate(c, false);
@@ -802,11 +896,19 @@ tpar_status fused_impl(const Call& c, const tpar_plan* user_plan, void* user_ws,
         a.slice = slice;
         return launch_small_nvfp4(a, c.gscale, K, slice, threads, ipt, stream, pdl);
     }
-    // Dynamic global scale: phase A (the fused pass, folding |out_norm| into
-    // the device amax), then phase B (quantise out_norm, publish g, reset).
     uint32_t* ws = nullptr;
     if ((st = workspace_for(user_ws, stream, &ws)) != TPAR_OK)
         return st;
+    // On request: one cooperative launch buffers the rows in shared memory
+    // across a grid barrier (no out_norm re-read, no second launch).
+    if (c.flags & TPAR_FORCE_GRID) {
+        int gg = 0, grows = 0, gthreads = 0, gvpt = 0;
+        if (!grid_nvfp4_shape(c.T, c.d, c.n_ranks, sm, &gg, &grows, &gthreads, &gvpt))
+            return TPAR_ERR_UNSUPPORTED;
+        return launch_grid_nvfp4(a, c.gscale, ws, gg, grows, gthreads, gvpt, stream);
+    }
+    // Dynamic global scale: phase A (the fused pass, folding |out_norm| into
+    // the device amax), then phase B (quantise out_norm, publish g, reset).
     a.amax_bits = ws;
     a.codes = nullptr;
     a.scales = nullptr;

@@ -66,6 +66,10 @@ inline const void* stream_kernel_for(int qmode, int nr, int vpt, bool f16)
 // nr and ipt items per thread (1, 2, 4).
 const void* small_kernel_for(int nr, int ipt, bool f16);
 
+// Cooperative single-launch dynamic-scale NVFP4 kernel (nvfp4_grid.cuh) for
+// rank bound nr and vpt (1, 2) vectors per thread.
+const void* grid_kernel_for(int nr, int vpt, bool f16);
+
 const void* reduce_kernel_for(int nr, bool f16);
 const void* residual_add_kernel_ptr(bool f16);
 const void* quantize_kernel_for(bool dynamic, bool f16);

@@ -42,6 +42,9 @@ def fused_cases(tp):
         ("rows prefetch vpt2", 2, 300, 16384, dict()),
         ("stream", 4, 70, 4096, dict(flags=tp.TPAR_FORCE_STREAM)),
         ("nvfp4 single launch", 4, 8, 8192, dict(nvfp4=True)),
+        ("nvfp4 cooperative grid", 4, 100, 4096, dict(nvfp4=True, flags=tp.TPAR_FORCE_GRID)),
+        ("nvfp4 cooperative grid, rows buffered", 8, 400, 2048,
+         dict(nvfp4=True, scales_128x4=True, flags=tp.TPAR_FORCE_GRID)),
         ("nvfp4 two pass", 4, 333, 4096, dict(nvfp4=True)),
         ("nvfp4 given", 4, 40, 4096, dict(nvfp4=True, global_scale=g)),
         ("nvfp4 given 128x4", 4, 300, 4096, dict(nvfp4=True, global_scale=g, scales_128x4=True)),
@@ -91,13 +94,15 @@ def run_shrink(tp):
     """TPAR_DEBUG_SHRINK: the last vector of the [T, d] tensors is out of the
     checked extent."""
     P = tp.TparPlan
-    forms = [("row", dict(flags=tp.TPAR_FORCE_ROW)), ("cluster", dict(flags=tp.TPAR_FORCE_CLUSTER)),
-             ("rows prefetch", dict(plan=P(3, 1, 256, 1, 152))), ("stream", dict(flags=tp.TPAR_FORCE_STREAM)),
-             ("nvfp4 single launch", dict(nvfp4=True)), ("nvfp4 two pass", dict(nvfp4=True, flags=tp.TPAR_FORCE_ROW))]
-    T, d, n = 6, 2048, 4
-    w = synth.Workload("shrink", n, T, d, 1e-5, 0.5, seed=3)
-    dev = to_device(synth.make_inputs(w))
-    for name, kw in forms:
+    forms = [("row", 6, dict(flags=tp.TPAR_FORCE_ROW)), ("cluster", 6, dict(flags=tp.TPAR_FORCE_CLUSTER)),
+             ("rows prefetch", 6, dict(plan=P(3, 1, 256, 1, 152))), ("stream", 6, dict(flags=tp.TPAR_FORCE_STREAM)),
+             ("nvfp4 single launch", 6, dict(nvfp4=True)),
+             ("nvfp4 two pass", 6, dict(nvfp4=True, flags=tp.TPAR_FORCE_ROW)),
+             ("nvfp4 cooperative grid", 40, dict(nvfp4=True, flags=tp.TPAR_FORCE_GRID))]
+    d, n = 2048, 4
+    for name, T, kw in forms:
+        w = synth.Workload("shrink", n, T, d, 1e-5, 0.5, seed=3)
+        dev = to_device(synth.make_inputs(w))
         kw = dict(kw)
         base = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, **kw)
         torch.cuda.synchronize()
@@ -105,8 +110,8 @@ def run_shrink(tp):
         on = torch.full((T, d), 7.0, dtype=torch.bfloat16, device="cuda")
         orr = torch.full((T, d), 7.0, dtype=torch.bfloat16, device="cuda")
         kw["flags"] = kw.get("flags", 0) | tp.TPAR_DEBUG_SHRINK
-        out = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, out_norm=on,
-                               out_residual=orr, **kw)
+        tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, out_norm=on, out_residual=orr,
+                         **kw)
         torch.cuda.synchronize()
         code = tp.tpar_device_error(torch.cuda.current_device())
         assert code & tp.TPAR_DEVERR_INDEX, f"{name}: the shrunk extent was not reported ({code:#x})"
@@ -115,8 +120,8 @@ def run_shrink(tp):
         # rows before the last are the plain call's bits
         assert torch.equal(on[:T - 1].view(torch.int16), base["out_norm"][:T - 1].view(torch.int16)), name
         assert torch.equal(orr[:T - 1].view(torch.int16), base["out_residual"][:T - 1].view(torch.int16)), name
-        if kw.get("nvfp4"):
-            assert torch.equal(out["codes"][:T - 1], base["codes"][:T - 1]), name
+        # (NVFP4 codes are not compared: the shortened last row can move the
+        # global amax, hence g and every code)
     # the standalone quantiser: the last vector's codes are skipped
     x = dev["partials"][0]
     codes, _, _ = tp.nvfp4_quantize(x)
@@ -125,7 +130,7 @@ def run_shrink(tp):
     c2, _, _ = tp.nvfp4_quantize(x, flags=tp.TPAR_DEBUG_SHRINK)
     torch.cuda.synchronize()
     assert tp.tpar_device_error(torch.cuda.current_device()) & tp.TPAR_DEVERR_INDEX
-    assert torch.equal(c2[:T - 1], codes[:T - 1])
+    assert torch.equal(c2[:-1], codes[:-1])  # the input is unchanged, so is g
 
 
 def main():

@@ -324,3 +324,14 @@ def test_debug_build_exports_the_same_abi(tp):
     assert call(tp, flags=tp.TPAR_DRY_RUN | tp.TPAR_DEBUG_SHRINK) == UNSUPPORTED
     assert tp.tpar_fp8_quantize(BASE, 8, 4096, BASE + 64 * MB, BASE + 80 * MB,
                                 tp.TPAR_DRY_RUN | tp.TPAR_DEBUG_SHRINK, 0, check=False) == INVALID
+
+
+def test_force_grid_flag_checks(tp):
+    """TPAR_FORCE_GRID is the dynamic-scale NVFP4 path only, exclusive with
+    the other kernel-forcing flags."""
+    F, D = tp.TPAR_FORCE_GRID, tp.TPAR_DRY_RUN
+    nv = dict(codes=BASE + 200 * MB, scales=BASE + 240 * MB, g=BASE + 250 * MB)
+    assert call(tp, flags=D | F, **nv) == OK
+    assert call(tp, flags=D | F) == INVALID                                   # no NVFP4
+    assert call(tp, flags=D | F | tp.TPAR_GSCALE_GIVEN, **nv) == INVALID      # given scale
+    assert call(tp, flags=D | F | tp.TPAR_FORCE_ROW, **nv) == INVALID         # two kernels forced

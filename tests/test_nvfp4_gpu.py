@@ -164,28 +164,65 @@ def test_workspace_is_left_zeroed_and_reused():
         assert int(ws.abs().sum().item()) == 0
 
 
-@pytest.mark.parametrize("T,d,n", [(1, 8192, 4), (3, 8192, 4), (8, 4096, 8), (16, 2048, 2), (32, 8192, 4),
-                                   (7, 1024, 16), (5, 256, 1), (32, 4096, 8)])
-def test_single_launch_dynamic_matches_two_pass(T, d, n):
-    """Few tokens: one cluster owns the tensor and exchanges the amax on chip
-    (one launch). It must give exactly the bits of the two-kernel path, and
-    both are bit-exact against the oracle quantiser on out_norm."""
+@pytest.mark.parametrize("T,d,n,dt", [
+    (1, 8192, 4, "bf16"), (3, 8192, 4, "bf16"), (8, 4096, 8, "bf16"), (16, 2048, 2, "bf16"),  # one cluster
+    (7, 1024, 16, "bf16"), (5, 256, 1, "bf16"),
+    (17, 8192, 4, "bf16"), (32, 8192, 4, "bf16"), (32, 4096, 8, "bf16"), (64, 8192, 4, "bf16"),  # grid
+    (152, 4096, 8, "bf16"), (153, 4096, 8, "bf16"), (300, 8192, 2, "bf16"), (1024, 2048, 16, "bf16"),
+    (1824, 8192, 4, "bf16"), (100, 4096, 4, "fp16"), (77, 8192, 16, "bf16"), (40, 272, 3, "bf16"),
+    (1825, 8192, 4, "bf16"),  # rows no longer fit on chip: the two-kernel path on both sides
+    (4, 2048, 4, "bf16"),     # the grid form also runs a few rows (below)
+])
+def test_single_launch_dynamic_matches_two_pass(T, d, n, dt):
+    """Dynamic global scale in one launch: for T <= 16 one cluster owns the
+    tensor and exchanges the amax on chip (the automatic choice); with
+    TPAR_FORCE_GRID, up to ~1800 rows of d=8192, a cooperative grid keeps its
+    rows in shared memory across a grid barrier. Either must give exactly
+    the bits of the two-kernel path, and both are bit-exact against the
+    oracle quantiser on out_norm."""
     tp = lib()
     w = synth.NVFP4.with_(T=T, d=d, n_ranks=n, seed=T * 13 + d + n)
-    inputs = synth.make_inputs(w)
+    inputs = synth.make_inputs(w, dtype=torch.float16 if dt == "fp16" else torch.bfloat16)
     dev = to_device(inputs)
-    one = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True)
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    fits = (-(-T // sm)) * (d // 8) * 16 <= 200 * 1024
+    grid = T > 16 and fits
+    one = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True,
+                           flags=tp.TPAR_FORCE_GRID if grid else 0)
     two = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True,
                            flags=tp.TPAR_FORCE_ROW)
     torch.cuda.synchronize()
     for k in ("out_norm", "out_residual", "codes", "scales", "global_scale"):
-        assert torch.equal(one[k].view(torch.int16) if one[k].dtype == torch.bfloat16 else one[k],
-                           two[k].view(torch.int16) if two[k].dtype == torch.bfloat16 else two[k]), k
+        a16 = one[k].dtype in (torch.bfloat16, torch.float16)
+        assert torch.equal(one[k].view(torch.int16) if a16 else one[k],
+                           two[k].view(torch.int16) if a16 else two[k]), k
     ref = oracle_rows(inputs, slice(None), w.eps)
     assert_close_to_ref(one["out_norm"], ref["y"], "single-launch out_norm")
     assert_close_to_ref(one["out_residual"], ref["h"], "single-launch out_residual")
     assert_nvfp4_bit_exact(one["out_norm"], one["codes"], one["scales"], one["global_scale"], what="single")
+    if T <= 16 and d <= 8192:  # the grid form on a few rows gives the same bits
+        gr = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True,
+                              flags=tp.TPAR_FORCE_GRID)
+        torch.cuda.synchronize()
+        assert torch.equal(gr["codes"], two["codes"]) and torch.equal(gr["scales"], two["scales"])
     assert tp.tpar_device_error(torch.cuda.current_device()) == 0
+
+
+def test_grid_path_limits():
+    """TPAR_FORCE_GRID: rows that do not fit on chip, or a call that is not
+    dynamic-scale NVFP4, are refused before any launch."""
+    tp = lib()
+    w = synth.NVFP4.with_(T=1825, d=8192)
+    dev = to_device(synth.make_inputs(w))
+    with pytest.raises(tp.TparError, match="UNSUPPORTED"):
+        tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True,
+                         flags=tp.TPAR_FORCE_GRID)
+    with pytest.raises(tp.TparError, match="INVALID"):
+        tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, flags=tp.TPAR_FORCE_GRID)
+    g = torch.tensor([0.1], dtype=torch.float32, device="cuda")
+    with pytest.raises(tp.TparError, match="INVALID"):
+        tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True, global_scale=g,
+                         flags=tp.TPAR_FORCE_GRID)
 
 
 

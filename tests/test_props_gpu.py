@@ -55,11 +55,15 @@ def test_graph_replay_matches_eager():
     assert same_bits(out_n, eager["out_norm"]) and same_bits(out_r, eager["out_residual"])
 
 
-def test_graph_capture_of_dynamic_nvfp4():
+@pytest.mark.parametrize("T,grid", [(8, False), (64, True), (400, True), (64, False), (4096, False)])
+def test_graph_capture_of_dynamic_nvfp4(T, grid):
+    """Every dynamic-scale form under graph capture and replay: one cluster
+    (T=8), the cooperative grid (TPAR_FORCE_GRID) and the two kernels."""
     tp = lib()
-    w = synth.NVFP4.with_(T=8, d=4096)
+    w = synth.NVFP4.with_(T=T, d=4096)
+    flags = tp.TPAR_FORCE_GRID if grid else 0
     dev = to_device(synth.make_inputs(w))
-    eager = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True)
+    eager = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True, flags=flags)
     outs = {k: torch.empty_like(v) for k, v in eager.items() if v is not None}
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -67,11 +71,11 @@ def test_graph_capture_of_dynamic_nvfp4():
 
     def call():
         from residual_rmsnorm_gb300 import _abi
-        _abi.tpar_fused_rmsnorm(
+        _abi.tpar_fused_rmsnorm_ex(
             [p.data_ptr() for p in dev["partials"]], w.n_ranks, dev["residual"].data_ptr(),
             dev["gamma"].data_ptr(), w.eps, w.T, w.d, outs["out_norm"].data_ptr(),
             outs["out_residual"].data_ptr(), outs["codes"].data_ptr(), outs["scales"].data_ptr(),
-            outs["global_scale"].data_ptr(), torch.cuda.current_stream().cuda_stream)
+            outs["global_scale"].data_ptr(), flags, None, 0, torch.cuda.current_stream().cuda_stream)
 
     with torch.cuda.stream(s):
         call()
@@ -85,6 +89,7 @@ def test_graph_capture_of_dynamic_nvfp4():
     torch.cuda.synchronize()
     for k, v in outs.items():
         assert same_bits(v, eager[k]), k
+    assert tp.tpar_device_error(torch.cuda.current_device()) == 0
 
 
 def test_guard_bands_untouched():
