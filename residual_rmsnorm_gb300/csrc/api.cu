@@ -167,8 +167,13 @@ tpar_status current_sm_count(int* sm)
     return sm_count_of(dev, sm);
 }
 
-cudaError_t launch(const void* fn, dim3 grid, dim3 block, void* arg, cudaStream_t stream, int cluster_x,
-                   bool pdl, size_t smem = 0)
+// Every launch of the library: kernel `fn` with its parameter array, an
+// optional cluster width, PDL (programmatic stream serialization: the kernel
+// may start while its predecessor finishes and waits for it in-kernel),
+// dynamic shared memory, and an optional cooperative launch (all CTAs
+// resident at once; never combined with PDL).
+cudaError_t launch_args(const void* fn, dim3 grid, dim3 block, void** args, cudaStream_t stream, int cluster_x,
+                        bool pdl, size_t smem = 0, bool cooperative = false)
 {
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof cfg);
@@ -176,7 +181,7 @@ cudaError_t launch(const void* fn, dim3 grid, dim3 block, void* arg, cudaStream_
     cfg.blockDim = block;
     cfg.dynamicSmemBytes = smem;
     cfg.stream = stream;
-    cudaLaunchAttribute attrs[2];
+    cudaLaunchAttribute attrs[3];
     unsigned na = 0;
     if (cluster_x > 1) {
         attrs[na].id = cudaLaunchAttributeClusterDimension;
@@ -185,15 +190,27 @@ cudaError_t launch(const void* fn, dim3 grid, dim3 block, void* arg, cudaStream_
         attrs[na].val.clusterDim.z = 1;
         ++na;
     }
-    if (pdl) {
+    if (pdl && !cooperative) {
         attrs[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
         attrs[na].val.programmaticStreamSerializationAllowed = 1;
         ++na;
     }
+    if (cooperative) {
+        attrs[na].id = cudaLaunchAttributeCooperative;
+        attrs[na].val.cooperative = 1;
+        ++na;
+    }
     cfg.attrs = attrs;
     cfg.numAttrs = na;
-    void* args[1] = {arg};
     return cudaLaunchKernelExC(&cfg, fn, args);
+}
+
+// The same for a kernel whose one parameter is a __grid_constant__ struct.
+cudaError_t launch(const void* fn, dim3 grid, dim3 block, void* arg, cudaStream_t stream, int cluster_x,
+                   bool pdl, size_t smem = 0, bool cooperative = false)
+{
+    void* args[1] = {arg};
+    return launch_args(fn, grid, block, args, stream, cluster_x, pdl, smem, cooperative);
 }
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
@@ -545,19 +562,10 @@ tpar_status launch_stream(const FusedArgs& a, int qmode, const tpar_plan& p, cud
     const size_t smem = static_cast<size_t>(sa.stages) * row_bytes + 16u * sa.stages;
     if (set_attr_once(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
         return TPAR_ERR_CUDA;
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(static_cast<unsigned>(p.grid_rows));
-    cfg.blockDim = dim3(static_cast<unsigned>(p.threads + 32));
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute at;
-    at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at.val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = &at;
-    cfg.numAttrs = pdl ? 1 : 0;
-    void* args[1] = {&sa};
-    return cudaLaunchKernelExC(&cfg, fn, args) == cudaSuccess ? TPAR_OK : TPAR_ERR_CUDA;
+    return launch(fn, dim3(static_cast<unsigned>(p.grid_rows)), dim3(static_cast<unsigned>(p.threads + 32)), &sa,
+                  stream, 1, pdl, smem) == cudaSuccess
+               ? TPAR_OK
+               : TPAR_ERR_CUDA;
 }
 
 tpar_status launch_rows(const FusedArgs& a, int qmode, const tpar_plan& p, cudaStream_t stream, bool pdl)
@@ -829,19 +837,11 @@ tpar_status launch_grid_nvfp4(const FusedArgs& a, float* gscale, uint32_t* ws, i
     ga.gscale = gscale;
     ga.ws = ws;
     ga.rows = rows;
-    cudaLaunchConfig_t cfg;
-    std::memset(&cfg, 0, sizeof cfg);
-    cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(static_cast<unsigned>(threads));
-    cfg.dynamicSmemBytes = static_cast<size_t>(rows) * a.nvec * 16;
-    cfg.stream = stream;
-    cudaLaunchAttribute at;
-    at.id = cudaLaunchAttributeCooperative;  // every CTA resident: the grid barrier can complete
-    at.val.cooperative = 1;
-    cfg.attrs = &at;
-    cfg.numAttrs = 1;
-    void* args[1] = {&ga};
-    return cudaLaunchKernelExC(&cfg, fn, args) == cudaSuccess ? TPAR_OK : TPAR_ERR_CUDA;
+    // cooperative: every CTA resident, so the grid barrier can complete
+    return launch(fn, dim3(static_cast<unsigned>(grid)), dim3(static_cast<unsigned>(threads)), &ga, stream, 1, false,
+                  static_cast<size_t>(rows) * a.nvec * 16, true) == cudaSuccess
+               ? TPAR_OK
+               : TPAR_ERR_CUDA;
 }
 
 tpar_status fused_impl(const Call& c, const tpar_plan* user_plan, void* user_ws, cudaStream_t stream)
@@ -993,18 +993,8 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
         uint4* outr = static_cast<uint4*>(out_residual);
         int64_t n = nvec;
         void* args[4] = {&red, &res, &outr, &n};
-        cudaLaunchConfig_t cfg;
-        std::memset(&cfg, 0, sizeof cfg);
         const void* k2 = tpar::residual_add_kernel_ptr((flags & TPAR_DTYPE_FP16) != 0);
-        cfg.gridDim = dim3(flat_grid(nvec, sm, k2));
-        cfg.blockDim = dim3(256);
-        cfg.stream = stream;
-        cudaLaunchAttribute at;
-        at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        at.val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = &at;
-        cfg.numAttrs = pdl ? 1 : 0;
-        if (cudaLaunchKernelExC(&cfg, k2, args) != cudaSuccess)
+        if (launch_args(k2, dim3(flat_grid(nvec, sm, k2)), dim3(256), args, stream, 1, pdl) != cudaSuccess)
             return TPAR_ERR_CUDA;
     }
     // K3: out_norm = RMSNorm(out_residual) (+ amax for a dynamic NVFP4 scale)
@@ -1068,18 +1058,8 @@ tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* co
         const uint4* xv = static_cast<const uint4*>(x);
         int64_t nvec = T * d / 8;
         void* args[3] = {&xv, &nvec, &ws};
-        cudaLaunchConfig_t cfg;
-        std::memset(&cfg, 0, sizeof cfg);
         const void* ka = tpar::amax_kernel_ptr((flags & TPAR_DTYPE_FP16) != 0);
-        cfg.gridDim = dim3(flat_grid(nvec, sm, ka));
-        cfg.blockDim = dim3(256);
-        cfg.stream = stream;
-        cudaLaunchAttribute at;
-        at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        at.val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = &at;
-        cfg.numAttrs = pdl ? 1 : 0;
-        if (cudaLaunchKernelExC(&cfg, ka, args) != cudaSuccess)
+        if (launch_args(ka, dim3(flat_grid(nvec, sm, ka)), dim3(256), args, stream, 1, pdl) != cudaSuccess)
             return TPAR_ERR_CUDA;
     }
     st = launch_quantize(x, T, d, codes, scales, global_scale, ws, !given, sm, stream, pdl, flags);
@@ -1194,18 +1174,8 @@ tpar_status tpar_fp8_quantize(const void* x, int64_t T, int64_t d, uint8_t* code
         const uint4* xv = static_cast<const uint4*>(x);
         int64_t n = nvec;
         void* args[3] = {&xv, &n, &ws};
-        cudaLaunchConfig_t cfg;
-        std::memset(&cfg, 0, sizeof cfg);
         const void* ka = tpar::amax_kernel_ptr((flags & TPAR_DTYPE_FP16) != 0);
-        cfg.gridDim = dim3(flat_grid(nvec, sm, ka));
-        cfg.blockDim = dim3(256);
-        cfg.stream = stream;
-        cudaLaunchAttribute at;
-        at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        at.val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = &at;
-        cfg.numAttrs = pdl ? 1 : 0;
-        if (cudaLaunchKernelExC(&cfg, ka, args) != cudaSuccess)
+        if (launch_args(ka, dim3(flat_grid(nvec, sm, ka)), dim3(256), args, stream, 1, pdl) != cudaSuccess)
             return TPAR_ERR_CUDA;
     }
     tpar::Fp8Args f;
@@ -1377,18 +1347,8 @@ extern "C" tpar_status tpar_unfused_rmsnorm_noalloc(const void* const* partials,
         uint4* outr = static_cast<uint4*>(out_residual);
         int64_t n = nvec;
         void* args[4] = {&red, &res, &outr, &n};
-        cudaLaunchConfig_t cfg;
-        std::memset(&cfg, 0, sizeof cfg);
         const void* k2 = tpar::residual_add_kernel_ptr((flags & TPAR_DTYPE_FP16) != 0);
-        cfg.gridDim = dim3(flat_grid(nvec, sm, k2));
-        cfg.blockDim = dim3(256);
-        cfg.stream = stream;
-        cudaLaunchAttribute at;
-        at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
-        at.val.programmaticStreamSerializationAllowed = 1;
-        cfg.attrs = &at;
-        cfg.numAttrs = pdl ? 1 : 0;
-        if (cudaLaunchKernelExC(&cfg, k2, args) != cudaSuccess)
+        if (launch_args(k2, dim3(flat_grid(nvec, sm, k2)), dim3(256), args, stream, 1, pdl) != cudaSuccess)
             return TPAR_ERR_CUDA;
     }
     // K3: out_norm = RMSNorm(out_residual) (+ amax for a dynamic NVFP4 scale)
