@@ -485,11 +485,12 @@ tpar_status plan_impl(int64_t T, int64_t d, int n_ranks, int sm_count, uint32_t 
         // Latency path. A CTA that owns a whole row pulls (N+1)*2d bytes
         // through one SM (~120 GB/s per SM measured on GB300); the cluster
         // exchange of the 32-vector partial sums costs ~0.2-0.3 us. Split
-        // rows of >= 64 KB over a cluster while T <= 32, into slices of
+        // rows of >= 64 KB over a cluster while T <= 48, into slices of
         // >= 10 KB (measured: N=4 d=8192 T=8 2.30 us split 8 ways vs 2.88
-        // whole; N=8 d=8192 T=32 3.16 vs 3.50; N=8 d=4096 T=8 a tie at 2.49).
+        // whole; N=8 d=8192 T=32 3.16 vs 3.50, T=33 3.15 vs 3.61, T=48 3.66
+        // vs 3.80, T=64 mixed, T=96 slower; N=8 d=4096 T=8 a tie at 2.49).
         const int64_t row_bytes = static_cast<int64_t>(n_ranks + 1) * d * 2;
-        if (T <= 32 && row_bytes >= 64 * 1024) {
+        if (T <= 48 && row_bytes >= 64 * 1024) {
             while (split < 16 && row_bytes / (2 * split) >= 10 * 1024 && T * (2 * split) <= 2 * sm_count &&
                    nvec / (2 * split) >= 32)
                 split *= 2;

@@ -213,7 +213,7 @@ def test_planner_covers_every_row(tp, sm):
                 s = -(-(-(-nvec // p.split)) // 32) * 32
                 assert p.threads * p.vec_per_thread >= s
                 assert s >= 32 or p.split == 2
-                assert T <= 32 and T * p.split <= 2 * sm  # rows are split only when few
+                assert T <= 48 and T * p.split <= 2 * sm  # rows are split only when few
             else:
                 assert p.split == 1 and p.threads * p.vec_per_thread >= nvec
             assert 1 <= p.grid_rows <= min(T, 65535)
@@ -227,6 +227,9 @@ def test_planner_choices_for_the_pages_shapes(tp):
     for T in (1, 4, 8, 16, 32):
         p = tp.tpar_plan_launch(T, 8192, 8, 152)
         assert (p.kernel, p.split, p.threads) == (1, 8, 128), T
+    # just past 32 rows: still split, as far as 2 CTAs per SM allow
+    assert (tp.tpar_plan_launch(33, 8192, 8, 152).kernel, tp.tpar_plan_launch(33, 8192, 8, 152).split) == (1, 8)
+    assert (tp.tpar_plan_launch(48, 8192, 8, 152).kernel, tp.tpar_plan_launch(48, 8192, 8, 152).split) == (1, 4)
     assert tp.tpar_plan_launch(64, 8192, 8, 152).kernel == 0
     # 82 KB rows (N=4, d=8192): split 8 ways; 25 KB rows (N=2, d=4096): whole
     assert tp.tpar_plan_launch(8, 8192, 4, 152).split == 8

@@ -5,7 +5,7 @@ import pytest
 import torch
 
 import synth
-from gpu_helpers import (ATOL, RTOL, assert_close_to_ref, lib, oracle_rows, to_device,
+from gpu_helpers import (ATOL, RTOL, assert_close_to_ref, assert_nvfp4_bit_exact, lib, oracle_rows, to_device,
                          unfused_extra_tolerance)
 
 pytestmark = pytest.mark.gpu
@@ -258,3 +258,42 @@ def test_nvfp4_given_scale_identical_across_plans():
         torch.cuda.synchronize()
         assert torch.equal(out["codes"], ref["codes"]) and torch.equal(out["scales"], ref["scales"]), \
             plan.as_dict()
+
+
+@pytest.mark.parametrize("T", [8, 300])
+def test_concurrent_streams_with_their_own_workspaces(T):
+    """Dynamic-scale calls on two unordered streams, each with its own caller
+    workspace, run at the same time without disturbing each other (each
+    sees only its own amax), alongside a plain call on a third stream."""
+    tp = lib()
+    ws = [torch.zeros(tp.tpar_workspace_bytes() // 4, dtype=torch.int32, device="cuda") for _ in range(2)]
+    sets = []
+    for i, scale in enumerate((40.0, 0.25)):
+        w = synth.NVFP4.with_(T=T, d=4096, seed=100 + i)
+        x = synth.make_inputs(w, device="cuda")
+        x["partials"] = [(p.float() * scale).to(torch.bfloat16) for p in x["partials"]]
+        sets.append((w, x))
+    plain_w = synth.PREFILL.with_(T=512, d=4096)
+    plain = synth.make_inputs(plain_w, device="cuda")
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    torch.cuda.synchronize()
+    outs = [None, None]
+    for rep in range(5):
+        for i, ((w, x), s) in enumerate(zip(sets, streams[:2])):
+            with torch.cuda.stream(s):
+                outs[i] = tp.fused_rmsnorm(x["partials"], x["residual"], x["gamma"], w.eps, nvfp4=True,
+                                           workspace=ws[i], stream=s)
+        with torch.cuda.stream(streams[2]):
+            p_out = tp.fused_rmsnorm(plain["partials"], plain["residual"], plain["gamma"], plain_w.eps,
+                                     stream=streams[2])
+    torch.cuda.synchronize()
+    for i, (w, x) in enumerate(sets):
+        o = outs[i]
+        assert_nvfp4_bit_exact(o["out_norm"], o["codes"], o["scales"], o["global_scale"], what=f"stream {i}")
+        amax = o["out_norm"].float().abs().max().item()
+        assert o["global_scale"].item() == np.float32(np.float32(amax) / np.float32(2688.0))
+        assert int(ws[i].abs().sum().item()) == 0
+    rows = np.array([0, 255, 511])
+    ref = oracle_rows(plain, rows, plain_w.eps)
+    assert_close_to_ref(p_out["out_norm"][rows], ref["y"], "third stream")
+    assert tp.tpar_device_error(torch.cuda.current_device()) == 0
