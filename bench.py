@@ -379,6 +379,42 @@ def cpu_oracle_baseline(w, budget_s=10.0, max_calls=100000):
             "sample": f"{n} oracle calls of {w.name} ({dt:.1f} s, single-threaded C, fp64)"}
 
 
+def cpu_oracle_parallel(w, budget_s=5.0, max_calls=100000):
+    """The same oracle over all host cores: each call's rows are split into
+    one chunk per thread (rows are independent; the C oracle runs without the
+    interpreter lock), the oracle itself unchanged."""
+    import concurrent.futures as cf
+    import numpy as np
+    import oracle
+    import synth
+    x = synth.make_inputs(w)
+    parts = [synth.bits(p) for p in x["partials"]]
+    res = synth.bits(x["residual"])
+    gam = synth.bits(x["gamma"])
+    cores = len(os.sched_getaffinity(0))
+    k = max(1, min(cores, w.T))
+    chunks = [c for c in np.array_split(np.arange(w.T), k) if c.size]
+    sl = [(c[0], c[-1] + 1) for c in chunks]
+    args = [([p[a:b] for p in parts], res[a:b]) for a, b in sl]
+
+    def one(i):
+        pp, rr = args[i]
+        oracle.fused_rmsnorm(pp, rr, gam, w.eps, want_ref=False)
+
+    with cf.ThreadPoolExecutor(max_workers=len(sl)) as ex:
+        list(ex.map(one, range(len(sl))))
+        n = 0
+        t0 = time.perf_counter()
+        while n < max_calls:
+            list(ex.map(one, range(len(sl))))
+            n += 1
+            if time.perf_counter() - t0 >= budget_s:
+                break
+        dt = time.perf_counter() - t0
+    return {"value": round(dt / n * 1e6, 3), "unit": UNIT, "cores": len(sl), "kind": "oracle",
+            "sample": f"{n} calls of {w.name}, rows split over {len(sl)} threads ({dt:.1f} s)"}
+
+
 # ------------------------------------------------------------------ arms
 
 def reference_arm(args, w):
@@ -518,6 +554,7 @@ def ours_arm(args, w):
 
     if rank == 0:
         cpu = cpu_oracle_baseline(w, budget_s=args.cpu_seconds)
+        cpu_par = cpu_oracle_parallel(w, budget_s=max(0.5, args.cpu_seconds / 2))
         line = {
             "metric": METRIC, "value": round(us_per_call_job, 4), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 4),
@@ -549,6 +586,7 @@ def ours_arm(args, w):
             "clocks": clocks,
             "l2_hot_us_per_call": round(us_hot, 4),
             "cpu_baseline": cpu,
+            "cpu_baseline_all_cores": cpu_par,
             "kernel_src_sha": sha,
         }
         if sweep is not None:
