@@ -110,7 +110,7 @@ __device__ __forceinline__ void add8(const uint4& v, float f[8])
     f[6] += bf16_lo(v.w); f[7] += bf16_hi(v.w);
 }
 
-// Round 2 floats to bf16 (nearest even); lo lands in the low half.
+// Round two floats to bf16 (nearest even); lo lands in the low half.
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
 {
     __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
