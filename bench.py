@@ -463,6 +463,7 @@ def ours_arm(args, w):
     from residual_rmsnorm_gb300 import build
     build.build()
     import residual_rmsnorm_gb300 as tp
+    import synth
     tp.tpar_init(local_rank)
 
     # ---- main workload: graph of 1000 calls, L2-cold input sets
@@ -491,6 +492,14 @@ def ours_arm(args, w):
     ms_step = ms_total / args.steps
     us_per_call_rank = ms_step * 1e3 / CALLS_PER_STEP
     us_per_call_job = job_us_per_call(ms_total, args.steps, CALLS_PER_STEP, world)
+
+    # the PDL graph floor: the same call on one 16-byte vector per tensor
+    # (N=1, T=1, d=8), i.e. launch, one memory round trip and the grid's end
+    w0 = synth.Workload("one vector", 1, 1, 8, 1e-5, 0.5)
+    fs = CallSet(w0, seed=0, device=device)
+    g_floor = capture(torch, lambda i: fs.call(tp, w0, torch.cuda.current_stream().cuda_stream), CALLS_PER_STEP)
+    us_floor = time_graph(torch, g_floor, 20, 3) * 1e3 / CALLS_PER_STEP
+    del g_floor, fs
 
     # L2-hot variant (all calls on one input set), for reference
     g_hot = capture(torch, lambda i: sets[0].call(tp, w, torch.cuda.current_stream().cuda_stream),
@@ -574,7 +583,10 @@ def ours_arm(args, w):
                          "measured" else "fallback 6.8 TB/s",
                          "algorithmic_bytes_per_launch": per_call,
                          "frac_of_nominal_7900_gbs": round(achieved / NOMINAL_HBM_GBS, 4),
-                         "note": "T=8 decode is latency-bound: the whole call moves 0.73 MB"},
+                         "note": "T=8 decode is latency-bound: the whole call moves 0.73 MB",
+                         "latency_floor_us_per_call": round(us_floor, 4),
+                         "latency_floor_how": "the same 1000-call PDL graph on one 16-byte vector per tensor "
+                                              "(N=1, T=1, d=8)"},
             "e2e": {"value": round(us_e2e_job, 4), "unit": UNIT,
                     "h2d_bytes_per_step": in_bytes * CALLS_PER_STEP,
                     "d2h_bytes_per_step": out_bytes * CALLS_PER_STEP,
