@@ -357,7 +357,94 @@ def measure_sweep(torch, tp, device):
                      "frac_of_measured_hbm": round(b / us / 1e3 / peak, 4)})
         torch.cuda.empty_cache()
     out["nvfp4_dynamic_N4_d8192"] = rows
+    out["patterns"] = measure_patterns(torch, tp, device)
     return out
+
+
+def measure_patterns(torch, tp, device):
+    """Every output pattern at the decode (N=8 [8, 4096], 1000-call graph,
+    input sets > 2x L2) and prefill (N=8 [4096, 8192], eager calls over two
+    input sets) shapes, each with its own algorithmic bytes:
+      norm (bf16 / fp16)        (N+3) T d 2 + 2d
+      all-reduce + residual     (N+2) T d 2
+      NVFP4, given g, no norm   (N+2) T d 2 + T d / 2 + T d / 16 + 2d   (row-major or 128x4 scales)
+      FP8, given s, no norm     (N+2) T d 2 + T d + 2d
+      FP8, dynamic s            (N+3) T d 2 + T d + T d 2 (re-read) + 2d
+    """
+    import synth
+    peak, _ = measured_hbm_peak()
+    st = torch.cuda.current_stream()
+    rows = []
+    for shape, w, calls in (("decode", synth.DECODE_8B, CALLS_PER_STEP), ("prefill", synth.PREFILL, 0)):
+        n, T, d = w.n_ranks, w.T, w.d
+        td = T * d
+        base = (n + 3) * td * 2 + 2 * d
+        pats = [("norm bf16", torch.bfloat16, base), ("norm fp16", torch.float16, base),
+                ("allreduce + residual", torch.bfloat16, (n + 2) * td * 2),
+                ("nvfp4 given g, no norm", torch.bfloat16, (n + 2) * td * 2 + td // 2 + td // 16 + 2 * d),
+                ("nvfp4 given g, no norm, 128x4 scales", torch.bfloat16,
+                 (n + 2) * td * 2 + td // 2 + td // 16 + 2 * d),
+                ("fp8 given s, no norm", torch.bfloat16, (n + 2) * td * 2 + td + 2 * d),
+                ("fp8 dynamic s", torch.bfloat16, (n + 3) * td * 2 + td + td * 2 + 2 * d)]
+        for name, dt, nbytes in pats:
+            per = (n + 3) * td * 2
+            n_sets = 2 if shape == "prefill" else min(calls, n_sets_for(per, l2_bytes(torch)))
+            sets = []
+            for i in range(n_sets):
+                x = synth.make_inputs(w, device=device, seed=i, dtype=dt)
+                o = {"on": torch.empty((T, d), dtype=dt, device=device),
+                     "or": torch.empty((T, d), dtype=dt, device=device),
+                     "codes": torch.empty(td, dtype=torch.uint8, device=device),
+                     "scales": torch.empty(tp.scales_128x4_bytes(T, d), dtype=torch.uint8, device=device),
+                     "g": torch.full((1,), 0.02, dtype=torch.float32, device=device)}
+                sets.append((x, o))
+            f16 = tp.TPAR_DTYPE_FP16 if dt == torch.float16 else 0
+
+            def call(i, name=name, sets=sets, f16=f16, n=n, T=T, d=d, w=w):
+                x, o = sets[i % len(sets)]
+                ps = [p.data_ptr() for p in x["partials"]]
+                r, g = x["residual"].data_ptr(), x["gamma"].data_ptr()
+                sh = torch.cuda.current_stream().cuda_stream
+                if name.startswith("norm"):
+                    tp.tpar_fused_rmsnorm_ex(ps, n, r, g, w.eps, T, d, o["on"].data_ptr(), o["or"].data_ptr(),
+                                             0, 0, 0, f16, None, 0, sh)
+                elif name.startswith("allreduce"):
+                    tp.tpar_fused_rmsnorm_ex(ps, n, r, 0, 0.0, T, d, 0, o["or"].data_ptr(), 0, 0, 0, 0, None, 0,
+                                             sh)
+                elif name.startswith("nvfp4"):
+                    fl = tp.TPAR_GSCALE_GIVEN | (tp.TPAR_SCALES_128X4 if "128x4" in name else 0)
+                    tp.tpar_fused_rmsnorm_ex(ps, n, r, g, w.eps, T, d, 0, o["or"].data_ptr(),
+                                             o["codes"].data_ptr(), o["scales"].data_ptr(), o["g"].data_ptr(),
+                                             fl, None, 0, sh)
+                elif name == "fp8 given s, no norm":
+                    tp.tpar_fused_rmsnorm_fp8(ps, n, r, g, w.eps, T, d, 0, o["or"].data_ptr(), o["codes"].data_ptr(),
+                                              o["g"].data_ptr(), tp.TPAR_GSCALE_GIVEN, sh)
+                else:
+                    tp.tpar_fused_rmsnorm_fp8(ps, n, r, g, w.eps, T, d, o["on"].data_ptr(), o["or"].data_ptr(),
+                                              o["codes"].data_ptr(), o["g"].data_ptr(), 0, sh)
+
+            if shape == "decode":
+                gr = capture(torch, call, calls)
+                us = time_graph(torch, gr, 5, 2) * 1e3 / calls
+                del gr
+            else:
+                for i in range(3):
+                    call(i)
+                torch.cuda.synchronize()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(st)
+                for i in range(20):
+                    call(i)
+                e1.record(st)
+                e1.synchronize()
+                us = e0.elapsed_time(e1) * 1e3 / 20
+            rows.append({"shape": f"{shape} N{n} T{T} d{d}", "pattern": name, "us_per_call": round(us, 3),
+                         "algorithmic_bytes": nbytes, "GBps": round(nbytes / us / 1e3, 1),
+                         "frac_of_measured_hbm": round(nbytes / us / 1e3 / peak, 4)})
+            del sets
+            torch.cuda.empty_cache()
+    return rows
 
 
 def cpu_oracle_baseline(w, budget_s=10.0, max_calls=100000):
