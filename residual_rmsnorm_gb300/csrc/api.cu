@@ -743,10 +743,12 @@ bool small_nvfp4_shape(int64_t T, int64_t d, int* K, int* slice, int* threads, i
     return false;
 }
 
-tpar_status launch_small_nvfp4(const FusedArgs& a, float* gscale, int K, int slice, int threads, int ipt,
-                               cudaStream_t stream, bool pdl)
+// The single-launch dynamic-scale kernel (NVFP4, or FP8 with `fp8`): one
+// cluster of K CTAs owns the tensor (shape from small_nvfp4_shape).
+tpar_status launch_small_dynamic(const FusedArgs& a, float* gscale, int K, int slice, int threads, int ipt,
+                                 cudaStream_t stream, bool pdl, bool fp8)
 {
-    const void* fn = tpar::small_kernel_for(tpar::rank_bound(a.n_ranks), ipt, a.f16);
+    const void* fn = tpar::small_kernel_for(tpar::rank_bound(a.n_ranks), ipt, a.f16, fp8);
     if (!fn)
         return TPAR_ERR_UNSUPPORTED;
     if (K > 8 && set_attr_once(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
@@ -895,7 +897,7 @@ tpar_status fused_impl(const Call& c, const tpar_plan* user_plan, void* user_ws,
     int K = 0, slice = 0, threads = 0, ipt = 0;
     if (!user_plan && forced_kernels(c.flags) == 0 && small_nvfp4_shape(c.T, c.d, &K, &slice, &threads, &ipt)) {
         a.slice = slice;
-        return launch_small_nvfp4(a, c.gscale, K, slice, threads, ipt, stream, pdl);
+        return launch_small_dynamic(a, c.gscale, K, slice, threads, ipt, stream, pdl, false);
     }
     uint32_t* ws = nullptr;
     if ((st = workspace_for(user_ws, stream, &ws)) != TPAR_OK)
@@ -1118,6 +1120,14 @@ tpar_status tpar_fused_rmsnorm_fp8(const void* const* partials, int n_ranks, con
         a.q8 = reinterpret_cast<uint2*>(fp8_codes);
         a.gscale = fp8_scale;
         return launch_fused(a, tpar::kQuantFp8Given, p, stream, pdl);
+    }
+    // Dynamic scale, few tokens: one cluster owns the tensor and exchanges
+    // the amax on chip (one launch, no workspace), as for NVFP4.
+    int K = 0, slice = 0, threads = 0, ipt = 0;
+    if (forced_kernels(c.flags) == 0 && small_nvfp4_shape(T, d, &K, &slice, &threads, &ipt)) {
+        a.slice = slice;
+        a.q8 = reinterpret_cast<uint2*>(fp8_codes);
+        return launch_small_dynamic(a, fp8_scale, K, slice, threads, ipt, stream, pdl, true);
     }
     uint32_t* ws = nullptr;
     if ((st = workspace_for(nullptr, stream, &ws)) != TPAR_OK)

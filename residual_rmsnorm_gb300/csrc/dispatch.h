@@ -62,9 +62,9 @@ inline const void* stream_kernel_for(int qmode, int nr, int vpt, bool f16)
     return f16 ? stream_kernel_fp16(qmode, nr, vpt) : stream_kernel_bf16(qmode, nr, vpt);
 }
 
-// Single-launch dynamic-scale NVFP4 kernel (nvfp4_small.cuh) for rank bound
-// nr and ipt items per thread (1, 2, 4).
-const void* small_kernel_for(int nr, int ipt, bool f16);
+// Single-launch dynamic-scale kernel (nvfp4_small.cuh) for rank bound nr,
+// ipt items per thread (1, 2, 4), NVFP4 or (fp8) per-tensor FP8 output.
+const void* small_kernel_for(int nr, int ipt, bool f16, bool fp8);
 
 // Cooperative single-launch dynamic-scale NVFP4 kernel (nvfp4_grid.cuh) for
 // rank bound nr and vpt (1, 2) vectors per thread.

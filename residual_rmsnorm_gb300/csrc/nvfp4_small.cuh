@@ -1,9 +1,10 @@
-// nvfp4_small.cuh -- single-launch fused epilogue with a dynamic NVFP4
-// global scale, for a few decode tokens.
+// nvfp4_small.cuh -- single-launch fused epilogue with a dynamic quantisation
+// scale (NVFP4, or per-tensor FP8), for a few decode tokens.
 //
-// The dynamic scale g = amax(|out_norm|) / (6 * 448) depends on every element
-// of the tensor, so in general it needs two passes (phase A + phase B). When
-// the whole [T, d] tensor fits one thread-block cluster, one launch suffices:
+// A dynamic scale -- NVFP4's g = amax(|out_norm|) / (6 * 448), FP8's s =
+// amax(|out_norm|) / 448 -- depends on every element of the tensor, so in
+// general it needs two passes (the fused pass + a quantiser). When the whole
+// [T, d] tensor fits one thread-block cluster, one launch suffices:
 // CTA k of the cluster owns the vector slice [k*slice, (k+1)*slice) of every
 // row, and the cluster
 //   1. sums the ranks and the residual of all its items (fp32 registers),
@@ -11,7 +12,7 @@
 //      (st.async into the peers' shared memory, counted on an mbarrier),
 //      adds them in the canonical order of every kernel and normalises,
 //   3. exchanges its local amax of the emitted bf16 values the same way,
-//   4. quantises its items from registers with the cluster-wide g.
+//   4. quantises its items from registers with the cluster-wide scale.
 // No re-read of out_norm, no workspace, no second launch. The arithmetic is
 // the same as the two-pass path ("Deep Dive: AllReduce and AllReduce Fusion
 // in TensorRT-LLM", 6.3 and 6.5), in the same order: results are
@@ -26,13 +27,14 @@ constexpr int kSmallMaxRanks = 16;  // cluster size bound
 constexpr int kSmallMaxRows = 32;
 
 struct SmallArgs {
-    FusedArgs f;       // inputs, outputs (out_norm may be null), T, nvec, eps
-    float* gscale;     // output: g
+    FusedArgs f;       // inputs, outputs (out_norm may be null), codes/scales or q8, T, nvec, eps
+    float* gscale;     // output: NVFP4 g, or the FP8 dequantisation scale s
     int slice;         // vectors per CTA (a multiple of 32); slice * gridDim.x == nvec
 };
 
-template <int NR, int IPT, bool F16>
-__global__ void __launch_bounds__(512) nvfp4_small_kernel(const __grid_constant__ SmallArgs sa)
+// FP8 = false: NVFP4 codes and block scales; true: per-tensor FP8 (E4M3) codes.
+template <int NR, int IPT, bool F16, bool FP8>
+__global__ void __launch_bounds__(512) small_dynamic_kernel(const __grid_constant__ SmallArgs sa)
 {
     const FusedArgs& a = sa.f;
     pdl_wait();
@@ -164,7 +166,7 @@ __global__ void __launch_bounds__(512) nvfp4_small_kernel(const __grid_constant_
         }
     }
 
-    // ---- 3. cluster-wide amax of |out_norm|, then g = amax / 2688
+    // ---- 3. cluster-wide amax of |out_norm|, then g = amax / 2688 (FP8: s = amax / 448)
     {
         const float m = warp_max(amax_local);
         if (lane == 0)
@@ -185,10 +187,31 @@ __global__ void __launch_bounds__(512) nvfp4_small_kernel(const __grid_constant_
     float amax = 0.0f;
     for (int p = 0; p < K; ++p)
         amax = fmaxf(amax, xmax[p]);
-    const float g = __fdiv_rn(amax, 2688.0f);
+    const float g = __fdiv_rn(amax, FP8 ? 448.0f : 2688.0f);
     if (k == 0 && tid == 0)
         *sa.gscale = g;
     cluster_arrive_relaxed();  // done with the peers; matched at exit
+
+    if constexpr (FP8) {
+        // ---- 4. per-tensor FP8: code = E4M3(y * min(1/s, FLT_MAX)), as the FP8 quantiser
+        const float inv = fp8_inverse_scale(g);
+#pragma unroll
+        for (int j = 0; j < IPT; ++j) {
+            const int i = tid + j * B;
+            if (i < items) {
+                const int64_t gv = static_cast<int64_t>(i / slice) * a.nvec + vbeg + i % slice;
+                float q[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    q[e] = __fmul_rn(h[j][e], inv);
+                const uint2 c = e4m3x8_from_f32(q);
+                if (TPAR_IN_RANGE(a.err, gv, a.n_vec_total))
+                    asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(a.q8 + gv), "r"(c.x), "r"(c.y) : "memory");
+            }
+        }
+        cluster_wait_acquire();  // no CTA leaves while a peer may still push to it
+        return;
+    }
 
     // ---- 4. quantise this thread's items (a block = the vectors of a lane pair)
 #pragma unroll

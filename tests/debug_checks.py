@@ -81,6 +81,8 @@ def run_fused(tp):
     dev = to_device(inputs)
     tp.unfused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True)
     tp.fused_rmsnorm_fp8(dev["partials"], dev["residual"], dev["gamma"], w.eps)
+    small = to_device(synth.make_inputs(w.with_(T=8)))  # dynamic FP8 in one cluster
+    tp.fused_rmsnorm_fp8(small["partials"], small["residual"], small["gamma"], w.eps)
     tp.allreduce_sum(dev["partials"], dev["residual"])
     tp.nvfp4_quantize(dev["partials"][0], scales_128x4=True)
     tp.fp8_quantize(dev["partials"][0])

@@ -368,3 +368,24 @@ def test_scales_128x4_padding_rows_untouched(flags):
                              g.data_ptr(), fl, None, 0, torch.cuda.current_stream().cuda_stream)
     torch.cuda.synchronize()
     assert_nvfp4_bit_exact(out_norm, codes, scales, g, what=f"padding {flags}", scales_128x4=True, sf_fill=0xA5)
+
+
+@pytest.mark.parametrize("T,d,n,dt", [(1, 8192, 4, "bf16"), (8, 4096, 8, "bf16"), (16, 2048, 2, "bf16"),
+                                      (5, 512, 16, "bf16"), (8, 4096, 4, "fp16"), (3, 1024, 1, "bf16")])
+def test_fp8_single_launch_matches_two_pass(T, d, n, dt):
+    """Dynamic-scale FP8 for a few rows: one cluster owns the tensor (one
+    launch). Its outputs are the bits of the fused pass + FP8 quantiser, and
+    the codes are bit-exact against the oracle quantiser on out_norm."""
+    tp = lib()
+    w = synth.PREFILL.with_(T=T, d=d, n_ranks=n, seed=T + d + n)
+    inputs = synth.make_inputs(w, dtype=torch.float16 if dt == "fp16" else torch.bfloat16)
+    dev = to_device(inputs)
+    one = tp.fused_rmsnorm_fp8(dev["partials"], dev["residual"], dev["gamma"], w.eps)
+    two = tp.fused_rmsnorm_fp8(dev["partials"], dev["residual"], dev["gamma"], w.eps, flags=tp.TPAR_FORCE_ROW)
+    torch.cuda.synchronize()
+    for k in ("out_norm", "out_residual"):
+        assert torch.equal(one[k].view(torch.int16), two[k].view(torch.int16)), k
+    assert torch.equal(one["codes"], two["codes"]) and one["scale"].item() == two["scale"].item()
+    oc, os_ = oracle.fp8_quantize(synth.bits(one["out_norm"]), dtype=dt)
+    assert np.array_equal(one["codes"].cpu().numpy(), oc) and np.float32(one["scale"].item()) == os_
+    assert tp.tpar_device_error(torch.cuda.current_device()) == 0
