@@ -215,6 +215,11 @@ class CallSet:
             self.g.data_ptr() if self.g is not None else 0, flags, plan, 0, stream_handle)
 
 
+def nvtx(torch, name):
+    """An NVTX range around a benchmark case (visible to ncu / nsys by name)."""
+    return torch.cuda.nvtx.range(name)
+
+
 def capture(torch, fn, calls):
     """CUDA graph of `calls` invocations of fn(i) on a side stream."""
     s = torch.cuda.Stream()
@@ -425,7 +430,8 @@ def measure_patterns(torch, tp, device):
 
             if shape == "decode":
                 gr = capture(torch, call, calls)
-                us = time_graph(torch, gr, 5, 2) * 1e3 / calls
+                with nvtx(torch, f"pattern {name}, {shape}"):
+                    us = time_graph(torch, gr, 5, 2) * 1e3 / calls
                 del gr
             else:
                 for i in range(3):
@@ -567,11 +573,12 @@ def ours_arm(args, w):
     st = torch.cuda.current_stream()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(st)
-    for _ in range(args.steps):
-        g.replay()
-    e1.record(st)
-    e1.synchronize()
+    with nvtx(torch, f"timed region: {args.steps} x {CALLS_PER_STEP} calls of {w.name}"):
+        e0.record(st)
+        for _ in range(args.steps):
+            g.replay()
+        e1.record(st)
+        e1.synchronize()
     barrier(dist, device)
     clocks = sampler.stop()
     ms_total = e0.elapsed_time(e1)
@@ -585,7 +592,8 @@ def ours_arm(args, w):
     w0 = synth.Workload("one vector", 1, 1, 8, 1e-5, 0.5)
     fs = CallSet(w0, seed=0, device=device)
     g_floor = capture(torch, lambda i: fs.call(tp, w0, torch.cuda.current_stream().cuda_stream), CALLS_PER_STEP)
-    us_floor = time_graph(torch, g_floor, 20, 3) * 1e3 / CALLS_PER_STEP
+    with nvtx(torch, "latency floor: one-vector calls"):
+        us_floor = time_graph(torch, g_floor, 20, 3) * 1e3 / CALLS_PER_STEP
     del g_floor, fs
 
     # L2-hot variant (all calls on one input set), for reference
@@ -619,7 +627,8 @@ def ours_arm(args, w):
     g_e2e = capture(torch, lambda i: call_at(host_in[i % n_host].data_ptr(), host_out[i % n_host].data_ptr()),
                     CALLS_PER_STEP)
     e2e_steps = max(3, min(args.steps, 50))
-    ms_e2e = max_over_ranks(dist, time_graph(torch, g_e2e, e2e_steps, 3), device)
+    with nvtx(torch, "e2e: calls on pinned host buffers"):
+        ms_e2e = max_over_ranks(dist, time_graph(torch, g_e2e, e2e_steps, 3), device)
     us_e2e_job = job_us_per_call(ms_e2e, 1, CALLS_PER_STEP, world)
     del g_e2e
 
@@ -636,7 +645,8 @@ def ours_arm(args, w):
         host_out[i % n_host].copy_(dev_out[k], non_blocking=True)
 
     g_st = capture(torch, staged_call, CALLS_PER_STEP)
-    ms_st = max_over_ranks(dist, time_graph(torch, g_st, e2e_steps, 3), device)
+    with nvtx(torch, "e2e: staged copies + calls"):
+        ms_st = max_over_ranks(dist, time_graph(torch, g_st, e2e_steps, 3), device)
     us_staged_job = job_us_per_call(ms_st, 1, CALLS_PER_STEP, world)
     del g_st, dev_in, dev_out
 
@@ -648,7 +658,8 @@ def ours_arm(args, w):
 
     sweep = None
     if not args.no_sweep and rank == 0:
-        sweep = measure_sweep(torch, tp, device)
+        with nvtx(torch, "sweeps"):
+            sweep = measure_sweep(torch, tp, device)
 
     if rank == 0:
         cpu = cpu_oracle_baseline(w, budget_s=args.cpu_seconds)

@@ -100,6 +100,16 @@ typedef void* tpar_stream_t;
                                    unfused and FP8-quantiser entry points
                                    TPAR_ERR_INVALID_ARG                       */
 
+#define TPAR_DEBUG_WAIT_TIMEOUT 0x400u /* debug builds only, fused entry points:
+                                   the cluster exchange, the single-launch
+                                   kernel's exchanges and the grid barrier
+                                   wait for one more arrival than will come,
+                                   so their bounded waits expire and set the
+                                   TPAR_DEVERR_* bit (a test of the timeout
+                                   path; results stay correct, as every real
+                                   arrival has landed by then); release
+                                   builds return TPAR_ERR_UNSUPPORTED        */
+
 /* Bits of the device error word (tpar_device_error). */
 #define TPAR_DEVERR_CLUSTER_WAIT 0x1u /* a bounded wait of the cluster-split
                                          kernel's exchange expired            */

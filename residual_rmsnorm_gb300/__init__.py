@@ -23,7 +23,9 @@ from ._abi import (  # noqa: F401
     TPAR_DRY_RUN,
     TPAR_SCALES_128X4,
     TPAR_DEBUG_SHRINK,
+    TPAR_DEBUG_WAIT_TIMEOUT,
     TPAR_DEVERR_CLUSTER_WAIT,
+    TPAR_DEVERR_GRID_WAIT,
     TPAR_DEVERR_INDEX,
     TPAR_DEVERR_SMALL_WAIT,
     TPAR_DEVERR_STREAM_WAIT,

@@ -26,6 +26,7 @@ TPAR_DTYPE_FP16 = 0x40
 TPAR_SCALES_128X4 = 0x80
 TPAR_DEBUG_SHRINK = 0x100
 TPAR_FORCE_GRID = 0x200
+TPAR_DEBUG_WAIT_TIMEOUT = 0x400
 TPAR_DEVERR_CLUSTER_WAIT = 0x1
 TPAR_DEVERR_STREAM_WAIT = 0x2
 TPAR_DEVERR_SMALL_WAIT = 0x4

@@ -377,7 +377,7 @@ tpar_status validate(const Call& c, bool unfused)
         return TPAR_ERR_INVALID_ARG;
     if ((c.flags & TPAR_SCALES_128X4) && (c.fp8 || c.d % 64 != 0))
         return TPAR_ERR_INVALID_ARG;
-    if (c.flags & TPAR_DEBUG_SHRINK) {
+    if (c.flags & (TPAR_DEBUG_SHRINK | TPAR_DEBUG_WAIT_TIMEOUT)) {
         if (unfused)
             return TPAR_ERR_INVALID_ARG;
         if (!kDebugBuild)
@@ -708,6 +708,7 @@ FusedArgs fused_args(const Call& c)
     a.sf_tiles = scale_tiles(c.d, c.flags);
     a.n_vec_total = checked_vectors(c.T, c.d, c.flags);
     a.n_scales = scale_bytes(c.T, c.d, c.flags);
+    a.dbg_extra_wait = (c.flags & TPAR_DEBUG_WAIT_TIMEOUT) ? 1 : 0;
     return a;
 }
 
@@ -1079,7 +1080,7 @@ tpar_status tpar_fused_rmsnorm_fp8(const void* const* partials, int n_ranks, con
     const bool given = (flags & TPAR_GSCALE_GIVEN) != 0;
     Call c{partials, n_ranks, residual, gamma, eps, T, d, out_norm, out_residual, nullptr, nullptr, nullptr,
            flags & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_FORCE_ROW | TPAR_FORCE_CLUSTER | TPAR_DTYPE_FP16 |
-                    TPAR_SCALES_128X4 | TPAR_DEBUG_SHRINK),
+                    TPAR_SCALES_128X4 | TPAR_DEBUG_SHRINK | TPAR_DEBUG_WAIT_TIMEOUT),
            nullptr, true};
     tpar_status st = validate(c, false);
     if (st != TPAR_OK)

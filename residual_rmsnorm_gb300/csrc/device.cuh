@@ -33,6 +33,15 @@ __device__ __forceinline__ bool dbg_in_range(uint32_t* err, int64_t i, int64_t n
 #define TPAR_IN_RANGE(err, i, n) true
 #endif
 
+// Debug builds only: with TPAR_DEBUG_WAIT_TIMEOUT a wait expects one more
+// arrival (4 more bytes, one more CTA) than will ever come, so that the
+// bounded wait expires and the timeout path can be tested. 0 in release.
+#ifdef TPAR_DEBUG
+#define TPAR_EXTRA_WAIT(args) ((args).dbg_extra_wait)
+#else
+#define TPAR_EXTRA_WAIT(args) 0
+#endif
+
 // ---------------------------------------------------------------- memory
 
 // Read-once input (a partial): non-coherent path, no L1 allocation.

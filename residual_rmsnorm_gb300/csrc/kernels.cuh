@@ -57,6 +57,7 @@ struct FusedArgs {
     // [T, d] tensor (T * nvec) and scale bytes
     int64_t n_vec_total;
     int64_t n_scales;
+    int dbg_extra_wait;  // debug builds, TPAR_DEBUG_WAIT_TIMEOUT: 1 (see TPAR_EXTRA_WAIT)
 };
 
 // Byte offset of the scale of row t, 16-element block c in the 128x4 tiled
@@ -285,7 +286,7 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT, CLUSTER))
             const uint32_t parity = static_cast<uint32_t>(it >> 1) & 1u;
             const uint32_t bar = smem_addr(&xbar[buf]);
             if (tid == 0)
-                mbar_arrive_expect_tx(bar, 4u * static_cast<uint32_t>(nW));
+                mbar_arrive_expect_tx(bar, 4u * static_cast<uint32_t>(nW + TPAR_EXTRA_WAIT(a)));
 #pragma unroll
             for (int j = 0; j < VPT; ++j) {
                 const float s = warp_sum(ss[j]);

@@ -166,7 +166,8 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT, false))
         __threadfence();
         atomicAdd(ga.ws + 3, 1u);
         const uint64_t t0 = global_ns();
-        while (*reinterpret_cast<volatile uint32_t*>(ga.ws + 3) < static_cast<uint32_t>(G)) {
+        const uint32_t arrivals = static_cast<uint32_t>(G + TPAR_EXTRA_WAIT(a));
+        while (*reinterpret_cast<volatile uint32_t*>(ga.ws + 3) < arrivals) {
             if (global_ns() - t0 > kGridWaitNs) {
                 if (a.err)
                     atomicOr(a.err, TPAR_DEVERR_GRID_WAIT);

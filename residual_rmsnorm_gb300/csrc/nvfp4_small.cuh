@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(512) small_dynamic_kernel(const __grid_constan
     cluster_wait_acquire();  // the peers' mbarriers are initialised
     const uint32_t bar0 = smem_addr(&xbar[0]);
     if (tid == 0)
-        mbar_arrive_expect_tx(bar0, 4u * static_cast<uint32_t>(T * nW));
+        mbar_arrive_expect_tx(bar0, 4u * static_cast<uint32_t>(T * nW + TPAR_EXTRA_WAIT(a)));
 #pragma unroll
     for (int j = 0; j < IPT; ++j) {
         const float s = warp_sum(ss[j]);
@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(512) small_dynamic_kernel(const __grid_constan
     if (warp == 0) {
         const float cm = warp_max(lane < nwarps ? wmax[lane] : 0.0f);
         if (lane == 0)
-            mbar_arrive_expect_tx(bar1, 4u * static_cast<uint32_t>(K));
+            mbar_arrive_expect_tx(bar1, 4u * static_cast<uint32_t>(K + TPAR_EXTRA_WAIT(a)));
         if (lane < K && TPAR_IN_RANGE(a.err, k, kSmallMaxRanks))
             st_async_f32(cluster_addr(smem_addr(&xmax[k]), static_cast<uint32_t>(lane)), cm,
                          cluster_addr(bar1, static_cast<uint32_t>(lane)));

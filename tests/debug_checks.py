@@ -7,6 +7,8 @@ and the results must match the oracle. Then the checks check themselves:
 with TPAR_DEBUG_SHRINK the [T, d] extent is one vector short, so the last
 vector's accesses must be reported (TPAR_DEVERR_INDEX) and skipped, leaving
 that vector's outputs untouched while every other row equals a plain call.
+Last, the bounded waits are made to expire (TPAR_DEBUG_WAIT_TIMEOUT) and must
+be reported, with the context left usable.
 """
 import os
 import sys
@@ -135,6 +137,36 @@ def run_shrink(tp):
     assert torch.equal(c2[:-1], codes[:-1])  # the input is unchanged, so is g
 
 
+def run_timeouts(tp):
+    """TPAR_DEBUG_WAIT_TIMEOUT: a wait expects one more arrival than will
+    come, so its %globaltimer bound (200 ms) expires. The kernel must report
+    it in the device error word and finish; every real arrival has landed by
+    then, so the outputs equal a plain call's, and the next plain call finds
+    the context usable and the error word clean."""
+    cases = [("cluster exchange", synth.DECODE_70B.with_(T=8), dict(), tp.TPAR_DEVERR_CLUSTER_WAIT),
+             ("single-cluster NVFP4", synth.NVFP4.with_(T=8), dict(nvfp4=True), tp.TPAR_DEVERR_SMALL_WAIT),
+             ("cooperative grid", synth.NVFP4.with_(T=40, d=2048), dict(nvfp4=True, flags=tp.TPAR_FORCE_GRID),
+              tp.TPAR_DEVERR_GRID_WAIT)]
+    for name, w, kw, bit in cases:
+        dev = to_device(synth.make_inputs(w))
+        base = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, **kw)
+        torch.cuda.synchronize()
+        expect_clean(tp, name + " plain")
+        kw2 = dict(kw, flags=kw.get("flags", 0) | tp.TPAR_DEBUG_WAIT_TIMEOUT)
+        out = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, **kw2)
+        torch.cuda.synchronize()
+        code = tp.tpar_device_error(torch.cuda.current_device())
+        assert code & bit, f"{name}: the expired wait was not reported ({code:#x})"
+        for k in ("out_norm", "out_residual"):
+            assert torch.equal(out[k].view(torch.int16), base[k].view(torch.int16)), (name, k)
+        if kw.get("nvfp4"):
+            assert torch.equal(out["codes"], base["codes"]) and torch.equal(out["scales"], base["scales"]), name
+        again = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, **kw)
+        torch.cuda.synchronize()
+        expect_clean(tp, name + " after the timeout")
+        assert torch.equal(again["out_norm"].view(torch.int16), base["out_norm"].view(torch.int16)), name
+
+
 def main():
     assert os.environ.get("TPAR_DEBUG") == "1", "run with TPAR_DEBUG=1"
     tp = lib()
@@ -142,6 +174,7 @@ def main():
     expect_clean(tp, "start")
     run_fused(tp)
     run_shrink(tp)
+    run_timeouts(tp)
     print("debug checks passed")
 
 

@@ -325,6 +325,7 @@ def test_debug_build_exports_the_same_abi(tp):
     assert dbg.tpar_debug_build() == 1
     assert tp.tpar_debug_build() is False
     assert call(tp, flags=tp.TPAR_DRY_RUN | tp.TPAR_DEBUG_SHRINK) == UNSUPPORTED
+    assert call(tp, flags=tp.TPAR_DRY_RUN | tp.TPAR_DEBUG_WAIT_TIMEOUT) == UNSUPPORTED
     assert tp.tpar_fp8_quantize(BASE, 8, 4096, BASE + 64 * MB, BASE + 80 * MB,
                                 tp.TPAR_DRY_RUN | tp.TPAR_DEBUG_SHRINK, 0, check=False) == INVALID
 
