@@ -447,3 +447,33 @@ def test_host_resident_tensors(case, n, T, d):
     ref = oracle_rows(inputs, slice(None), w.eps)
     assert_close_to_ref(orr, ref["h"], f"{case} host out_residual")
     assert_close_to_ref(on, ref["y"], f"{case} host out_norm")
+
+
+@pytest.mark.parametrize("form", ["row", "cluster", "rows_prefetch", "stream", "nvfp4_one_cluster", "nvfp4_grid",
+                                  "nvfp4_two_kernels", "fp8_one_cluster"])
+def test_in_place_residual_every_form(form):
+    """out_residual may be exactly the residual buffer: every kernel form reads
+    an element's residual before writing its new value, whatever the order in
+    which it stores."""
+    tp = lib()
+    shapes = {"row": (4, 100, 2048), "cluster": (8, 8, 4096), "rows_prefetch": (4, 400, 2048),
+              "stream": (4, 70, 4096), "nvfp4_one_cluster": (4, 8, 8192), "nvfp4_grid": (4, 40, 2048),
+              "nvfp4_two_kernels": (4, 333, 4096), "fp8_one_cluster": (8, 8, 4096)}
+    n, T, d = shapes[form]
+    w = synth.Workload(f"in place {form}", n, T, d, 1e-5, 0.5, seed=T + d)
+    inputs = synth.make_inputs(w)
+    dev = to_device(inputs)
+    res = dev["residual"].clone()
+    flags = {"row": tp.TPAR_FORCE_ROW, "stream": tp.TPAR_FORCE_STREAM, "nvfp4_grid": tp.TPAR_FORCE_GRID}.get(form, 0)
+    if form.startswith("fp8"):
+        out = tp.fused_rmsnorm_fp8(dev["partials"], res, dev["gamma"], w.eps, out_residual=res)
+    else:
+        out = tp.fused_rmsnorm(dev["partials"], res, dev["gamma"], w.eps, out_residual=res,
+                               nvfp4=form.startswith("nvfp4"), flags=flags)
+    torch.cuda.synchronize()
+    ref = oracle_rows(inputs, slice(None), w.eps)
+    assert_close_to_ref(res, ref["h"], f"{form} in-place residual")
+    assert_close_to_ref(out["out_norm"], ref["y"], f"{form} out_norm")
+    if form.startswith("nvfp4"):
+        assert_nvfp4_bit_exact(out["out_norm"], out["codes"], out["scales"], out["global_scale"], what=form)
+    assert tp.tpar_device_error(torch.cuda.current_device()) == 0
