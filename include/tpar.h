@@ -39,6 +39,9 @@
  *     device.
  *   - Arguments are checked on the host before anything is launched; a
  *     rejected call writes nothing. No exception crosses this interface.
+ *   - An entry point takes only the flags its comment lists; any other bit
+ *     (a flag it does not implement, or an undefined bit) is
+ *     TPAR_ERR_INVALID_ARG, never silently ignored.
  *   - Kernels launch with programmatic dependent launch (PDL) unless
  *     TPAR_NO_PDL is given: they wait for the preceding kernel on the stream
  *     to finish before reading any input.
@@ -223,6 +226,8 @@ tpar_status tpar_fused_rmsnorm(const void* const* partials, int n_ranks, const v
  *          in the 128x4 tiled GEMM layout (NVFP4 outputs required, d % 64
  *          == 0, buffer of TPAR_SCALES_128X4_BYTES(T, d) bytes, none of
  *          which may overlap another tensor); TPAR_ERR_INVALID_ARG otherwise.
+ *          TPAR_FORCE_GRID, TPAR_DTYPE_FP16, TPAR_DRY_RUN, and the debug
+ *          build's TPAR_DEBUG_SHRINK / TPAR_DEBUG_WAIT_TIMEOUT (above).
  *   plan   NULL for the automatic plan, else a complete plan to launch
  *          (validated: TPAR_ERR_INVALID_ARG if it does not cover a row).
  *   workspace  NULL for the device workspace, else a caller-owned device
@@ -246,8 +251,8 @@ tpar_status tpar_fused_rmsnorm_ex(const void* const* partials, int n_ranks, cons
  *   reduced      caller scratch, bf16 [T, d], must not overlap anything else
  *   out_residual required here (the norm reads it back)
  *   out_norm     required
- *   flags        TPAR_GSCALE_GIVEN, TPAR_NO_PDL, TPAR_SCALES_128X4 (as in
- *                tpar_fused_rmsnorm_ex)
+ *   flags        TPAR_GSCALE_GIVEN, TPAR_NO_PDL, TPAR_SCALES_128X4,
+ *                TPAR_DTYPE_FP16, TPAR_DRY_RUN (as in tpar_fused_rmsnorm_ex)
  * Other arguments as tpar_fused_rmsnorm.
  */
 tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const void* residual,
@@ -349,7 +354,8 @@ int64_t tpar_workspace_bytes(void);
  * calls no cudaMalloc, cudaFree or allocating routine.
  *
  * Arguments, results and rounding are those of tpar_unfused_rmsnorm without
- * `reduced`. T * d above TPAR_NOALLOC_MAX_ELEMENTS is rejected with
+ * `reduced`; flags: TPAR_GSCALE_GIVEN, TPAR_NO_PDL, TPAR_DRY_RUN,
+ * TPAR_DTYPE_FP16. T * d above TPAR_NOALLOC_MAX_ELEMENTS is rejected with
  * TPAR_ERR_SCRATCH_TOO_SMALL before anything is launched.
  *
  * The first call on a device looks up the array's device address

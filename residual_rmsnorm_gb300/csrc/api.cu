@@ -32,6 +32,23 @@ constexpr bool kDebugBuild = true;   // kernels check their indices (TPAR_IN_RAN
 constexpr bool kDebugBuild = false;
 #endif
 
+// Every flag an entry point accepts; a bit outside its set (an unknown bit,
+// or a flag that entry point does not implement) is TPAR_ERR_INVALID_ARG
+// rather than silently ignored.
+constexpr uint32_t kFlagsFused = TPAR_GSCALE_GIVEN | TPAR_FORCE_ROW | TPAR_FORCE_CLUSTER | TPAR_NO_PDL |
+                                 TPAR_DRY_RUN | TPAR_FORCE_STREAM | TPAR_DTYPE_FP16 | TPAR_SCALES_128X4 |
+                                 TPAR_DEBUG_SHRINK | TPAR_FORCE_GRID | TPAR_DEBUG_WAIT_TIMEOUT;
+constexpr uint32_t kFlagsUnfused = TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_DRY_RUN | TPAR_DTYPE_FP16 | TPAR_SCALES_128X4;
+constexpr uint32_t kFlagsNoAlloc = TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_DRY_RUN | TPAR_DTYPE_FP16;
+constexpr uint32_t kFlagsNvfp4Quantize =
+    TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_DRY_RUN | TPAR_DTYPE_FP16 | TPAR_SCALES_128X4 | TPAR_DEBUG_SHRINK;
+constexpr uint32_t kFlagsFusedFp8 = TPAR_GSCALE_GIVEN | TPAR_FORCE_ROW | TPAR_FORCE_CLUSTER | TPAR_NO_PDL |
+                                    TPAR_DRY_RUN | TPAR_DTYPE_FP16 | TPAR_DEBUG_SHRINK | TPAR_DEBUG_WAIT_TIMEOUT;
+constexpr uint32_t kFlagsFp8Quantize = TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_DRY_RUN | TPAR_DTYPE_FP16;
+constexpr uint32_t kFlagsPlan = TPAR_FORCE_ROW | TPAR_FORCE_CLUSTER | TPAR_FORCE_STREAM;
+
+bool flags_within(uint32_t flags, uint32_t allowed) { return (flags & ~allowed) == 0; }
+
 // The extent the debug index checks allow for a [T, d] tensor: T * d / 8
 // vectors, one fewer under the TPAR_DEBUG_SHRINK self-test.
 int64_t checked_vectors(int64_t T, int64_t d, uint32_t flags)
@@ -946,6 +963,8 @@ tpar_status tpar_fused_rmsnorm_ex(const void* const* partials, int n_ranks, cons
                                   uint8_t* nvfp4_scales, float* global_scale, uint32_t flags,
                                   const tpar_plan* plan, void* workspace, tpar_stream_t stream)
 {
+    if (!flags_within(flags, kFlagsFused))
+        return TPAR_ERR_INVALID_ARG;
     Call c{partials, n_ranks, residual, gamma, eps, T, d, out_norm, out_residual,
            nvfp4_codes, nvfp4_scales, global_scale, flags, nullptr};
     return fused_impl(c, plan, workspace, static_cast<cudaStream_t>(stream));
@@ -957,6 +976,8 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
                                  uint8_t* nvfp4_codes, uint8_t* nvfp4_scales, float* global_scale,
                                  uint32_t flags, tpar_stream_t stream_)
 {
+    if (!flags_within(flags, kFlagsUnfused))
+        return TPAR_ERR_INVALID_ARG;
     Call c{partials, n_ranks, residual, gamma, eps, T, d, out_norm, out_residual,
            nvfp4_codes, nvfp4_scales, global_scale,
            flags & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_DTYPE_FP16 | TPAR_SCALES_128X4 | TPAR_DEBUG_SHRINK),
@@ -1026,6 +1047,8 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
 tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* codes, uint8_t* scales,
                                 float* global_scale, uint32_t flags, tpar_stream_t stream_)
 {
+    if (!flags_within(flags, kFlagsNvfp4Quantize))
+        return TPAR_ERR_INVALID_ARG;
     if (T < 0 || d < 16 || d % 16 != 0)
         return TPAR_ERR_INVALID_ARG;
     if (d > TPAR_MAX_HIDDEN)
@@ -1077,6 +1100,8 @@ tpar_status tpar_fused_rmsnorm_fp8(const void* const* partials, int n_ranks, con
                                    void* out_residual, uint8_t* fp8_codes, float* fp8_scale, uint32_t flags,
                                    tpar_stream_t stream_)
 {
+    if (!flags_within(flags, kFlagsFusedFp8))
+        return TPAR_ERR_INVALID_ARG;
     const bool given = (flags & TPAR_GSCALE_GIVEN) != 0;
     Call c{partials, n_ranks, residual, gamma, eps, T, d, out_norm, out_residual, nullptr, nullptr, nullptr,
            flags & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_FORCE_ROW | TPAR_FORCE_CLUSTER | TPAR_DTYPE_FP16 |
@@ -1154,6 +1179,8 @@ tpar_status tpar_fused_rmsnorm_fp8(const void* const* partials, int n_ranks, con
 tpar_status tpar_fp8_quantize(const void* x, int64_t T, int64_t d, uint8_t* codes, float* scale, uint32_t flags,
                               tpar_stream_t stream_)
 {
+    if (!flags_within(flags, kFlagsFp8Quantize))
+        return TPAR_ERR_INVALID_ARG;
     if (T < 0 || d < 8 || d % 8 != 0)
         return TPAR_ERR_INVALID_ARG;
     if (d > TPAR_MAX_HIDDEN)
@@ -1208,6 +1235,8 @@ tpar_status tpar_fp8_quantize(const void* x, int64_t T, int64_t d, uint8_t* code
 
 tpar_status tpar_plan_launch(int64_t T, int64_t d, int n_ranks, int sm_count, uint32_t flags, tpar_plan* out)
 {
+    if (!flags_within(flags, kFlagsPlan))
+        return TPAR_ERR_INVALID_ARG;
     return plan_impl(T, d, n_ranks, sm_count, flags, out);
 }
 
@@ -1306,6 +1335,8 @@ extern "C" tpar_status tpar_unfused_rmsnorm_noalloc(const void* const* partials,
                                                     float* global_scale, uint32_t flags,
                                                     tpar_stream_t stream_)
 {
+    if (!flags_within(flags, kFlagsNoAlloc))
+        return TPAR_ERR_INVALID_ARG;
     if (T > 0 && d > 0 && T > kNoAllocMaxElems / d)
         return TPAR_ERR_SCRATCH_TOO_SMALL;
     const uint32_t fl = flags & (TPAR_GSCALE_GIVEN | TPAR_NO_PDL | TPAR_DRY_RUN | TPAR_DTYPE_FP16);

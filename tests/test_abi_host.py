@@ -339,3 +339,31 @@ def test_force_grid_flag_checks(tp):
     assert call(tp, flags=D | F) == INVALID                                   # no NVFP4
     assert call(tp, flags=D | F | tp.TPAR_GSCALE_GIVEN, **nv) == INVALID      # given scale
     assert call(tp, flags=D | F | tp.TPAR_FORCE_ROW, **nv) == INVALID         # two kernels forced
+
+
+def test_unsupported_flags_are_refused_not_ignored(tp):
+    """Each entry point refuses a flag it does not implement (and any
+    undefined bit) instead of silently ignoring it."""
+    D = tp.TPAR_DRY_RUN
+    undefined = 0x80000
+    assert call(tp, flags=D | undefined) == INVALID
+    parts = [BASE + r * 4 * MB for r in range(4)]
+    nv = (BASE + 200 * MB, BASE + 240 * MB, BASE + 250 * MB)
+    u = lambda fl: tp.tpar_unfused_rmsnorm(parts, 4, BASE + 64 * MB, BASE + 96 * MB, 1e-5, 8, 4096,
+                                           BASE + 300 * MB, BASE + 128 * MB, BASE + 160 * MB, *nv, fl, 0,
+                                           check=False)
+    assert u(D) == OK and u(D | tp.TPAR_FORCE_STREAM) == INVALID and u(D | tp.TPAR_FORCE_GRID) == INVALID
+    na = lambda fl: tp.tpar_unfused_rmsnorm_noalloc(parts, 4, BASE + 64 * MB, BASE + 96 * MB, 1e-5, 8, 4096,
+                                                    BASE + 128 * MB, BASE + 160 * MB, *nv, fl, 0, check=False)
+    assert na(D) == OK and na(D | tp.TPAR_SCALES_128X4) == INVALID and na(D | tp.TPAR_FORCE_ROW) == INVALID
+    q = lambda fl: tp.tpar_nvfp4_quantize(BASE, 8, 4096, BASE + 64 * MB, BASE + 80 * MB, BASE + 90 * MB, fl, 0,
+                                          check=False)
+    assert q(D) == OK and q(D | tp.TPAR_FORCE_ROW) == INVALID and q(D | undefined) == INVALID
+    f = lambda fl: tp.tpar_fused_rmsnorm_fp8(parts, 4, BASE + 64 * MB, BASE + 96 * MB, 1e-5, 8, 4096,
+                                             BASE + 128 * MB, BASE + 160 * MB, BASE + 200 * MB, BASE + 240 * MB, fl,
+                                             0, check=False)
+    assert f(D) == OK and f(D | tp.TPAR_FORCE_STREAM) == INVALID and f(D | tp.TPAR_FORCE_GRID) == INVALID
+    assert tp.tpar_fp8_quantize(BASE, 8, 4096, BASE + 64 * MB, BASE + 80 * MB, D | tp.TPAR_FORCE_ROW, 0,
+                                check=False) == INVALID
+    with pytest.raises(tp.TparError):
+        tp.tpar_plan_launch(8, 4096, 8, 152, tp.TPAR_GSCALE_GIVEN)
