@@ -674,7 +674,7 @@ def ours_arm(args, w):
                        "l2_policy": (f"inputs larger than L2: calls rotate over {n_sets} input sets, "
                                      f"{n_sets * per_call / 2**20:.0f} MiB vs L2 "
                                      f"{l2_bytes(torch) / 2**20:.0f} MiB"),
-                       "parallelism": f"replicas x{world}"},
+                       "parallelism": f"dp{world} (each rank its own calls, no collective)"},
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                          "frac": round(achieved / peak, 4), "traffic": traffic,
                          "peak_source": f"{peak_kind} (MEASURED_PEAKS.json hbm_gbs)" if peak_kind ==
