@@ -485,8 +485,9 @@ tpar_status plan_impl(int64_t T, int64_t d, int n_ranks, int sm_count, uint32_t 
     const int nvec = static_cast<int>(d / 8);
     int split = 1;
     // The TMA-fed stream kernel is built and tested but measured slower than
-    // the row kernel at prefill (117-120 us vs 111.6 us for N=8, T=4096,
-    // d=8192), so it runs only when asked for.
+    // the prefetching kernel at prefill (117-120 us vs 110-112 us for N=8,
+    // T=4096, d=8192) and than the cluster kernel at decode (4.7-5.8 vs
+    // 2.4-2.5 us), so it runs only when asked for.
     if (flags & TPAR_FORCE_STREAM) {
         // Bandwidth path: one persistent CTA per SM, fed by TMA bulk copies.
         tpar_plan p;

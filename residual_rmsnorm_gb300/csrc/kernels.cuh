@@ -7,13 +7,16 @@
 // residual add -> store residual_out -> RMSNorm(gamma) -> store norm_out ->
 // optional NVFP4 (6.5), in that order, without an intermediate trip to HBM.
 //
-// One kernel covers both regimes:
+// This kernel has two forms (the prefetching persistent form for many rows
+// is rows_prefetch_kernel, rows.cuh):
 //   * row kernel (CLUSTER = false): one CTA owns a whole row; the row's sum
 //     of squares is reduced with warp shuffles and one shared-memory step.
 //   * cluster kernel (CLUSTER = true): a row is split across the `split` CTAs
 //     of a thread-block cluster so that a handful of decode tokens still
-//     spreads over ~all SMs; the CTAs exchange their partial sums of squares
-//     through distributed shared memory behind one cluster barrier.
+//     spreads over many SMs; every warp pushes its 32-vector partial sum of
+//     squares into the same slot of every peer's shared memory (st.async,
+//     counted on the peer's mbarrier, bounded wait), and each CTA adds them
+//     in the canonical order.
 // Thread k of a CTA owns the 16-byte vectors vbeg + k + j*blockDim.x,
 // j < VPT, of its slice of the row, so every load and store instruction of a
 // warp touches 512 contiguous bytes.
