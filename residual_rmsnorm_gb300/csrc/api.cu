@@ -239,12 +239,17 @@ int forced_kernels(uint32_t flags)
 }
 
 // Ring depth of the stream kernel for rows of row_bytes: ~192 KB of shared
-// memory in flight per SM, at least 2 stages.
+// memory in flight per SM, at least 2 stages. Rows of the stream kernel are
+// at most 512 x 8 vectors (64 KB), so there are always >= 3 stages and the
+// ring plus its 16-byte stage barriers stays within kStreamSmemMax.
+constexpr int kStreamRingBytes = 192 * 1024;
+constexpr int kStreamMaxStages = 48;
+constexpr int kStreamSmemMax = kStreamRingBytes + 16 * kStreamMaxStages;
 int stream_stages(int64_t row_bytes)
 {
-    int64_t s = (192 * 1024) / row_bytes;
-    if (s > 48)
-        s = 48;
+    int64_t s = kStreamRingBytes / row_bytes;
+    if (s > kStreamMaxStages)
+        s = kStreamMaxStages;
     return static_cast<int>(s < 2 ? 2 : s);
 }
 
@@ -258,8 +263,10 @@ int rows_stages(int64_t d, int nsrc)
     return static_cast<int>(std::min<int64_t>(s, tpar::kRowsMaxStages));
 }
 
-// cudaFuncSetAttribute once per (kernel, attribute, value): a host call,
-// kept off the per-call path.
+// cudaFuncSetAttribute, skipped while the (device, kernel, attribute) entry
+// already holds `value`: a host call, kept off the per-call path. A new value
+// is set and replaces the entry, so a lowered limit is never mistaken for a
+// higher one set earlier.
 cudaError_t set_attr_once(const void* fn, cudaFuncAttribute attr, int value)
 {
     struct Entry {
@@ -275,11 +282,20 @@ cudaError_t set_attr_once(const void* fn, cudaFuncAttribute attr, int value)
     if (cudaGetDevice(&dev) != cudaSuccess)
         return cudaFuncSetAttribute(fn, attr, value);
     std::lock_guard<std::mutex> lock(mu);
+    int slot = -1;
     for (int i = 0; i < used; ++i)
-        if (done[i].device == dev && done[i].fn == fn && done[i].attr == attr && done[i].value == value)
-            return cudaSuccess;
+        if (done[i].device == dev && done[i].fn == fn && done[i].attr == attr) {
+            if (done[i].value == value)
+                return cudaSuccess;
+            slot = i;
+            break;
+        }
     const cudaError_t e = cudaFuncSetAttribute(fn, attr, value);
-    if (e == cudaSuccess && used < 128)
+    if (e != cudaSuccess)
+        return e;
+    if (slot >= 0)
+        done[slot].value = value;
+    else if (used < 128)
         done[used++] = Entry{dev, fn, attr, value};
     return e;
 }
@@ -579,7 +595,11 @@ tpar_status launch_stream(const FusedArgs& a, int qmode, const tpar_plan& p, cud
     sa.stages = stream_stages(row_bytes);
     sa.consumers = p.threads;
     const size_t smem = static_cast<size_t>(sa.stages) * row_bytes + 16u * sa.stages;
-    if (set_attr_once(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) != cudaSuccess)
+    if (smem > static_cast<size_t>(kStreamSmemMax))
+        return TPAR_ERR_UNSUPPORTED;
+    // one limit for every row size, so calls of different sizes never
+    // re-set it between launches
+    if (set_attr_once(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kStreamSmemMax) != cudaSuccess)
         return TPAR_ERR_CUDA;
     return launch(fn, dim3(static_cast<unsigned>(p.grid_rows)), dim3(static_cast<unsigned>(p.threads + 32)), &sa,
                   stream, 1, pdl, smem) == cudaSuccess
@@ -627,6 +647,8 @@ tpar_status launch_fused(const FusedArgs& a, int qmode, const tpar_plan& p, cuda
     }
     FusedArgs args = a;
     args.err = device_error_word();
+    // the vectors of a row each CTA owns, from the plan (every caller's)
+    args.slice = p.kernel == 1 ? slice_for(a.nvec, p.split) : a.nvec;
     dim3 grid(static_cast<unsigned>(p.split), static_cast<unsigned>(p.grid_rows), 1);
     dim3 block(static_cast<unsigned>(p.threads), 1, 1);
     if (launch(fn, grid, block, &args, stream, p.kernel == 1 ? p.split : 1, pdl) != cudaSuccess)
@@ -906,7 +928,6 @@ tpar_status fused_impl(const Call& c, const tpar_plan* user_plan, void* user_ws,
                    : TPAR_ERR_CUDA;
     }
     FusedArgs a = fused_args(c);
-    a.slice = p.kernel == 1 ? slice_for(a.nvec, p.split) : a.nvec;
     if (!nvfp4)
         return launch_fused(a, tpar::kQuantNone, p, stream, pdl);
     if (given)
@@ -1142,7 +1163,6 @@ tpar_status tpar_fused_rmsnorm_fp8(const void* const* partials, int n_ranks, con
         return st;
     const bool pdl = (flags & TPAR_NO_PDL) == 0;
     FusedArgs a = fused_args(c);
-    a.slice = p.kernel == 1 ? slice_for(a.nvec, p.split) : a.nvec;
     if (given) {
         a.q8 = reinterpret_cast<uint2*>(fp8_codes);
         a.gscale = fp8_scale;

@@ -18,13 +18,21 @@ from . import _abi
 _DTYPES = (torch.bfloat16, torch.float16)
 
 
-def _check_bf16(name, t, shape=None, dtype=None):
-    """A CUDA, contiguous tensor of the call's element type (bf16, or fp16 for
-    the whole call), of the given shape."""
+def _check_place(name, t, device=None):
+    """On the call's CUDA device, or in pinned host memory."""
+    if t.device.type == "cuda":
+        if device is not None and t.device != device:
+            raise ValueError(f"{name} is on {t.device}, the call runs on {device}")
+    elif not (t.device.type == "cpu" and t.is_pinned()):
+        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory (no CPU compute path exists)")
+
+
+def _check_bf16(name, t, shape=None, dtype=None, device=None):
+    """A contiguous tensor of the call's element type (bf16, or fp16 for the
+    whole call), of the given shape, on the call's device or pinned."""
     if not isinstance(t, torch.Tensor):
         raise TypeError(f"{name} must be a torch.Tensor")
-    if t.device.type != "cuda" and not (t.device.type == "cpu" and t.is_pinned()):
-        raise ValueError(f"{name} must be a CUDA tensor or pinned host memory (no CPU compute path exists)")
+    _check_place(name, t, device)
     want = dtype if dtype is not None else t.dtype
     if t.dtype not in _DTYPES or t.dtype != want:
         raise TypeError(f"{name} must be {want if dtype is not None else 'bf16 or fp16'}, got {t.dtype}")
@@ -37,6 +45,20 @@ def _check_bf16(name, t, shape=None, dtype=None):
 def _stream_handle(device, stream):
     s = stream if stream is not None else torch.cuda.current_stream(device)
     return s.cuda_stream
+
+
+def _check_scale(name, t, device):
+    """A one-element fp32 scale (input or output) on the call's device."""
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != torch.float32 or t.numel() != 1 or t.device != device:
+        raise ValueError(f"{name} must be a 1-element fp32 tensor on {device}")
+
+
+def _shape_2d(name, t):
+    if not isinstance(t, torch.Tensor) or t.dim() != 2:
+        raise ValueError(f"{name} must be a 2-D [T, d] tensor")
+    return tuple(t.shape)
 
 
 def _device_of(*tensors) -> torch.device:
@@ -60,10 +82,31 @@ def _nvfp4_outputs(T, d, device, global_scale, scales_128x4=False):
         given = False
     else:
         g = global_scale
-        if g.dtype != torch.float32 or g.numel() != 1 or g.device.type != "cuda":
-            raise ValueError("global_scale must be a 1-element fp32 CUDA tensor")
+        _check_scale("global_scale", g, device)
         given = True
     return codes, scales, g, given
+
+
+def _epilogue_inputs(partials, residual, gamma, flags):
+    """Check the inputs of an epilogue call: N >= 1 partials [T, d] of one
+    element type, the residual (or None) and gamma [d] (or None for the
+    all-reduce-only pattern), all on one device. Returns (partials, T, d,
+    dtype, device, flags with TPAR_DTYPE_FP16 for fp16)."""
+    partials = list(partials)
+    if not partials:
+        raise ValueError("need at least one partial")
+    T, d = _shape_2d("partials[0]", partials[0])
+    dev = _device_of(*partials, residual, gamma)
+    dt = partials[0].dtype
+    if dt == torch.float16:
+        flags |= _abi.TPAR_DTYPE_FP16
+    for i, p in enumerate(partials):
+        _check_bf16(f"partials[{i}]", p, (T, d), dt, dev)
+    if residual is not None:
+        _check_bf16("residual", residual, (T, d), dt, dev)
+    if gamma is not None:
+        _check_bf16("gamma", gamma, (d,), dt, dev)
+    return partials, T, d, dt, dev, flags
 
 
 def fused_rmsnorm(partials, residual, gamma, eps: float, *, out_norm=None, out_residual=None,
@@ -81,26 +124,16 @@ def fused_rmsnorm(partials, residual, gamma, eps: float, *, out_norm=None, out_r
     read (TPAR_SCALES_128X4; d % 64 == 0; padding rows zero).
     Returns dict(out_norm, out_residual, codes, scales, global_scale).
     """
-    partials = list(partials)
-    if not partials:
-        raise ValueError("need at least one partial")
-    T, d = partials[0].shape
-    dev = _device_of(*partials, residual, gamma)
-    dt = partials[0].dtype
-    if dt == torch.float16:
-        flags |= _abi.TPAR_DTYPE_FP16
-    for i, p in enumerate(partials):
-        _check_bf16(f"partials[{i}]", p, (T, d), dt)
-    if residual is not None:
-        _check_bf16("residual", residual, (T, d), dt)
-    _check_bf16("gamma", gamma, (d,), dt)
+    if gamma is None:
+        raise ValueError("gamma is required (allreduce_sum is the pattern without a norm)")
+    partials, T, d, dt, dev, flags = _epilogue_inputs(partials, residual, gamma, flags)
     if out_norm is None and (emit_norm or not nvfp4 or global_scale is None):
         out_norm = torch.empty((T, d), dtype=dt, device=dev)
     if out_norm is not None:
-        _check_bf16("out_norm", out_norm, (T, d), dt)
+        _check_bf16("out_norm", out_norm, (T, d), dt, dev)
     if out_residual is None:
         out_residual = torch.empty((T, d), dtype=dt, device=dev)
-    _check_bf16("out_residual", out_residual, (T, d), dt)
+    _check_bf16("out_residual", out_residual, (T, d), dt, dev)
     codes = scales = g = None
     if nvfp4:
         codes, scales, g, given = _nvfp4_outputs(T, d, dev, global_scale, scales_128x4)
@@ -123,20 +156,9 @@ def fused_rmsnorm(partials, residual, gamma, eps: float, *, out_norm=None, out_r
 def allreduce_sum(partials, residual=None, *, out=None, flags: int = 0, stream=None):
     """The all-reduce-only pattern: out = bf16(sum(partials) [+ residual]), one
     rounding, no norm (``tpar_fused_rmsnorm`` with out_norm = gamma = NULL)."""
-    partials = list(partials)
-    if not partials:
-        raise ValueError("need at least one partial")
-    T, d = partials[0].shape
-    dev = _device_of(*partials, residual)
-    dt = partials[0].dtype
-    if dt == torch.float16:
-        flags |= _abi.TPAR_DTYPE_FP16
-    for i, p in enumerate(partials):
-        _check_bf16(f"partials[{i}]", p, (T, d), dt)
-    if residual is not None:
-        _check_bf16("residual", residual, (T, d), dt)
+    partials, T, d, dt, dev, flags = _epilogue_inputs(partials, residual, None, flags)
     out = torch.empty((T, d), dtype=dt, device=dev) if out is None else out
-    _check_bf16("out", out, (T, d), dt)
+    _check_bf16("out", out, (T, d), dt, dev)
     with torch.cuda.device(dev):
         _abi.tpar_fused_rmsnorm_ex(
             [p.data_ptr() for p in partials], len(partials),
@@ -149,21 +171,15 @@ def unfused_rmsnorm(partials, residual, gamma, eps: float, *, reduced=None, out_
                     out_residual=None, nvfp4: bool = False, global_scale=None, scales_128x4: bool = False,
                     flags: int = 0, stream=None):
     """The same epilogue as separate kernels through HBM (the comparison baseline)."""
-    partials = list(partials)
-    T, d = partials[0].shape
-    dev = _device_of(*partials, residual, gamma)
-    dt = partials[0].dtype
-    if dt == torch.float16:
-        flags |= _abi.TPAR_DTYPE_FP16
-    for i, p in enumerate(partials):
-        _check_bf16(f"partials[{i}]", p, (T, d), dt)
-    if residual is not None:
-        _check_bf16("residual", residual, (T, d), dt)
-    _check_bf16("gamma", gamma, (d,), dt)
+    if gamma is None:
+        raise ValueError("gamma is required")
+    partials, T, d, dt, dev, flags = _epilogue_inputs(partials, residual, gamma, flags)
     reduced = torch.empty((T, d), dtype=dt, device=dev) if reduced is None else reduced
     out_norm = torch.empty((T, d), dtype=dt, device=dev) if out_norm is None else out_norm
     out_residual = (torch.empty((T, d), dtype=dt, device=dev)
                     if out_residual is None else out_residual)
+    for name, t in (("reduced", reduced), ("out_norm", out_norm), ("out_residual", out_residual)):
+        _check_bf16(name, t, (T, d), dt, dev)
     codes = scales = g = None
     if nvfp4:
         codes, scales, g, given = _nvfp4_outputs(T, d, dev, global_scale, scales_128x4)
@@ -186,11 +202,11 @@ def nvfp4_quantize(x, global_scale: torch.Tensor | None = None, scales_128x4: bo
                    stream=None):
     """NVFP4 quantisation of a bf16 [T, d] CUDA tensor -> (codes, scales, global_scale).
     ``scales_128x4=True``: scales flat in the 128x4 tiled GEMM layout."""
-    _check_bf16("x", x)
-    T, d = x.shape
+    T, d = _shape_2d("x", x)
+    dev = _device_of(x)
+    _check_bf16("x", x, None, None, dev)
     if x.dtype == torch.float16:
         flags |= _abi.TPAR_DTYPE_FP16
-    dev = _device_of(x)
     codes, scales, g, given = _nvfp4_outputs(T, d, dev, global_scale, scales_128x4)
     if given:
         flags |= _abi.TPAR_GSCALE_GIVEN
@@ -207,24 +223,18 @@ def fused_rmsnorm_fp8(partials, residual, gamma, eps: float, *, scale: torch.Ten
     """sum + residual -> RMSNorm -> per-tensor FP8 (E4M3). ``scale`` (a 1-element
     fp32 tensor) given: calibrated single pass; None: s = amax/448 computed.
     Returns dict(out_norm, out_residual, codes uint8 [T, d], scale)."""
-    partials = list(partials)
-    T, d = partials[0].shape
-    dev = _device_of(*partials, residual, gamma)
-    dt = partials[0].dtype
-    if dt == torch.float16:
-        flags |= _abi.TPAR_DTYPE_FP16
-    for i, p in enumerate(partials):
-        _check_bf16(f"partials[{i}]", p, (T, d), dt)
-    if residual is not None:
-        _check_bf16("residual", residual, (T, d), dt)
-    _check_bf16("gamma", gamma, (d,), dt)
+    if gamma is None:
+        raise ValueError("gamma is required")
+    partials, T, d, dt, dev, flags = _epilogue_inputs(partials, residual, gamma, flags)
     out_norm = torch.empty((T, d), dtype=dt, device=dev) if (emit_norm or scale is None) else None
     out_residual = torch.empty((T, d), dtype=dt, device=dev) if out_residual is None else out_residual
+    _check_bf16("out_residual", out_residual, (T, d), dt, dev)
     codes = torch.empty((T, d), dtype=torch.uint8, device=dev)
     if scale is None:
         s = torch.empty((1,), dtype=torch.float32, device=dev)
     else:
         s = scale
+        _check_scale("scale", s, dev)
         flags |= _abi.TPAR_GSCALE_GIVEN
     with torch.cuda.device(dev):
         _abi.tpar_fused_rmsnorm_fp8(
@@ -237,16 +247,17 @@ def fused_rmsnorm_fp8(partials, residual, gamma, eps: float, *, scale: torch.Ten
 
 def fp8_quantize(x, scale: torch.Tensor | None = None, flags: int = 0, stream=None):
     """Per-tensor FP8 (E4M3) quantisation of a bf16 [T, d] CUDA tensor -> (codes, scale)."""
-    _check_bf16("x", x)
-    T, d = x.shape
+    T, d = _shape_2d("x", x)
+    dev = _device_of(x)
+    _check_bf16("x", x, None, None, dev)
     if x.dtype == torch.float16:
         flags |= _abi.TPAR_DTYPE_FP16
-    dev = _device_of(x)
     codes = torch.empty((T, d), dtype=torch.uint8, device=dev)
     if scale is None:
         s = torch.empty((1,), dtype=torch.float32, device=dev)
     else:
         s = scale
+        _check_scale("scale", s, dev)
         flags |= _abi.TPAR_GSCALE_GIVEN
     with torch.cuda.device(dev):
         _abi.tpar_fp8_quantize(x.data_ptr(), T, d, codes.data_ptr(), s.data_ptr(), flags,

@@ -297,3 +297,48 @@ def test_concurrent_streams_with_their_own_workspaces(T):
     ref = oracle_rows(plain, rows, plain_w.eps)
     assert_close_to_ref(p_out["out_norm"][rows], ref["y"], "third stream")
     assert tp.tpar_device_error(torch.cuda.current_device()) == 0
+
+
+def test_stream_kernel_rows_of_changing_size():
+    """The TMA-fed kernel's shared-memory ring depends on the row size. Calls
+    whose rings grow, shrink and grow again on one kernel instantiation must
+    all launch and give the row kernel's bits."""
+    tp = lib()
+    for d in (2048, 1024, 2048, 8192, 1024, 8192, 4096):
+        w = synth.Workload("stream sizes", 4, 20, d, 1e-5, 0.5, seed=d)
+        dev = to_device(synth.make_inputs(w))
+        a = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, flags=tp.TPAR_FORCE_STREAM)
+        b = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, flags=tp.TPAR_FORCE_ROW)
+        torch.cuda.synchronize()
+        assert same_bits(a["out_norm"], b["out_norm"]), d
+        assert same_bits(a["out_residual"], b["out_residual"]), d
+    assert tp.tpar_device_error(torch.cuda.current_device()) == 0
+
+
+@pytest.mark.parametrize("nvfp4", [False, True])
+@pytest.mark.parametrize("T,d,form", [(8, 16384, 1), (1, 32768, 1), (20, 32768, 1), (400, 2048, 3), (37, 4096, 0)])
+def test_unfused_norm_kernel_in_every_form(T, d, form, nvfp4):
+    """The unfused path's norm kernel (K3) runs whichever form the planner
+    picks for one source: a cluster split for long rows at few tokens, the
+    prefetching kernel for many rows, else one CTA per row. Each must match
+    the oracle and, bit for bit, the one-source fused call on K2's output."""
+    tp = lib()
+    sm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    assert tp.tpar_plan_launch(T, d, 1, sm).kernel == form
+    w = synth.Workload("unfused forms", 4, T, d, 1e-6, 0.5, seed=T + d)
+    inputs = synth.make_inputs(w)
+    dev = to_device(inputs)
+    u = tp.unfused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=nvfp4)
+    one = tp.fused_rmsnorm([u["out_residual"]], None, dev["gamma"], w.eps, flags=tp.TPAR_FORCE_ROW)
+    torch.cuda.synchronize()
+    assert tp.tpar_device_error(torch.cuda.current_device()) == 0
+    rows = np.unique([0, T // 2, T - 1])
+    sub = {"partials": [p[rows] for p in inputs["partials"]], "residual": inputs["residual"][rows],
+           "gamma": inputs["gamma"]}
+    ref = oracle_rows(sub, slice(None), w.eps)
+    eh, ey = unfused_extra_tolerance(sub, ref, w.eps)
+    assert_close_to_ref(u["out_residual"][rows], ref["h"], "unfused out_residual", extra=eh)
+    assert_close_to_ref(u["out_norm"][rows], ref["y"], "unfused out_norm", extra=ey)
+    assert same_bits(u["out_norm"], one["out_norm"])
+    if nvfp4:
+        assert_nvfp4_bit_exact(u["out_norm"], u["codes"], u["scales"], u["global_scale"], what="unfused")
