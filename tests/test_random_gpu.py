@@ -3,15 +3,20 @@ oracle: ranks (1..16, odd counts included), T (0..700), d (any multiple of 8
 up to 9216; 16 or 64 when the output needs it), element type, residual
 present or not, output pattern (norm, sum only, NVFP4 given / dynamic, 128x4
 scales, FP8) and forced kernel form (row, cluster, TMA-fed, cooperative
-grid). The cases are drawn once from a fixed
-seed, so a failure names a reproducible case."""
+grid). A second sweep covers the rest of the API: the unfused entry point
+(plain and with NVFP4), the standalone NVFP4 and FP8 quantisers, the FP8
+and NVFP4 given-scale patterns without a bf16 norm output, and the
+in-place residual, with d up to the largest supported hidden size. The
+cases are drawn once from fixed seeds, so a failure names a reproducible
+case."""
 import numpy as np
 import pytest
 import torch
 
 import oracle
 import synth
-from gpu_helpers import assert_close_to_ref, assert_nvfp4_bit_exact, lib, oracle_rows, to_device
+from gpu_helpers import (assert_close_to_ref, assert_nvfp4_bit_exact, lib, oracle_rows, to_device,
+                         unfused_extra_tolerance)
 
 pytestmark = pytest.mark.gpu
 
@@ -85,4 +90,131 @@ def test_random_case(case):
                 assert_nvfp4_bit_exact(out["out_norm"], out["codes"], out["scales"], out["global_scale"],
                                        given=float(np.float32(0.05)) if given else None, what=f"case {i}",
                                        scales_128x4=mode == "nvfp4_128x4")
+    assert tp.tpar_device_error(torch.cuda.current_device()) == 0
+
+
+API_MODES = ("unfused", "unfused_nvfp4_dyn", "unfused_nvfp4_given", "unfused_128x4", "quant_nvfp4_dyn",
+             "quant_nvfp4_given", "quant_128x4", "quant_fp8_dyn", "quant_fp8_given", "fp8_given",
+             "fp8_given_no_norm", "nvfp4_given_no_norm", "norm_inplace", "nvfp4_dyn_inplace")
+
+
+def _api_cases(n_cases=200, seed=2025):
+    rng = np.random.default_rng(seed)
+    out = []
+    for i in range(n_cases):
+        n = int(rng.choice([1, 2, 3, 4, 5, 8, 11, 16]))
+        T = int(rng.choice([0, 1, 2, 3, 5, 8, 13, 16, 17, 31, 33, 47, 48, 49, 64, 100, 229, 300, 457]))
+        mode = str(rng.choice(API_MODES))
+        step = 64 if "128x4" in mode else (16 if "nvfp4" in mode else 8)
+        if rng.random() < 0.5:
+            d = int(step * rng.integers(1, 32768 // step + 1))
+        else:  # wide rows: the cluster split and the largest hidden sizes
+            d = int(rng.choice([8192, 12288, 16384, 20480, 24576, 28672, 32768]))
+        if n * T * d > 40_000_000:  # keep the oracle quick
+            T = max(1, 40_000_000 // (n * d))
+        residual = bool(rng.random() < 0.8)
+        dtype = "fp16" if rng.random() < 0.25 else "bf16"
+        force = str(rng.choice(["auto", "auto", "row", "cluster"]))
+        out.append((i, n, T, d, mode, residual, dtype, force))
+    return out
+
+
+def _sub(inputs, rows):
+    return {"partials": [p[rows] for p in inputs["partials"]],
+            "residual": None if inputs["residual"] is None else inputs["residual"][rows],
+            "gamma": inputs["gamma"]}
+
+
+@pytest.mark.parametrize("case", _api_cases(),
+                         ids=lambda c: f"a{c[0]}-N{c[1]}-T{c[2]}-d{c[3]}-{c[4]}-{c[6]}-{c[7]}")
+def test_random_api_case(case):
+    i, n, T, d, mode, residual, dtype, force = case
+    tp = lib()
+    dt = torch.float16 if dtype == "fp16" else torch.bfloat16
+    w = synth.Workload(f"random api {i}", n, T, d, 1e-5, 0.5, seed=5000 + i)
+    inputs = synth.make_inputs(w, dtype=dt)
+    if not residual:
+        inputs = dict(inputs, residual=None)
+    dev = to_device(inputs)
+    flags = {"auto": 0, "row": tp.TPAR_FORCE_ROW, "cluster": tp.TPAR_FORCE_CLUSTER}[force]
+    if force == "cluster" and d < 32:
+        flags = 0
+    rows = np.arange(T) if T <= 64 else np.unique(np.concatenate([[0, T - 1],
+                                                                  np.random.default_rng(i).choice(T, 24)]))
+    gv = 0.05
+    g = torch.tensor([gv], dtype=torch.float32, device="cuda")
+    given = float(np.float32(gv))
+    what = f"api case {i} {mode}"
+
+    if mode.startswith("unfused"):
+        nv = mode != "unfused"
+        out = tp.unfused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=nv,
+                                 global_scale=g if mode == "unfused_nvfp4_given" else None,
+                                 scales_128x4=mode == "unfused_128x4")
+        torch.cuda.synchronize()
+        if T:
+            sub = _sub(inputs, rows)
+            ref = oracle_rows(sub, slice(None), w.eps, residual=residual)
+            eh, ey = unfused_extra_tolerance(sub, ref, w.eps)
+            assert_close_to_ref(out["out_residual"][rows], ref["h"], what + " out_residual", extra=eh)
+            assert_close_to_ref(out["out_norm"][rows], ref["y"], what + " out_norm", extra=ey)
+            if nv:
+                assert_nvfp4_bit_exact(out["out_norm"], out["codes"], out["scales"], out["global_scale"],
+                                       given=given if mode == "unfused_nvfp4_given" else None, what=what,
+                                       scales_128x4=mode == "unfused_128x4")
+    elif mode.startswith("quant_"):
+        x = dev["partials"][0]
+        if mode == "quant_fp8_dyn" or mode == "quant_fp8_given":
+            codes, s = tp.fp8_quantize(x, scale=g if mode == "quant_fp8_given" else None)
+            torch.cuda.synchronize()
+            if T:
+                oc, os_ = oracle.fp8_quantize(synth.bits(x), scale=given if mode == "quant_fp8_given" else None,
+                                              dtype=dtype)
+                assert np.array_equal(codes.cpu().numpy(), oc), what
+                assert np.float32(s.item()) == os_, what
+        else:
+            codes, scales, gg = tp.nvfp4_quantize(x, global_scale=g if mode == "quant_nvfp4_given" else None,
+                                                  scales_128x4=mode == "quant_128x4")
+            torch.cuda.synchronize()
+            if T:
+                assert_nvfp4_bit_exact(x, codes, scales, gg, given=given if mode == "quant_nvfp4_given" else None,
+                                       what=what, scales_128x4=mode == "quant_128x4")
+    elif mode.startswith("fp8_given"):
+        full = tp.fused_rmsnorm_fp8(dev["partials"], dev["residual"], dev["gamma"], w.eps, scale=g, flags=flags)
+        part = tp.fused_rmsnorm_fp8(dev["partials"], dev["residual"], dev["gamma"], w.eps, scale=g, flags=flags,
+                                    emit_norm=mode == "fp8_given")
+        torch.cuda.synchronize()
+        if T:
+            ref = oracle_rows(inputs, rows, w.eps, residual=residual)
+            assert_close_to_ref(full["out_norm"][rows], ref["y"], what + " out_norm")
+            assert_close_to_ref(part["out_residual"][rows], ref["h"], what + " out_residual")
+            oc, _ = oracle.fp8_quantize(synth.bits(full["out_norm"]), scale=given, dtype=dtype)
+            assert np.array_equal(full["codes"].cpu().numpy(), oc), what
+            assert torch.equal(part["codes"], full["codes"]), what  # with or without the bf16 output
+    elif mode == "nvfp4_given_no_norm":
+        full = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True, global_scale=g,
+                                flags=flags)
+        part = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True, global_scale=g,
+                                emit_norm=False, flags=flags)
+        torch.cuda.synchronize()
+        assert part["out_norm"] is None
+        if T:
+            ref = oracle_rows(inputs, rows, w.eps, residual=residual)
+            assert_close_to_ref(full["out_norm"][rows], ref["y"], what + " out_norm")
+            assert_close_to_ref(part["out_residual"][rows], ref["h"], what + " out_residual")
+            assert_nvfp4_bit_exact(full["out_norm"], part["codes"], part["scales"], given, given=given, what=what)
+    else:  # norm_inplace, nvfp4_dyn_inplace: out_residual is the residual tensor itself
+        nv = mode == "nvfp4_dyn_inplace"
+        target = dev["residual"]
+        out = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=nv, flags=flags,
+                               out_residual=target)
+        torch.cuda.synchronize()
+        if T:
+            ref = oracle_rows(inputs, rows, w.eps, residual=residual)
+            assert_close_to_ref(out["out_residual"][rows], ref["h"], what + " out_residual")
+            assert_close_to_ref(out["out_norm"][rows], ref["y"], what + " out_norm")
+            if target is not None:
+                assert out["out_residual"].data_ptr() == target.data_ptr()
+            if nv:
+                assert_nvfp4_bit_exact(out["out_norm"], out["codes"], out["scales"], out["global_scale"], what=what)
     assert tp.tpar_device_error(torch.cuda.current_device()) == 0
