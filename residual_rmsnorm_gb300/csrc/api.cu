@@ -717,8 +717,21 @@ tpar_status launch_quantize(const void* x, int64_t T, int64_t d, uint8_t* codes,
     q.err = device_error_word();
     q.n_vec_total = checked_vectors(T, d, flags);
     q.n_scales = scale_bytes(T, d, flags);
+    // Two 16-element blocks per thread once that gives every SM at least two
+    // CTAs; a smaller tensor takes one 16-byte vector per thread (four times
+    // the warps), since there the block-scale arithmetic of too few warps per
+    // SM sets the time. Measured on GB300 in the dynamic NVFP4 call, N=4,
+    // d=8192 (us, two blocks vs one vector per thread): T=32 5.98 vs 5.54,
+    // 128 8.33 vs 7.37, 256 12.23 vs 11.84, 512 16.76 vs 17.32, 1024 24.8
+    // vs 25.8, 16384 339 vs 360.
     const void* fn = tpar::quantize_kernel_for(dynamic, f16);
-    const unsigned grid = flat_grid(q.nvec / 2, sm_count, fn, 2);  // two 16-element blocks per thread
+    unsigned grid;
+    if (ceil_div(q.nvec / 2, 256 * 2) >= 2 * static_cast<int64_t>(sm_count)) {
+        grid = flat_grid(q.nvec / 2, sm_count, fn, 2);
+    } else {
+        fn = tpar::quantize_vec_kernel_for(dynamic, f16);
+        grid = flat_grid(q.nvec, sm_count, fn, 1);
+    }
     if (launch(fn, dim3(grid), dim3(256), &q, stream, 1, pdl) != cudaSuccess)
         return TPAR_ERR_CUDA;
     return TPAR_OK;
@@ -952,7 +965,7 @@ tpar_status fused_impl(const Call& c, const tpar_plan* user_plan, void* user_ws,
     }
     // Dynamic global scale: phase A (the fused pass, folding |out_norm| into
     // the device amax), then phase B (quantise out_norm, publish g, reset).
-    a.amax_bits = ws;
+    a.amax_bits = ws + 1;  // the amax half of the workspace word
     a.codes = nullptr;
     a.scales = nullptr;
     if ((st = launch_fused(a, tpar::kQuantAmax, p, stream, pdl)) != TPAR_OK)
@@ -1049,7 +1062,7 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
     Call k3{k3_in, 1, nullptr, gamma, eps, T, d, out_norm, nullptr, nullptr, nullptr, nullptr,
             TPAR_FORCE_ROW | (flags & TPAR_DTYPE_FP16), nullptr};
     FusedArgs a = fused_args(k3);
-    a.amax_bits = ws;
+    a.amax_bits = ws ? ws + 1 : nullptr;
     tpar_plan p;  // the norm kernel the fused path would pick for one source
     if ((st = plan_impl(T, d, 1, sm, 0u, &p)) != TPAR_OK)
         return st;
@@ -1106,7 +1119,8 @@ tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* co
             return st;
         const uint4* xv = static_cast<const uint4*>(x);
         int64_t nvec = T * d / 8;
-        void* args[3] = {&xv, &nvec, &ws};
+        uint32_t* amax_bits = ws + 1;
+        void* args[3] = {&xv, &nvec, &amax_bits};
         const void* ka = tpar::amax_kernel_ptr((flags & TPAR_DTYPE_FP16) != 0);
         if (launch_args(ka, dim3(flat_grid(nvec, sm, ka)), dim3(256), args, stream, 1, pdl) != cudaSuccess)
             return TPAR_ERR_CUDA;
@@ -1179,7 +1193,7 @@ tpar_status tpar_fused_rmsnorm_fp8(const void* const* partials, int n_ranks, con
     uint32_t* ws = nullptr;
     if ((st = workspace_for(nullptr, stream, &ws)) != TPAR_OK)
         return st;
-    a.amax_bits = ws;
+    a.amax_bits = ws + 1;
     if ((st = launch_fused(a, tpar::kQuantAmax, p, stream, pdl)) != TPAR_OK)
         return st;
     tpar::Fp8Args f;
@@ -1233,7 +1247,8 @@ tpar_status tpar_fp8_quantize(const void* x, int64_t T, int64_t d, uint8_t* code
             return st;
         const uint4* xv = static_cast<const uint4*>(x);
         int64_t n = nvec;
-        void* args[3] = {&xv, &n, &ws};
+        uint32_t* amax_bits = ws + 1;
+        void* args[3] = {&xv, &n, &amax_bits};
         const void* ka = tpar::amax_kernel_ptr((flags & TPAR_DTYPE_FP16) != 0);
         if (launch_args(ka, dim3(flat_grid(nvec, sm, ka)), dim3(256), args, stream, 1, pdl) != cudaSuccess)
             return TPAR_ERR_CUDA;
@@ -1319,7 +1334,7 @@ int tpar_debug_build(void) { return kDebugBuild ? 1 : 0; }
 // device with cudaGetSymbolAddress and passed to the kernels.
 namespace {
 
-constexpr int64_t kNoAllocHeaderBytes = 256;  // [0] amax bits, [1] completion counter
+constexpr int64_t kNoAllocHeaderBytes = 256;  // the dynamic-scale word: [0] quantiser count, [1] amax bits
 constexpr int64_t kNoAllocMaxElems = TPAR_NOALLOC_MAX_ELEMENTS;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocHeaderBytes + 2 * kNoAllocMaxElems];
@@ -1420,7 +1435,7 @@ extern "C" tpar_status tpar_unfused_rmsnorm_noalloc(const void* const* partials,
     Call k3{k3_in, 1, nullptr, gamma, eps, T, d, out_norm, nullptr, nullptr, nullptr, nullptr,
             TPAR_FORCE_ROW | (flags & TPAR_DTYPE_FP16), nullptr};
     FusedArgs a = fused_args(k3);
-    a.amax_bits = (nvfp4 && !given) ? ws : nullptr;
+    a.amax_bits = (nvfp4 && !given) ? ws + 1 : nullptr;
     tpar_plan p;
     if ((st = plan_impl(T, d, 1, sm, TPAR_FORCE_ROW, &p)) != TPAR_OK)
         return st;

@@ -46,7 +46,7 @@ struct FusedArgs {
     uint8_t* scales;                   // [T, d/16] row-major, or 128x4 tiles (sf_tiles)
     uint2* q8;                         // FP8 codes [T, d] = 8 bytes per input vector
     const float* gscale;               // given g (kQuantGiven)
-    uint32_t* amax_bits;               // running max of |out_norm| bits (kQuantAmax)
+    uint32_t* amax_bits;               // running max of |out_norm| bits (kQuantAmax): ws + 1
     uint32_t* err;                     // device error word (bounded wait expired) or null
     int64_t T;
     bool f16;                          // host: tensors are binary16 (picks the F16 instantiation)
@@ -159,6 +159,24 @@ __device__ __forceinline__ void cta_amax_atomic(float v, uint32_t* amax_bits, fl
         if (lane == 0 && c > 0.0f)
             atomicMax(amax_bits, __float_as_uint(c));  // |y| >= 0 orders like its bits
     }
+}
+
+// The dynamic-scale workspace keeps one 64-bit word at ws[0..1]: the high
+// half (ws[1]) is the running max of |out_norm| bits, folded in by the fused
+// pass (atomicMax on the half), the low half (ws[0]) counts the quantiser
+// CTAs that have read it. A quantiser CTA reads the max and counts itself in
+// one 64-bit atomic add; the CTA that brings the count to the grid size
+// zeroes the word for the next call. Every read of the word is an atomic on
+// that one location, so coherence orders the zeroing after all of them and
+// no fence is needed (a fence before a counter would cost each CTA a wait for
+// its own stores on the kernel's tail). Returns the max.
+__device__ __forceinline__ float take_amax_and_count(uint32_t* ws)
+{
+    unsigned long long* w = reinterpret_cast<unsigned long long*>(ws);
+    const unsigned long long old = atomicAdd(w, 1ull);
+    if (static_cast<uint32_t>(old) == gridDim.x - 1u)
+        *reinterpret_cast<volatile unsigned long long*>(w) = 0ull;
+    return __uint_as_float(static_cast<uint32_t>(old >> 32));
 }
 
 // Largest CTA a fused-kernel instantiation is built for: wide rows (VPT >= 2),
@@ -343,7 +361,7 @@ struct QuantArgs {
     uint32_t* codes;     // one word (8 codes) per vector
     uint8_t* scales;     // one byte per pair of vectors
     float* gscale;       // given: input; dynamic: output
-    uint32_t* ws;        // dynamic: ws[0] = amax bits, ws[1] = completion counter
+    uint32_t* ws;        // dynamic: the 64-bit word at ws[0..1] (take_amax_and_count)
     int64_t nvec;        // T * d / 8 (even)
     bool f16;            // host: x is binary16 (picks the F16 instantiation)
     int kb;              // blocks per row, d / 16
@@ -388,9 +406,10 @@ __device__ __forceinline__ void quantize_block(const QuantArgs& a, float g, int6
 // four 16-byte loads issued before either is used), so the block-scale
 // arithmetic (two IEEE divisions and the E4M3 round trip) runs once per
 // block. The first iteration's loads go out before the global scale is
-// known. In dynamic mode thread 0 of each CTA reads amax from the workspace
-// (g = amax / 2688) and, after its own blocks, counts the CTA as done; the
-// last CTA zeroes the workspace for the next call (no CTA waits on another).
+// known. In dynamic mode thread 0 of each CTA takes amax from the workspace
+// word and counts its CTA in the same atomic (take_amax_and_count; g = amax
+// / 2688); the CTA that counts last zeroes the word for the next call (no
+// CTA waits on another).
 template <bool DYNAMIC, bool F16>
 __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __grid_constant__ QuantArgs a)
 {
@@ -401,7 +420,7 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __grid_consta
     if (threadIdx.x == 0) {
         float g;
         if constexpr (DYNAMIC) {
-            g = __fdiv_rn(__uint_as_float(*reinterpret_cast<volatile uint32_t*>(a.ws)), 2688.0f);
+            g = __fdiv_rn(take_amax_and_count(a.ws), 2688.0f);
             if (blockIdx.x == 0)
                 *a.gscale = g;
         } else {
@@ -434,14 +453,76 @@ __global__ void __launch_bounds__(256) nvfp4_quantize_kernel(const __grid_consta
         b += 2 * stride;
         load_pair(b);
     }
-    if constexpr (DYNAMIC) {
-        if (threadIdx.x == 0) {
-            __threadfence();
-            if (atomicAdd(a.ws + 1, 1u) == gridDim.x - 1) {
-                a.ws[0] = 0u;
-                a.ws[1] = 0u;
+}
+
+// The same quantiser with one 16-byte vector (8 elements) per thread and
+// iteration: a 16-element block is the vectors 2b, 2b + 1 of a lane pair,
+// which exchange their maxima with one shuffle and each derive the block
+// scale (the fused kernels' layout). Four times the threads of
+// nvfp4_quantize_kernel for the same tensor, for tensors too small to fill
+// the GPU with that kernel: there the block-scale arithmetic (two IEEE
+// divisions and the E4M3 round trip per block) of a few warps per SM sets
+// the time. Each thread's next vector is loaded before the current one is
+// quantised; the warp's loop bound is uniform, so every lane joins the
+// shuffle. Same arithmetic, same outputs, same workspace protocol.
+template <bool DYNAMIC, bool F16>
+__global__ void __launch_bounds__(256) nvfp4_quantize_vec_kernel(const __grid_constant__ QuantArgs a)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+
+    __shared__ float g_sh;
+    if (threadIdx.x == 0) {
+        float g;
+        if constexpr (DYNAMIC) {
+            g = __fdiv_rn(take_amax_and_count(a.ws), 2688.0f);
+            if (blockIdx.x == 0)
+                *a.gscale = g;
+        } else {
+            g = *a.gscale;
+        }
+        g_sh = g;
+    }
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;  // a multiple of 32
+    int64_t v = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    int64_t w0 = v - (threadIdx.x & 31);  // the warp's first vector: a warp-uniform bound
+    auto load = [&](int64_t u) {
+        return (u < a.nvec && TPAR_IN_RANGE(a.err, u, a.n_vec_total)) ? ld_reuse(a.x + u)
+                                                                      : make_uint4(0u, 0u, 0u, 0u);
+    };
+    uint4 xv = load(v);
+    __syncthreads();
+    const float g = g_sh;
+    for (; w0 < a.nvec; w0 += stride, v += stride) {
+        const uint4 next = load(v + stride);
+        float x[8];
+        unpack8_dt(xv, x, F16);
+        float bmax = 0.0f;
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+            bmax = fmaxf(bmax, fabsf(x[e]));
+        bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));  // v, v ^ 1: one block
+        if (v < a.nvec) {
+            uint32_t sbyte;
+            const float inv = nvfp4_block_scale(g, bmax, sbyte);
+            float q[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                q[e] = __fmul_rn(x[e], inv);
+            if (TPAR_IN_RANGE(a.err, v, a.n_vec_total))
+                st_u32(a.codes + v, e2m1x8_from_f32(q));
+            if ((v & 1) == 0) {
+                const int64_t b = v >> 1;
+                int64_t si = b;
+                if (a.sf_tiles) {
+                    const int64_t t = b / a.kb;
+                    si = scale_offset_128x4(t, static_cast<int>(b - t * a.kb), a.sf_tiles);
+                }
+                if (TPAR_IN_RANGE(a.err, si, a.n_scales))
+                    st_u8(a.scales + si, sbyte);
             }
         }
+        xv = next;
     }
 }
 
@@ -453,7 +534,7 @@ struct Fp8Args {
     const uint4* x;    // bf16 [T, d] as T*d/8 vectors
     uint2* codes;      // [T, d] E4M3 bytes, 8 per vector
     float* scale;      // given: input; dynamic: output
-    uint32_t* ws;      // dynamic: ws[0] = amax bits, ws[1] = completion counter
+    uint32_t* ws;      // dynamic: the 64-bit word at ws[0..1] (take_amax_and_count)
     int64_t nvec;
     bool f16;          // host: x is binary16 (picks the F16 instantiation)
 };
@@ -467,7 +548,7 @@ __global__ void __launch_bounds__(256) fp8_quantize_kernel(const __grid_constant
     if (threadIdx.x == 0) {
         float s;
         if constexpr (DYNAMIC) {
-            s = __fdiv_rn(__uint_as_float(*reinterpret_cast<volatile uint32_t*>(a.ws)), 448.0f);
+            s = __fdiv_rn(take_amax_and_count(a.ws), 448.0f);
             if (blockIdx.x == 0)
                 *a.scale = s;
         } else {
@@ -505,16 +586,6 @@ __global__ void __launch_bounds__(256) fp8_quantize_kernel(const __grid_constant
         }
         v += 2 * stride;
         load_pair(v);
-    }
-    if constexpr (DYNAMIC) {
-        // thread 0 read the workspace above; count the CTA, the last resets
-        if (threadIdx.x == 0) {
-            __threadfence();
-            if (atomicAdd(a.ws + 1, 1u) == gridDim.x - 1) {
-                a.ws[0] = 0u;
-                a.ws[1] = 0u;
-            }
-        }
     }
 }
 

@@ -28,7 +28,7 @@ namespace tpar {
 struct GridArgs {
     FusedArgs f;   // inputs, outputs (out_norm may be null), codes, scales, T, nvec
     float* gscale; // output: g
-    uint32_t* ws;  // workspace: [0] amax bits, [1] exit count, [3] barrier arrivals
+    uint32_t* ws;  // workspace: [1] amax bits, [0] exit count, [3] barrier arrivals
     int rows;      // rows per CTA buffered in shared memory (ceil(T / gridDim.x))
 };
 
@@ -162,7 +162,7 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT, false))
         for (int w = 0; w < nwarps; ++w)
             c = fmaxf(c, red[w]);
         if (c > 0.0f)
-            atomicMax(ga.ws, __float_as_uint(c));  // |y| >= 0 orders like its bits
+            atomicMax(ga.ws + 1, __float_as_uint(c));  // |y| >= 0 orders like its bits
         __threadfence();
         atomicAdd(ga.ws + 3, 1u);
         const uint64_t t0 = global_ns();
@@ -176,7 +176,7 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT, false))
             __nanosleep(64);
         }
         __threadfence();
-        const float g = __fdiv_rn(__uint_as_float(*reinterpret_cast<volatile uint32_t*>(ga.ws)), 2688.0f);
+        const float g = __fdiv_rn(__uint_as_float(*reinterpret_cast<volatile uint32_t*>(ga.ws + 1)), 2688.0f);
         g_sh = g;
         if (blockIdx.x == 0)
             *ga.gscale = g;
@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT, false))
     // ---- the last CTA to have read the amax zeroes the workspace
     if (tid == 0) {
         __threadfence();
-        if (atomicAdd(ga.ws + 1, 1u) == static_cast<uint32_t>(G) - 1) {
+        if (atomicAdd(ga.ws, 1u) == static_cast<uint32_t>(G) - 1) {
             ga.ws[0] = 0u;
             ga.ws[3] = 0u;
             ga.ws[1] = 0u;

@@ -6,9 +6,10 @@
 
 namespace tpar {
 
-// amax of |x| over a bf16 tensor into ws[0] (for the standalone quantiser).
+// amax of |x| over a bf16 tensor, folded into the workspace's amax half
+// (amax_bits = ws + 1; for the standalone quantiser).
 template <bool F16>
-__global__ void __launch_bounds__(256) amax_kernel(const uint4* x, int64_t nvec, uint32_t* ws)
+__global__ void __launch_bounds__(256) amax_kernel(const uint4* x, int64_t nvec, uint32_t* amax_bits)
 {
     pdl_wait();
     pdl_launch_dependents();
@@ -23,7 +24,7 @@ __global__ void __launch_bounds__(256) amax_kernel(const uint4* x, int64_t nvec,
     }
     m = warp_max(m);
     if ((threadIdx.x & 31) == 0 && m > 0.0f)
-        atomicMax(ws, __float_as_uint(m));
+        atomicMax(amax_bits, __float_as_uint(m));
 }
 
 // K2: out_residual = bf16(reduced + residual) (a copy when residual is null).
@@ -78,6 +79,15 @@ const void* quantize_kernel_for(bool dynamic, bool f16)
                        : reinterpret_cast<const void*>(&nvfp4_quantize_kernel<false, true>);
     return dynamic ? reinterpret_cast<const void*>(&nvfp4_quantize_kernel<true, false>)
                    : reinterpret_cast<const void*>(&nvfp4_quantize_kernel<false, false>);
+}
+
+const void* quantize_vec_kernel_for(bool dynamic, bool f16)
+{
+    if (f16)
+        return dynamic ? reinterpret_cast<const void*>(&nvfp4_quantize_vec_kernel<true, true>)
+                       : reinterpret_cast<const void*>(&nvfp4_quantize_vec_kernel<false, true>);
+    return dynamic ? reinterpret_cast<const void*>(&nvfp4_quantize_vec_kernel<true, false>)
+                   : reinterpret_cast<const void*>(&nvfp4_quantize_vec_kernel<false, false>);
 }
 
 const void* amax_kernel_ptr(bool f16)

@@ -389,3 +389,35 @@ def test_fp8_single_launch_matches_two_pass(T, d, n, dt):
     oc, os_ = oracle.fp8_quantize(synth.bits(one["out_norm"]), dtype=dt)
     assert np.array_equal(one["codes"].cpu().numpy(), oc) and np.float32(one["scale"].item()) == os_
     assert tp.tpar_device_error(torch.cuda.current_device()) == 0
+
+
+@pytest.mark.parametrize("layout", ["rowmajor", "128x4"])
+@pytest.mark.parametrize("dtype", ["bf16", "fp16"])
+def test_both_quantiser_kernels(layout, dtype):
+    """The quantiser runs two 16-element blocks per thread once that gives
+    every SM two CTAs (ceil(T * d / 8192) >= 2 * SMs), else one 16-byte vector per
+    thread with a lane pair per block. Just below and at that size, in the
+    standalone quantiser (given and dynamic scale) and as phase B of the
+    dynamic fused call, both must give the oracle's bits."""
+    tp = lib()
+    sm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    dt = torch.float16 if dtype == "fp16" else torch.bfloat16
+    d = 8192 if layout == "128x4" else 2064
+    t_thr = (2 * sm - 1) * 8192 // d + 1  # the smallest T with two blocks per thread
+    for T in (t_thr - 1, t_thr):
+        w = synth.NVFP4.with_(T=T, d=d, n_ranks=2, seed=T)
+        inputs = synth.make_inputs(w, dtype=dt)
+        dev = to_device(inputs)
+        x = dev["partials"][0]
+        g = torch.tensor([0.03], dtype=torch.float32, device="cuda")
+        for given in (None, g):
+            codes, scales, gs = tp.nvfp4_quantize(x, global_scale=given, scales_128x4=layout == "128x4")
+            torch.cuda.synchronize()
+            assert_nvfp4_bit_exact(x, codes, scales, gs, given=None if given is None else float(np.float32(0.03)),
+                                   what=f"standalone T={T} {layout} {dtype}", scales_128x4=layout == "128x4")
+        out = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True,
+                               scales_128x4=layout == "128x4")
+        torch.cuda.synchronize()
+        assert_nvfp4_bit_exact(out["out_norm"], out["codes"], out["scales"], out["global_scale"],
+                               what=f"fused T={T} {layout} {dtype}", scales_128x4=layout == "128x4")
+    assert tp.tpar_device_error(torch.cuda.current_device()) == 0
