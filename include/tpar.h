@@ -195,11 +195,13 @@ tpar_status tpar_init(int device);
  *                all NULL (no quantisation) or all non-NULL. codes [T, d/2],
  *                scales [T, d/16] E4M3 bytes, global_scale -> one device fp32.
  *                Here global_scale is an OUTPUT: g = amax(|out_norm|) / 2688
- *                over the whole [T, d] tensor, computed on the device. For
- *                T <= 16 and d a multiple of 512 (or 256, 128 ...) one
- *                thread-block cluster owns the whole tensor and the call is a
- *                single launch; otherwise it is two (the fused pass, then a
- *                quantiser re-reading out_norm). Both give identical bits.
+ *                over the whole [T, d] tensor, computed on the device. When
+ *                one thread-block cluster of K <= 16 CTAs can own the tensor
+ *                with one 16-byte vector per thread (d/8 a multiple of 32K,
+ *                T * d/8 <= 512K: T <= 8 at d = 8192, T <= 16 at d = 4096)
+ *                the call is a single launch; otherwise it is two (the fused
+ *                pass, then a quantiser re-reading out_norm). Both give
+ *                identical bits.
  *   stream       cudaStream_t
  *
  * The dynamic-scale path uses the device workspace from tpar_init (made on

@@ -765,33 +765,30 @@ FusedArgs fused_args(const Call& c)
     return a;
 }
 
-// Shape of the single-launch dynamic-NVFP4 path: one cluster of K CTAs, each
-// owning `slice` vectors (a multiple of 32) of every row, at most 4 items of
-// 16 bytes per thread. Returns false when the tensor does not fit one cluster.
-// T <= kSmallNvfp4Rows: measured faster than phase A + phase B up to there
-// (N=4, d=8192: 2.65 / 3.79 / 5.24 us at T = 1 / 8 / 16 vs 4.48 / 5.42 / 5.52;
-// at T = 32 one cluster is too few SMs, 9.2 vs 5.6 us).
-constexpr int64_t kSmallNvfp4Rows = 16;
-
+// Shape of the single-launch dynamic-scale path: one cluster of K CTAs, each
+// owning `slice` vectors (a multiple of 32) of every row, one item of 16
+// bytes per thread, at most 512 per CTA. Returns false when the tensor does
+// not fit, and the call takes phase A + phase B. Measured on GB300 (us,
+// one cluster vs two kernels): N=4 d=8192 T=8 3.90 vs 4.21, T=10 (two
+// items per thread) 4.58 vs 4.35, T=16 5.31 vs 4.45; N=8 d=4096 T=16 (one
+// item) 4.18 vs 4.48; N=8 d=8192 T=8 4.20 vs 4.48, T=10 4.97 vs 4.55. With
+// two items per thread the cluster's 16 SMs carry too much of the tensor.
 bool small_nvfp4_shape(int64_t T, int64_t d, int* K, int* slice, int* threads, int* ipt)
 {
     const int64_t nvec = d / 8;
-    if (T < 1 || T > kSmallNvfp4Rows || T > tpar::kSmallMaxRows)
+    if (T < 1 || T > tpar::kSmallMaxRows)
         return false;
     for (int k = 16; k >= 2; k /= 2) {
         if (nvec % (static_cast<int64_t>(k) * 32) != 0)
             continue;
         const int64_t sl = nvec / k;
         const int64_t items = T * sl;
-        if (items > 4 * 512)
+        if (items > 512)
             return false;
-        int v = 1;
-        while (v < 4 && ceil_div(items, v) > 512)
-            v *= 2;
         *K = k;
         *slice = static_cast<int>(sl);
-        *ipt = v;
-        *threads = static_cast<int>(ceil_div(ceil_div(items, v), 32) * 32);
+        *ipt = 1;
+        *threads = static_cast<int>(ceil_div(items, 32) * 32);
         return true;
     }
     return false;

@@ -63,7 +63,7 @@ inline const void* stream_kernel_for(int qmode, int nr, int vpt, bool f16)
 }
 
 // Single-launch dynamic-scale kernel (nvfp4_small.cuh) for rank bound nr,
-// ipt items per thread (1, 2, 4), NVFP4 or (fp8) per-tensor FP8 output.
+// ipt items per thread (only 1 is built), NVFP4 or (fp8) per-tensor FP8 output.
 const void* small_kernel_for(int nr, int ipt, bool f16, bool fp8);
 
 // Cooperative single-launch dynamic-scale NVFP4 kernel (nvfp4_grid.cuh) for

@@ -174,8 +174,9 @@ def test_workspace_is_left_zeroed_and_reused():
     (4, 2048, 4, "bf16"),     # the grid form also runs a few rows (below)
 ])
 def test_single_launch_dynamic_matches_two_pass(T, d, n, dt):
-    """Dynamic global scale in one launch: for T <= 16 one cluster owns the
-    tensor and exchanges the amax on chip (the automatic choice); with
+    """Dynamic global scale in one launch: when one cluster can own the
+    tensor with one vector per thread (T <= 8 at d = 8192, T <= 16 at
+    d = 4096) it exchanges the amax on chip (the automatic choice); with
     TPAR_FORCE_GRID, up to ~1800 rows of d=8192, a cooperative grid keeps its
     rows in shared memory across a grid barrier. Either must give exactly
     the bits of the two-kernel path, and both are bit-exact against the
