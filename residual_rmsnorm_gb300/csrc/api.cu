@@ -529,6 +529,19 @@ tpar_status plan_impl(int64_t T, int64_t d, int n_ranks, int sm_count, uint32_t 
                    nvec / (2 * split) >= 32)
                 split *= 2;
         }
+        // Just past one row per SM, one CTA per row leaves the SMs that get
+        // a second row to set the time; rows of 80-320 KB split over an
+        // 8-CTA cluster spread the same bytes evenly. Measured on GB300 over
+        // N in {2, 4, 8, 16} and d in {4096 .. 32768} (one CTA per row /
+        // split 8, at T = SMs + 1 / + 48): N=4 d=8192 1.09 / 1.06, N=8
+        // d=8192 1.09 / 1.05, N=4 d=32768 1.38 / 1.17, N=2 d=32768 1.44 /
+        // 1.22, N=16 d=4096 1.06 / 1.01. Outside that: 4-CTA splits (rows
+        // under 80 KB) 0.92-0.95, N=8 d=32768 (576 KB rows) 0.79-0.94, and
+        // near 1.5 rows per SM several shapes lose (0.96-0.97 at T=228); at
+        // one row per SM one CTA per row stays faster.
+        if (T > sm_count && 20 * T <= 27 * static_cast<int64_t>(sm_count) && row_bytes >= 80 * 1024 &&
+            row_bytes <= 320 * 1024 && nvec >= 512)
+            split = 8;
         if ((flags & TPAR_FORCE_CLUSTER) && split == 1) {
             if (nvec < 4)
                 return TPAR_ERR_UNSUPPORTED;

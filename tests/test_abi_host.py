@@ -213,7 +213,8 @@ def test_planner_covers_every_row(tp, sm):
                 s = -(-(-(-nvec // p.split)) // 32) * 32
                 assert p.threads * p.vec_per_thread >= s
                 assert s >= 32 or p.split == 2
-                assert T <= 48 and T * p.split <= 2 * sm  # rows are split only when few
+                # rows are split when few, or just past one row per SM to even the load
+                assert (T <= 48 and T * p.split <= 2 * sm) or (sm < T and 20 * T <= 27 * sm and p.split == 8)
             else:
                 assert p.split == 1 and p.threads * p.vec_per_thread >= nvec
             assert 1 <= p.grid_rows <= min(T, 65535)
@@ -245,13 +246,23 @@ def test_planner_choices_for_the_pages_shapes(tp):
     # no prefetch where a row of every source outgrows the ring, or T <= SMs
     assert tp.tpar_plan_launch(4096, 16384, 8, 152).kernel == 0
     assert tp.tpar_plan_launch(4096, 32768, 1, 152).kernel == 0
-    assert tp.tpar_plan_launch(228, 8192, 8, 152).kernel == 0
     assert tp.tpar_plan_launch(229, 8192, 8, 152).kernel == 3
+    # just past one row per SM (up to 1.35 rows per SM): rows of 80-320 KB
+    # split over an 8-CTA cluster to even the per-SM load
+    assert tp.tpar_plan_launch(152, 8192, 8, 152).kernel == 0
+    for T in (153, 200, 205):
+        p = tp.tpar_plan_launch(T, 8192, 8, 152)
+        assert (p.kernel, p.split, p.threads, p.grid_rows) == (1, 8, 128, T), T
+    assert tp.tpar_plan_launch(206, 8192, 8, 152).kernel == 0
+    assert tp.tpar_plan_launch(160, 4096, 8, 152).kernel == 0   # 73 KB rows stay whole
+    assert tp.tpar_plan_launch(160, 32768, 8, 152).kernel == 0  # 590 KB rows stay whole
+    assert tp.tpar_plan_launch(160, 32768, 4, 152).split == 8   # 320 KB rows split
+    assert tp.tpar_plan_launch(160, 8192, 2, 152).kernel == 0   # 49 KB rows stay whole
     assert tp.tpar_plan_launch(4096, 1024, 8, 152).kernel == 0  # rows of 128 vectors
     p = tp.tpar_plan_launch(4096, 8192, 8, 152, tp.TPAR_FORCE_STREAM)
     assert (p.kernel, p.split, p.threads, p.vec_per_thread, p.grid_rows) == (2, 1, 512, 2, 152)
     # short rows and mid-size batches: one CTA per row, capped at 512 threads for > 8 ranks
-    p = tp.tpar_plan_launch(200, 8192, 16, 152)
+    p = tp.tpar_plan_launch(100, 8192, 16, 152)
     assert (p.kernel, p.threads, p.vec_per_thread) == (0, 512, 2)
     assert tp.tpar_plan_launch(4096, 2048, 8, 152).kernel == 3
     assert tp.tpar_plan_launch(4096, 8192, 8, 152, tp.TPAR_FORCE_ROW).kernel == 0
