@@ -320,23 +320,28 @@ def measure_sweep(torch, tp, device):
     del cs, reduced
     torch.cuda.empty_cache()
 
-    # prefill T sweep, N=8 d=8192: the automatic plan (the prefetching row
-    # kernel once T exceeds the SM count) against one CTA per row without
-    # prefetch; eager calls rotating over input sets totalling > 2x L2
+    # prefill T sweep, N=8 d=8192: the automatic plan (an 8-CTA cluster per
+    # row just past one row per SM, the prefetching row kernel above 1.5 rows
+    # per SM) against one CTA per row without prefetch; CUDA graphs of calls
+    # rotating over input sets totalling > 2x L2, so the device time is
+    # measured rather than the host's launch rate
     rows = []
     for T in (128, 160, 256, 512, 1024, 2048, 4096):
         w = synth.PREFILL.with_(T=T)
         b = fused_bytes(w.n_ranks, T, w.d)
         n_sets = min(8, n_sets_for(b, l2_bytes(torch)))
         sets = [CallSet(w, seed=i, device=device) for i in range(n_sets)]
-        k = [0]
+        calls = 40 if T <= 1024 else 16
 
-        def rot(flags, sets=sets, w=w):
-            sets[k[0] % len(sets)].call(tp, w, st.cuda_stream, flags=flags)
-            k[0] += 1
+        def graph_us(flags, sets=sets, w=w, calls=calls):
+            g = capture(torch, lambda i: sets[i % len(sets)].call(tp, w, torch.cuda.current_stream().cuda_stream,
+                                                                   flags=flags), calls)
+            us = time_graph(torch, g, 5, 2) * 1e3 / calls
+            del g
+            return us
 
-        us_auto = ev_time(lambda: rot(0), reps=24)
-        us_row = ev_time(lambda: rot(tp.TPAR_FORCE_ROW), reps=24)
+        us_auto = graph_us(0)
+        us_row = graph_us(tp.TPAR_FORCE_ROW)
         plan = tp.tpar_plan_launch(T, w.d, w.n_ranks, torch.cuda.get_device_properties(device).multi_processor_count)
         rows.append({"N": 8, "T": T, "d": w.d, "auto_kernel": plan.kernel, "auto_us": round(us_auto, 2),
                      "row_us": round(us_row, 2), "auto_frac_of_measured_hbm": round(b / us_auto / 1e3 / peak, 4),
@@ -350,14 +355,11 @@ def measure_sweep(torch, tp, device):
     for T in synth.NVFP4_TS:
         w = synth.NVFP4.with_(T=T)
         b = fused_bytes(w.n_ranks, T, w.d, nvfp4=True)
-        if b * 2 < l2_bytes(torch) * 2:
-            g, sets = decode_graph(torch, tp, w, device, 100, nvfp4=True)
-            us = time_graph(torch, g, 5, 2) * 1e3 / 100
-            del g, sets
-        else:
-            cs = CallSet(w, seed=0, device=device, nvfp4=True)
-            us = ev_time(lambda: cs.call(tp, w, st.cuda_stream), reps=10)
-            del cs
+        # graphs of calls rotating over sets totalling > 2x L2 (fewer calls,
+        # and two sets, once one call outgrows the L2)
+        g, sets = decode_graph(torch, tp, w, device, 100 if b < l2_bytes(torch) else 10, nvfp4=True)
+        us = time_graph(torch, g, 5, 2) * 1e3 / (100 if b < l2_bytes(torch) else 10)
+        del g, sets
         rows.append({"N": 4, "T": T, "d": w.d, "us_per_call": round(us, 3), "GBps": round(b / us / 1e3, 1),
                      "frac_of_measured_hbm": round(b / us / 1e3 / peak, 4)})
         torch.cuda.empty_cache()
