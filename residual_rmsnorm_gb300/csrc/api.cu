@@ -833,11 +833,10 @@ tpar_status launch_small_dynamic(const FusedArgs& a, float* gscale, int K, int s
 // buffering its ceil(T / grid) rows of emitted values in shared memory.
 // False when a row needs more than kGridMaxVpt vectors per thread or the
 // rows do not fit the buffer. Not planned automatically: measured slower
-// than phase A + phase B on GB300 at every T from 17 to 1824 except 256
-// (N=4, d=8192, 100-call graphs: 6.70 vs 5.35 us at T=17, 8.46 vs 8.33 at
-// 128, 12.0 vs 12.2 at 256, 29.2 vs 25.0 at 1024, 51.3 vs 40.5 at 1824): a
-// cooperative launch cannot start early under PDL, and its rows get no
-// prefetch.
+// than phase A + phase B on GB300 at every T from 17 to 1824 (N=4, d=8192,
+// 100-call graphs: 7.1 vs 4.9 us at T=32, 8.5 vs 7.1 at 128, 12.1 vs 11.3
+// at 256, 29.2 vs 24.6 at 1024): a cooperative launch cannot start early
+// under PDL, and its rows get no prefetch.
 bool grid_nvfp4_shape(int64_t T, int64_t d, int n_ranks, int sm_count, int* grid, int* rows, int* threads, int* vpt)
 {
     const int64_t nvec = d / 8;
