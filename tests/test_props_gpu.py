@@ -342,3 +342,36 @@ def test_unfused_norm_kernel_in_every_form(T, d, form, nvfp4):
     assert same_bits(u["out_norm"], one["out_norm"])
     if nvfp4:
         assert_nvfp4_bit_exact(u["out_norm"], u["codes"], u["scales"], u["global_scale"], what="unfused")
+
+
+@pytest.mark.parametrize("n,d", [(4, 8192), (2, 32768), (16, 4096)])
+@pytest.mark.parametrize("extra", [0, 52])
+def test_mid_batch_cluster_split(n, d, extra):
+    """Just past one row per SM the planner splits rows of 80-320 KB over an
+    8-CTA cluster. That form gives the oracle's values and, bit for bit, the
+    one-CTA-per-row result, plain and with NVFP4 (dynamic and given scale)."""
+    tp = lib()
+    sm = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    T = sm + 1 + extra
+    p = tp.tpar_plan_launch(T, d, n, sm)
+    assert (p.kernel, p.split) == (1, 8), p.as_dict()
+    w = synth.NVFP4.with_(T=T, d=d, n_ranks=n, seed=T + d)
+    inputs = synth.make_inputs(w)
+    dev = to_device(inputs)
+    g = torch.tensor([0.04], dtype=torch.float32, device="cuda")
+    for kw in (dict(), dict(nvfp4=True), dict(nvfp4=True, global_scale=g)):
+        a = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, **kw)
+        b = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, flags=tp.TPAR_FORCE_ROW, **kw)
+        torch.cuda.synchronize()
+        for k in ("out_norm", "out_residual", "codes", "scales", "global_scale"):
+            if a[k] is not None:
+                assert same_bits(a[k], b[k]), (k, kw.keys())
+        if kw.get("nvfp4"):
+            given = None if kw.get("global_scale") is None else float(np.float32(0.04))
+            assert_nvfp4_bit_exact(a["out_norm"], a["codes"], a["scales"], a["global_scale"], given=given,
+                                   what="mid-batch split")
+    rows = np.unique([0, 1, T // 2, T - 1])
+    ref = oracle_rows(inputs, rows, w.eps)
+    assert_close_to_ref(a["out_norm"][rows], ref["y"], "mid-batch split out_norm")
+    assert_close_to_ref(a["out_residual"][rows], ref["h"], "mid-batch split out_residual")
+    assert tp.tpar_device_error(torch.cuda.current_device()) == 0
