@@ -422,3 +422,56 @@ def test_both_quantiser_kernels(layout, dtype):
         assert_nvfp4_bit_exact(out["out_norm"], out["codes"], out["scales"], out["global_scale"],
                                what=f"fused T={T} {layout} {dtype}", scales_128x4=layout == "128x4")
     assert tp.tpar_device_error(torch.cuda.current_device()) == 0
+
+
+def test_dynamic_scale_word_across_mixed_calls_in_one_graph():
+    """Back-to-back dynamic-scale calls of different sizes in one CUDA graph:
+    the one-cluster kernel, phase B with one vector per thread and with two
+    blocks per thread, each with its own grid. Every call must read only its
+    own amax (g = amax(|out_norm|) / 2688 exactly) and the workspace word must
+    end zeroed, replay after replay."""
+    tp = lib()
+    ws = torch.zeros(tp.tpar_workspace_bytes() // 4, dtype=torch.int32, device="cuda")
+    calls = []
+    for i, T in enumerate((8, 40, 300, 9, 700, 1500, 3, 333)):
+        w = synth.NVFP4.with_(T=T, d=2048, n_ranks=2, seed=700 + i)
+        x = synth.make_inputs(w, device="cuda")
+        scale = (1.0, 30.0, 0.01, 4.0, 0.3, 7.0, 100.0, 0.05)[i]  # a different amax per call
+        x["partials"] = [(p.float() * scale).to(torch.bfloat16) for p in x["partials"]]
+        outs = {"out_norm": torch.empty((T, w.d), dtype=torch.bfloat16, device="cuda"),
+                "out_residual": torch.empty((T, w.d), dtype=torch.bfloat16, device="cuda"),
+                "codes": torch.empty((T, w.d // 2), dtype=torch.uint8, device="cuda"),
+                "scales": torch.empty((T, w.d // 16), dtype=torch.uint8, device="cuda"),
+                "g": torch.empty((1,), dtype=torch.float32, device="cuda")}
+        calls.append((w, x, outs))
+
+    def run_all():
+        from residual_rmsnorm_gb300 import _abi
+        for w, x, o in calls:
+            _abi.tpar_fused_rmsnorm_ex(
+                [p.data_ptr() for p in x["partials"]], w.n_ranks, x["residual"].data_ptr(), x["gamma"].data_ptr(),
+                w.eps, w.T, w.d, o["out_norm"].data_ptr(), o["out_residual"].data_ptr(), o["codes"].data_ptr(),
+                o["scales"].data_ptr(), o["g"].data_ptr(), 0, None, ws.data_ptr(),
+                torch.cuda.current_stream().cuda_stream)
+
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        run_all()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=s):
+            run_all()
+    torch.cuda.current_stream().wait_stream(s)
+    for rep in range(3):
+        for _, _, o in calls:
+            o["g"].fill_(-1.0)
+        graph.replay()
+        torch.cuda.synchronize()
+        for w, _, o in calls:
+            amax = np.float32(o["out_norm"].float().abs().max().item())
+            assert o["g"].item() == np.float32(amax / np.float32(2688.0)), (rep, w.T)
+        assert int(ws.abs().sum().item()) == 0, rep
+    w, _, o = calls[4]
+    assert_nvfp4_bit_exact(o["out_norm"], o["codes"], o["scales"], o["g"], what="mixed graph T=700")
+    assert tp.tpar_device_error(torch.cuda.current_device()) == 0
