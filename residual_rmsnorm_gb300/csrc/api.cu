@@ -985,6 +985,65 @@ tpar_status fused_impl(const Call& c, const tpar_plan* user_plan, void* user_ws,
     return st;
 }
 
+// The unfused chain, after its arguments are validated (T > 0): K1 reduced
+// = bf16(sum of partials); K2 out_residual = bf16(reduced + residual); K3
+// out_norm = RMSNorm(out_residual) on the norm kernel the planner picks for
+// one source, folding |out_norm| into the workspace word `ws` for a dynamic
+// NVFP4 scale; K4 the NVFP4 quantiser. `ws` is null unless the scale is
+// dynamic; a failed quantiser launch leaves it zeroed.
+tpar_status run_unfused(const Call& c, uint32_t* ws, int sm, cudaStream_t stream)
+{
+    const bool pdl = (c.flags & TPAR_NO_PDL) == 0;
+    const bool f16 = (c.flags & TPAR_DTYPE_FP16) != 0;
+    const bool nvfp4 = c.codes != nullptr;
+    const bool dynamic = nvfp4 && (c.flags & TPAR_GSCALE_GIVEN) == 0;
+    const int64_t nvec = c.T * c.d / 8;
+
+    // K1: reduced = bf16(sum of partials)
+    ReduceArgs ra;
+    std::memset(&ra, 0, sizeof ra);
+    for (int r = 0; r < c.n_ranks; ++r)
+        ra.partials[r] = static_cast<const uint4*>(c.partials[r]);
+    ra.reduced = static_cast<uint4*>(c.reduced);
+    ra.nvec = nvec;
+    ra.n_ranks = c.n_ranks;
+    ra.f16 = f16;
+    const void* k1 = tpar::reduce_kernel_for(tpar::rank_bound(c.n_ranks), f16);
+    if (launch(k1, dim3(flat_grid(nvec, sm, k1)), dim3(256), &ra, stream, 1, pdl) != cudaSuccess)
+        return TPAR_ERR_CUDA;
+    // K2: out_residual = bf16(reduced + residual)
+    {
+        const uint4* red = static_cast<const uint4*>(c.reduced);
+        const uint4* res = static_cast<const uint4*>(c.residual);
+        uint4* outr = static_cast<uint4*>(c.out_residual);
+        int64_t n = nvec;
+        void* args[4] = {&red, &res, &outr, &n};
+        const void* k2 = tpar::residual_add_kernel_ptr(f16);
+        if (launch_args(k2, dim3(flat_grid(nvec, sm, k2)), dim3(256), args, stream, 1, pdl) != cudaSuccess)
+            return TPAR_ERR_CUDA;
+    }
+    // K3: out_norm = RMSNorm(out_residual) (+ amax for a dynamic NVFP4 scale)
+    const void* k3_in[1] = {c.out_residual};
+    Call k3{k3_in, 1, nullptr, c.gamma, c.eps, c.T, c.d, c.out_norm, nullptr, nullptr, nullptr, nullptr,
+            c.flags & TPAR_DTYPE_FP16, nullptr};
+    FusedArgs a = fused_args(k3);
+    a.amax_bits = dynamic ? ws + 1 : nullptr;
+    tpar_plan p;  // the norm kernel the fused path would pick for one source
+    tpar_status st = plan_impl(c.T, c.d, 1, sm, 0u, &p);
+    if (st != TPAR_OK)
+        return st;
+    if ((st = launch_fused(a, dynamic ? tpar::kQuantAmax : tpar::kQuantNone, p, stream, pdl)) != TPAR_OK)
+        return st;
+    // K4: the separate NVFP4 quantiser
+    if (nvfp4) {
+        st = launch_quantize(c.out_norm, c.T, c.d, c.codes, c.scales, c.gscale, dynamic ? ws : nullptr, dynamic, sm,
+                             stream, pdl, c.flags);
+        if (st != TPAR_OK && dynamic)
+            cudaMemsetAsync(ws, 0, 8, stream);
+    }
+    return st;
+}
+
 }  // namespace
 
 extern "C" {
@@ -1035,57 +1094,10 @@ tpar_status tpar_unfused_rmsnorm(const void* const* partials, int n_ranks, const
     int sm = 0;
     if ((st = current_sm_count(&sm)) != TPAR_OK)
         return st;
-    const bool pdl = (flags & TPAR_NO_PDL) == 0;
-    const bool nvfp4 = nvfp4_codes != nullptr;
-    const bool given = (flags & TPAR_GSCALE_GIVEN) != 0;
-    const int64_t nvec = T * d / 8;
     uint32_t* ws = nullptr;
-    if (nvfp4 && !given && (st = workspace_for(nullptr, stream, &ws)) != TPAR_OK)
+    if (nvfp4_codes && !(flags & TPAR_GSCALE_GIVEN) && (st = workspace_for(nullptr, stream, &ws)) != TPAR_OK)
         return st;
-
-    // K1: reduced = bf16(sum of partials)
-    ReduceArgs ra;
-    std::memset(&ra, 0, sizeof ra);
-    for (int r = 0; r < n_ranks; ++r)
-        ra.partials[r] = static_cast<const uint4*>(partials[r]);
-    ra.reduced = static_cast<uint4*>(reduced);
-    ra.nvec = nvec;
-    ra.n_ranks = n_ranks;
-    ra.f16 = (flags & TPAR_DTYPE_FP16) != 0;
-    const void* k1 = tpar::reduce_kernel_for(tpar::rank_bound(n_ranks), ra.f16);
-    if (launch(k1, dim3(flat_grid(nvec, sm, k1)), dim3(256), &ra, stream, 1, pdl) != cudaSuccess)
-        return TPAR_ERR_CUDA;
-    // K2: out_residual = bf16(reduced + residual)
-    {
-        const uint4* red = static_cast<const uint4*>(reduced);
-        const uint4* res = static_cast<const uint4*>(residual);
-        uint4* outr = static_cast<uint4*>(out_residual);
-        int64_t n = nvec;
-        void* args[4] = {&red, &res, &outr, &n};
-        const void* k2 = tpar::residual_add_kernel_ptr((flags & TPAR_DTYPE_FP16) != 0);
-        if (launch_args(k2, dim3(flat_grid(nvec, sm, k2)), dim3(256), args, stream, 1, pdl) != cudaSuccess)
-            return TPAR_ERR_CUDA;
-    }
-    // K3: out_norm = RMSNorm(out_residual) (+ amax for a dynamic NVFP4 scale)
-    const void* k3_in[1] = {out_residual};
-    Call k3{k3_in, 1, nullptr, gamma, eps, T, d, out_norm, nullptr, nullptr, nullptr, nullptr,
-            TPAR_FORCE_ROW | (flags & TPAR_DTYPE_FP16), nullptr};
-    FusedArgs a = fused_args(k3);
-    a.amax_bits = ws ? ws + 1 : nullptr;
-    tpar_plan p;  // the norm kernel the fused path would pick for one source
-    if ((st = plan_impl(T, d, 1, sm, 0u, &p)) != TPAR_OK)
-        return st;
-    if ((st = launch_fused(a, (nvfp4 && !given) ? tpar::kQuantAmax : tpar::kQuantNone, p, stream, pdl)) !=
-        TPAR_OK)
-        return st;
-    // K4: the separate NVFP4 quantiser
-    if (nvfp4) {
-        st = launch_quantize(out_norm, T, d, nvfp4_codes, nvfp4_scales, global_scale, ws, !given, sm, stream,
-                             pdl, c.flags);
-        if (st != TPAR_OK && ws)
-            cudaMemsetAsync(ws, 0, 8, stream);
-    }
-    return st;
+    return run_unfused(c, ws, sm, stream);
 }
 
 tpar_status tpar_nvfp4_quantize(const void* x, int64_t T, int64_t d, uint8_t* codes, uint8_t* scales,
@@ -1405,55 +1417,12 @@ extern "C" tpar_status tpar_unfused_rmsnorm_noalloc(const void* const* partials,
     int sm = 0;
     if ((st = current_sm_count(&sm)) != TPAR_OK)
         return st;
-    const bool pdl = (fl & TPAR_NO_PDL) == 0;
-    const bool nvfp4 = nvfp4_codes != nullptr;
-    const bool given = (fl & TPAR_GSCALE_GIVEN) != 0;
-    const int64_t nvec = T * d / 8;
-    uint32_t* ws = reinterpret_cast<uint32_t*>(scratch);
-    if (nvfp4 && !given) {
-        // The accumulator must start at zero; the array keeps the last call's contents.
+    uint32_t* ws = nullptr;
+    if (nvfp4_codes && !(fl & TPAR_GSCALE_GIVEN)) {
+        // The workspace word must start at zero; the array keeps the last call's contents.
+        ws = reinterpret_cast<uint32_t*>(scratch);
         if (cudaMemsetAsync(ws, 0, 2 * sizeof(uint32_t), stream) != cudaSuccess)
             return TPAR_ERR_CUDA;
     }
-
-    // K1: reduced = bf16(sum of partials)
-    ReduceArgs ra;
-    std::memset(&ra, 0, sizeof ra);
-    for (int r = 0; r < n_ranks; ++r)
-        ra.partials[r] = static_cast<const uint4*>(partials[r]);
-    ra.reduced = static_cast<uint4*>(reduced);
-    ra.nvec = nvec;
-    ra.n_ranks = n_ranks;
-    ra.f16 = (flags & TPAR_DTYPE_FP16) != 0;
-    const void* k1 = tpar::reduce_kernel_for(tpar::rank_bound(n_ranks), ra.f16);
-    if (launch(k1, dim3(flat_grid(nvec, sm, k1)), dim3(256), &ra, stream, 1, pdl) != cudaSuccess)
-        return TPAR_ERR_CUDA;
-    // K2: out_residual = bf16(reduced + residual)
-    {
-        const uint4* red = static_cast<const uint4*>(reduced);
-        const uint4* res = static_cast<const uint4*>(residual);
-        uint4* outr = static_cast<uint4*>(out_residual);
-        int64_t n = nvec;
-        void* args[4] = {&red, &res, &outr, &n};
-        const void* k2 = tpar::residual_add_kernel_ptr((flags & TPAR_DTYPE_FP16) != 0);
-        if (launch_args(k2, dim3(flat_grid(nvec, sm, k2)), dim3(256), args, stream, 1, pdl) != cudaSuccess)
-            return TPAR_ERR_CUDA;
-    }
-    // K3: out_norm = RMSNorm(out_residual) (+ amax for a dynamic NVFP4 scale)
-    const void* k3_in[1] = {out_residual};
-    Call k3{k3_in, 1, nullptr, gamma, eps, T, d, out_norm, nullptr, nullptr, nullptr, nullptr,
-            TPAR_FORCE_ROW | (flags & TPAR_DTYPE_FP16), nullptr};
-    FusedArgs a = fused_args(k3);
-    a.amax_bits = (nvfp4 && !given) ? ws + 1 : nullptr;
-    tpar_plan p;
-    if ((st = plan_impl(T, d, 1, sm, TPAR_FORCE_ROW, &p)) != TPAR_OK)
-        return st;
-    if ((st = launch_fused(a, (nvfp4 && !given) ? tpar::kQuantAmax : tpar::kQuantNone, p, stream, pdl)) !=
-        TPAR_OK)
-        return st;
-    // K4: the separate NVFP4 quantiser
-    if (nvfp4)
-        st = launch_quantize(out_norm, T, d, nvfp4_codes, nvfp4_scales, global_scale, given ? nullptr : ws,
-                             !given, sm, stream, pdl, fl & TPAR_DTYPE_FP16);
-    return st;
+    return run_unfused(c, ws, sm, stream);
 }

@@ -53,7 +53,7 @@ __global__ void __launch_bounds__(fused_max_threads(NR, VPT, false))
     const int nvec = a.nvec;
     const int64_t G = gridDim.x;
     const int nW = (nvec + 31) >> 5;
-    const int64_t buf_vecs = static_cast<int64_t>(ga.rows) * nvec;  // extent checked by debug builds
+    [[maybe_unused]] const int64_t buf_vecs = static_cast<int64_t>(ga.rows) * nvec;  // checked by debug builds
     __shared__ float wsh[2][kMaxRowWarps];
     __shared__ float red[32];
     __shared__ float g_sh;

@@ -209,34 +209,32 @@ __global__ void __launch_bounds__(512) small_dynamic_kernel(const __grid_constan
                     asm volatile("st.global.v2.u32 [%0], {%1, %2};" ::"l"(a.q8 + gv), "r"(c.x), "r"(c.y) : "memory");
             }
         }
-        cluster_wait_acquire();  // no CTA leaves while a peer may still push to it
-        return;
-    }
-
-    // ---- 4. quantise this thread's items (a block = the vectors of a lane pair)
+    } else {
+        // ---- 4. quantise this thread's items (a block = the vectors of a lane pair)
 #pragma unroll
-    for (int j = 0; j < IPT; ++j) {
-        const int i = tid + j * B;
-        float bmax = 0.0f;
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            bmax = fmaxf(bmax, fabsf(h[j][e]));
-        bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));
-        if (i < items) {
-            const int t = i / slice;
-            const int v = vbeg + i % slice;
-            const int64_t gv = static_cast<int64_t>(t) * a.nvec + v;
-            uint32_t sbyte;
-            const float inv = nvfp4_block_scale(g, bmax, sbyte);
-            float q[8];
+        for (int j = 0; j < IPT; ++j) {
+            const int i = tid + j * B;
+            float bmax = 0.0f;
 #pragma unroll
             for (int e = 0; e < 8; ++e)
-                q[e] = __fmul_rn(h[j][e], inv);
-            if (TPAR_IN_RANGE(a.err, gv, a.n_vec_total))
-                st_u32(a.codes + gv, e2m1x8_from_f32(q));
-            const int64_t si = scale_index(a.sf_tiles, gv >> 1, t, v);
-            if ((gv & 1) == 0 && TPAR_IN_RANGE(a.err, si, a.n_scales))
-                st_u8(a.scales + si, sbyte);
+                bmax = fmaxf(bmax, fabsf(h[j][e]));
+            bmax = fmaxf(bmax, __shfl_xor_sync(0xffffffffu, bmax, 1));
+            if (i < items) {
+                const int t = i / slice;
+                const int v = vbeg + i % slice;
+                const int64_t gv = static_cast<int64_t>(t) * a.nvec + v;
+                uint32_t sbyte;
+                const float inv = nvfp4_block_scale(g, bmax, sbyte);
+                float q[8];
+#pragma unroll
+                for (int e = 0; e < 8; ++e)
+                    q[e] = __fmul_rn(h[j][e], inv);
+                if (TPAR_IN_RANGE(a.err, gv, a.n_vec_total))
+                    st_u32(a.codes + gv, e2m1x8_from_f32(q));
+                const int64_t si = scale_index(a.sf_tiles, gv >> 1, t, v);
+                if ((gv & 1) == 0 && TPAR_IN_RANGE(a.err, si, a.n_scales))
+                    st_u8(a.scales + si, sbyte);
+            }
         }
     }
     cluster_wait_acquire();  // no CTA leaves while a peer may still push to it

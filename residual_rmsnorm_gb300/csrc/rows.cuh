@@ -76,7 +76,7 @@ __global__ void __launch_bounds__(1024) rows_prefetch_kernel(const __grid_consta
     const int nsrc = a.n_ranks + (a.residual ? 1 : 0);
     const int64_t G = gridDim.x;
     const int nW = (nvec + 31) >> 5;
-    const int64_t ring_vecs = static_cast<int64_t>(S) * nsrc * nvec;  // extent checked by debug builds
+    [[maybe_unused]] const int64_t ring_vecs = static_cast<int64_t>(S) * nsrc * nvec;  // checked by debug builds
     __shared__ float wsh[2][kMaxRowWarps];  // per-32-vector partial sums of squares, by row parity
 
     // copy this thread's vectors of row t (every source) into stage s
