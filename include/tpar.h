@@ -62,7 +62,10 @@ typedef enum tpar_status {
     TPAR_ERR_UNSUPPORTED = 3,  /* valid but outside what this build handles   */
     TPAR_ERR_CUDA = 4,         /* a CUDA runtime call or launch failed        */
     TPAR_ERR_NOT_INITIALIZED = 5, /* needs tpar_init() first (during capture) */
-    TPAR_ERR_SCRATCH_TOO_SMALL = 6 /* T*d above TPAR_NOALLOC_MAX_ELEMENTS     */
+    TPAR_ERR_SCRATCH_TOO_SMALL = 6, /* T*d above TPAR_NOALLOC_MAX_ELEMENTS    */
+    TPAR_ERR_TIMEOUT = 7,      /* tpar_check: a bounded device wait expired   */
+    TPAR_ERR_INDEX = 8         /* tpar_check, debug builds: an index check
+                                  skipped an out-of-range access             */
 } tpar_status;
 
 /* A cudaStream_t, passed as an opaque pointer so this header needs no CUDA
@@ -326,6 +329,18 @@ tpar_status tpar_plan_launch(int64_t T, int64_t d, int n_ranks, int sm_count, ui
  * not for the hot path.
  */
 tpar_status tpar_device_error(int device, uint32_t* code);
+
+/*
+ * tpar_check -- synchronise `stream`, then read and clear the current
+ * device's error word (as tpar_device_error). Returns TPAR_ERR_CUDA if the
+ * synchronisation reports a CUDA error, TPAR_ERR_TIMEOUT if a bounded device
+ * wait expired since the last read (the outputs of the call that met it are
+ * wrong), TPAR_ERR_INDEX if a debug build's index check skipped an access,
+ * else TPAR_OK. Device-side failures are reported here rather than by the
+ * asynchronous calls themselves; a diagnostic, not for the hot path, and not
+ * to be called while `stream` is being captured.
+ */
+tpar_status tpar_check(tpar_stream_t stream);
 
 /*
  * tpar_debug_build -- 1 if this library was compiled with -DTPAR_DEBUG: every

@@ -29,6 +29,8 @@ from ._abi import (  # noqa: F401
     TPAR_DEVERR_INDEX,
     TPAR_DEVERR_SMALL_WAIT,
     TPAR_DEVERR_STREAM_WAIT,
+    TPAR_ERR_INDEX,
+    TPAR_ERR_TIMEOUT,
     TparError,
     TparPlan,
     library,
@@ -38,6 +40,7 @@ from ._abi import (  # noqa: F401
     tpar_fused_rmsnorm_ex,
     tpar_fused_rmsnorm_fp8,
     tpar_fp8_quantize,
+    tpar_check,
     tpar_debug_build,
     tpar_device_error,
     tpar_init,
@@ -58,5 +61,5 @@ __all__ = [
     "fp8_quantize", "tpar_fused_rmsnorm_fp8", "tpar_fp8_quantize", "TparError", "TparPlan",
     "tpar_init", "tpar_fused_rmsnorm", "tpar_fused_rmsnorm_ex", "tpar_unfused_rmsnorm",
     "tpar_nvfp4_quantize", "tpar_unfused_rmsnorm_noalloc", "tpar_plan_launch", "tpar_status_string", "tpar_version",
-    "tpar_workspace_bytes", "tpar_device_error", "tpar_debug_build", "library", "library_path",
+    "tpar_workspace_bytes", "tpar_device_error", "tpar_check", "tpar_debug_build", "library", "library_path",
 ]

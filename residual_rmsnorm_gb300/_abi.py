@@ -42,8 +42,10 @@ def scales_128x4_bytes(T: int, d: int) -> int:
 _STATUS = {
     0: "TPAR_OK", 1: "TPAR_ERR_INVALID_ARG", 2: "TPAR_ERR_MISALIGNED",
     3: "TPAR_ERR_UNSUPPORTED", 4: "TPAR_ERR_CUDA", 5: "TPAR_ERR_NOT_INITIALIZED",
-    6: "TPAR_ERR_SCRATCH_TOO_SMALL",
+    6: "TPAR_ERR_SCRATCH_TOO_SMALL", 7: "TPAR_ERR_TIMEOUT", 8: "TPAR_ERR_INDEX",
 }
+TPAR_ERR_TIMEOUT = 7
+TPAR_ERR_INDEX = 8
 TPAR_NOALLOC_MAX_ELEMENTS = 8 * 1024 * 1024
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
@@ -113,6 +115,8 @@ def library() -> ctypes.CDLL:
         lib.tpar_debug_build.restype = i32
         lib.tpar_device_error.argtypes = [i32, ctypes.POINTER(ctypes.c_uint32)]
         lib.tpar_device_error.restype = i32
+        lib.tpar_check.argtypes = [P]
+        lib.tpar_check.restype = i32
         lib.tpar_workspace_bytes.argtypes = []
         lib.tpar_workspace_bytes.restype = i64
         lib.tpar_status_string.argtypes = [i32]
@@ -220,6 +224,13 @@ def tpar_plan_launch(T, d, n_ranks, sm_count, flags=0) -> TparPlan:
     _check(library().tpar_plan_launch(T, d, n_ranks, sm_count, flags, ctypes.byref(plan)),
            "tpar_plan_launch")
     return plan
+
+
+def tpar_check(stream=0) -> int:
+    """Synchronise the stream (a cudaStream_t as an int; 0 = the legacy default
+    stream), then read and clear the current device's error word. Returns the
+    status (TPAR_ERR_TIMEOUT, TPAR_ERR_INDEX, TPAR_ERR_CUDA or 0); raises nothing."""
+    return int(library().tpar_check(_p(stream)))
 
 
 def tpar_device_error(device: int) -> int:

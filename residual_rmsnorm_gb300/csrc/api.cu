@@ -1325,6 +1325,26 @@ tpar_status tpar_device_error(int device, uint32_t* code)
     return TPAR_OK;
 }
 
+tpar_status tpar_check(tpar_stream_t stream)
+{
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return TPAR_ERR_CUDA;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess)
+        return TPAR_ERR_CUDA;
+    uint32_t code = 0;
+    const tpar_status st = tpar_device_error(dev, &code);
+    if (st != TPAR_OK)
+        return st;
+    const uint32_t waits =
+        TPAR_DEVERR_CLUSTER_WAIT | TPAR_DEVERR_STREAM_WAIT | TPAR_DEVERR_SMALL_WAIT | TPAR_DEVERR_GRID_WAIT;
+    if (code & waits)
+        return TPAR_ERR_TIMEOUT;
+    if (code & TPAR_DEVERR_INDEX)
+        return TPAR_ERR_INDEX;
+    return TPAR_OK;
+}
+
 const char* tpar_status_string(tpar_status s)
 {
     switch (s) {
@@ -1336,6 +1356,8 @@ const char* tpar_status_string(tpar_status s)
     case TPAR_ERR_NOT_INITIALIZED: return "device workspace missing: call tpar_init before stream capture";
     case TPAR_ERR_SCRATCH_TOO_SMALL:
         return "T*d exceeds the static scratch of the no-allocation entry point (TPAR_NOALLOC_MAX_ELEMENTS)";
+    case TPAR_ERR_TIMEOUT: return "a bounded device-side wait expired: that call's outputs are wrong";
+    case TPAR_ERR_INDEX: return "debug build: an index check skipped an out-of-range access";
     default: return "unknown status";
     }
 }

@@ -117,8 +117,12 @@ def run_shrink(tp):
         tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, out_norm=on, out_residual=orr,
                          **kw)
         torch.cuda.synchronize()
-        code = tp.tpar_device_error(torch.cuda.current_device())
-        assert code & tp.TPAR_DEVERR_INDEX, f"{name}: the shrunk extent was not reported ({code:#x})"
+        if name == "row":  # the same report through tpar_check (which also clears the word)
+            assert tp.tpar_check(torch.cuda.current_stream().cuda_stream) == tp.TPAR_ERR_INDEX, name
+            assert tp.tpar_check(torch.cuda.current_stream().cuda_stream) == 0, name
+        else:
+            code = tp.tpar_device_error(torch.cuda.current_device())
+            assert code & tp.TPAR_DEVERR_INDEX, f"{name}: the shrunk extent was not reported ({code:#x})"
         # the last 16-byte vector (8 elements) was never written
         assert torch.all(on[T - 1, d - 8:] == 7.0) and torch.all(orr[T - 1, d - 8:] == 7.0), name
         # rows before the last are the plain call's bits
@@ -154,9 +158,12 @@ def run_timeouts(tp):
         expect_clean(tp, name + " plain")
         kw2 = dict(kw, flags=kw.get("flags", 0) | tp.TPAR_DEBUG_WAIT_TIMEOUT)
         out = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, **kw2)
-        torch.cuda.synchronize()
-        code = tp.tpar_device_error(torch.cuda.current_device())
-        assert code & bit, f"{name}: the expired wait was not reported ({code:#x})"
+        if name == "cluster exchange":  # through tpar_check, which synchronises and clears
+            assert tp.tpar_check(torch.cuda.current_stream().cuda_stream) == tp.TPAR_ERR_TIMEOUT, name
+        else:
+            torch.cuda.synchronize()
+            code = tp.tpar_device_error(torch.cuda.current_device())
+            assert code & bit, f"{name}: the expired wait was not reported ({code:#x})"
         for k in ("out_norm", "out_residual"):
             assert torch.equal(out[k].view(torch.int16), base[k].view(torch.int16)), (name, k)
         if kw.get("nvfp4"):

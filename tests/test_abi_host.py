@@ -58,8 +58,9 @@ def test_header_compiles_as_c():
 
 
 def test_status_strings_and_version(tp):
-    for s in range(6):
-        assert tp.tpar_status_string(s)
+    for s in range(9):
+        assert tp.tpar_status_string(s) and "unknown" not in tp.tpar_status_string(s)
+    assert "unknown" in tp.tpar_status_string(9)
     assert tp.tpar_version() >= 100
     assert tp.tpar_workspace_bytes() >= 8
 
@@ -378,3 +379,12 @@ def test_unsupported_flags_are_refused_not_ignored(tp):
                                 check=False) == INVALID
     with pytest.raises(tp.TparError):
         tp.tpar_plan_launch(8, 4096, 8, 152, tp.TPAR_GSCALE_GIVEN)
+
+
+def test_check_reports_without_a_device(tp):
+    """tpar_check synchronises the stream before reading the error word: with
+    no CUDA device that fails and is reported as TPAR_ERR_CUDA, not raised."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present (covered by the debug-build GPU checks)")
+    assert tp.tpar_check(0) == 4
