@@ -73,7 +73,7 @@ typedef enum tpar_status {
 typedef void* tpar_stream_t;
 
 #define TPAR_MAX_RANKS 16
-#define TPAR_MAX_HIDDEN 32768
+#define TPAR_MAX_HIDDEN 65536
 
 /* Flags for the _ex / unfused / quantize entry points. */
 #define TPAR_GSCALE_GIVEN 0x1u  /* *global_scale is an INPUT (calibrated g)   */

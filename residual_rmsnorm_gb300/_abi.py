@@ -15,7 +15,7 @@ import torch  # noqa: F401  -- loads PyTorch's CUDA runtime first, so the
 # library below binds to the same libcudart.so.13 instance.
 
 TPAR_MAX_RANKS = 16
-TPAR_MAX_HIDDEN = 32768
+TPAR_MAX_HIDDEN = 65536
 TPAR_GSCALE_GIVEN = 0x1
 TPAR_FORCE_ROW = 0x2
 TPAR_FORCE_CLUSTER = 0x4

@@ -300,6 +300,9 @@ cudaError_t set_attr_once(const void* fn, cudaFuncAttribute attr, int value)
     return e;
 }
 
+// Vectors of a row one CTA can own: 512 threads x 8 vectors (d = 32768).
+constexpr int kMaxVectorsPerCta = 4096;
+
 int pow2_at_least(int64_t n)
 {
     int p = 1;
@@ -500,6 +503,11 @@ tpar_status plan_impl(int64_t T, int64_t d, int n_ranks, int sm_count, uint32_t 
         return TPAR_ERR_INVALID_ARG;
     const int nvec = static_cast<int>(d / 8);
     int split = 1;
+    // One CTA holds at most 512 threads x 8 vectors of a row (d <= 32768);
+    // wider rows are always split over a cluster (up to 16 CTAs of 512 x 2).
+    const bool wide = nvec > kMaxVectorsPerCta;
+    if (wide && (flags & (TPAR_FORCE_ROW | TPAR_FORCE_STREAM)))
+        return TPAR_ERR_UNSUPPORTED;
     // The TMA-fed stream kernel is built and tested but measured slower than
     // the prefetching kernel at prefill (117-120 us vs 110-112 us for N=8,
     // T=4096, d=8192) and than the cluster kernel at decode (4.7-5.8 vs
@@ -542,7 +550,7 @@ tpar_status plan_impl(int64_t T, int64_t d, int n_ranks, int sm_count, uint32_t 
         if (T > sm_count && 20 * T <= 27 * static_cast<int64_t>(sm_count) && row_bytes >= 80 * 1024 &&
             row_bytes <= 320 * 1024 && nvec >= 512)
             split = 8;
-        if ((flags & TPAR_FORCE_CLUSTER) && split == 1) {
+        if ((wide || (flags & TPAR_FORCE_CLUSTER)) && split == 1) {
             if (nvec < 4)
                 return TPAR_ERR_UNSUPPORTED;
             split = 2;

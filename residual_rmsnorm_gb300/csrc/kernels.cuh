@@ -27,7 +27,7 @@
 namespace tpar {
 
 constexpr int kMaxRanks = 16;
-constexpr int kMaxRowWarps = 128;  // 32-vector groups of the widest row (d = 32768)
+constexpr int kMaxRowWarps = 256;  // 32-vector groups of the widest row (d = 65536)
 
 enum QuantMode : int {
     kQuantNone = 0,     // bf16 outputs only

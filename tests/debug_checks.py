@@ -52,6 +52,8 @@ def fused_cases(tp):
         ("nvfp4 given 128x4", 4, 300, 4096, dict(nvfp4=True, global_scale=g, scales_128x4=True)),
         ("nvfp4 dynamic 128x4", 2, 7, 8192, dict(nvfp4=True, scales_128x4=True)),
         ("ragged", 5, 3, 8200, dict()),
+        ("widest rows", 4, 5, 65536, dict()),
+        ("widest rows nvfp4", 2, 40, 65536, dict(nvfp4=True)),
         ("no residual", 3, 260, 2048, dict(residual=None)),
     ]
 

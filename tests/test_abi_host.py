@@ -107,7 +107,7 @@ def test_dry_run_accepts_a_valid_call(tp):
     (dict(d=0), INVALID),
     (dict(d=12), INVALID),
     (dict(d=4), INVALID),
-    (dict(d=32768 + 8), UNSUPPORTED),
+    (dict(d=65536 + 8), UNSUPPORTED),
     (dict(eps=-1.0), INVALID),
     (dict(eps=float("inf")), INVALID),
     (dict(eps=float("nan")), INVALID),
@@ -196,7 +196,8 @@ def test_unfused_and_quantize_checks(tp):
 
 @pytest.mark.parametrize("sm", [152, 148, 132])
 def test_planner_covers_every_row(tp, sm):
-    for d in list(range(8, 1025, 8)) + [2048, 4096, 5120, 7168, 8192, 12288, 16384, 24576, 32768]:
+    for d in list(range(8, 1025, 8)) + [2048, 4096, 5120, 7168, 8192, 12288, 16384, 24576, 32768, 32776,
+                                        40960, 65536]:
         nvec = d // 8
         for T in (1, 2, 3, 4, 8, 16, 32, 64, 76, 77, 152, 4096, 70000):
             p = tp.tpar_plan_launch(T, d, 8, sm)
@@ -215,7 +216,8 @@ def test_planner_covers_every_row(tp, sm):
                 assert p.threads * p.vec_per_thread >= s
                 assert s >= 32 or p.split == 2
                 # rows are split when few, or just past one row per SM to even the load
-                assert (T <= 48 and T * p.split <= 2 * sm) or (sm < T and 20 * T <= 27 * sm and p.split == 8)
+                assert ((T <= 48 and T * p.split <= 2 * sm) or (sm < T and 20 * T <= 27 * sm and p.split == 8)
+                        or nvec > 4096)  # rows wider than one CTA always split
             else:
                 assert p.split == 1 and p.threads * p.vec_per_thread >= nvec
             assert 1 <= p.grid_rows <= min(T, 65535)
@@ -270,6 +272,15 @@ def test_planner_choices_for_the_pages_shapes(tp):
     assert tp.tpar_plan_launch(8, 8192, 8, 152, tp.TPAR_FORCE_STREAM).kernel == 2
     assert tp.tpar_plan_launch(1, 8192, 8, 152, tp.TPAR_FORCE_ROW).kernel == 0
     assert tp.tpar_plan_launch(4096, 4096, 8, 152, tp.TPAR_FORCE_CLUSTER).kernel == 1
+    # rows wider than 4096 vectors (d > 32768) are always split over a cluster
+    # of CTAs of up to 512 threads x 2 vectors; no other form holds them
+    for T in (1, 8, 64, 4096):
+        p = tp.tpar_plan_launch(T, 65536, 8, 152)
+        assert p.kernel == 1 and p.threads * p.vec_per_thread * p.split >= 8192, (T, p.as_dict())
+    for fl in (tp.TPAR_FORCE_ROW, tp.TPAR_FORCE_STREAM):
+        with pytest.raises(tp.TparError):
+            tp.tpar_plan_launch(8, 65536, 8, 152, fl)
+    assert call(tp, d=65536, T=2) == OK  # accepted by the fused entry point (dry run)
 
 
 def test_fp8_entry_point_checks(tp):

@@ -477,3 +477,40 @@ def test_in_place_residual_every_form(form):
     if form.startswith("nvfp4"):
         assert_nvfp4_bit_exact(out["out_norm"], out["codes"], out["scales"], out["global_scale"], what=form)
     assert tp.tpar_device_error(torch.cuda.current_device()) == 0
+
+
+@pytest.mark.parametrize("n,T,d,dt", [(1, 1, 65536, "bf16"), (4, 3, 65536, "bf16"), (16, 2, 65536, "bf16"),
+                                      (2, 33, 40976, "bf16"), (4, 200, 65536, "bf16"), (8, 160, 32776, "bf16"),
+                                      (3, 7, 65536, "fp16")])
+def test_widest_rows(n, T, d, dt):
+    """Hidden sizes above one CTA's 4096 vectors (d > 32768, up to 65536):
+    always split over a cluster. Against the oracle (sampled rows), NVFP4
+    bit-exact with dynamic and given scale, the unfused path within its
+    bound, and bit-identical to an explicit cluster request."""
+    tp = lib()
+    w = synth.Workload(f"wide N{n} T{T} d{d}", n, T, d, 1e-5, 0.5, seed=n + T + d)
+    inputs = synth.make_inputs(w, dtype=torch.float16 if dt == "fp16" else torch.bfloat16)
+    dev = to_device(inputs)
+    out = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps)
+    forced = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, flags=tp.TPAR_FORCE_CLUSTER)
+    torch.cuda.synchronize()
+    rows = np.unique([0, T // 2, T - 1])
+    ref = oracle_rows(inputs, rows, w.eps)
+    assert_close_to_ref(out["out_norm"][rows], ref["y"], "wide out_norm")
+    assert_close_to_ref(out["out_residual"][rows], ref["h"], "wide out_residual")
+    assert torch.equal(out["out_norm"].view(torch.int16), forced["out_norm"].view(torch.int16))
+    if d % 16 == 0:
+        g = torch.tensor([0.02], dtype=torch.float32, device="cuda")
+        for given in (None, g):
+            q = tp.fused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps, nvfp4=True, global_scale=given)
+            torch.cuda.synchronize()
+            assert_nvfp4_bit_exact(q["out_norm"], q["codes"], q["scales"], q["global_scale"],
+                                   given=None if given is None else float(np.float32(0.02)), what="wide")
+    u = tp.unfused_rmsnorm(dev["partials"], dev["residual"], dev["gamma"], w.eps)
+    torch.cuda.synchronize()
+    from gpu_helpers import unfused_extra_tolerance
+    sub = {"partials": [p[rows] for p in inputs["partials"]], "residual": inputs["residual"][rows],
+           "gamma": inputs["gamma"]}
+    eh, ey = unfused_extra_tolerance(sub, ref, w.eps)
+    assert_close_to_ref(u["out_norm"][rows], ref["y"], "wide unfused out_norm", extra=ey)
+    assert tp.tpar_device_error(torch.cuda.current_device()) == 0
