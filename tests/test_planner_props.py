@@ -1,0 +1,64 @@
+"""Property test of the launch planner (host only): for random shapes and
+SM counts every automatic plan is accepted by the library's own plan check
+(a dry run with the plan passed back explicitly), covers its row, and keeps
+the documented forms: rows split over a cluster only when few, just past one
+row per SM, or wider than one CTA; the prefetching kernel only above 1.5 rows
+per SM."""
+import pytest
+
+hyp = pytest.importorskip("hypothesis")
+st = pytest.importorskip("hypothesis.strategies")
+
+BASE = 0x7F0000000000
+GB = 1 << 30
+
+
+@pytest.fixture(scope="module")
+def tp():
+    from residual_rmsnorm_gb300 import build
+    build.build()
+    import residual_rmsnorm_gb300 as tp
+    tp.library()
+    return tp
+
+
+@hyp.settings(max_examples=400, deadline=None)
+@hyp.given(T=st.integers(1, 100000), d8=st.integers(1, 8192), n=st.integers(1, 16), sm=st.integers(40, 200))
+def test_automatic_plans_are_valid(tp, T, d8, n, sm):
+    d = 8 * d8
+    nvec = d8
+    p = tp.tpar_plan_launch(T, d, n, sm)
+    assert p.kernel in (0, 1, 3)
+    assert 1 <= p.grid_rows <= min(T, 65535)
+    if p.kernel == 0:
+        assert p.split == 1 and p.threads * p.vec_per_thread >= nvec and nvec <= 4096
+    elif p.kernel == 1:
+        slice_ = -(-(-(-nvec // p.split)) // 32) * 32
+        assert 2 <= p.split <= 16 and p.threads * p.vec_per_thread >= slice_ and p.vec_per_thread <= 2
+        assert (T <= 48) or (sm < T and 20 * T <= 27 * sm) or nvec > 4096
+    else:
+        assert 2 * T > 3 * sm and 256 <= nvec <= 2048 and p.grid_rows == min(T, sm)
+    # the plan the planner chose passes the library's own check for these sizes
+    parts = [BASE + r * GB for r in range(n)]
+    if T * d * 2 < GB // 2:  # keep the fake tensors apart
+        st_ = tp.tpar_fused_rmsnorm_ex(parts, n, BASE + 20 * GB, BASE + 21 * GB, 1e-5, T, d, BASE + 22 * GB,
+                                       BASE + 23 * GB, 0, 0, 0, tp.TPAR_DRY_RUN, p, 0, 0, check=False)
+        assert st_ == 0, (T, d, n, sm, p.as_dict(), st_)
+
+
+@hyp.settings(max_examples=200, deadline=None)
+@hyp.given(T=st.integers(1, 5000), d8=st.integers(1, 8192), n=st.integers(1, 16), sm=st.integers(40, 200))
+def test_forced_forms(tp, T, d8, n, sm):
+    d = 8 * d8
+    wide = d8 > 4096
+    for flag, kernel in ((tp.TPAR_FORCE_ROW, 0), (tp.TPAR_FORCE_STREAM, 2)):
+        if wide:
+            with pytest.raises(tp.TparError):
+                tp.tpar_plan_launch(T, d, n, sm, flag)
+        else:
+            try:
+                assert tp.tpar_plan_launch(T, d, n, sm, flag).kernel == kernel
+            except tp.TparError:
+                assert flag == tp.TPAR_FORCE_STREAM  # rows the TMA-fed kernel cannot hold
+    if d8 >= 4:
+        assert tp.tpar_plan_launch(T, d, n, sm, tp.TPAR_FORCE_CLUSTER).kernel == 1
