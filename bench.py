@@ -575,12 +575,18 @@ def ours_arm(args, w):
     st = torch.cuda.current_stream()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    # one event between steps as well, for the per-step spread
+    marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps - 1)]
     with nvtx(torch, f"timed region: {args.steps} x {CALLS_PER_STEP} calls of {w.name}"):
         e0.record(st)
-        for _ in range(args.steps):
+        for k in range(args.steps):
             g.replay()
+            if k < args.steps - 1:
+                marks[k].record(st)
         e1.record(st)
         e1.synchronize()
+    edges = [e0] + marks + [e1]
+    step_us = sorted(edges[k].elapsed_time(edges[k + 1]) * 1e3 / CALLS_PER_STEP for k in range(args.steps))
     barrier(dist, device)
     clocks = sampler.stop()
     ms_total = e0.elapsed_time(e1)
@@ -699,6 +705,10 @@ def ours_arm(args, w):
                                   "buffers and a D2H copy of the outputs around each call"},
             "gpu_launches": args.steps * CALLS_PER_STEP,
             "clocks": clocks,
+            "us_per_call_stats": {"median": round(statistics.median(step_us), 4),
+                                  "p10": round(step_us[int(0.1 * (len(step_us) - 1))], 4),
+                                  "p90": round(step_us[int(round(0.9 * (len(step_us) - 1)))], 4),
+                                  "steps": len(step_us), "note": "this rank's steps, each a 1000-call graph"},
             "l2_hot_us_per_call": round(us_hot, 4),
             "cpu_baseline": cpu,
             "cpu_baseline_all_cores": cpu_par,
