@@ -393,7 +393,11 @@ tpar_status tpar_unfused_rmsnorm_noalloc(const void* const* partials, int n_rank
 /* Static message for a status code. */
 const char* tpar_status_string(tpar_status status);
 
-/* Library version, major * 10000 + minor * 100 + patch. */
+/* Library version, major * 10000 + minor * 100 + patch: the TPAR_VERSION this
+ * header describes. A caller built against this header can require
+ * tpar_version() >= TPAR_VERSION of the library it loads. 0.2.0 added
+ * tpar_check, TPAR_ERR_TIMEOUT / TPAR_ERR_INDEX and hidden sizes up to 65536. */
+#define TPAR_VERSION 200
 int tpar_version(void);
 
 #ifdef __cplusplus

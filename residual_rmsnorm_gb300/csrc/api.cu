@@ -1381,7 +1381,7 @@ const char* tpar_status_string(tpar_status s)
     }
 }
 
-int tpar_version(void) { return 100; }
+int tpar_version(void) { return TPAR_VERSION; }
 
 int tpar_debug_build(void) { return kDebugBuild ? 1 : 0; }
 

@@ -47,7 +47,7 @@ static int failures = 0;
 
 static int host_mode(void)
 {
-    CHECK(tpar_version() >= 100, "version %d", tpar_version());
+    CHECK(tpar_version() >= TPAR_VERSION, "version %d", tpar_version());
     for (int s = 0; s <= 6; ++s)
         CHECK(tpar_status_string((tpar_status)s) != NULL && tpar_status_string((tpar_status)s)[0] != 0,
               "status string %d", s);

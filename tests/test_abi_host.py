@@ -61,7 +61,8 @@ def test_status_strings_and_version(tp):
     for s in range(9):
         assert tp.tpar_status_string(s) and "unknown" not in tp.tpar_status_string(s)
     assert "unknown" in tp.tpar_status_string(9)
-    assert tp.tpar_version() >= 100
+    header_version = int(re.search(r"#define TPAR_VERSION (\d+)", open(HEADER).read()).group(1))
+    assert tp.tpar_version() == header_version >= 200
     assert tp.tpar_workspace_bytes() >= 8
 
 
