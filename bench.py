@@ -47,7 +47,7 @@ CALLS_PER_STEP = 1000
 # dram bytes (read + write) per launch of the fused kernel, from one ncu
 # capture of the decode workload; valid only for the kernel sources it was
 # taken on (sha256 over residual_rmsnorm_gb300/csrc at that time).
-NCU_TRAFFIC = {"kernel_src_sha": "25f8d3c116855c48", "decode llama3-8b N8 T8 d4096": 611072 + 0}
+NCU_TRAFFIC = {"kernel_src_sha": "c88e11c292a66c02", "decode llama3-8b N8 T8 d4096": 611584 + 0}
 
 
 def kernel_sources_sha() -> str:
